@@ -1,0 +1,141 @@
+/*
+ * spectree.h -- C ABI of the GB300 (sm_103a) token-tree verification library (libspectree.so).
+ *
+ * The library computes the verification step of EAGLE-style speculative decoding:
+ *
+ *   1. spec_tree_attention: tree-masked attention.  Every node of the draft tree attends to its
+ *      sequence's KV-cache prefix and to its own ancestors (itself included), as given by parent
+ *      indices.  Defined by the EAGLE paper explainer, "Static tree" section (all tree paths are
+ *      verified in one forward pass under a tree attention mask) and the speculative-decoding
+ *      survey explainer, verification taxonomy ("Token Tree verification").
+ *
+ *   2. spec_tree_verify: speculative-sampling accept/reject over the tree.  Survey explainer,
+ *      "Formal Definition": draft x~_i is accepted if r < min(1, q_i(x~_i) / p_i(x~_i)); at the first
+ *      rejection c the next token is drawn from norm(max(0, q_c - p_c)); with temperature 0 the test
+ *      is greedy argmax matching (taxonomy table, "Greedy verification").
+ *
+ * Conventions shared by every entry point
+ *   - All array arguments are DEVICE pointers (cudaMalloc'd or managed memory) owned by the caller.
+ *     The library never allocates, frees or retains them and keeps no state between calls.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy default stream) and
+ *     performs no host<->device synchronisation.  Calls on different streams are independent as
+ *     long as they do not share output or workspace buffers.
+ *   - Argument errors are reported synchronously, before anything is launched, by a negative
+ *     return value (spec_err_t).  A launch failure returns SPEC_ERR_CUDA.
+ *   - Content errors found on the device are reported per sequence in `status[b]` (SPEC_ST_* bits;
+ *     `status` may be NULL).  Each call overwrites status[b] for every b.  A flagged sequence gets
+ *     -1 in its integer outputs and zeros in its attention rows; other sequences are unaffected.
+ *   - No kernel traps, asserts or waits without bound: every device-side wait gives up after a
+ *     fixed number of polls and sets SPEC_ST_TIMEOUT.
+ *   - Node 0 of every tree is the root (the last committed token, whose key/value is written at
+ *     cache slot L_b like every other node).  tree_parent[b][0] == -1 and
+ *     0 <= tree_parent[b][i] < i for i >= 1 (parents precede children).  1 <= N <= 64.
+ */
+#ifndef SPECTREE_H
+#define SPECTREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = -1, /* bad shape, NULL required pointer, T < 0 or non-finite, ... */
+  SPEC_ERR_UNSUPPORTED = -2, /* shape outside what the kernels implement (e.g. D not 64/128)  */
+  SPEC_ERR_WORKSPACE = -3,   /* workspace NULL or smaller than the *_workspace() query        */
+  SPEC_ERR_CUDA = -4         /* a CUDA runtime / driver call or a launch failed               */
+} spec_err_t;
+
+/* per-sequence status bits (int32 status[B]) */
+#define SPEC_ST_BAD_TREE 1   /* tree_parent[b][0] != -1, or tree_parent[b][i] outside [0, i)       */
+#define SPEC_ST_BAD_LEN 2    /* prefix_lens[b] < 0 or prefix_lens[b] + N > Lmax                    */
+#define SPEC_ST_BAD_TOKEN 4  /* a draft token tree_tokens[b][i >= 1] outside [0, V)                */
+#define SPEC_ST_NONFINITE 8  /* NaN or +Inf in a target-logit row that was read, or a bad p value  */
+#define SPEC_ST_TIMEOUT 16   /* a bounded device-side wait gave up                                 */
+
+/* ------------------------------------------------------------------------------------------------
+ * Tree attention
+ * ------------------------------------------------------------------------------------------------
+ * Workspace bytes spec_tree_attention needs for these sizes on the current device (split-KV
+ * partial results).  Returns 0 for invalid sizes.
+ */
+size_t spec_tree_attention_workspace(int B, int N, int Hq, int Hkv, int D, int Lmax);
+
+/*
+ * Tree-masked attention of the draft tree's queries (one layer).
+ *
+ *   q           bf16 [B, N, Hq, D]      query of node i, head h (RoPE already applied)
+ *   k_cache     bf16 [B, Hkv, Lmax, D]  keys; prefix at slots 0..L_b-1, node i's key at slot L_b+i
+ *   v_cache     bf16 [B, Hkv, Lmax, D]  values, same slots
+ *   prefix_lens int32 [B]               L_b, the committed prefix length of sequence b
+ *   tree_parent int32 [B, N]            parent index of every node (see conventions)
+ *   out         bf16 [B, N, Hq, D]      attention output
+ *   out_lse     fp32 [B, Hq, N] or NULL natural-log sum-exp of the scaled scores per row
+ *   softmax_scale                       score scale (usually 1/sqrt(D))
+ *   workspace   device scratch of at least spec_tree_attention_workspace(...) bytes, 16-byte
+ *               aligned; contents need not be initialised and are garbage afterwards
+ *   status      int32 [B] or NULL       SPEC_ST_BAD_TREE / SPEC_ST_BAD_LEN / SPEC_ST_TIMEOUT
+ *
+ * Node i, query head h sees the keys {0..L_b-1} U {L_b + j : j ancestor of i or j == i}, using KV
+ * head h / (Hq/Hkv).  Supported: D in {64, 128}, Hq % Hkv == 0, Hq/Hkv <= 16, N*Hq/Hkv rows per
+ * KV head, Lmax >= N.  q, k_cache, v_cache and out must be 16-byte aligned.
+ */
+int spec_tree_attention(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* prefix_lens, const int32_t* tree_parent, void* out,
+                        float* out_lse, int B, int N, int Hq, int Hkv, int D, int Lmax,
+                        float softmax_scale, void* workspace, size_t workspace_bytes,
+                        int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * Speculative-sampling verification
+ * ------------------------------------------------------------------------------------------------
+ * Workspace bytes spec_tree_verify needs (per-node statistics and decisions).  0 if invalid.
+ */
+size_t spec_tree_verify_workspace(int B, int N, int V);
+
+/*
+ * Accept/reject the draft tree of every sequence and draw its bonus token.
+ *
+ *   target_logits fp32 [B, N, V]  row j: target logits for the token after node j's path
+ *   draft_probs   fp32 [B, N, V]  row j: draft distribution p_j the children of j were drawn from
+ *                                 (already tempered by the caller); may be NULL iff temperature==0
+ *   tree_tokens   int32 [B, N]    token of node i (entry 0, the root, is not read)
+ *   tree_parent   int32 [B, N]
+ *   uniforms      fp32 [B, N]     entry i >= 1: the test uniform r_i of node i, in [0, 1);
+ *                                 entry 0: the uniform u of the bonus-token draw
+ *   temperature   >= 0; q_j = softmax(l_j / T); 0 selects greedy verification
+ *   out_accept_len      int32 [B]        accepted drafts (depth of the last accepted node)
+ *   out_accepted_tokens int32 [B, N]     tokens on the accepted path (root excluded), -1 padded
+ *   out_bonus_token     int32 [B]        token drawn where the walk stopped
+ *   out_accepted_nodes  int32 [B, N] or NULL   node indices of the accepted path, -1 padded
+ *   out_child_q         fp32 [B, N] or NULL    q value used in node i's own test (the current
+ *                                 residual's probability of x~_i); -1 where node i was not tested
+ *                                 (an earlier sibling was accepted) and at the root; at T == 0 it
+ *                                 is 1 or 0 (token equals / differs from the parent's argmax)
+ *   workspace     at least spec_tree_verify_workspace(B, N, V) bytes, 16-byte aligned
+ *   status        int32 [B] or NULL  SPEC_ST_BAD_TREE / SPEC_ST_BAD_TOKEN / SPEC_ST_NONFINITE /
+ *                                 SPEC_ST_TIMEOUT
+ *
+ * Tree rule (the pages give the chain form only): the children of the current node are tried in
+ * ascending index against the current target distribution, which is replaced by its normalised
+ * residual norm(max(0, q - p)) after each rejection (kept if that residual is all zero).  The
+ * emitted tokens of the step are the accepted tokens followed by the bonus token.
+ */
+int spec_tree_verify(const float* target_logits, const float* draft_probs,
+                     const int32_t* tree_tokens, const int32_t* tree_parent,
+                     const float* uniforms, float temperature, int B, int N, int V,
+                     int32_t* out_accept_len, int32_t* out_accepted_tokens,
+                     int32_t* out_bonus_token, int32_t* out_accepted_nodes, float* out_child_q,
+                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* Human-readable text for a spec_err_t return value or a SPEC_ST_* bit. */
+const char* spec_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECTREE_H */

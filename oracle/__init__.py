@@ -1,0 +1,21 @@
+"""CPU oracle for the token-tree verification step (test infrastructure, not product code).
+
+A plain, slow, float64 NumPy restatement of what the method computes, written from the method's
+published definitions:
+
+* ``oracle.attention`` -- tree-masked attention: every draft-tree node attends to its sequence's
+  KV-cache prefix and to its own ancestors (itself included), found by walking parent pointers.
+  EAGLE paper explainer, "Static tree" section; speculative-decoding survey explainer, "Token Tree
+  verification" paragraph.
+* ``oracle.verify`` -- speculative-sampling accept/reject over the tree, the walk to the accepted
+  path and the resample of the bonus token from norm(max(0, q - p)); temperature 0 is greedy
+  argmax matching.  Survey explainer, "Formal Definition" (draft / verify / accept-reject
+  equations) and the verification taxonomy table.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg import this package.
+It shares no code with the CUDA path and imports nothing from it.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_*.py`` against library routines,
+closed forms, exact rational enumeration and brute force (none re-types the oracle's formulas).
+"""
+from . import attention, verify  # noqa: F401

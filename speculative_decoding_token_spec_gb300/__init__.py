@@ -1,0 +1,22 @@
+"""GB300-native token-tree verification for EAGLE-style speculative decoding.
+
+Two calls make up the hot path, both hand-written CUDA for sm_103a behind a C ABI
+(``include/spectree.h``, built into ``libspectree.so``):
+
+* ``spec_tree_attention`` -- tree-masked split-KV attention of the draft tree's queries over each
+  sequence's KV-cache prefix and the node's own ancestors;
+* ``spec_tree_verify`` -- speculative-sampling accept/reject over the tree, the walk to the accepted
+  path and the bonus-token resample (greedy argmax matching at temperature 0).
+
+The Python functions of the same names only marshal torch tensors into pointers and the current
+CUDA stream.  There is no CPU fallback: a missing library raises.
+"""
+from ._binding import (  # noqa: F401
+    SpecError,
+    spec_tree_attention,
+    spec_tree_attention_workspace,
+    spec_tree_verify,
+    spec_tree_verify_workspace,
+    spec_status_string,
+    lib,
+)

@@ -1,0 +1,182 @@
+"""Thin ctypes binding of libspectree (argument marshalling only).
+
+Each function takes torch CUDA tensors, checks dtypes / contiguity, allocates the outputs it is
+not given (torch owns device memory), and calls the C entry point of the same name with raw
+device pointers and the current CUDA stream.  Every step of the computation runs in the library's
+kernels; if the library is missing or fails to load, these functions raise -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+from . import build as _build
+
+_LIB = None
+_LOCK = threading.Lock()
+
+SPEC_OK = 0
+ERRORS = {-1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_UNSUPPORTED", -3: "SPEC_ERR_WORKSPACE",
+          -4: "SPEC_ERR_CUDA"}
+ST_BAD_TREE, ST_BAD_LEN, ST_BAD_TOKEN, ST_NONFINITE, ST_TIMEOUT = 1, 2, 4, 8, 16
+
+
+class SpecError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} returned {code} ({ERRORS.get(code, '?')}): "
+                         f"{spec_status_string(code)}")
+
+
+_c_int, _c_size, _vp, _c_float = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+
+_SIGNATURES = {
+    "spec_tree_attention_workspace": (_c_size, [_c_int] * 6),
+    "spec_tree_attention": (_c_int, [_vp] * 7 + [_c_int] * 6 + [_c_float, _vp, _c_size, _vp, _vp]),
+    "spec_tree_verify_workspace": (_c_size, [_c_int] * 3),
+    "spec_tree_verify": (_c_int, [_vp] * 5 + [_c_float] + [_c_int] * 3 + [_vp] * 5
+                         + [_vp, _c_size, _vp, _vp]),
+    "spec_status_string": (ctypes.c_char_p, [_c_int]),
+}
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib(build_if_missing: bool = True):
+    """Load libspectree.so (building it first if it is absent)."""
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            path = lib_path()
+            if not os.path.exists(path):
+                if not build_if_missing:
+                    raise RuntimeError(f"libspectree not built ({path} missing)")
+                _build.build()
+            handle = ctypes.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype, fn.argtypes = res, args
+            _LIB = handle
+    return _LIB
+
+
+def spec_status_string(code: int) -> str:
+    try:
+        return lib().spec_status_string(int(code)).decode()
+    except Exception:  # pragma: no cover - only used inside error messages
+        return ERRORS.get(code, "unknown")
+
+
+# ----------------------------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, dtype, shape, device):
+    torch = _torch()
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device or t.device.type != "cuda":
+        raise ValueError(f"{name} must live on {device}")
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def spec_tree_attention_workspace(B, N, Hq, Hkv, D, Lmax) -> int:
+    return int(lib().spec_tree_attention_workspace(B, N, Hq, Hkv, D, Lmax))
+
+
+def spec_tree_verify_workspace(B, N, V) -> int:
+    return int(lib().spec_tree_verify_workspace(B, N, V))
+
+
+def spec_tree_attention(q, k_cache, v_cache, prefix_lens, tree_parent, softmax_scale=None,
+                        out=None, out_lse=None, want_lse=True, workspace=None, status=None,
+                        stream=None):
+    """Tree-masked attention; returns (out bf16 [B,N,Hq,D], lse fp32 [B,Hq,N] or None, status)."""
+    torch = _torch()
+    B, N, Hq, D = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    dev = q.device
+    _check(q, "q", torch.bfloat16, (B, N, Hq, D), dev)
+    _check(k_cache, "k_cache", torch.bfloat16, (B, Hkv, Lmax, D), dev)
+    _check(v_cache, "v_cache", torch.bfloat16, (B, Hkv, Lmax, D), dev)
+    _check(prefix_lens, "prefix_lens", torch.int32, (B,), dev)
+    _check(tree_parent, "tree_parent", torch.int32, (B, N), dev)
+    if out is None:
+        out = torch.empty((B, N, Hq, D), dtype=torch.bfloat16, device=dev)
+    if out_lse is None and want_lse:
+        out_lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    if status is None:
+        status = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws_bytes = spec_tree_attention_workspace(B, N, Hq, Hkv, D, Lmax)
+    if workspace is None:
+        workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
+    scale = (1.0 / math.sqrt(D)) if softmax_scale is None else float(softmax_scale)
+    rc = lib().spec_tree_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(prefix_lens), _ptr(tree_parent), _ptr(out),
+        _ptr(out_lse), B, N, Hq, Hkv, D, Lmax, scale, _ptr(workspace), workspace.numel(),
+        _ptr(status), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_tree_attention", rc)
+    return out, out_lse, status
+
+
+def spec_tree_verify(target_logits, draft_probs, tree_tokens, tree_parent, uniforms, temperature,
+                     outputs=None, workspace=None, status=None, want_nodes=True,
+                     want_child_q=False, stream=None):
+    """Speculative-sampling verification; returns a dict of device tensors.
+
+    Keys: accept_len [B], accepted_tokens [B,N], bonus [B], accepted_nodes [B,N] (if want_nodes),
+    child_q [B,N] (if want_child_q), status [B].
+    """
+    torch = _torch()
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    _check(target_logits, "target_logits", torch.float32, (B, N, V), dev)
+    if draft_probs is not None:
+        _check(draft_probs, "draft_probs", torch.float32, (B, N, V), dev)
+    _check(tree_tokens, "tree_tokens", torch.int32, (B, N), dev)
+    _check(tree_parent, "tree_parent", torch.int32, (B, N), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, N), dev)
+    o = dict(outputs or {})
+    i32 = dict(dtype=torch.int32, device=dev)
+    o.setdefault("accept_len", torch.empty((B,), **i32))
+    o.setdefault("accepted_tokens", torch.empty((B, N), **i32))
+    o.setdefault("bonus", torch.empty((B,), **i32))
+    if want_nodes:
+        o.setdefault("accepted_nodes", torch.empty((B, N), **i32))
+    if want_child_q:
+        o.setdefault("child_q", torch.empty((B, N), dtype=torch.float32, device=dev))
+    o["status"] = status if status is not None else torch.empty((B,), **i32)
+    ws_bytes = spec_tree_verify_workspace(B, N, V)
+    if workspace is None:
+        workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
+    rc = lib().spec_tree_verify(
+        _ptr(target_logits), _ptr(draft_probs), _ptr(tree_tokens), _ptr(tree_parent),
+        _ptr(uniforms), float(temperature), B, N, V, _ptr(o["accept_len"]),
+        _ptr(o["accepted_tokens"]), _ptr(o["bonus"]), _ptr(o.get("accepted_nodes")),
+        _ptr(o.get("child_q")), _ptr(workspace), workspace.numel(), _ptr(o["status"]),
+        _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_tree_verify", rc)
+    return o

@@ -1,0 +1,258 @@
+"""Seeded synthetic inputs for the token-tree verification step.
+
+This module only *draws inputs*: draft trees, draft tokens, KV caches, queries, target logits,
+draft-model probabilities and the uniforms the method consumes.  It holds none of the
+verification arithmetic (no tree-attention, no accept/reject, no residual, no sampling of the
+bonus token); both the CUDA path and the CPU oracle are fed from here.
+
+Shapes follow the workloads of the EAGLE paper explainer ("Static tree" section: a 60-node tree of
+depth 6 with at most 10 nodes per level, Vicuna-7B) and of the speculative-decoding survey explainer
+("Formal Definition": drafts are sampled from the draft distribution, one uniform per test).  The
+pages measure on MT-bench / Spec-Bench with real models; those are not available, so these seeded
+tensors stand in for them by shape and value distribution only.
+
+Everything is numpy (PCG64 through ``default_rng`` seeded with integer lists, which is identical on
+x86_64 and aarch64).  bf16 tensors are returned as ``uint16`` bit patterns (round-to-nearest-even
+from float32) so that both sides read exactly the same values.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional, Sequence
+
+import numpy as np
+
+__all__ = [
+    "AttnCase", "VerifyCase", "CONFIGS", "make_tree", "chain_tree", "make_attention_case",
+    "make_verify_case", "bf16_bits", "bf16_to_f64", "config",
+]
+
+
+# ----------------------------------------------------------------------------------------------
+# bf16 bit handling (input preparation only)
+# ----------------------------------------------------------------------------------------------
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round to bf16 (nearest-even, via float32) and return the uint16 bit patterns."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float64."""
+    u = bits.astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+# ----------------------------------------------------------------------------------------------
+# draft trees
+# ----------------------------------------------------------------------------------------------
+def chain_tree(n: int) -> np.ndarray:
+    """Parent array of a chain: node i's parent is i-1, node 0 is the root (parent -1)."""
+    par = np.arange(-1, n - 1, dtype=np.int32)
+    return par
+
+
+def make_tree(rng: np.random.Generator, n: int, depth: int, width_cap: int) -> np.ndarray:
+    """Random static draft tree: the root plus ``n-1`` draft nodes on levels 1..depth.
+
+    Every level starts with one node; the remaining nodes are added one at a time to a uniformly
+    random level that is still below ``width_cap``.  Each node picks a uniformly random parent on
+    the previous level.  Nodes are numbered level by level, and within a level by parent, so the
+    numbering is breadth-first and every parent index is smaller than its child's.
+    """
+    if n < 1:
+        raise ValueError("n must be >= 1")
+    drafts = n - 1
+    if drafts == 0:
+        return np.array([-1], dtype=np.int32)
+    depth = min(depth, drafts)
+    if drafts > depth * width_cap:
+        raise ValueError("tree does not fit the depth/width caps")
+    widths = [1] * depth
+    for _ in range(drafts - depth):
+        open_levels = [lv for lv in range(depth) if widths[lv] < width_cap]
+        widths[open_levels[int(rng.integers(len(open_levels)))]] += 1
+    parent = [-1]
+    prev = [0]
+    for lv in range(depth):
+        pars = sorted(int(prev[int(rng.integers(len(prev)))]) for _ in range(widths[lv]))
+        first = len(parent)
+        parent.extend(pars)
+        prev = list(range(first, first + widths[lv]))
+    return np.asarray(parent, dtype=np.int32)
+
+
+# ----------------------------------------------------------------------------------------------
+# configurations
+# ----------------------------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class Config:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    prefix: tuple          # ("fixed", L) or ("uniform", lo, hi)
+    N: int
+    tree: str              # "chain" or "static"
+    depth: int
+    width: int
+    V: int
+    sigma_t: float
+    sigma_d: float
+    temperatures: tuple
+    qkv_fp32: bool = False  # the tiny case draws fp32 Q/K/V (rounded to bf16 for the kernels)
+    cfg_id: int = 0
+
+
+CONFIGS = {
+    # CPU-seconds case: chain of 5 nodes (depth 4), vocab 1000.
+    "tiny": Config("tiny", 1, 4, 4, 64, ("fixed", 128), 5, "chain", 4, 1, 1000, 2.0, 0.5,
+                   (1.0,), qkv_fp32=True, cfg_id=1),
+    # EAGLE static tree (60 nodes, depth 6, width <= 10) on a Vicuna-7B attention shape.
+    "eagle_vicuna7b": Config("eagle_vicuna7b", 1, 32, 32, 128, ("fixed", 1024), 60, "static", 6,
+                             10, 32000, 3.0, 1.0, (0.0, 1.0), cfg_id=2),
+    # Batched LLaMA-3-8B-like GQA, prefixes uniform in [512, 4096].
+    "llama3_8b_gqa": Config("llama3_8b_gqa", 16, 32, 8, 128, ("uniform", 512, 4096), 60, "static",
+                            6, 10, 128256, 3.0, 1.5, (0.7,), cfg_id=3),
+    # Long-context 70B-like GQA.  The target-logit spread is not stated for this shape; the
+    # batched GQA shape's 3.0 is used.
+    "llama70b_longctx": Config("llama70b_longctx", 4, 64, 8, 128, ("fixed", 32768), 60, "static",
+                               6, 10, 128256, 3.0, 1.0, (1.0,), cfg_id=4),
+    # Verification stress sweep (tree size, temperature and draft noise vary per case).
+    "stress": Config("stress", 64, 32, 32, 128, ("fixed", 2048), 60, "static", 6, 10, 32000, 3.0,
+                     1.0, (0.0, 0.5, 1.0, 1.5), cfg_id=5),
+}
+
+
+def config(name: str, **overrides) -> Config:
+    return dataclasses.replace(CONFIGS[name], **overrides)
+
+
+def _rng(seed: int, cfg_id: int, b: int, stream: int) -> np.random.Generator:
+    return np.random.default_rng([int(seed), int(cfg_id), int(b), int(stream)])
+
+
+def _prefix_lens(cfg: Config, seed: int) -> np.ndarray:
+    if cfg.prefix[0] == "fixed":
+        return np.full(cfg.B, cfg.prefix[1], dtype=np.int32)
+    lo, hi = cfg.prefix[1], cfg.prefix[2]
+    rng = _rng(seed, cfg.cfg_id, 10_000, 7)
+    return rng.integers(lo, hi + 1, size=cfg.B).astype(np.int32)
+
+
+def _tree(cfg: Config, seed: int, b: int) -> np.ndarray:
+    if cfg.tree == "chain":
+        return chain_tree(cfg.N)
+    return make_tree(_rng(seed, cfg.cfg_id, b, 1), cfg.N, cfg.depth, cfg.width)
+
+
+# ----------------------------------------------------------------------------------------------
+# attention inputs
+# ----------------------------------------------------------------------------------------------
+@dataclasses.dataclass
+class AttnCase:
+    q: np.ndarray             # uint16 bf16 bits [B, N, Hq, D]
+    k_cache: np.ndarray       # uint16 bf16 bits [B, Hkv, Lmax, D]; node i's key at slot L_b + i
+    v_cache: np.ndarray       # uint16 bf16 bits [B, Hkv, Lmax, D]
+    prefix_lens: np.ndarray   # int32 [B]
+    tree_parent: np.ndarray   # int32 [B, N]
+    scale: float
+    Lmax: int
+
+    @property
+    def shape(self):
+        B, N, Hq, D = self.q.shape
+        return B, N, Hq, self.k_cache.shape[1], D
+
+
+def make_attention_case(cfg: Config, seed: int = 0, lmax_pad: int = 0,
+                        prefix_lens: Optional[Sequence[int]] = None) -> AttnCase:
+    """Q, K, V ~ N(0, 1) rounded to bf16; the tree's own keys sit right after each prefix."""
+    B, N, Hq, Hkv, D = cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D
+    lens = (np.asarray(prefix_lens, dtype=np.int32) if prefix_lens is not None
+            else _prefix_lens(cfg, seed))
+    Lmax = int(lens.max()) + N + int(lmax_pad)
+    q = np.empty((B, N, Hq, D), dtype=np.uint16)
+    k = np.empty((B, Hkv, Lmax, D), dtype=np.uint16)
+    v = np.empty((B, Hkv, Lmax, D), dtype=np.uint16)
+    par = np.empty((B, N), dtype=np.int32)
+    for b in range(B):
+        rng = _rng(seed, cfg.cfg_id, b, 2)
+        q[b] = bf16_bits(rng.standard_normal((N, Hq, D), dtype=np.float32))
+        k[b] = bf16_bits(rng.standard_normal((Hkv, Lmax, D), dtype=np.float32))
+        v[b] = bf16_bits(rng.standard_normal((Hkv, Lmax, D), dtype=np.float32))
+        par[b] = _tree(cfg, seed, b)
+    return AttnCase(q, k, v, lens, par, 1.0 / float(np.sqrt(D)), Lmax)
+
+
+# ----------------------------------------------------------------------------------------------
+# verification inputs
+# ----------------------------------------------------------------------------------------------
+@dataclasses.dataclass
+class VerifyCase:
+    target_logits: np.ndarray  # float32 [B, N, V]: row j = target logits after node j's path
+    draft_probs: np.ndarray    # float32 [B, N, V]: row j = draft distribution at node j
+    tree_tokens: np.ndarray    # int32 [B, N]: token of node i (node 0 = last committed token)
+    tree_parent: np.ndarray    # int32 [B, N]
+    uniforms: np.ndarray       # float32 [B, N]: [b, i>=1] test uniform r_i, [b, 0] resample u
+    temperature: float
+
+    @property
+    def shape(self):
+        return self.target_logits.shape
+
+
+def _draft_distribution(draft_logits: np.ndarray, T: float) -> np.ndarray:
+    """The synthetic draft model's output distribution at temperature T (T=0 uses T=1)."""
+    t = T if T > 0 else 1.0
+    z = draft_logits.astype(np.float64) / t
+    z -= z.max(axis=-1, keepdims=True)
+    e = np.exp(z)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def make_verify_case(cfg: Config, T: float, seed: int = 0, sigma_d: Optional[float] = None,
+                     tree_parent: Optional[np.ndarray] = None) -> VerifyCase:
+    """Target logits ~ N(0, sigma_t^2); draft logits = target + N(0, sigma_d^2).
+
+    Draft tokens: for T > 0 each draft node's token is an independent draw from its parent's draft
+    distribution (siblings are i.i.d., with replacement).  For T = 0 the children of a node take the
+    top-k tokens of the parent's draft logits in descending order, so siblings are distinct.
+    Uniforms are k / 2^24 with integer k, exact in float32 and always below 1.
+    """
+    B, N, V = cfg.B, cfg.N, cfg.V
+    sd = cfg.sigma_d if sigma_d is None else float(sigma_d)
+    tl = np.empty((B, N, V), dtype=np.float32)
+    dp = np.empty((B, N, V), dtype=np.float32)
+    tok = np.empty((B, N), dtype=np.int32)
+    par = np.empty((B, N), dtype=np.int32)
+    uni = np.empty((B, N), dtype=np.float32)
+    for b in range(B):
+        rng = _rng(seed, cfg.cfg_id, b, 3)
+        pb = (np.asarray(tree_parent[b], dtype=np.int32) if tree_parent is not None
+              else _tree(cfg, seed, b))
+        par[b] = pb
+        target = rng.standard_normal((N, V), dtype=np.float32) * np.float32(cfg.sigma_t)
+        draft = target + rng.standard_normal((N, V), dtype=np.float32) * np.float32(sd)
+        tl[b] = target
+        p64 = _draft_distribution(draft, T)
+        dp[b] = p64.astype(np.float32)
+        tok[b, 0] = int(rng.integers(V))
+        rank = np.zeros(N, dtype=np.int64)
+        order_cache = {}
+        for i in range(1, N):
+            j = int(pb[i])
+            if T > 0:
+                cdf = np.cumsum(p64[j])
+                x = float(rng.random()) * cdf[-1]
+                tok[b, i] = int(min(np.searchsorted(cdf, x, side="right"), V - 1))
+            else:
+                if j not in order_cache:
+                    order_cache[j] = np.argsort(-draft[j].astype(np.float64), kind="stable")
+                tok[b, i] = int(order_cache[j][rank[j]])
+                rank[j] += 1
+        uni[b] = rng.integers(0, 1 << 24, size=N).astype(np.float32) / np.float32(1 << 24)
+    return VerifyCase(tl, dp, tok, par, uni, float(T))
