@@ -1,0 +1,69 @@
+// Internal interface between the C-ABI host code and the verify / attention kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace spectree {
+
+// Per (sequence, node) record written by the node kernel and read by the walk kernel.
+struct NodeStat {
+  float m;        // max target logit of the row (raw logit units)
+  int argmax;     // lowest index attaining the max
+  double s;       // sum_y exp((l_y - m) / T)
+  int first_acc;  // accepted child, or -1 when every child was rejected
+  int nrej;       // children rejected before first_acc (all of them if none was accepted)
+  int flags;      // SPEC_ST_NONFINITE if the row (or a gathered draft probability) was bad
+  int pad;
+};
+static_assert(sizeof(NodeStat) == 32, "NodeStat layout");
+
+struct VerifyArgs {
+  const float* logits;
+  const float* probs;
+  const int32_t* tokens;
+  const int32_t* parent;
+  const float* uniforms;
+  float T;
+  int B, N, V;
+  int32_t* accept_len;
+  int32_t* acc_tokens;
+  int32_t* bonus;
+  int32_t* acc_nodes;
+  float* child_q;
+  int32_t* status;
+  NodeStat* stats;  // [B, N]
+  double* beta;     // [B, N, kMaxNodes] residual normalisers, by rejection count
+};
+
+size_t verify_workspace_bytes(int B, int N, int V);
+cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s);
+
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* prefix_lens;
+  const int32_t* parent;
+  void* out;
+  float* lse;
+  int B, N, Hq, Hkv, D, Lmax;
+  float scale;
+  int32_t* status;
+  void* workspace;
+  size_t ws_bytes;
+};
+
+struct AttnPlan {
+  int warps;        // compute warps per CTA (16 query rows each)
+  int row_blocks;   // CTAs along the query rows of one KV head
+  int splits;       // split-KV factor
+  int tiles;        // 64-key tiles covering Lmax
+  size_t ws_bytes;  // partial results
+};
+
+bool attn_plan(int B, int N, int Hq, int Hkv, int D, int Lmax, int num_sms, AttnPlan* plan);
+cudaError_t launch_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream_t s);
+
+}  // namespace spectree

@@ -1,0 +1,130 @@
+// C ABI of libspectree: argument checks, launch planning and kernel launches (host code).
+// Declarations and their documentation: include/spectree.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "spectree.h"
+
+using namespace spectree;
+
+namespace {
+
+int sm_count() {
+  static int cache[64] = {0};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_tree_attention_workspace(int B, int N, int Hq, int Hkv, int D, int Lmax) {
+  AttnPlan plan;
+  if (!attn_plan(B, N, Hq, Hkv, D, Lmax, sm_count(), &plan)) return 0;
+  return plan.ws_bytes;
+}
+
+int spec_tree_attention(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* prefix_lens, const int32_t* tree_parent, void* out,
+                        float* out_lse, int B, int N, int Hq, int Hkv, int D, int Lmax,
+                        float softmax_scale, void* workspace, size_t workspace_bytes,
+                        int32_t* status, void* stream) {
+  if (!q || !k_cache || !v_cache || !prefix_lens || !tree_parent || !out) return SPEC_ERR_INVALID_ARG;
+  if (B < 1 || B > 65535 || N < 1 || N > kMaxNodes || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 ||
+      Lmax < N || !std::isfinite(softmax_scale))
+    return SPEC_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
+  if ((long long)B * Hkv * (long long)Lmax >= (1ll << 31)) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return SPEC_ERR_INVALID_ARG;
+  const int sms = sm_count();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  AttnPlan plan;
+  if (!attn_plan(B, N, Hq, Hkv, D, Lmax, sms, &plan)) return SPEC_ERR_INVALID_ARG;
+  if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes || !aligned16(workspace)))
+    return SPEC_ERR_WORKSPACE;
+  AttnArgs a{q, k_cache, v_cache, prefix_lens, tree_parent, out, out_lse, B, N, Hq, Hkv, D,
+             Lmax, softmax_scale, status, workspace, workspace_bytes};
+  cudaError_t e = launch_attention(a, plan, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+size_t spec_tree_verify_workspace(int B, int N, int V) {
+  if (B < 1 || N < 1 || N > kMaxNodes || V < 1) return 0;
+  return verify_workspace_bytes(B, N, V);
+}
+
+int spec_tree_verify(const float* target_logits, const float* draft_probs,
+                     const int32_t* tree_tokens, const int32_t* tree_parent,
+                     const float* uniforms, float temperature, int B, int N, int V,
+                     int32_t* out_accept_len, int32_t* out_accepted_tokens,
+                     int32_t* out_bonus_token, int32_t* out_accepted_nodes, float* out_child_q,
+                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+  if (!target_logits || !tree_tokens || !tree_parent || !uniforms || !out_accept_len ||
+      !out_accepted_tokens || !out_bonus_token)
+    return SPEC_ERR_INVALID_ARG;
+  if (!std::isfinite(temperature) || temperature < 0.f) return SPEC_ERR_INVALID_ARG;
+  if (temperature > 0.f && !draft_probs) return SPEC_ERR_INVALID_ARG;
+  if (B < 1 || B > 65535 || N < 1 || N > kMaxNodes || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (!aligned16(target_logits) || (draft_probs && !aligned16(draft_probs)))
+    return SPEC_ERR_INVALID_ARG;
+  const size_t need = verify_workspace_bytes(B, N, V);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SPEC_ERR_WORKSPACE;
+  const int sms = sm_count();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  VerifyArgs a;
+  a.logits = target_logits;
+  a.probs = draft_probs;
+  a.tokens = tree_tokens;
+  a.parent = tree_parent;
+  a.uniforms = uniforms;
+  a.T = temperature;
+  a.B = B;
+  a.N = N;
+  a.V = V;
+  a.accept_len = out_accept_len;
+  a.acc_tokens = out_accepted_tokens;
+  a.bonus = out_bonus_token;
+  a.acc_nodes = out_accepted_nodes;
+  a.child_q = out_child_q;
+  a.status = status;
+  a.stats = reinterpret_cast<NodeStat*>(ws);
+  a.beta = reinterpret_cast<double*>(ws + (size_t)B * N * sizeof(NodeStat));
+  cudaError_t e = launch_verify(a, sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+const char* spec_status_string(int code) {
+  switch (code) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument (shape, pointer, alignment or temperature)";
+    case SPEC_ERR_UNSUPPORTED: return "shape not supported by the kernels";
+    case SPEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SPEC_ERR_CUDA: return "CUDA runtime or launch failure";
+    case SPEC_ST_BAD_TREE: return "bad tree: parent[0] != -1 or parent[i] not in [0, i)";
+    case SPEC_ST_BAD_LEN: return "bad prefix length: L_b < 0 or L_b + N > Lmax";
+    case SPEC_ST_BAD_TOKEN: return "draft token outside [0, V)";
+    case SPEC_ST_NONFINITE: return "NaN/Inf in a target-logit row or a bad draft probability";
+    case SPEC_ST_TIMEOUT: return "a bounded device-side wait gave up";
+    default: return "unknown status code";
+  }
+}
+
+}  // extern "C"

@@ -220,7 +220,8 @@ def make_verify_case(cfg: Config, T: float, seed: int = 0, sigma_d: Optional[flo
 
     Draft tokens: for T > 0 each draft node's token is an independent draw from its parent's draft
     distribution (siblings are i.i.d., with replacement).  For T = 0 the children of a node take the
-    top-k tokens of the parent's draft logits in descending order, so siblings are distinct.
+    top-k tokens of the parent's draft logits in descending order, so siblings are distinct (when a
+    node has more children than the vocabulary has tokens, the ranking wraps around).
     Uniforms are k / 2^24 with integer k, exact in float32 and always below 1.
     """
     B, N, V = cfg.B, cfg.N, cfg.V
@@ -252,7 +253,7 @@ def make_verify_case(cfg: Config, T: float, seed: int = 0, sigma_d: Optional[flo
             else:
                 if j not in order_cache:
                     order_cache[j] = np.argsort(-draft[j].astype(np.float64), kind="stable")
-                tok[b, i] = int(order_cache[j][rank[j]])
+                tok[b, i] = int(order_cache[j][rank[j] % V])
                 rank[j] += 1
         uni[b] = rng.integers(0, 1 << 24, size=N).astype(np.float32) / np.float32(1 << 24)
     return VerifyCase(tl, dp, tok, par, uni, float(T))
