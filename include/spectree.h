@@ -23,8 +23,10 @@
  *   - Argument errors are reported synchronously, before anything is launched, by a negative
  *     return value (spec_err_t).  A launch failure returns SPEC_ERR_CUDA.
  *   - Content errors found on the device are reported per sequence in `status[b]` (SPEC_ST_* bits;
- *     `status` may be NULL).  Each call overwrites status[b] for every b.  A flagged sequence gets
- *     -1 in its integer outputs and zeros in its attention rows; other sequences are unaffected.
+ *     `status` may be NULL).  Bits are OR-ed into status[b] with atomics and never cleared by the
+ *     library (sticky, like an error flag): zero the array before the first call and whenever the
+ *     caller has handled the errors.  A flagged sequence gets -1 in its integer outputs and zeros
+ *     in its attention rows; other sequences are unaffected.
  *   - No kernel traps, asserts or waits without bound: every device-side wait gives up after a
  *     fixed number of polls and sets SPEC_ST_TIMEOUT.
  *   - Node 0 of every tree is the root (the last committed token, whose key/value is written at
@@ -77,11 +79,11 @@ size_t spec_tree_attention_workspace(int B, int N, int Hq, int Hkv, int D, int L
  *   softmax_scale                       score scale (usually 1/sqrt(D))
  *   workspace   device scratch of at least spec_tree_attention_workspace(...) bytes, 16-byte
  *               aligned; contents need not be initialised and are garbage afterwards
- *   status      int32 [B] or NULL       SPEC_ST_BAD_TREE / SPEC_ST_BAD_LEN / SPEC_ST_TIMEOUT
+ *   status      int32 [B] or NULL       SPEC_ST_BAD_TREE / SPEC_ST_BAD_LEN / SPEC_ST_TIMEOUT (OR-ed)
  *
  * Node i, query head h sees the keys {0..L_b-1} U {L_b + j : j ancestor of i or j == i}, using KV
- * head h / (Hq/Hkv).  Supported: D in {64, 128}, Hq % Hkv == 0, Hq/Hkv <= 16, N*Hq/Hkv rows per
- * KV head, Lmax >= N.  q, k_cache, v_cache and out must be 16-byte aligned.
+ * head h / (Hq/Hkv).  Supported: D in {64, 128}, Hq % Hkv == 0, Lmax >= N, B * Hkv * Lmax < 2^31.
+ * q, k_cache, v_cache, out and workspace must be 16-byte aligned.
  */
 int spec_tree_attention(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* prefix_lens, const int32_t* tree_parent, void* out,
@@ -116,8 +118,9 @@ size_t spec_tree_verify_workspace(int B, int N, int V);
  *                                 (an earlier sibling was accepted) and at the root; at T == 0 it
  *                                 is 1 or 0 (token equals / differs from the parent's argmax)
  *   workspace     at least spec_tree_verify_workspace(B, N, V) bytes, 16-byte aligned
- *   status        int32 [B] or NULL  SPEC_ST_BAD_TREE / SPEC_ST_BAD_TOKEN / SPEC_ST_NONFINITE /
- *                                 SPEC_ST_TIMEOUT
+ *   status        int32 [B] or NULL  SPEC_ST_BAD_TREE / SPEC_ST_BAD_TOKEN / SPEC_ST_NONFINITE
+ *                                 (OR-ed); target_logits, draft_probs and workspace must be 16-byte
+ *                                 aligned; B <= 65535
  *
  * Tree rule (the pages give the chain form only): the children of the current node are tried in
  * ascending index against the current target distribution, which is replaced by its normalised

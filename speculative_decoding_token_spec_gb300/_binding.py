@@ -127,7 +127,7 @@ def spec_tree_attention(q, k_cache, v_cache, prefix_lens, tree_parent, softmax_s
     if out_lse is None and want_lse:
         out_lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
     if status is None:
-        status = torch.empty((B,), dtype=torch.int32, device=dev)
+        status = torch.zeros((B,), dtype=torch.int32, device=dev)  # bits are OR-ed in
     ws_bytes = spec_tree_attention_workspace(B, N, Hq, Hkv, D, Lmax)
     if workspace is None:
         workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
@@ -167,7 +167,7 @@ def spec_tree_verify(target_logits, draft_probs, tree_tokens, tree_parent, unifo
         o.setdefault("accepted_nodes", torch.empty((B, N), **i32))
     if want_child_q:
         o.setdefault("child_q", torch.empty((B, N), dtype=torch.float32, device=dev))
-    o["status"] = status if status is not None else torch.empty((B,), **i32)
+    o["status"] = status if status is not None else torch.zeros((B,), **i32)  # bits are OR-ed in
     ws_bytes = spec_tree_verify_workspace(B, N, V)
     if workspace is None:
         workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
