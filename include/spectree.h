@@ -48,7 +48,8 @@ typedef enum {
   SPEC_ERR_INVALID_ARG = -1, /* bad shape, NULL required pointer, T < 0 or non-finite, ... */
   SPEC_ERR_UNSUPPORTED = -2, /* shape outside what the kernels implement (e.g. D not 64/128)  */
   SPEC_ERR_WORKSPACE = -3,   /* workspace NULL or smaller than the *_workspace() query        */
-  SPEC_ERR_CUDA = -4         /* a CUDA runtime / driver call or a launch failed               */
+  SPEC_ERR_CUDA = -4,        /* a CUDA runtime / driver call or a launch failed               */
+  SPEC_ERR_NOALLOC_LIMIT = -5 /* B * N above SPEC_NOALLOC_MAX_NODES (spec_tree_verify_noalloc)  */
 } spec_err_t;
 
 /* per-sequence status bits (int32 status[B]) */
@@ -133,6 +134,31 @@ int spec_tree_verify(const float* target_logits, const float* draft_probs,
                      int32_t* out_accept_len, int32_t* out_accepted_tokens,
                      int32_t* out_bonus_token, int32_t* out_accepted_nodes, float* out_child_q,
                      void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * Verification without a workspace argument
+ * ------------------------------------------------------------------------------------------------
+ * The pages have no counterpart to this entry point; it exists for callers that cannot allocate
+ * device scratch memory -- for example a serving engine that hands all free GPU memory to its
+ * KV cache at start-up and allows no cudaMalloc afterwards, or a plugin host that gives a kernel
+ * only its input and output buffers.
+ *
+ * Same arguments, outputs and results as spec_tree_verify, minus the workspace.  The scratch lives
+ * in one fixed device array inside the library (SPEC_NOALLOC_MAX_NODES * 544 bytes, about 2.2 MB,
+ * held on every GPU that loads the library until the process exits).  Calls with
+ * B * N > SPEC_NOALLOC_MAX_NODES return SPEC_ERR_NOALLOC_LIMIT.  The first call on a device looks
+ * up the array's device address with that device current; make it before any stream capture.
+ * All calls share the array (it keeps the last call's contents, none of which needs to start at
+ * zero), so calls whose kernels may overlap on the GPU race: serialise them on one stream.
+ * Allocates nothing (no cudaMalloc / cudaFree / allocating library call).
+ */
+#define SPEC_NOALLOC_MAX_NODES 4096
+int spec_tree_verify_noalloc(const float* target_logits, const float* draft_probs,
+                             const int32_t* tree_tokens, const int32_t* tree_parent,
+                             const float* uniforms, float temperature, int B, int N, int V,
+                             int32_t* out_accept_len, int32_t* out_accepted_tokens,
+                             int32_t* out_bonus_token, int32_t* out_accepted_nodes,
+                             float* out_child_q, int32_t* status, void* stream);
 
 /* Human-readable text for a spec_err_t return value or a SPEC_ST_* bit. */
 const char* spec_status_string(int code);

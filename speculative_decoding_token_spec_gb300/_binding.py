@@ -180,3 +180,44 @@ def spec_tree_verify(target_logits, draft_probs, tree_tokens, tree_parent, unifo
     if rc != SPEC_OK:
         raise SpecError("spec_tree_verify", rc)
     return o
+
+
+# ----------------------------------------------------------------------------------------------
+# verification without a workspace argument
+# ----------------------------------------------------------------------------------------------
+_NOALLOC_ARGS = [_vp] * 5 + [_c_float] + [_c_int] * 3 + [_vp] * 5 + [_vp, _vp]
+NOALLOC_MAX_NODES = 4096
+
+
+def spec_tree_verify_noalloc(target_logits, draft_probs, tree_tokens, tree_parent, uniforms,
+                             temperature, outputs=None, status=None, stream=None):
+    """spec_tree_verify for callers that cannot provide device scratch memory.
+
+    The library keeps the scratch in a fixed device array (B * N <= 4096 nodes per call), so
+    this path allocates nothing on the device besides outputs the caller did not pass.  Calls must
+    not overlap on the GPU: they share that array.
+    """
+    torch = _torch()
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    _check(target_logits, "target_logits", torch.float32, (B, N, V), dev)
+    if draft_probs is not None:
+        _check(draft_probs, "draft_probs", torch.float32, (B, N, V), dev)
+    _check(tree_tokens, "tree_tokens", torch.int32, (B, N), dev)
+    _check(tree_parent, "tree_parent", torch.int32, (B, N), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, N), dev)
+    o = dict(outputs or {})
+    i32 = dict(dtype=torch.int32, device=dev)
+    o.setdefault("accept_len", torch.empty((B,), **i32))
+    o.setdefault("accepted_tokens", torch.empty((B, N), **i32))
+    o.setdefault("bonus", torch.empty((B,), **i32))
+    o["status"] = status if status is not None else torch.zeros((B,), **i32)
+    fn = lib().spec_tree_verify_noalloc
+    fn.restype, fn.argtypes = _c_int, _NOALLOC_ARGS
+    rc = fn(_ptr(target_logits), _ptr(draft_probs), _ptr(tree_tokens), _ptr(tree_parent),
+            _ptr(uniforms), float(temperature), B, N, V, _ptr(o["accept_len"]),
+            _ptr(o["accepted_tokens"]), _ptr(o["bonus"]), _ptr(o.get("accepted_nodes")),
+            _ptr(o.get("child_q")), _ptr(o["status"]), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_tree_verify_noalloc", rc)
+    return o

@@ -118,6 +118,8 @@ const char* spec_status_string(int code) {
     case SPEC_ERR_UNSUPPORTED: return "shape not supported by the kernels";
     case SPEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case SPEC_ERR_CUDA: return "CUDA runtime or launch failure";
+    case SPEC_ERR_NOALLOC_LIMIT:
+      return "B * N exceeds SPEC_NOALLOC_MAX_NODES, the fixed scratch of spec_tree_verify_noalloc";
     case SPEC_ST_BAD_TREE: return "bad tree: parent[0] != -1 or parent[i] not in [0, i)";
     case SPEC_ST_BAD_LEN: return "bad prefix length: L_b < 0 or L_b + N > Lmax";
     case SPEC_ST_BAD_TOKEN: return "draft token outside [0, V)";
