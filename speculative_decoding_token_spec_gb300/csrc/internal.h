@@ -14,8 +14,8 @@ struct NodeStat {
   double s;       // sum_y exp((l_y - m) / T)
   int first_acc;  // accepted child, or -1 when every child was rejected
   int nrej;       // children rejected before first_acc (all of them if none was accepted)
-  int flags;      // SPEC_ST_NONFINITE if the row (or a gathered draft probability) was bad
-  int pad;
+  int flags;      // SPEC_ST_NONFINITE / SPEC_ST_TIMEOUT met while processing the node
+  int bonus;      // token drawn if the walk stops at this node (-1: not a possible stop)
 };
 static_assert(sizeof(NodeStat) == 32, "NodeStat layout");
 
@@ -35,9 +35,12 @@ struct VerifyArgs {
   int32_t* status;
   NodeStat* stats;  // [B, N]
   double* beta;     // [B, N, kMaxNodes] residual normalisers, by rejection count
+  unsigned long long* counters;  // [B] arrival counters: (call generation << 16) | arrivals
+  unsigned long long gen;        // this call's generation (48 bits)
 };
 
 size_t verify_workspace_bytes(int B, int N, int V);
+bool verify_supported(int V);  // the row slices of a cluster fit in shared memory
 cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s);
 
 struct AttnArgs {
@@ -56,6 +59,7 @@ struct AttnArgs {
 };
 
 struct AttnPlan {
+  bool tc;          // tcgen05 / TMEM kernel (128-row blocks) instead of the mma.sync one
   int warps;        // compute warps per CTA (16 query rows each)
   int row_blocks;   // CTAs along the query rows of one KV head
   int splits;       // split-KV factor

@@ -4,6 +4,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -82,6 +83,7 @@ int spec_tree_verify(const float* target_logits, const float* draft_probs,
   if (!std::isfinite(temperature) || temperature < 0.f) return SPEC_ERR_INVALID_ARG;
   if (temperature > 0.f && !draft_probs) return SPEC_ERR_INVALID_ARG;
   if (B < 1 || B > 65535 || N < 1 || N > kMaxNodes || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (!verify_supported(V)) return SPEC_ERR_UNSUPPORTED;
   if (!aligned16(target_logits) || (draft_probs && !aligned16(draft_probs)))
     return SPEC_ERR_INVALID_ARG;
   const size_t need = verify_workspace_bytes(B, N, V);
@@ -107,6 +109,10 @@ int spec_tree_verify(const float* target_logits, const float* draft_probs,
   a.status = status;
   a.stats = reinterpret_cast<NodeStat*>(ws);
   a.beta = reinterpret_cast<double*>(ws + (size_t)B * N * sizeof(NodeStat));
+  a.counters = reinterpret_cast<unsigned long long*>(ws + (size_t)B * N * sizeof(NodeStat) +
+                                                     (size_t)B * N * kMaxNodes * sizeof(double));
+  static std::atomic<unsigned long long> call_gen{1};
+  a.gen = call_gen.fetch_add(1) & 0xFFFFFFFFFFFFull;
   cudaError_t e = launch_verify(a, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

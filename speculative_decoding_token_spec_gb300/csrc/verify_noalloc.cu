@@ -7,13 +7,15 @@
 // its workspace in one fixed, file-scope device array instead.
 //
 // Properties of that array:
-//   * Size: room for B * N <= SPEC_NOALLOC_MAX_NODES tree nodes per call (about 2.2 MB).  Every
+//   * Size: room for B * N <= SPEC_NOALLOC_MAX_NODES tree nodes per call (about 2.3 MB).  Every
 //     GPU on which the library is loaded holds it until the process exits.
 //   * Set-up: the first call on a device looks up the array's device address (cudaGetSymbolAddress)
 //     with that device current and caches it; make that first call before any stream capture.
 //   * Sharing: all calls share the one array and it keeps the previous call's contents.  Nothing in
-//     it has to start at zero (each call writes every entry it reads), but calls whose kernels may
-//     overlap on the GPU (different streams, or concurrent host threads) race on it.
+//     it has to start at zero: each call writes every statistics entry it reads, and the
+//     per-sequence arrival counters carry the generation of the call that wrote them, so a count
+//     left by an earlier call is ignored.  Calls whose kernels may overlap on the GPU (different
+//     streams, or concurrent host threads) race on it.
 //   * No allocation: no cudaMalloc, cudaFree or allocating library routine is called.
 #include <cuda_runtime.h>
 
@@ -27,7 +29,9 @@ using namespace spectree;
 
 namespace {
 
-constexpr size_t kPerNode = sizeof(NodeStat) + kMaxNodes * sizeof(double);
+// per node: its statistics record and residual normalisers; per sequence (B <= B * N): one
+// arrival counter
+constexpr size_t kPerNode = sizeof(NodeStat) + kMaxNodes * sizeof(double) + sizeof(unsigned long long);
 constexpr size_t kScratchBytes = (size_t)SPEC_NOALLOC_MAX_NODES * kPerNode;
 
 // The fixed scratch.  In host code `g_verify_scratch` names a host-side stand-in, not device
