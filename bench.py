@@ -290,21 +290,21 @@ def run_ours(args):
 
     bufs = [make_copy() for _ in range(copies)]
 
-    def step(c, ev=None):
-        if ev is not None:
-            ev[0].record()
+    def attn(c):
         st.spec_tree_attention(c["q"], c["k"], c["v"], c["lens"], c["parent"],
                                softmax_scale=ac.scale, out=c["out"], out_lse=c["lse"],
                                workspace=c["ws_a"], status=c["st_a"])
-        if ev is not None:
-            ev[1].record()
+
+    def verify(c):
         st.spec_tree_verify(c["logits"], c["probs"] if T > 0 else None, c["tokens"], c["parent"],
                             c["unif"], T, outputs=c["vout"], workspace=c["ws_v"],
                             status=c["st_v"])
-        if ev is not None:
-            ev[2].record()
 
-    launches_per_step = (2 if ws_attn > 0 else 1) + 2
+    def step(c):
+        attn(c)
+        verify(c)
+
+    launches_per_step = 2  # one tree-attention kernel, one verification kernel
 
     # warm-up (eager), also validates the call path
     for i in range(max(args.warmup, 3)):
@@ -312,94 +312,60 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert int(bufs[0]["st_a"].sum()) == 0 and int(bufs[0]["st_v"].sum()) == 0, "status"
 
-    # CUDA graphs: one step per copy, with per-call events
+    # CUDA graphs: one step per rotated copy, nothing between the kernels (so each launch can
+    # overlap the previous kernel's tail through programmatic dependent launch)
     K = args.steps
-    def timing_event():
-        try:  # recorded as a graph node when captured (not a capture-internal dependency)
-            return torch.cuda.Event(enable_timing=True, external=True)
-        except TypeError:
-            return None
-
-    evs = [[timing_event() for _ in range(3)] for _ in range(copies)]
-    if any(e is None for row in evs for e in row):
-        evs = None
-    g_full = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g_full, stream=s):
-            for i in range(copies):
-                step(bufs[i], evs[i] if evs else None)
-    rem = K % copies
-    g_rem = None
-    if rem:
-        g_rem = torch.cuda.CUDAGraph()
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(s):
-            with torch.cuda.graph(g_rem, stream=s):
-                for i in range(rem):
-                    step(bufs[i])
+            with torch.cuda.graph(g, stream=s):
+                for i in range(n):
+                    fn(bufs[i])
+        return g
+
+    g_full = capture(step, copies)
+    rem = K % copies
+    g_rem = capture(step, rem) if rem else None
+    g_attn, g_ver = capture(attn, copies), capture(verify, copies)
     torch.cuda.current_stream().wait_stream(s)
     for _ in range(2):
         g_full.replay()
     torch.cuda.synchronize()
 
-    def time_calls_separately(reps=20):
-        out = []
-        for which in ("attn", "verify"):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(s):
-                with torch.cuda.graph(g, stream=s):
-                    for c in bufs:
-                        if which == "attn":
-                            st.spec_tree_attention(c["q"], c["k"], c["v"], c["lens"], c["parent"],
-                                                   softmax_scale=ac.scale, out=c["out"],
-                                                   out_lse=c["lse"], workspace=c["ws_a"],
-                                                   status=c["st_a"])
-                        else:
-                            st.spec_tree_verify(c["logits"], c["probs"] if T > 0 else None,
-                                                c["tokens"], c["parent"], c["unif"], T,
-                                                outputs=c["vout"], workspace=c["ws_v"],
-                                                status=c["st_v"])
-            torch.cuda.current_stream().wait_stream(s)
-            g.replay()
-            torch.cuda.synchronize()
-            a0 = torch.cuda.Event(enable_timing=True)
-            a1 = torch.cuda.Event(enable_timing=True)
-            a0.record()
-            for _ in range(reps):
-                g.replay()
-            a1.record()
-            torch.cuda.synchronize()
-            out.append(a0.elapsed_time(a1) / (reps * copies))
-        return out
+    def timed(fn):
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        a0.record()
+        fn()
+        a1.record()
+        torch.cuda.synchronize()
+        barrier()
+        return a0.elapsed_time(a1)
 
-    # ---- timed region
+    # ---- timed region: K steps
     props = torch.cuda.get_device_properties(dev)
     clocks = ClockSampler(getattr(props, "uuid", None) and f"GPU-{props.uuid}" or local)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
     clocks.start()
-    t_start.record()
-    for _ in range(K // copies):
-        g_full.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    t_end.record()
-    torch.cuda.synchronize()
+
+    def run_steps():
+        for _ in range(K // copies):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+
+    total_ms = timed(run_steps)
+    # ---- per-call timed regions: the same rotated copies, one kernel kind per graph
+    reps = max(1, K // copies)
+    attn_ms = timed(lambda: [g_attn.replay() for _ in range(reps)]) / (reps * copies)
+    ver_ms = timed(lambda: [g_ver.replay() for _ in range(reps)]) / (reps * copies)
     clk = clocks.stop()
-    barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    per_call = "events inside the timed graphs (last replay, averaged over the copies)"
-    try:
-        if not evs or K // copies == 0:
-            raise RuntimeError("no in-graph events")
-        attn_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / copies
-        ver_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / copies
-    except Exception:
-        attn_ms, ver_ms = time_calls_separately()
-        per_call = "separate graphs of each call over the same rotated copies"
+    per_call = ("separate timed regions of the same length, each replaying graphs of one call over "
+                "the rotated copies (back-to-back launches of that kernel)")
 
     # max over ranks, sum of units
     units = B * N * K

@@ -62,8 +62,10 @@ typedef enum {
 /* ------------------------------------------------------------------------------------------------
  * Tree attention
  * ------------------------------------------------------------------------------------------------
- * Workspace bytes spec_tree_attention needs for these sizes on the current device (split-KV
- * partial results).  Returns 0 for invalid sizes.
+ * Workspace bytes spec_tree_attention needs for these sizes on the current device.  This
+ * implementation combines its split-KV partial results on chip and returns 0 (as it does for
+ * invalid sizes); callers that pass a buffer of the returned size keep working if a later version
+ * needs scratch.
  */
 size_t spec_tree_attention_workspace(int B, int N, int Hq, int Hkv, int D, int Lmax);
 
@@ -77,14 +79,16 @@ size_t spec_tree_attention_workspace(int B, int N, int Hq, int Hkv, int D, int L
  *   tree_parent int32 [B, N]            parent index of every node (see conventions)
  *   out         bf16 [B, N, Hq, D]      attention output
  *   out_lse     fp32 [B, Hq, N] or NULL natural-log sum-exp of the scaled scores per row
- *   softmax_scale                       score scale (usually 1/sqrt(D))
+ *   softmax_scale                       score scale, finite and > 0 (usually 1/sqrt(D))
  *   workspace   device scratch of at least spec_tree_attention_workspace(...) bytes, 16-byte
- *               aligned; contents need not be initialised and are garbage afterwards
+ *               aligned (NULL when that is 0); contents need not be initialised and are garbage
+ *               afterwards
  *   status      int32 [B] or NULL       SPEC_ST_BAD_TREE / SPEC_ST_BAD_LEN / SPEC_ST_TIMEOUT (OR-ed)
  *
  * Node i, query head h sees the keys {0..L_b-1} U {L_b + j : j ancestor of i or j == i}, using KV
  * head h / (Hq/Hkv).  Supported: D in {64, 128}, Hq % Hkv == 0, Lmax >= N, B * Hkv * Lmax < 2^31.
- * q, k_cache, v_cache, out and workspace must be 16-byte aligned.
+ * q, k_cache, v_cache, out and workspace must be 16-byte aligned.  Cache slots past L_b + N are
+ * never used and may hold any bits (NaN included).
  */
 int spec_tree_attention(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* prefix_lens, const int32_t* tree_parent, void* out,

@@ -129,13 +129,13 @@ def spec_tree_attention(q, k_cache, v_cache, prefix_lens, tree_parent, softmax_s
     if status is None:
         status = torch.zeros((B,), dtype=torch.int32, device=dev)  # bits are OR-ed in
     ws_bytes = spec_tree_attention_workspace(B, N, Hq, Hkv, D, Lmax)
-    if workspace is None:
-        workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
     scale = (1.0 / math.sqrt(D)) if softmax_scale is None else float(softmax_scale)
     rc = lib().spec_tree_attention(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(prefix_lens), _ptr(tree_parent), _ptr(out),
-        _ptr(out_lse), B, N, Hq, Hkv, D, Lmax, scale, _ptr(workspace), workspace.numel(),
-        _ptr(status), _stream(stream))
+        _ptr(out_lse), B, N, Hq, Hkv, D, Lmax, scale, _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _ptr(status), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_tree_attention", rc)
     return out, out_lse, status

@@ -59,12 +59,12 @@ struct AttnArgs {
 };
 
 struct AttnPlan {
-  bool tc;          // tcgen05 / TMEM kernel (128-row blocks) instead of the mma.sync one
-  int warps;        // compute warps per CTA (16 query rows each)
-  int row_blocks;   // CTAs along the query rows of one KV head
-  int splits;       // split-KV factor
-  int tiles;        // 64-key tiles covering Lmax
-  size_t ws_bytes;  // partial results
+  int kg;               // key groups per 128-row MMA block: 2 when the head's R <= 64 rows
+  int row_blocks;       // CTAs along the query rows of one KV head
+  int splits;           // split-KV factor = cluster size (<= 8)
+  int tiles;            // 64-key tiles covering Lmax
+  int tiles_per_split;
+  size_t ws_bytes;      // device scratch needed (0: the splits are combined on chip)
 };
 
 bool attn_plan(int B, int N, int Hq, int Hkv, int D, int Lmax, int num_sms, AttnPlan* plan);

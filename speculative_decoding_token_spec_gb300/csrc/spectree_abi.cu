@@ -48,7 +48,7 @@ int spec_tree_attention(const void* q, const void* k_cache, const void* v_cache,
                         int32_t* status, void* stream) {
   if (!q || !k_cache || !v_cache || !prefix_lens || !tree_parent || !out) return SPEC_ERR_INVALID_ARG;
   if (B < 1 || B > 65535 || N < 1 || N > kMaxNodes || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 ||
-      Lmax < N || !std::isfinite(softmax_scale))
+      Lmax < N || !std::isfinite(softmax_scale) || !(softmax_scale > 0.f))
     return SPEC_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
   if ((long long)B * Hkv * (long long)Lmax >= (1ll << 31)) return SPEC_ERR_UNSUPPORTED;

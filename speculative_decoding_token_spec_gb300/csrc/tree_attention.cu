@@ -5,15 +5,37 @@
 // explainer, taxonomy "Token Tree verification".  Node i of sequence b attends to prefix slots
 // 0..L_b-1 and to the slots L_b + j of its ancestors j (itself included).
 //
-// Decomposition (flash-decode style): one CTA per (sequence, KV head, row block, split).  The
-// CTA's query rows are the tree nodes x the g query heads sharing the KV head (row = i * g + h).
-// K/V tiles of 64 keys stream through a 4-stage TMA ring (128-byte swizzled boxes, one mbarrier per
-// stage, bounded waits).  S = Q K^T and O += P V run on the tensor cores (mma.sync bf16 -> fp32);
-// the online softmax runs in registers in the log2 domain.  Tiles that reach past the prefix are
-// masked with the per-node ancestor bitmask built from the parent array in shared memory.  With
-// more than one split the CTA writes unnormalised partials (O, m, l) and a merge kernel combines
-// them by log-sum-exp weights.
+// Decomposition.  The query rows of one (sequence, KV head) are the tree nodes x the g query heads
+// sharing that KV head (row = i * g + h, R = N * g rows).  One CTA handles a block of 128 MMA rows
+// over one split of the key range; the splits of a (sequence, KV head, row block) form one
+// thread-block cluster and combine their partial results on chip at the end.
+//
+// Key groups.  A tcgen05 MMA always computes 128 rows.  When R <= 64 (multi-head attention over a
+// tree of up to 64 nodes) MMA rows 64..127 repeat query rows 0..63 and are paired with the next
+// 64-key tile: each pipeline step covers two tiles, every TMEM lane quadrant (and so every SM
+// sub-partition) does softmax work, and rows r and r + 64 end with partial results over disjoint
+// key sets that the final combine merges like two more splits.
+//
+// Warp roles (192 threads):
+//   warp 0       TMA producer: K/V tiles of 64 keys into a ring of 192 KB (6 tiles at D = 128),
+//                128-byte swizzled boxes; a split's first tiles are requested right at launch;
+//   warp 1       allocates TMEM; one lane issues the MMAs as soon as their inputs are ready:
+//                  S = Q K_t^T   (M = 128, N = 64 keys, K = D; Q and K from shared memory)
+//                  O += P_t V_t  (M = 128, N = D, K = 64 keys; P from TMEM, V from shared memory)
+//                with completions signalled by tcgen05.commit on mbarriers;
+//   warps 2..5   softmax, one MMA row (= TMEM lane) per thread: mask with the node's visibility
+//                bits (prefix, then the ancestors' tree slots), online softmax in the log2
+//                domain, P as bf16 pairs into TMEM for the PV MMA.  The reference max is only
+//                raised when a tile's max exceeds it by more than 8 (2^8 headroom in fp32); only
+//                then is the O row in TMEM rescaled.
+// Combine.  With key groups, rows r and r + 64 first merge inside the CTA (each thread of the pair
+// takes half of the columns).  Each row's unnormalised O, max m and sum l then go into the
+// shared memory of the cluster CTA that owns the row (row % splits) through distributed-shared-
+// memory stores; the owner weights the S partials by 2^(m - M) / sum(l 2^(m - M)) and writes the
+// bf16 output and the log-sum-exp.
 #include <cuda.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -21,8 +43,7 @@
 namespace spectree {
 
 constexpr int kTileKeys = 64;
-constexpr int kStages = 4;
-constexpr int kBoxBytes = kTileKeys * 128;  // one 64-key x 64-dim bf16 box
+constexpr int kMaxSplits = 8;  // portable cluster size
 
 struct AttnKParams {
   const __nv_bfloat16* q;
@@ -31,37 +52,11 @@ struct AttnKParams {
   const int32_t* prefix_lens;
   const int32_t* parent;
   int32_t* status;
-  float* part_o;   // [B, Hkv, splits, Rpad, D]
-  float2* part_ml; // [B, Hkv, splits, Rpad]  (m in log2 units of scaled scores, l)
-  int B, N, Hq, Hkv, g, R, Rpad, Lmax, D;
-  int splits, tiles_per_split, row_blocks, tiles_total;
+  int B, N, Hq, Hkv, g, R, Lmax;
+  int kg;  // key groups per MMA row block: 2 when R <= 64, else 1
+  int row_blocks, splits, tiles_per_split, tiles_total;
   float scale_log2;  // softmax_scale * log2(e)
 };
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
-      " {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -73,317 +68,6 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D>
-__host__ __device__ constexpr int stage_bytes() {
-  return 2 * (D / 64) * kBoxBytes;
-}
-
-template <int D, int WARPS>
-__host__ __device__ constexpr int attn_smem_bytes() {
-  return 1024 /*align slack*/ + kStages * stage_bytes<D>() + (D / 64) * (16 * WARPS) * 128 + 64;
-}
-
-template <int D, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32) tree_attn_kernel(
-    const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-    const AttnKParams p) {
-  constexpr int ROWS = 16 * WARPS;
-  constexpr int NBOX = D / 64;
-  constexpr int KSTEPS = D / 16;
-  constexpr int DT = D / 8;  // 8-wide output column tiles
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ int par_s[kMaxNodes];
-  __shared__ unsigned long long anc_s[kMaxNodes];
-  __shared__ int bad_s;
-
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  uint8_t* kv_base = base;                                   // kStages x (K boxes, V boxes)
-  uint8_t* q_base = base + kStages * stage_bytes<D>();       // NBOX x ROWS x 128 B
-  uint64_t* bars = reinterpret_cast<uint64_t*>(q_base + NBOX * ROWS * 128);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y / p.row_blocks, rb = blockIdx.y % p.row_blocks;
-  const int b = blockIdx.z;
-  const int N = p.N, g = p.g;
-
-  if (tid == 0) {
-    prefetch_tmap(&tmap_k);
-    prefetch_tmap(&tmap_v);
-  }
-  griddep_wait();  // every global access below may depend on the preceding kernel in the stream
-  griddep_launch_dependents();
-  if (tid < N) par_s[tid] = __ldg(p.parent + (size_t)b * N + tid);
-  const int L = __ldg(p.prefix_lens + b);
-  __syncthreads();
-  if (tid == 0) {
-    int st = build_ancestors(par_s, N, anc_s);
-    if (L < 0 || L + N > p.Lmax) st |= SPEC_ST_BAD_LEN;
-    bad_s = st;
-    if (st && split == 0 && kvh == 0 && rb == 0 && p.status) atomicOr(p.status + b, st);
-    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(bars + s), 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  const bool bad = bad_s != 0;
-
-  // this split's tiles
-  const int total_keys = bad ? 0 : L + N;
-  const int ntiles = (total_keys + kTileKeys - 1) / kTileKeys;
-  const int t_begin = split * p.tiles_per_split;
-  const int t_end = min(ntiles, t_begin + p.tiles_per_split);
-  const int my_tiles = max(0, t_end - t_begin);
-  const int row0 = (b * p.Hkv + kvh) * p.Lmax;  // first cache row of this (sequence, KV head)
-
-  auto issue = [&](int it) {
-    const int s = it % kStages;
-    const uint32_t bar = smem_u32(bars + s);
-    uint8_t* st = kv_base + s * stage_bytes<D>();
-    mbar_arrive_expect_tx(bar, stage_bytes<D>());
-    const int y = row0 + (t_begin + it) * kTileKeys;
-#pragma unroll
-    for (int bx = 0; bx < NBOX; ++bx) {
-      tma_load_2d(smem_u32(st + bx * kBoxBytes), &tmap_k, bar, bx * 64, y);
-      tma_load_2d(smem_u32(st + (NBOX + bx) * kBoxBytes), &tmap_v, bar, bx * 64, y);
-    }
-  };
-  if (tid == 0)
-    for (int it = 0; it < min(kStages, my_tiles); ++it) issue(it);
-
-  // Q rows of this CTA -> swizzled shared memory (zeros beyond R)
-  const int r_cta = rb * ROWS;
-  for (int c = tid; c < ROWS * (D / 8); c += WARPS * 32) {
-    const int row = c / (D / 8), ch = c % (D / 8);
-    const int r = r_cta + row;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < p.R) {
-      const int i = r / g, hl = r % g;
-      const __nv_bfloat16* src = p.q + (((size_t)b * N + i) * p.Hq + kvh * g + hl) * D + ch * 8;
-      v = __ldg(reinterpret_cast<const uint4*>(src));
-    }
-    *reinterpret_cast<uint4*>(q_base + (ch >> 3) * (ROWS * 128) + swz(row, ch & 7)) = v;
-  }
-  __syncthreads();
-
-  // Q fragments of this warp's 16 rows
-  uint32_t qa[KSTEPS][4];
-  {
-    const int m = lane >> 3;
-    const int row = warp * 16 + (m & 1) * 8 + (lane & 7);
-#pragma unroll
-    for (int ks = 0; ks < KSTEPS; ++ks) {
-      const int ch = ks * 2 + (m >> 1);
-      ldsm_x4(smem_u32(q_base + (ch >> 3) * (ROWS * 128) + swz(row, ch & 7)), qa[ks][0],
-              qa[ks][1], qa[ks][2], qa[ks][3]);
-    }
-  }
-
-  // rows handled by this thread: ra (fragment rows g) and ra + 8
-  const int ra = r_cta + warp * 16 + (lane >> 2);
-  const int node_a = min(ra / g, N - 1), node_b = min((ra + 8) / g, N - 1);
-  const unsigned long long anc_a = anc_s[node_a], anc_b = anc_s[node_b];
-
-  float o[DT][4];
-#pragma unroll
-  for (int i = 0; i < DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  bool timed_out = false;
-  int it = 0;
-
-  for (; it < my_tiles; ++it) {
-    const int s = it % kStages;
-    const bool ok = mbar_wait(smem_u32(bars + s), (it / kStages) & 1);
-    const uint8_t* kst = kv_base + s * stage_bytes<D>();
-    const uint8_t* vst = kst + NBOX * kBoxBytes;
-
-    // ---- S = Q K^T  (16 rows x 64 keys per warp)
-    float sc[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-    {
-      const int m = lane >> 3;
-#pragma unroll
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-        const uint8_t* kb = kst + (ks >> 2) * kBoxBytes;
-        const int ch = (ks & 3) * 2 + (m & 1);
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          const int key = np * 16 + (m >> 1) * 8 + (lane & 7);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(smem_u32(kb + swz(key, ch)), b0, b1, b2, b3);
-          mma_bf16(sc[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-          mma_bf16(sc[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-        }
-      }
-    }
-
-    // ---- scale, mask, online softmax
-    const int key0 = (t_begin + it) * kTileKeys;
-    const bool need_mask = key0 + kTileKeys > L;
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = sc[n][e] * p.scale_log2;
-        if (need_mask) {
-          const int col = key0 + n * 8 + 2 * (lane & 3) + (e & 1);
-          const int j = col - L;
-          const unsigned long long anc = (e < 2) ? anc_a : anc_b;
-          const bool vis = j < 0 || (j < N && ((anc >> j) & 1ull));
-          if (!vis) v = -INFINITY;
-        }
-        sc[n][e] = v;
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float mx = -INFINITY;
-#pragma unroll
-      for (int n = 0; n < 8; ++n) mx = fmaxf(mx, fmaxf(sc[n][2 * h], sc[n][2 * h + 1]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run[h], mx);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = exp2f(m_run[h] - m_use);
-      float rs = 0.f;
-#pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const float p0 = exp2f(sc[n][2 * h] - m_use);
-        const float p1 = exp2f(sc[n][2 * h + 1] - m_use);
-        sc[n][2 * h] = p0;
-        sc[n][2 * h + 1] = p1;
-        rs += p0 + p1;
-      }
-      l_run[h] = l_run[h] * alpha + rs;
-#pragma unroll
-      for (int dn = 0; dn < DT; ++dn) {
-        o[dn][2 * h] *= alpha;
-        o[dn][2 * h + 1] *= alpha;
-      }
-      m_run[h] = m_new;
-    }
-
-    // ---- O += P V
-    {
-      const int m = lane >> 3;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t a0 = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-        const uint32_t a1 = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-        const uint32_t a2 = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-        const uint32_t a3 = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-        const int key = kk * 16 + (m & 1) * 8 + (lane & 7);
-#pragma unroll
-        for (int dp = 0; dp < DT / 2; ++dp) {
-          const uint8_t* vb = vst + (dp >> 2) * kBoxBytes;
-          const int ch = (dp & 3) * 2 + (m >> 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(smem_u32(vb + swz(key, ch)), b0, b1, b2, b3);
-          mma_bf16(o[2 * dp], a0, a1, a2, a3, b0, b1);
-          mma_bf16(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
-        }
-      }
-    }
-
-    // ---- release the stage (all warps done with it) and refill it
-    if (__syncthreads_or(ok ? 0 : 1)) {
-      timed_out = true;
-      break;
-    }
-    if (tid == 0 && it + kStages < my_tiles) issue(it + kStages);
-  }
-  if (timed_out) {
-    // let the loads already issued land before the CTA exits (bounded as well)
-    if (tid == 0)
-      for (int j = it + 1; j < min(my_tiles, it + kStages + 1); ++j)
-        mbar_wait(smem_u32(bars + (j % kStages)), (j / kStages) & 1);
-    __syncthreads();
-  }
-
-  // full row sums across the quad
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
-  }
-
-  const int cq = 2 * (lane & 3);
-  if (p.splits == 1) {
-    // final output directly
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = ra + 8 * h;
-      if (r >= p.R) continue;
-      const int i = r / g, hl = r % g, hq = kvh * g + hl;
-      const bool live = !bad && !timed_out && l_run[h] > 0.f;
-      const float inv = live ? 1.f / l_run[h] : 0.f;
-      __nv_bfloat16* dst = p.out + (((size_t)b * N + i) * p.Hq + hq) * D + cq;
-#pragma unroll
-      for (int dn = 0; dn < DT; ++dn) {
-        *reinterpret_cast<__nv_bfloat162*>(dst + dn * 8) =
-            __floats2bfloat162_rn(o[dn][2 * h] * inv, o[dn][2 * h + 1] * inv);
-      }
-      if (p.lse && (lane & 3) == 0)
-        p.lse[((size_t)b * p.Hq + hq) * N + i] =
-            live ? (m_run[h] + log2f(l_run[h])) * 0.69314718055994531f : -INFINITY;
-    }
-    if (timed_out && tid == 0 && p.status) atomicOr(p.status + b, SPEC_ST_TIMEOUT);
-  } else {
-    const size_t slot = ((size_t)(b * p.Hkv + kvh) * p.splits + split) * p.Rpad;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = ra + 8 * h;  // < Rpad always
-      if ((lane & 3) == 0)
-        p.part_ml[slot + r] = make_float2(timed_out ? NAN : m_run[h], timed_out ? 0.f : l_run[h]);
-      if (l_run[h] > 0.f && !timed_out) {
-        float* dst = p.part_o + (slot + r) * D + cq;
-#pragma unroll
-        for (int dn = 0; dn < DT; ++dn)
-          *reinterpret_cast<float2*>(dst + dn * 8) = make_float2(o[dn][2 * h], o[dn][2 * h + 1]);
-      }
-    }
-  }
-}
-
-// ------------------------------------------------------------------------------------------------
-// 5th-generation tensor-core variant (tcgen05 + TMEM), warp-specialised
-// ------------------------------------------------------------------------------------------------
-// One CTA per (sequence, KV head, block of 128 query rows, split); 10 warps:
-//   warp 0       TMA producer: K/V tiles of 64 keys into a 4-stage ring (128-byte swizzle);
-//   warp 1       allocates TMEM; one lane issues the MMAs:
-//                  S_j = Q K_j^T   (M = 128 rows, N = 64 keys, K = D)  into TMEM S[j % 2]
-//                  O  += P_j V_j   (M = 128, N = D, K = 64 keys)        into TMEM O
-//                each completion is signalled through tcgen05.commit on an mbarrier;
-//   warps 2..9   softmax: query row r (= TMEM lane r) is shared by warps w and w + 4 of the same
-//                TMEM lane quadrant, each taking half of the row's 64 scores (and half of the O
-//                columns).  They mask with the node's ancestor bitmask past the prefix, exchange
-//                the row max through shared memory (named barrier per warp pair), and write P_j
-//                (bf16, swizzled, K-major) for the PV MMA.  The reference max is only raised when
-//                a tile's max exceeds it by more than 8 (2^8 headroom); only then is the O row in
-//                TMEM rescaled.  Row sums stay per half until the epilogue.
-// The QK MMA of tile j+1 is issued before the PV of tile j, so the softmax of one tile overlaps
-// the tensor-core work of the next.
-template <int D>
-struct TcCfg {
-  static constexpr int NB = D / 64;               // 64-dim swizzle boxes per row
-  static constexpr int KEYS = 64;                 // keys per tile
-  static constexpr int ST = 4;                    // K/V pipeline stages
-  static constexpr int BOX = KEYS * 128;          // [64 keys x 64 dims] bf16 box: 8 KB
-  static constexpr int STAGE = 2 * NB * BOX;      // K + V
-  static constexpr int QBOX = 128 * 128;          // [128 rows x 64 dims] bf16: 16 KB
-  static constexpr int PBUF = 128 * KEYS * 2;     // [128 rows x 64 keys] bf16: 16 KB
-  static constexpr int OFF_Q = ST * STAGE;
-  static constexpr int OFF_P = OFF_Q + NB * QBOX;
-  static constexpr int OFF_BAR = OFF_P + 2 * PBUF;
-  static constexpr int OFF_RED = OFF_BAR + 256;   // row-max exchange: [2 halves][128 rows] fp32
-  static constexpr int SMEM = 1024 + OFF_RED + 2 * 128 * 4;
-  static constexpr uint32_t TMEM_COLS = 256;      // S[0]: 0..63, S[1]: 64..127, O: 128..128+D
-  static constexpr uint32_t O_COL = 128;
-  static constexpr int THREADS = 320;
-  static constexpr int SOFTMAX_THREADS = 256;
-};
-
 __device__ __forceinline__ float ex2_approx(float x) {  // hardware 2^x (P is rounded to bf16)
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -394,26 +78,44 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// AND of v over the 64 threads of a softmax warp pair (also a barrier for the pair), so both warps
-// of a pair always take the same branch around their shared named barriers.
-__device__ __forceinline__ bool pair_and(int id, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.and.pred po, %2, 64, pi;\n"
-      " selp.u32 %0, 1, 0, po;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id)
-      : "memory");
-  return r != 0;
+template <int D>
+struct TcCfg {
+  static constexpr int NB = D / 64;               // 64-dim swizzle boxes per row
+  static constexpr int KEYS = kTileKeys;          // keys per tile
+  static constexpr int BOX = KEYS * 128;          // [64 keys x 64 dims] bf16 box: 8 KB
+  static constexpr int TILE = 2 * NB * BOX;       // K + V of one tile
+  static constexpr int RING = 192 * 1024;         // K/V ring
+  static constexpr int SLOTS = RING / TILE;       // 6 (D = 128) or 12 (D = 64) tiles
+  static constexpr int QBOX = 128 * 128;          // [128 rows x 64 dims] bf16: 16 KB
+  static constexpr int OFF_Q = RING;
+  static constexpr int OFF_BAR = OFF_Q + NB * QBOX;
+  static constexpr int SMEM = 1024 /*alignment slack*/ + OFF_BAR + 512;
+  // TMEM columns: S[0] 0..127, S[1] 128..255, O 256..256+D, P[buffer][key group] 384 + 64 b + 32 g
+  // (64 bf16 keys packed in 32 columns)
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t S_COLS = 128;
+  static constexpr uint32_t O_COL = 256;
+  static constexpr uint32_t P_COL = 384;
+  static constexpr int THREADS = 192;
+  static constexpr int RSTRIDE = D + 4;           // floats per exchanged row (padding: no bank clash)
+  static constexpr int STAGE_OFF = RING / 2;      // in-CTA key-group exchange, after the combine
+                                                  // receive area
+};
+// One CTA per SM: a second CTA on the SM would block in its 512-column TMEM allocation while the
+// first may be waiting for it at a cluster barrier.  More than half the SM's shared memory each
+// rules that out.
+static_assert(TcCfg<128>::SMEM > 116 * 1024 && TcCfg<64>::SMEM > 116 * 1024, "one CTA per SM");
+
+// Rows of one key group that one CTA of the cluster owns in the final combine.
+__host__ __device__ inline int owned_rows(int kg, int splits) {
+  return (128 / kg + splits - 1) / splits;
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1) tree_attn_tc_kernel(
+__global__ void __launch_bounds__(192, 1) tree_attn_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const AttnKParams p) {
   using C = TcCfg<D>;
-  constexpr int HALF = C::KEYS / 2;  // scores per softmax thread per tile
-  constexpr int DH = D / 2;          // O columns per softmax thread
   extern __shared__ uint8_t smem_raw[];
   __shared__ int par_s[kMaxNodes];
   __shared__ unsigned long long anc_s[kMaxNodes];
@@ -422,26 +124,24 @@ __global__ void __launch_bounds__(320, 1) tree_attn_tc_kernel(
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* kv = base;
+  uint8_t* ring = base;
   uint8_t* q_s = base + C::OFF_Q;
-  uint8_t* p_s = base + C::OFF_P;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::OFF_BAR);
-  float* red = reinterpret_cast<float*>(base + C::OFF_RED);  // [half][row]
-  const int B_FULL = 0, B_EMPTY = C::ST, B_SFULL = 2 * C::ST, B_SFREE = 2 * C::ST + 2,
-            B_PFULL = 2 * C::ST + 4, B_PV = 2 * C::ST + 6, B_DONE = 2 * C::ST + 7;
+  const int B_FULL = 0, B_EMPTY = C::SLOTS, B_SFULL = 2 * C::SLOTS, B_SFREE = 2 * C::SLOTS + 2,
+            B_PFULL = 2 * C::SLOTS + 4, B_PV = 2 * C::SLOTS + 6, B_DONE = 2 * C::SLOTS + 7;
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x;
+  const int split = blockIdx.x;  // == rank in the cluster (cluster dims = (splits, 1, 1))
   const int kvh = blockIdx.y / p.row_blocks, rb = blockIdx.y % p.row_blocks;
   const int b = blockIdx.z;
-  const int N = p.N, g = p.g;
+  const int N = p.N, g = p.g, kg = p.kg, S = p.splits;
 
   // ---- set-up, with the first K/V tiles in flight as early as possible
   const int tps = p.tiles_per_split;
   const int t_begin = split * tps;
   const int row0 = (b * p.Hkv + kvh) * p.Lmax;
-  const int spec = max(0, min(C::ST, min(tps, p.tiles_total - t_begin)));  // issued before L is known
+  const int spec = max(0, min(C::SLOTS, min(tps, p.tiles_total - t_begin)));  // before L is known
   if (tid == 0) {
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
@@ -449,14 +149,14 @@ __global__ void __launch_bounds__(320, 1) tree_attn_tc_kernel(
   griddep_wait();  // every global access below may depend on the preceding kernel in the stream
   griddep_launch_dependents();
   if (tid == 0) {
-    for (int i = 0; i < C::ST; ++i) {
+    for (int i = 0; i < C::SLOTS; ++i) {
       mbar_init(bar(B_FULL + i), 1);
       mbar_init(bar(B_EMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SFREE + i), C::SOFTMAX_THREADS);
-      mbar_init(bar(B_PFULL + i), C::SOFTMAX_THREADS);
+      mbar_init(bar(B_SFREE + i), 4);  // one arrival per softmax warp
+      mbar_init(bar(B_PFULL + i), 4);
     }
     mbar_init(bar(B_PV), 1);
     mbar_init(bar(B_DONE), 1);
@@ -465,8 +165,8 @@ __global__ void __launch_bounds__(320, 1) tree_attn_tc_kernel(
     // the split's first tiles do not depend on the prefix length: issue them now (a tile past
     // L_b + N is simply not consumed)
     for (int it = 0; it < spec; ++it) {
-      mbar_arrive_expect_tx(bar(B_FULL + it), C::STAGE);
-      uint8_t* st = kv + it * C::STAGE;
+      mbar_arrive_expect_tx(bar(B_FULL + it), C::TILE);
+      uint8_t* st = ring + it * C::TILE;
       const int y = row0 + (t_begin + it) * C::KEYS;
 #pragma unroll
       for (int bx = 0; bx < C::NB; ++bx) {
@@ -479,19 +179,20 @@ __global__ void __launch_bounds__(320, 1) tree_attn_tc_kernel(
   if (tid >= 64 && tid < 64 + N) par_s[tid - 64] = __ldg(p.parent + (size_t)b * N + (tid - 64));
   const int L = __ldg(p.prefix_lens + b);
 
-  // softmax threads: row r_loc (TMEM lane), half 0 (warps 2..5) or 1 (warps 6..9)
-  const int half = (warp >= 6) ? 1 : 0;
-  const int r_loc = 32 * (warp & 3) + lane;
-  const int r_glob = rb * 128 + r_loc;
-  if (warp >= 2) {  // Q rows -> swizzled shared memory (zeros beyond R); each half loads half
-    const bool live = r_glob < p.R;
-    const int i = live ? r_glob / g : 0, hl = live ? r_glob % g : 0;
-    const __nv_bfloat16* src = p.q + (((size_t)b * N + i) * p.Hq + kvh * g + hl) * D;
+  // softmax threads: MMA row r (TMEM lane r), key group gi, query row qrow of this KV head
+  const int r = 32 * (warp & 3) + lane;
+  const int gi = (kg == 2) ? (r >> 6) : 0;
+  const int qloc = (kg == 2) ? (r & 63) : r;  // row within this CTA's block of query rows
+  const int qrow = rb * 128 + qloc;
+  const bool live = qrow < p.R;
+  if (warp >= 2) {  // Q row -> swizzled shared memory (zeros for rows past R)
+    const int i = live ? qrow / g : 0, hl = live ? qrow % g : 0;
+    const uint4* src =
+        reinterpret_cast<const uint4*>(p.q + (((size_t)b * N + i) * p.Hq + kvh * g + hl) * D);
 #pragma unroll
-    for (int cc = 0; cc < D / 16; ++cc) {
-      const int ch = half * (D / 16) + cc;
-      const uint4 v = live ? __ldg(reinterpret_cast<const uint4*>(src) + ch) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(q_s + (ch >> 3) * C::QBOX + swz(r_loc, ch & 7)) = v;
+    for (int ch = 0; ch < D / 8; ++ch) {
+      const uint4 v = live ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(q_s + (ch >> 3) * C::QBOX + swz(r, ch & 7)) = v;
     }
     fence_async_smem();  // Q is read by the tensor cores (async proxy)
   }
@@ -524,6 +225,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_tc_kernel(
   const int ntiles = (total_keys + C::KEYS - 1) / C::KEYS;
   const int t_end = min(ntiles, t_begin + tps);
   const int my_tiles = max(0, t_end - t_begin);
+  const int U = (my_tiles + kg - 1) / kg;  // pipeline steps (kg tiles each)
 
   auto wait = [&](int i, uint32_t parity) -> bool {
     if (abort_s) return false;
@@ -532,15 +234,17 @@ __global__ void __launch_bounds__(320, 1) tree_attn_tc_kernel(
     return false;
   };
 
+  float m_used = -INFINITY, l = 0.f;  // softmax threads: running max (log2 units) and sum
+  bool ok_rows = true;                // softmax warps: every step completed (no timeout)
   if (warp == 0) {
     // ---------------- TMA producer
     if (lane == 0) {
       int issued = spec;
       for (int it = spec; it < my_tiles; ++it) {
-        const int s = it % C::ST;
-        if (it >= C::ST && !wait(B_EMPTY + s, ((it / C::ST) - 1) & 1)) break;
-        uint8_t* st = kv + s * C::STAGE;
-        mbar_arrive_expect_tx(bar(B_FULL + s), C::STAGE);
+        const int s = it % C::SLOTS;
+        if (it >= C::SLOTS && !wait(B_EMPTY + s, ((it / C::SLOTS) - 1) & 1)) break;
+        uint8_t* st = ring + s * C::TILE;
+        mbar_arrive_expect_tx(bar(B_FULL + s), C::TILE);
         const int y = row0 + (t_begin + it) * C::KEYS;
 #pragma unroll
         for (int bx = 0; bx < C::NB; ++bx) {
@@ -552,86 +256,127 @@ __global__ void __launch_bounds__(320, 1) tree_attn_tc_kernel(
       // never leave with a copy in flight: speculative tiles nobody consumed, or an abort
       // (bounded waits)
       if (abort_s || my_tiles < spec)
-        for (int it = max(0, issued - C::ST); it < issued; ++it)
-          if (abort_s || it >= my_tiles) mbar_wait(bar(B_FULL + it % C::ST), (it / C::ST) & 1);
+        for (int it = max(0, issued - C::SLOTS); it < issued; ++it)
+          if (abort_s || it >= my_tiles) mbar_wait(bar(B_FULL + it % C::SLOTS), (it / C::SLOTS) & 1);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer: QK of step u once its tiles landed and S[u % 2] is free (and
+    // the PV of step u - 2, which read the P buffer step u will rewrite, was issued before it);
+    // PV of step u once its P is written.  Whichever is ready goes first.
     if (lane == 0 && my_tiles > 0) {
       constexpr uint32_t IQK = idesc_bf16_f32(128, C::KEYS, false);
       constexpr uint32_t IPV = idesc_bf16_f32(128, D, true);
       const uint32_t q_addr = smem_u32(q_s);
-      auto issue_qk = [&](int j) -> bool {
-        const int s = j % C::ST;
-        if (!wait(B_FULL + s, (j / C::ST) & 1)) return false;
-        if (j >= 2 && !wait(B_SFREE + (j & 1), ((j >> 1) - 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(kv + s * C::STAGE);
+      int nq = 0, np = 0;
+      uint32_t idle = 0;
+      while (np < U) {
+        bool progressed = false;
+        if (nq < U && nq <= np + 1) {
+          const int t0 = nq * kg, nt = min(kg, my_tiles - t0);
+          bool rdy = nq < 2 || mbar_test(bar(B_SFREE + (nq & 1)), ((nq >> 1) - 1) & 1);
+          for (int k = 0; k < nt && rdy; ++k)
+            rdy = mbar_test(bar(B_FULL + (t0 + k) % C::SLOTS), ((t0 + k) / C::SLOTS) & 1);
+          if (rdy) {
+            tc_fence_after();
+            for (int k = 0; k < nt; ++k) {
+              const uint32_t k_addr = smem_u32(ring + ((t0 + k) % C::SLOTS) * C::TILE);
+              const uint32_t d = tmem + (uint32_t)((nq & 1) * C::S_COLS + k * C::KEYS);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t ad = smem_desc_sw128(q_addr + (ks >> 2) * C::QBOX + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(k_addr + (ks >> 2) * C::BOX + (ks & 3) * 32, 16, 1024);
-          tc_mma_bf16(tmem + (uint32_t)((j & 1) * C::KEYS), ad, bd, IQK, ks > 0 ? 1u : 0u);
+              for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t ad =
+                    smem_desc_sw128(q_addr + (ks >> 2) * C::QBOX + (ks & 3) * 32, 16, 1024);
+                const uint64_t bd =
+                    smem_desc_sw128(k_addr + (ks >> 2) * C::BOX + (ks & 3) * 32, 16, 1024);
+                tc_mma_bf16(d, ad, bd, IQK, ks > 0 ? 1u : 0u);
+              }
+            }
+            tc_commit(bar(B_SFULL + (nq & 1)));
+            ++nq;
+            progressed = true;
+          }
         }
-        tc_commit(bar(B_SFULL + (j & 1)));
-        return true;
-      };
-      bool ok = issue_qk(0);
-      for (int j = 0; ok && j < my_tiles; ++j) {
-        if (j + 1 < my_tiles && !issue_qk(j + 1)) break;
-        if (!wait(B_PFULL + (j & 1), (j >> 1) & 1)) break;
-        tc_fence_after();
-        const int s = j % C::ST;
-        const uint32_t v_addr = smem_u32(kv + s * C::STAGE + C::NB * C::BOX);
-        const uint32_t p_addr = smem_u32(p_s + (j & 1) * C::PBUF);
+        if (np < nq && mbar_test(bar(B_PFULL + (np & 1)), (np >> 1) & 1)) {
+          tc_fence_after();
+          const int t0 = np * kg, nt = min(kg, my_tiles - t0);
+          const uint32_t p_tm = tmem + C::P_COL + (uint32_t)((np & 1) * 64);
+          for (int k = 0; k < nt; ++k) {
+            const int s = (t0 + k) % C::SLOTS;
+            const uint32_t v_addr = smem_u32(ring + s * C::TILE + C::NB * C::BOX);
 #pragma unroll
-        for (int kk = 0; kk < C::KEYS / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(p_addr + kk * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(v_addr + kk * 2048, C::BOX, 1024);
-          tc_mma_bf16(tmem + C::O_COL, ad, bd, IPV, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < C::KEYS / 16; ++kk) {
+              const uint64_t bd = smem_desc_sw128(v_addr + kk * 2048, C::BOX, 1024);
+              tc_mma_bf16_ts(tmem + C::O_COL, p_tm + (uint32_t)(k * 32 + kk * 8), bd, IPV,
+                             (np > 0 || k > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(bar(B_EMPTY + s));  // the tile's slot is free once these MMAs complete
+          }
+          tc_commit(bar(B_PV));
+          ++np;
+          progressed = true;
         }
-        tc_commit(bar(B_PV));
-        tc_commit(bar(B_EMPTY + s));
+        if (progressed) {
+          idle = 0;
+        } else if (++idle > kSpinLimit || abort_s) {
+          abort_s = 1;
+          break;
+        } else {
+          __nanosleep(20);  // leave the issue slots to the softmax warp of this sub-partition
+        }
       }
       tc_commit(bar(B_DONE));  // every MMA issued above has completed once this phase completes
       mbar_wait(bar(B_DONE), 0);
     }
   } else {
-    // ---------------- softmax: half a query row per thread
-    const int node = min(r_glob / g, N - 1);
+    // ---------------- softmax: one MMA row per thread
+    const int node = min(qrow / g, N - 1);
     const unsigned long long anc = anc_s[node];
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    const int pair_bar = 1 + (warp & 3);  // named barrier shared by warps w and w + 4
     const float sc = p.scale_log2;
-    float m_used = -INFINITY, l = 0.f;
-    for (int j = 0; j < my_tiles; ++j) {
-      if (!pair_and(pair_bar, wait(B_SFULL + (j & 1), (j >> 1) & 1))) break;
+    const int tg = (kg == 2) ? (r & 63) : r;  // thread index within the key group
+    const int gthreads = 128 / kg;
+    if (kg == 2) {  // the other key group's P columns of this row stay zero in both buffers
+      float z[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) z[c] = 0.f;
+      tmem_st32(lane_base + C::P_COL + (uint32_t)((1 - gi) * 32), z);
+      tmem_st32(lane_base + C::P_COL + (uint32_t)(64 + (1 - gi) * 32), z);
+      tmem_wait_st();
+    }
+    for (int u = 0; u < U; ++u) {
+      const int t = u * kg + gi;  // this row's tile (>= my_tiles: past the split, all masked)
+      if (!__all_sync(0xffffffffu, wait(B_SFULL + (u & 1), (u >> 1) & 1))) {
+        ok_rows = false;
+        break;
+      }
       tc_fence_after();
-      float x[HALF];
-      tmem_ld32(lane_base + (uint32_t)((j & 1) * C::KEYS + half * HALF), x);
+      float xa[32], xb[32];
+      const uint32_t scol = (uint32_t)((u & 1) * C::S_COLS + gi * C::KEYS);
+      tmem_ld32(lane_base + scol, xa);
+      tmem_ld32(lane_base + scol + 32, xb);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar(B_SFREE + (j & 1)));  // S[j % 2] may be overwritten by QK of tile j + 2
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SFREE + (u & 1)));  // S[u % 2] may be overwritten
 
-      const int key0 = (t_begin + j) * C::KEYS + half * HALF;
-      float mx = -INFINITY;
-      if (key0 + HALF > L) {  // keys past the prefix: ancestor mask
-#pragma unroll
-        for (int c = 0; c < HALF; ++c) {
-          const int jj = key0 + c - L;
-          const bool vis = jj < 0 || (jj < N && ((anc >> jj) & 1ull));
-          x[c] = vis ? x[c] : -INFINITY;
-          mx = fmaxf(mx, x[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < HALF; ++c) mx = fmaxf(mx, x[c]);
+      // visibility of the tile's 64 keys (bit c: key key0 + c): the prefix part, then the
+      // tree slots L + j of the node's ancestors j.  One code path for every tile.
+      const int key0 = (t_begin + t) * C::KEYS;
+      unsigned long long vis = 0;
+      if (t < my_tiles) {
+        const int pre = L - key0;
+        vis = pre >= 64 ? ~0ull : (pre <= 0 ? 0ull : (1ull << pre) - 1ull);
+        const int j0 = key0 - L;
+        if (j0 > -64 && j0 < N) vis |= j0 >= 0 ? (anc >> j0) : (anc << -j0);
       }
-      // row max over both halves (scaled, log2 units)
-      red[half * 128 + r_loc] = mx;
-      named_bar_sync(pair_bar, 64);
-      const float mt = fmaxf(mx, red[(half ^ 1) * 128 + r_loc]) * sc;
-      named_bar_sync(pair_bar, 64);  // the exchange slot is reused next tile
+      const uint32_t vlo = (uint32_t)vis, vhi = (uint32_t)(vis >> 32);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        xa[c] = ((vlo >> c) & 1u) ? xa[c] : -INFINITY;
+        xb[c] = ((vhi >> c) & 1u) ? xb[c] : -INFINITY;
+        mx = fmaxf(mx, fmaxf(xa[c], xb[c]));
+      }
+      const float mt = mx * sc;  // scale > 0
       const bool raise = mt > m_used + 8.f;
       float factor = 1.f;
       if (raise) {
@@ -640,99 +385,174 @@ __global__ void __launch_bounds__(320, 1) tree_attn_tc_kernel(
       }
       const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
       float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pk[HALF / 2];
+      float pk[32];  // P as bf16 pairs (bit patterns), key 2c in the low half of column c
 #pragma unroll
-      for (int c = 0; c < HALF / 2; ++c) {
-        const float p0 = ex2_approx(fmaf(x[2 * c], sc, neg_m));
-        const float p1 = ex2_approx(fmaf(x[2 * c + 1], sc, neg_m));
-        rs0 += p0;
-        rs1 += p1;
-        pk[c] = pack_bf16(p0, p1);
+      for (int c = 0; c < 16; ++c) {
+        const float a0 = ex2_approx(fmaf(xa[2 * c], sc, neg_m));
+        const float a1 = ex2_approx(fmaf(xa[2 * c + 1], sc, neg_m));
+        const float b0 = ex2_approx(fmaf(xb[2 * c], sc, neg_m));
+        const float b1 = ex2_approx(fmaf(xb[2 * c + 1], sc, neg_m));
+        rs0 += a0 + a1;
+        rs1 += b0 + b1;
+        pk[c] = __uint_as_float(pack_bf16(a0, a1));
+        pk[16 + c] = __uint_as_float(pack_bf16(b0, b1));
       }
       l = l * factor + (rs0 + rs1);
-      uint8_t* prow = p_s + (j & 1) * C::PBUF;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        *reinterpret_cast<uint4*>(prow + swz(r_loc, half * 4 + cc)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      fence_async_smem();
-      // O rescale (only after the first tile, only if some row of this warp raised its max)
-      if (j > 0 && __any_sync(0xffffffffu, raise)) {
-        if (__all_sync(0xffffffffu, wait(B_PV, (j - 1) & 1))) {
+      tmem_st32(lane_base + C::P_COL + (uint32_t)((u & 1) * 64 + gi * 32), pk);
+      // The tile holding the last key L + N - 1: V rows past it hold whatever the cache holds
+      // there (possibly NaN); their P is 0, but 0 * NaN is not, so zero those rows.
+      if (t < my_tiles && key0 + C::KEYS > total_keys) {
+        const int s = t % C::SLOTS;
+        if (__all_sync(0xffffffffu, wait(B_FULL + s, (t / C::SLOTS) & 1))) {
+          const int nv = total_keys - key0;  // 1..63 valid keys
+          const int units = C::NB * (C::KEYS - nv) * 8;
+          for (int w = tg; w < units; w += gthreads) {
+            const int bx = w / ((C::KEYS - nv) * 8), rem = w % ((C::KEYS - nv) * 8);
+            *reinterpret_cast<uint4*>(ring + s * C::TILE + (C::NB + bx) * C::BOX +
+                                      (nv + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem();  // the zeros are read by the tensor cores (async proxy)
+        }
+      }
+      // O rescale (only after the first step, only if some row of this warp raised its max)
+      if (u > 0 && __any_sync(0xffffffffu, raise)) {
+        if (__all_sync(0xffffffffu, wait(B_PV, (u - 1) & 1))) {
           tc_fence_after();
-#pragma unroll
-          for (int c0 = 0; c0 < DH; c0 += 32) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
             float o[32];
-            tmem_ld32(lane_base + C::O_COL + half * DH + c0, o);
+            tmem_ld32(lane_base + C::O_COL + c0, o);
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] *= factor;
-            tmem_st32(lane_base + C::O_COL + half * DH + c0, o);
+            tmem_st32(lane_base + C::O_COL + c0, o);
           }
-          tmem_wait_st();
         }
       }
+      tmem_wait_st();  // P (and a rescaled O) are in TMEM before the PV MMA reads them
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL + (j & 1)));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL + (u & 1)));
     }
+    if (ok_rows && U > 0) ok_rows = __all_sync(0xffffffffu, wait(B_PV, (U - 1) & 1));
+    if (ok_rows && U > 0) tc_fence_after();
+  }
 
-    // ---------------- epilogue: row sum over both halves, then this thread's half of the row
-    red[half * 128 + r_loc] = l;
-    named_bar_sync(pair_bar, 64);
-    const float lrow = l + red[(half ^ 1) * 128 + r_loc];
-    const bool ok = __all_sync(0xffffffffu, my_tiles > 0 && wait(B_PV, (my_tiles - 1) & 1));
-    if (ok) tc_fence_after();
-    const bool live_row = r_glob < p.R;
-    const int i = r_glob / g, hq = kvh * g + r_glob % g;
-    if (p.splits == 1) {
-      const bool live = ok && !bad && lrow > 0.f;
-      const float inv = live ? 1.f / lrow : 0.f;
-      __nv_bfloat16* dst = p.out + (((size_t)b * N + i) * p.Hq + hq) * D + half * DH;
-#pragma unroll
-      for (int c0 = 0; c0 < DH; c0 += 32) {
+  // ---------------- combine across the cluster (all threads of every CTA take part)
+  // Partial of a row: (m, l, O) with m = NaN after a timeout and l = 0 when it saw no key.
+  const int QO = owned_rows(kg, S);
+  // [S][QO][RSTRIDE] partial rows, then one trash row that rows without data are pushed into (so
+  // the push has no branch), then the (m, l) pairs [S][QO].  The ring is idle now.
+  float* recv_o = reinterpret_cast<float*>(ring);
+  float2* recv_ml = reinterpret_cast<float2*>(recv_o + ((size_t)S * QO + 1) * C::RSTRIDE);
+  // key groups (kg == 2): rows r and r + 64 hold the same query over different keys.  Each of the
+  // two threads combines and pushes half of the columns; the other half of its own O row goes to
+  // the partner through shared memory.
+  float* stage = reinterpret_cast<float*>(ring + C::STAGE_OFF);   // [64][RSTRIDE]
+  float2* stage_ml = reinterpret_cast<float2*>(stage + 64 * C::RSTRIDE);  // [2][64]
+  const bool pushes_o = ok_rows && U > 0;  // warp-uniform: TMEM loads are warp-collective
+  const float m_own = ok_rows ? (l > 0.f ? m_used : -INFINITY) : NAN;
+  const float l_own = (ok_rows && l > 0.f) ? l : 0.f;
+  cluster_arrive_release();  // every CTA of the cluster is done with its ring (TMA copies drained)
+  cluster_wait_acquire();    // and its MMAs
+  if (warp >= 2 && kg == 2) {
+    stage_ml[gi * 64 + qloc] = make_float2(m_own, l_own);
+    if (pushes_o) {
+      const int c_give = (1 - gi) * (D / 2);
+#pragma unroll 1
+      for (int c0 = c_give; c0 < c_give + D / 2; c0 += 32) {
         float o[32];
-        if (ok) {
-          tmem_ld32(lane_base + C::O_COL + half * DH + c0, o);
-          tmem_wait_ld();
-        } else {
+        tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + C::O_COL + c0, o);
+        tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = 0.f;
-        }
-        if (live_row) {
+        for (int c = 0; c < 32; c += 4)
+          *reinterpret_cast<float4*>(stage + qloc * C::RSTRIDE + c0 + c) =
+              make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+      }
+    }
+    named_bar_sync(1, 128);  // the four softmax warps
+  }
+  if (warp >= 2) {
+    // this CTA's partial of the row: both key groups merged (kg == 2) or the row itself
+    const float2 other = kg == 2 ? stage_ml[(1 - gi) * 64 + qloc] : make_float2(-INFINITY, 0.f);
+    const bool timeout = isnan(m_own) || isnan(other.x);
+    const float mc = fmaxf(l_own > 0.f ? m_own : -INFINITY, other.y > 0.f ? other.x : -INFINITY);
+    const float f_own = l_own > 0.f ? ex2_approx(m_own - mc) : 0.f;
+    const float f_oth = other.y > 0.f ? ex2_approx(other.x - mc) : 0.f;
+    const float lc = l_own * f_own + other.y * f_oth;
+    const bool has = !timeout && lc > 0.f;
+    const int owner = qloc % S, ql = qloc / S;
+    if (live && gi == 0)
+      dsmem_store_v2(dsmem_addr(recv_ml + (size_t)split * QO + ql, owner),
+                     __float_as_uint(timeout ? NAN : (has ? mc : -INFINITY)),
+                     __float_as_uint(has ? lc : 0.f));
+    if (pushes_o) {
+      const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
+      const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE, owner);
+      const int c_lo = gi * (D / 2);  // kg == 1: gi == 0 and the whole row
+#pragma unroll 1
+      for (int c0 = c_lo; c0 < c_lo + D / kg; c0 += 32) {
+        float o[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + C::O_COL + c0, o);
+        tmem_wait_ld();
+        const float* st = stage + qloc * C::RSTRIDE + c0;  // not read when f_oth == 0
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            const uint4 w = make_uint4(pack_bf16(o[c] * inv, o[c + 1] * inv),
-                                       pack_bf16(o[c + 2] * inv, o[c + 3] * inv),
-                                       pack_bf16(o[c + 4] * inv, o[c + 5] * inv),
-                                       pack_bf16(o[c + 6] * inv, o[c + 7] * inv));
-            *reinterpret_cast<uint4*>(dst + c0 + c) = w;
-          }
+        for (int c = 0; c < 32; c += 4) {
+          const float4 pv = f_oth != 0.f ? *reinterpret_cast<const float4*>(st + c)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+          dsmem_store_v4(dst + (c0 + c) * 4,
+                         make_uint4(__float_as_uint(fmaf(o[c], f_own, pv.x * f_oth)),
+                                    __float_as_uint(fmaf(o[c + 1], f_own, pv.y * f_oth)),
+                                    __float_as_uint(fmaf(o[c + 2], f_own, pv.z * f_oth)),
+                                    __float_as_uint(fmaf(o[c + 3], f_own, pv.w * f_oth))));
         }
       }
-      if (half == 0 && live_row && p.lse)
+    }
+  }
+  cluster_arrive_release();
+  cluster_wait_acquire();
+  // owner: rows qloc = ql * S + split of this block, 8 output columns per item.  out =
+  // sum_e 2^(m_e - M) O_e / sum_e 2^(m_e - M) l_e over the row's S partials e (one per split).
+  const int E = S;
+  constexpr int C8 = D / 8;
+  for (int it = tid; it < QO * C8; it += C::THREADS) {
+    const int ql = it / C8, c = (it % C8) * 8, ql_loc = ql * S + split;
+    const int q = rb * 128 + ql_loc;
+    if (ql_loc >= 128 / kg || q >= p.R) continue;
+    // one online pass over the partials (selects, no branches in the body)
+    float M = -INFINITY, Ls = 0.f;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    bool timeout = false;
+    for (int e = 0; e < E; ++e) {
+      const float2 ml = recv_ml[(size_t)e * QO + ql];
+      timeout |= isnan(ml.x);
+      const bool has = ml.y > 0.f;  // partials without keys pushed no O row: never read it
+      const float mn = has ? fmaxf(M, ml.x) : M;
+      const float a = (M == mn) ? 1.f : ex2_approx(M - mn);
+      const float w = has ? ex2_approx(ml.x - mn) : 0.f;
+      const float* src = recv_o + ((size_t)e * QO + ql) * C::RSTRIDE + c;
+      const float4 v0 = *reinterpret_cast<const float4*>(src);
+      const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
+      const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] = fmaf(acc[k], a, has ? w * v[k] : 0.f);
+      Ls = fmaf(Ls, a, w * (has ? ml.y : 0.f));
+      M = mn;
+    }
+    const bool row_ok = !timeout && Ls > 0.f;
+    const float inv = row_ok ? __frcp_rn(Ls) : 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] *= inv;
+    const float Lsum = Ls;
+    const int i = q / g, hq = kvh * g + q % g;
+    *reinterpret_cast<uint4*>(p.out + (((size_t)b * N + i) * p.Hq + hq) * D + c) =
+        make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
+                   pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
+    if (c == 0) {
+      if (p.lse)
         p.lse[((size_t)b * p.Hq + hq) * N + i] =
-            live ? (m_used + log2f(lrow)) * 0.69314718055994531f : -INFINITY;
-      if (half == 0 && !ok && my_tiles > 0 && live_row && p.status)
-        atomicOr(p.status + b, SPEC_ST_TIMEOUT);
-    } else {
-      const size_t slot = ((size_t)(b * p.Hkv + kvh) * p.splits + split) * p.Rpad + r_glob;
-      const bool has = ok && lrow > 0.f;
-      if (half == 0) p.part_ml[slot] = make_float2((my_tiles > 0 && !ok) ? NAN : m_used, has ? lrow : 0.f);
-      if (ok) {  // warp-uniform: the TMEM loads are warp-collective
-        float* dst = p.part_o + slot * D + half * DH;
-#pragma unroll
-        for (int c0 = 0; c0 < DH; c0 += 32) {
-          float o[32];
-          tmem_ld32(lane_base + C::O_COL + half * DH + c0, o);
-          tmem_wait_ld();
-          if (has) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              *reinterpret_cast<float4*>(dst + c0 + c) =
-                  make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-          }
-        }
-      }
+            row_ok ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+      if (timeout && p.status) atomicOr(p.status + b, SPEC_ST_TIMEOUT);
     }
   }
   tc_fence_before();
@@ -743,115 +563,9 @@ __global__ void __launch_bounds__(320, 1) tree_attn_tc_kernel(
   }
 }
 
-// Combine the splits of one row: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-// One warp per (sequence, KV head, row).
-template <int D>
-__global__ void __launch_bounds__(256) tree_attn_merge_kernel(const AttnKParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 8 + warp;
-  const int kvh = blockIdx.y, b = blockIdx.z;
-  griddep_wait();
-  griddep_launch_dependents();
-  if (r >= p.R) return;
-  const size_t slot0 = (size_t)(b * p.Hkv + kvh) * p.splits * p.Rpad;
-  float M = -INFINITY;
-  bool timeout = false;
-  for (int s = 0; s < p.splits; ++s) {
-    const float2 ml = p.part_ml[slot0 + (size_t)s * p.Rpad + r];
-    if (isnan(ml.x)) timeout = true;
-    else if (ml.y > 0.f) M = fmaxf(M, ml.x);
-  }
-  constexpr int PER = D / 32;
-  float acc[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-  float Lsum = 0.f;
-  if (M != -INFINITY && !timeout) {
-    for (int s = 0; s < p.splits; ++s) {
-      const size_t idx = slot0 + (size_t)s * p.Rpad + r;
-      const float2 ml = p.part_ml[idx];
-      if (!(ml.y > 0.f)) continue;
-      const float w = exp2f(ml.x - M);
-      Lsum += w * ml.y;
-      const float* src = p.part_o + idx * D + lane * PER;
-      if constexpr (PER == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[2] += w * v.z;
-        acc[3] += w * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-      }
-    }
-  }
-  const bool live = Lsum > 0.f;
-  const float inv = live ? 1.f / Lsum : 0.f;
-  const int i = r / p.g, hq = kvh * p.g + r % p.g;
-  __nv_bfloat16* dst = p.out + (((size_t)b * p.N + i) * p.Hq + hq) * D + lane * PER;
-#pragma unroll
-  for (int k = 0; k < PER; k += 2)
-    *reinterpret_cast<__nv_bfloat162*>(dst + k) =
-        __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
-  if (lane == 0) {
-    if (p.lse)
-      p.lse[((size_t)b * p.Hq + hq) * p.N + i] =
-          live ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
-    if (timeout && p.status) atomicOr(p.status + b, SPEC_ST_TIMEOUT);
-  }
-}
-
 // ------------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------------
-template <int D, int WARPS>
-static int occupancy() {
-  int occ = 0;
-  auto kern = tree_attn_kernel<D, WARPS>;
-  constexpr int smem = attn_smem_bytes<D, WARPS>();
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
-    return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, WARPS * 32, smem) != cudaSuccess)
-    return 1;
-  return occ > 0 ? occ : 1;
-}
-
-bool attn_plan(int B, int N, int Hq, int Hkv, int D, int Lmax, int num_sms, AttnPlan* plan) {
-  if (B < 1 || N < 1 || N > kMaxNodes || Hkv < 1 || Hq < Hkv || Hq % Hkv || Lmax < N) return false;
-  if (D != 64 && D != 128) return false;
-  const int g = Hq / Hkv;
-  const int R = N * g;
-  plan->tc = true;          // tcgen05 / TMEM kernel: blocks of 128 query rows, 1 CTA per SM
-  plan->warps = 8;          // 128 rows per block (the row-block size of the tensor-core kernel)
-  const int rows = 128;
-  plan->row_blocks = (R + rows - 1) / rows;
-  plan->tiles = (Lmax + kTileKeys - 1) / kTileKeys;
-  int occ = 1;
-  const long long slots = (long long)(num_sms > 0 ? num_sms : 148) * occ;
-  const long long base = (long long)B * Hkv * plan->row_blocks;
-  int best = 1;
-  double best_cost = 1e300;
-  for (int s = 1; s <= plan->tiles && s <= 64; ++s) {
-    const int tps = (plan->tiles + s - 1) / s;
-    const long long waves = (base * s + slots - 1) / slots;
-    const double cost = (double)waves * (tps + 2.0);
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = s;
-    }
-  }
-  const int tps = (plan->tiles + best - 1) / best;
-  plan->splits = (plan->tiles + tps - 1) / tps;
-  const long long Rpad = (long long)plan->row_blocks * rows;
-  plan->ws_bytes = plan->splits > 1
-                       ? (size_t)B * Hkv * plan->splits * Rpad * ((size_t)D * 4 + 8) + 256
-                       : 0;
-  return true;
-}
-
 extern "C" typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                                void*, const cuuint64_t*, const cuuint64_t*,
                                                const cuuint32_t*, const cuuint32_t*,
@@ -860,16 +574,15 @@ extern "C" typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType
 
 static PFN_encodeTiled encode_fn() {
   static PFN_encodeTiled fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_encodeTiled>(p);
-  }
+  });
   return fn;
 }
 
@@ -886,53 +599,108 @@ static bool make_kv_map(CUtensorMap* m, const void* ptr, int D, long long rows) 
 }
 
 template <int D>
-static cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const AttnKParams& kp,
-                             const AttnPlan& plan, cudaStream_t s) {
-  auto kern = tree_attn_tc_kernel<D>;
-  constexpr int smem = TcCfg<D>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+static cudaLaunchConfig_t launch_config(int splits, dim3 grid, cudaStream_t s,
+                                        cudaLaunchAttribute (&attr)[2]) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(plan.splits, kp.Hkv * plan.row_blocks, kp.B);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(TcCfg<D>::THREADS);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = TcCfg<D>::SMEM;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, mk, mv, kp);
-  if (e != cudaSuccess || plan.splits == 1) return e;
-  cfg.gridDim = dim3((kp.R + 7) / 8, kp.Hkv, kp.B);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, tree_attn_merge_kernel<D>, kp);
+  cfg.numAttrs = 2;
+  return cfg;
 }
 
-template <int D, int WARPS>
-static cudaError_t launch_d(const CUtensorMap& mk, const CUtensorMap& mv, const AttnKParams& kp,
-                            const AttnPlan& plan, cudaStream_t s) {
-  auto kern = tree_attn_kernel<D, WARPS>;
-  constexpr int smem = attn_smem_bytes<D, WARPS>();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+// Opt the kernel into its shared-memory size on the current device (once per device).
+template <int D>
+static cudaError_t prepare_kernel() {
+  constexpr int kDev = 64;
+  static std::mutex mu;
+  static bool done[kDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(plan.splits, kp.Hkv * plan.row_blocks, kp.B);
-  cfg.blockDim = dim3(WARPS * 32);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, mk, mv, kp);
-  if (e != cudaSuccess || plan.splits == 1) return e;
-  cfg.gridDim = dim3((kp.R + 7) / 8, kp.Hkv, kp.B);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, tree_attn_merge_kernel<D>, kp);
+  if (dev < 0 || dev >= kDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(tree_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TcCfg<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+// Clusters of `splits` CTAs that fit on the device at once (0 if the query fails).
+template <int D>
+static int clusters_per_wave(int splits) {
+  constexpr int kDev = 64;
+  static std::mutex mu;
+  static int cache[kDev][kMaxSplits + 1] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDev) return 0;
+  if (prepare_kernel<D>() != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev][splits] == 0) {
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config<D>(splits, dim3(splits, 1, 1), nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tree_attn_kernel<D>, &cfg) != cudaSuccess || n < 1)
+      return 0;
+    cache[dev][splits] = n;
+  }
+  return cache[dev][splits];
+}
+
+bool attn_plan(int B, int N, int Hq, int Hkv, int D, int Lmax, int num_sms, AttnPlan* plan) {
+  if (B < 1 || N < 1 || N > kMaxNodes || Hkv < 1 || Hq < Hkv || Hq % Hkv || Lmax < N) return false;
+  if (D != 64 && D != 128) return false;
+  const int R = N * (Hq / Hkv);
+  plan->kg = R <= 64 ? 2 : 1;
+  plan->row_blocks = plan->kg == 2 ? 1 : (R + 127) / 128;
+  plan->tiles = (Lmax + kTileKeys - 1) / kTileKeys;
+  const long long units = (long long)B * Hkv * plan->row_blocks;
+  const int sms = num_sms > 0 ? num_sms : 148;
+  // cost = waves x (pipeline steps + fixed set-up / combine cost of about three steps)
+  int best = 1;
+  double best_cost = 1e300;
+  for (int s = 1; s <= kMaxSplits && s <= plan->tiles; ++s) {
+    const int tps = (plan->tiles + s - 1) / s;
+    if ((plan->tiles + tps - 1) / tps != s) continue;  // same split as a smaller s
+    const size_t rows = (size_t)s * owned_rows(plan->kg, s);
+    const size_t recv = (rows + 1) * (size_t)(D + 4) * 4 + rows * 8;  // + the trash row
+    if (recv > (size_t)(D == 128 ? TcCfg<128>::STAGE_OFF : TcCfg<64>::STAGE_OFF)) continue;
+    int per_wave = s == 1 ? sms : (D == 128 ? clusters_per_wave<128>(s) : clusters_per_wave<64>(s));
+    if (per_wave < 1) per_wave = s == 1 ? sms : sms / (2 * s);  // conservative guess
+    if (per_wave < 1) continue;
+    const long long waves = (units + per_wave - 1) / per_wave;
+    const double cost = (double)waves * ((tps + plan->kg - 1) / plan->kg + 3.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  plan->splits = best;
+  plan->tiles_per_split = (plan->tiles + best - 1) / best;
+  plan->ws_bytes = 0;  // the splits are combined on chip
+  return true;
+}
+
+template <int D>
+static cudaError_t launch_d(const CUtensorMap& mk, const CUtensorMap& mv, const AttnKParams& kp,
+                            cudaStream_t s) {
+  cudaError_t e = prepare_kernel<D>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg =
+      launch_config<D>(kp.splits, dim3(kp.splits, kp.Hkv * kp.row_blocks, kp.B), s, attr);
+  return cudaLaunchKernelEx(&cfg, tree_attn_kernel<D>, mk, mv, kp);
 }
 
 cudaError_t launch_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream_t s) {
@@ -953,24 +721,14 @@ cudaError_t launch_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream
   kp.Hkv = a.Hkv;
   kp.g = a.Hq / a.Hkv;
   kp.R = a.N * kp.g;
-  kp.Rpad = plan.row_blocks * (plan.tc ? 128 : 16 * plan.warps);
   kp.Lmax = a.Lmax;
-  kp.D = a.D;
-  kp.splits = plan.splits;
-  kp.tiles_per_split = (plan.tiles + plan.splits - 1) / plan.splits;
-  kp.tiles_total = plan.tiles;
+  kp.kg = plan.kg;
   kp.row_blocks = plan.row_blocks;
+  kp.splits = plan.splits;
+  kp.tiles_per_split = plan.tiles_per_split;
+  kp.tiles_total = plan.tiles;
   kp.scale_log2 = a.scale * 1.4426950408889634f;
-  const size_t o_bytes = (size_t)a.B * a.Hkv * plan.splits * kp.Rpad * a.D * 4;
-  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  kp.part_o = reinterpret_cast<float*>(ws);
-  kp.part_ml = reinterpret_cast<float2*>(ws + ((o_bytes + 255) & ~size_t(255)));
-  if (plan.tc) return a.D == 128 ? launch_tc<128>(mk, mv, kp, plan, s) : launch_tc<64>(mk, mv, kp, plan, s);
-  if (a.D == 128)
-    return plan.warps == 4 ? launch_d<128, 4>(mk, mv, kp, plan, s)
-                           : launch_d<128, 8>(mk, mv, kp, plan, s);
-  return plan.warps == 4 ? launch_d<64, 4>(mk, mv, kp, plan, s)
-                         : launch_d<64, 8>(mk, mv, kp, plan, s);
+  return a.D == 128 ? launch_d<128>(mk, mv, kp, s) : launch_d<64>(mk, mv, kp, s);
 }
 
 }  // namespace spectree

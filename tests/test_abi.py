@@ -96,3 +96,7 @@ def test_argument_errors_are_synchronous(lib):
     rc = lib.spec_tree_attention(*args, fake, null, 1, 5, 8, 8, 128, 4, 0.1, fake, 1 << 20,
                                  null, null)
     assert rc == -1   # Lmax < N
+    for scale in (0.0, -0.1, float("nan")):   # the softmax scale must be positive and finite
+        rc = lib.spec_tree_attention(*args, fake, null, 1, 5, 8, 8, 128, 200, scale, fake,
+                                     1 << 20, null, null)
+        assert rc == -1

@@ -118,6 +118,32 @@ def test_slots_beyond_tree_do_not_leak(dev):
     np.testing.assert_array_equal(a, b)
 
 
+def test_nan_in_unused_cache_slots(dev):
+    # Slots past L_b + N (the rest of the last 64-key tile and beyond) may hold anything a cache
+    # allocator left there, NaN included; none of it may reach the output.
+    cfg = W.config("eagle_vicuna7b", B=2, Hq=4, Hkv=2, N=13, depth=4, width=5)
+    case = W.make_attention_case(cfg, seed=10, prefix_lens=[150, 37], lmax_pad=300)
+    a, la, _ = P.run_attention_gpu(case, dev)
+    nan_bits = np.uint16(0x7FC0)
+    for b, L in enumerate(case.prefix_lens):
+        case.k_cache[b, :, L + cfg.N:] = nan_bits
+        case.v_cache[b, :, L + cfg.N:] = nan_bits
+    got = _check(case, dev)
+    assert np.isfinite(got).all()
+    b_, lb, _ = P.run_attention_gpu(case, dev)
+    np.testing.assert_array_equal(a, b_)
+    np.testing.assert_array_equal(la, lb)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(1, 1), (4, 1)])
+@pytest.mark.parametrize("L", [0, 100, 300, 520, 1000])
+def test_split_counts_single_head(dev, Hq, Hkv, L):
+    # One KV head per launch: the planner spreads the key range over 1..8 split CTAs (one
+    # cluster), with paired key groups (R = 60 <= 64) or one group (R = 240).
+    cfg = W.config("eagle_vicuna7b", B=1, Hq=Hq, Hkv=Hkv, N=60)
+    _check(W.make_attention_case(cfg, seed=L + Hq, prefix_lens=[L]), dev)
+
+
 def test_deterministic_repeat(dev):
     case = W.make_attention_case(W.config("eagle_vicuna7b"), seed=12)
     a, la, _ = P.run_attention_gpu(case, dev)
