@@ -148,7 +148,7 @@ int spec_tree_verify(const float* target_logits, const float* draft_probs,
  * only its input and output buffers.
  *
  * Same arguments, outputs and results as spec_tree_verify, minus the workspace.  The scratch lives
- * in one fixed device array inside the library (SPEC_NOALLOC_MAX_NODES * 552 bytes, about 2.3 MB,
+ * in one fixed device array inside the library (SPEC_NOALLOC_MAX_NODES * 40 bytes, 160 KB,
  * held on every GPU that loads the library until the process exits).  Calls with
  * B * N > SPEC_NOALLOC_MAX_NODES return SPEC_ERR_NOALLOC_LIMIT.  The first call on a device looks
  * up the array's device address with that device current; make it before any stream capture.

@@ -7,7 +7,7 @@
 
 namespace spectree {
 
-// Per (sequence, node) record written by the node kernel and read by the walk kernel.
+// Per (sequence, node) record written by the node's cluster and read by the walk.
 struct NodeStat {
   float m;        // max target logit of the row (raw logit units)
   int argmax;     // lowest index attaining the max
@@ -34,7 +34,6 @@ struct VerifyArgs {
   float* child_q;
   int32_t* status;
   NodeStat* stats;  // [B, N]
-  double* beta;     // [B, N, kMaxNodes] residual normalisers, by rejection count
   unsigned long long* counters;  // [B] arrival counters: (call generation << 16) | arrivals
   unsigned long long gen;        // this call's generation (48 bits)
 };

@@ -108,9 +108,7 @@ int spec_tree_verify(const float* target_logits, const float* draft_probs,
   a.child_q = out_child_q;
   a.status = status;
   a.stats = reinterpret_cast<NodeStat*>(ws);
-  a.beta = reinterpret_cast<double*>(ws + (size_t)B * N * sizeof(NodeStat));
-  a.counters = reinterpret_cast<unsigned long long*>(ws + (size_t)B * N * sizeof(NodeStat) +
-                                                     (size_t)B * N * kMaxNodes * sizeof(double));
+  a.counters = reinterpret_cast<unsigned long long*>(ws + (size_t)B * N * sizeof(NodeStat));
   static std::atomic<unsigned long long> call_gen{1};
   a.gen = call_gen.fetch_add(1) & 0xFFFFFFFFFFFFull;
   cudaError_t e = launch_verify(a, sms, static_cast<cudaStream_t>(stream));

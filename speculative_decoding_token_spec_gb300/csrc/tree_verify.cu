@@ -4,32 +4,37 @@
 // if r < min(1, q_i(x~_i) / p_i(x~_i)); at the first rejection c the next token is drawn from
 // norm(max(0, q_c - p_c)); greedy verification (taxonomy table) accepts a draft equal to the target's
 // argmax.  Tree form: children of the current node are tried in ascending index against the current
-// target distribution, which becomes its normalised residual after every rejection.
+// target distribution, which becomes its normalised residual after every rejection (and stays as it
+// is when that residual sums to zero).
 //
 // One kernel, grid (CL, N, B): a thread-block cluster of CL CTAs per (sequence, node).
-//   * Each CTA of an internal node's cluster copies its slice of the node's target-logit row into
-//     shared memory with bulk async copies (all bytes in flight at once).  At T > 0 the cluster
-//     reduces the row max M, then every logit is replaced by e(y) = exp((l_y - M)/T) in place and
-//     summed; at T = 0 it takes the argmax.  Every warp pushes its partial into every CTA of the
-//     cluster (remote stores) and, after one cluster barrier, each warp combines all partials.
-//   * The children are tested in index order with the division-free test r * p * D < n (q = n / D,
-//     see "Precision"); each rejection builds the next residual in a shared-memory buffer (one
-//     multiply-subtract per element) and reduces its normaliser beta.  A node whose children are all
-//     rejected draws its own bonus token from the last residual, since the walk stops there
-//     whenever it reaches it.  For small problems leaves are processed too (bonus from q_leaf or the
-//     argmax).
-//   * The last cluster of a sequence to finish (a per-sequence arrival counter in the workspace,
-//     reset by that cluster) walks the tree from the root along the accepted children and writes
-//     the outputs; for large problems it also draws the bonus at a leaf terminal.
+//   * Each CTA copies its slice of the node's target-logit row (and, for an internal node at T > 0,
+//     of the draft row) into shared memory with bulk async copies, padded with neutral values so
+//     that every thread owns a run of `ch` consecutive elements (a multiple of 4).  Runs are in
+//     element order across (rank, warp, lane), so per-thread totals give the row's CDF at run
+//     boundaries.
+//   * T > 0, statistics: each thread takes the max m_t of its run, replaces its logits by
+//     e_t(y) = 2^((l_y - m_t) k), k = log2(e) / T, and sums them; warps combine (m, s) pairs, and
+//     one cluster exchange of the warp pairs gives M and S = sum_y exp((l_y - M) / T).  The thread
+//     keeps f_t = 2^((m_t - M) k), so e(y) = e_t(y) f_t.
+//   * Residual rounds in closed form: with w_0 = e, D_0 = S and after rejections 1..k,
+//     w_k(y) = max(0, e(y) - c_k p(y)), c_k = D_0 + ... + D_{k-1}, D_k = sum_y w_k(y), and the
+//     current distribution is w_k / D_k.  A round is one pass (one FMA per element) and one cluster
+//     exchange; a zero D_k freezes the distribution, and nothing after it needs a pass.
+//   * Each child is tested with the division-free r * p(x) * D < n(x), n(x) = w(x) tracked in fp64
+//     from an exactly formed exp argument; see "Precision".
+//   * Bonus draw (inverse CDF, y = min{y : C(y) > u * total}): the warp totals of the current
+//     weights are known from the last exchange, the thread totals from the last pass, so only the
+//     crossing thread's run is scanned (by its warp) -- no extra pass over the row.
+//   * The last cluster of a sequence to finish (a per-sequence arrival counter in the workspace)
+//     walks the tree from the root along the accepted children and writes the outputs; when leaves
+//     were not processed (large problems) it draws the bonus at a leaf terminal itself.
 //
-// Precision.  Element terms are fp32 (expf once per element).  Every sum is a compensated fp32 sum
-// per thread and a double-float (pair of fp32) sum across threads and CTAs: on this part a dependent
-// fp64 operation costs 64 cycles and an fp64 division or exp about 1000, so fp64 stays off the
-// sequential chains.  The accept decisions compare in fp64 without division: with q^(0)(x) =
-// e(x)/S, e(x) = exp((l_x - M)/T), each child keeps a numerator n(x) and the node a common
-// denominator D; after a rejection n <- max(0, n - p(x) D) and D <- D beta, so q^(t)(x) = n/D and
-// r * p(x) < q(x) becomes r * p(x) * D < n.  e(x) is expf of an argument computed exactly as a
-// double-float, times (1 + its low part): relative error within expf's 2 ulp.
+// Precision.  Element weights are fp32 (hardware 2^x on an argument formed as (l - m) * k).  Every
+// sum is a compensated fp32 sum per thread and a double-float (pair of fp32) sum across threads and
+// CTAs (fp64 arithmetic on this part costs 64 cycles per dependent operation, 1 us per division).
+// The accept decisions compare in fp64: n(x) starts as exp((l_x - M)/T) with the argument formed
+// exactly as a double-float, and after a rejection n <- max(0, n - p(x) D), D <- D_k.
 #include <cooperative_groups.h>
 #include <float.h>
 
@@ -46,8 +51,8 @@ constexpr uint32_t kBulkChunk = 32768;  // bytes per bulk copy instruction
 
 // One warp's partial result, published to the whole cluster (32 bytes: two 16-byte stores).
 struct __align__(16) WarpPart {
-  float m;     // max (stats) / value (argmax)
-  int idx;     // argmax index / last positive weight
+  float m;     // max (statistics) / value (argmax)
+  int idx;     // argmax index
   float s_hi;  // sum (double-float)
   float s_lo;
   int flags;
@@ -67,21 +72,20 @@ struct VerifySmem {
   int terminal;
   int flags;
   int is_last;
-  int found[2];
-  float red_f[kVWarps];
+  int found;
   float g_r[kMaxNodes];         // children's test uniforms
-  WarpPart wp[2][8 * kVWarps];  // ping-pong: every warp partial of the cluster, pushed here
-  float inv_beta[kMaxNodes];
-  float g_lx[kMaxNodes];  // gathered target logit / draft probability of each child's token
+  float g_lx[kMaxNodes];        // gathered target logit / draft probability of each child's token
   float g_px[kMaxNodes];
-  double g_n[kMaxNodes];  // numerators n(x~) of the children's current q values
+  double g_n[kMaxNodes];        // numerators n(x~) of the children's current q values
+  WarpPart wp[2][8 * kVWarps];  // ping-pong: every warp partial of the cluster, pushed here
+  DF wtot[8 * kVWarps];         // warp totals of the current sampling weights (e(y) scale)
   NodeStat st[kMaxNodes];
 };
 
-__device__ __forceinline__ bool bad_value(float v) { return !(v <= FLT_MAX); }  // NaN or +Inf
-
-__device__ __forceinline__ float scaled_exp(float l, float M, float invT) {
-  return expf(__fmul_rn(__fsub_rn(l, M), invT));
+__device__ __forceinline__ float ex2f(float x) {  // hardware 2^x
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -89,9 +93,10 @@ __device__ __forceinline__ float scaled_exp(float l, float M, float invT) {
 // ------------------------------------------------------------------------------------------------
 // Elements [lo, hi) of the row belong to this CTA.  [blo, bhi) is the 16-byte aligned part that is
 // bulk-copied; the rest (at most 3 elements at each end of the row) is loaded with plain loads.
-// Element e sits at buf[e - sbase]; sbase keeps the bulk part 16-byte aligned in shared memory.
+// Element y sits at buf[y - sbase]; sbase keeps the bulk part 16-byte aligned in shared memory.
+// Thread t owns buffer positions [t ch, (t + 1) ch); positions outside [lo, hi) - sbase are pads.
 struct Slice {
-  int lo, hi, blo, bhi, sbase;
+  int lo, hi, blo, bhi, sbase, ch;
 };
 
 __device__ __forceinline__ Slice make_slice(const float* row, int V, int rank, int cl) {
@@ -105,19 +110,23 @@ __device__ __forceinline__ Slice make_slice(const float* row, int V, int rank, i
   s.lo = (rank == 0) ? 0 : s.blo;
   s.hi = (rank == cl - 1) ? V : s.bhi;
   s.sbase = (rank == 0 && a0 > 0) ? a0 - 4 : s.lo;
+  const int nbuf = s.hi - s.sbase;
+  s.ch = 4 * ((nbuf + 4 * kVThreads - 1) / (4 * kVThreads));
   return s;
 }
 
-// Floats of shared memory one slice buffer needs for (V, CL).
+// Floats of shared memory one slice buffer needs for (V, CL): the widest slice (with its ragged
+// ends) rounded up to whole runs.
 static inline int slice_capacity(int V, int cl) {
-  const int nvec = V / 4 + 1;
-  return 4 * ((nvec + cl - 1) / cl) + 16;
+  const int nbuf = 4 * ((V / 4 + 1 + cl - 1) / cl) + 8;
+  return kVThreads * 4 * ((nbuf + 4 * kVThreads - 1) / (4 * kVThreads));
 }
 
 // Issue the copies of the slice into buf (thread 0 issues the bulk part; the ragged ends are
-// loaded by the first threads).  Completion: the barrier's phase, then __syncthreads().
+// loaded by the first threads) and fill the pads with `pad`.  Completion: the barrier's phase,
+// then __syncthreads().
 __device__ __forceinline__ void stage_slice(const float* row, const Slice& s, float* buf,
-                                            uint32_t bar) {
+                                            uint32_t bar, float pad) {
   if (threadIdx.x == 0) {
     const uint32_t bytes = uint32_t(s.bhi - s.blo) * 4u;
     mbar_arrive_expect_tx(bar, bytes);
@@ -125,9 +134,13 @@ __device__ __forceinline__ void stage_slice(const float* row, const Slice& s, fl
     for (uint32_t off = 0; off < bytes; off += kBulkChunk)
       bulk_load(dst + off, row + s.blo + off / 4, min(kBulkChunk, bytes - off), bar);
   }
+  const int t = threadIdx.x;
   const int head = s.blo - s.lo, tail = s.hi - s.bhi;
-  if ((int)threadIdx.x < head) buf[s.lo + threadIdx.x - s.sbase] = __ldg(row + s.lo + threadIdx.x);
-  if ((int)threadIdx.x < tail) buf[s.bhi + threadIdx.x - s.sbase] = __ldg(row + s.bhi + threadIdx.x);
+  if (t < head) buf[s.lo + t - s.sbase] = __ldg(row + s.lo + t);
+  if (t < tail) buf[s.bhi + t - s.sbase] = __ldg(row + s.bhi + t);
+  const int pre = s.lo - s.sbase, post0 = s.hi - s.sbase, post1 = kVThreads * s.ch;
+  if (t < pre) buf[t] = pad;
+  for (int i = post0 + t; i < post1; i += kVThreads) buf[i] = pad;
 }
 
 // Wait for a staged slice (phase `parity` of its barrier: 0 for the barrier's first use in this
@@ -142,40 +155,8 @@ __device__ __forceinline__ int wait_slice(uint32_t bar, uint32_t parity = 0) {
   return st;
 }
 
-// Calls f(idx, n) for every element run of the slice (idx = element - sbase): n = 4 over the
-// aligned body (16-byte aligned in shared memory), then n = 1 for the ragged ends.
-template <class F>
-__device__ __forceinline__ void for_slice4(const Slice& s, F&& f) {
-  const int off = s.blo - s.sbase;
-  const int nv = (s.bhi - s.blo) >> 2;
-  for (int i = threadIdx.x; i < nv; i += kVThreads) f(off + 4 * i, 4);
-  const int head = s.blo - s.lo, tail = s.hi - s.bhi;
-  if ((int)threadIdx.x < head) f(s.lo + threadIdx.x - s.sbase, 1);
-  if ((int)threadIdx.x < tail) f(s.bhi + threadIdx.x - s.sbase, 1);
-}
-
-__device__ __forceinline__ void load_run(const float* buf, int idx, int n, float (&v)[4]) {
-  if (n == 4) {
-    const float4 q = *reinterpret_cast<const float4*>(buf + idx);
-    v[0] = q.x;
-    v[1] = q.y;
-    v[2] = q.z;
-    v[3] = q.w;
-  } else {
-    v[0] = buf[idx];
-  }
-}
-
-__device__ __forceinline__ void store_run(float* buf, int idx, int n, const float (&v)[4]) {
-  if (n == 4) {
-    *reinterpret_cast<float4*>(buf + idx) = make_float4(v[0], v[1], v[2], v[3]);
-  } else {
-    buf[idx] = v[0];
-  }
-}
-
 // ------------------------------------------------------------------------------------------------
-// cluster-wide reductions: warp partial -> every warp combines all CL * 8 partials
+// cluster exchanges: warp partial -> every warp of every CTA reads all CL * 8 partials
 // ------------------------------------------------------------------------------------------------
 template <int CL>
 __device__ __forceinline__ void cluster_barrier() {
@@ -205,24 +186,18 @@ __device__ __forceinline__ void publish(VerifySmem& sm, int slot, int rank, cons
   cluster_barrier<CL>();
 }
 
-// Partial e (= rank * 8 + warp) of the cluster, or `fill` past the end (local read).
+// Partials 2 * lane and 2 * lane + 1 (entries past CL * 8 read as `fill`).
 template <int CL>
-__device__ __forceinline__ WarpPart entry(VerifySmem& sm, int slot, int e, const WarpPart& fill) {
-  return (e < CL * kVWarps) ? sm.wp[slot][e] : fill;
-}
-
-template <int CL>
-__device__ DF reduce_sum(VerifySmem& sm, int slot, int& flags) {
+__device__ __forceinline__ void entries(const VerifySmem& sm, int slot, const WarpPart& fill,
+                                        WarpPart& a, WarpPart& b) {
   const int l = threadIdx.x & 31;
-  const WarpPart fill{0.f, 0, 0.f, 0.f, 0, {0, 0, 0}};
-  const WarpPart a = entry<CL>(sm, slot, 2 * l, fill), b = entry<CL>(sm, slot, 2 * l + 1, fill);
-  flags |= __reduce_or_sync(0xffffffffu, a.flags | b.flags);
-  return warp_sum_df(df_add(DF{a.s_hi, a.s_lo}, DF{b.s_hi, b.s_lo}));
+  a = (2 * l < CL * kVWarps) ? sm.wp[slot][2 * l] : fill;
+  b = (2 * l + 1 < CL * kVWarps) ? sm.wp[slot][2 * l + 1] : fill;
 }
 
-// argmax with lowest index on ties; NaN never wins.
+// argmax with lowest index on ties (indices compared unsigned); NaN never wins.
 __device__ __forceinline__ void argmax_merge(float& bv, int& bi, float v, int i) {
-  if (v > bv || (v == bv && i < bi)) {
+  if (v > bv || (v == bv && (unsigned)i < (unsigned)bi)) {
     bv = v;
     bi = i;
   }
@@ -237,11 +212,56 @@ __device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
   }
 }
 
+// ------------------------------------------------------------------------------------------------
+// passes over a thread's run
+// ------------------------------------------------------------------------------------------------
+// A run of n4 = ch / 4 float4s starting at lane-dependent offsets: read in place order, the eight
+// lanes of a quarter-warp would hit the same banks whenever n4 is even.  Each thread visits its
+// float4s rotated by rot(lane) (c -> (c + rot) mod n4), which spreads every quarter-warp over all
+// 32 banks: with d = gcd(n4, 8), lane * n4 mod 8 repeats every 8 / d lanes and rot adds
+// (lane mod 8) * d / 8 to tell the repeats apart.
+struct RunWalk {
+  int n4, rot;
+  __device__ __forceinline__ explicit RunWalk(int ch) {
+    n4 = ch >> 2;
+    const int d = min(n4 & -n4, 8);
+    rot = ((threadIdx.x & 7) * d) >> 3;
+  }
+  __device__ __forceinline__ int at(int c) const {  // c-th visited float4 of the run
+    const int cc = c + rot;
+    return cc >= n4 ? cc - n4 : cc;
+  }
+};
+
+// T = 0: argmax of the row (cluster-wide), NaN / +Inf flagged.
 template <int CL>
-__device__ void reduce_argmax(VerifySmem& sm, int slot, float& gv, int& gi, int& flags) {
-  const int l = threadIdx.x & 31;
-  const WarpPart fill{-INFINITY, 0x7fffffff, 0.f, 0.f, 0, {0, 0, 0}};
-  const WarpPart a = entry<CL>(sm, slot, 2 * l, fill), b = entry<CL>(sm, slot, 2 * l + 1, fill);
+__device__ void cluster_argmax(const Slice& s, const float* lbuf, int lflags, int rank, int& slot,
+                               float& gv, int& gi, int& flags, VerifySmem& sm) {
+  const float4* L4 = reinterpret_cast<const float4*>(lbuf + threadIdx.x * s.ch);
+  const int y0 = threadIdx.x * s.ch + s.sbase;  // element of the run's first position
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  bool bad = false;
+  const RunWalk rw(s.ch);
+  for (int c = 0; c < rw.n4; ++c) {
+    const int q = rw.at(c);
+    const float4 v = L4[q];
+    bad |= !(v.x <= FLT_MAX) | !(v.y <= FLT_MAX) | !(v.z <= FLT_MAX) | !(v.w <= FLT_MAX);
+    argmax_merge(bv, bi, v.x, y0 + 4 * q);  // index tie-break: the visiting order is rotated
+    argmax_merge(bv, bi, v.y, y0 + 4 * q + 1);
+    argmax_merge(bv, bi, v.z, y0 + 4 * q + 2);
+    argmax_merge(bv, bi, v.w, y0 + 4 * q + 3);
+  }
+  if (bi == 0x7fffffff) {  // nothing above -inf: the run's first real element (pads are -inf)
+    const int first = max(y0, s.lo);
+    bi = first < min(y0 + s.ch, s.hi) ? first : 0x7fffffff;
+  }
+  warp_argmax(bv, bi);
+  const int f = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0) | lflags;
+  publish<CL>(sm, slot, rank, WarpPart{bv, bi, 0.f, 0.f, f, {0, 0, 0}});
+  WarpPart a, b;
+  entries<CL>(sm, slot, WarpPart{-INFINITY, 0x7fffffff, 0.f, 0.f, 0, {0, 0, 0}}, a, b);
+  slot ^= 1;
   gv = a.m;
   gi = a.idx;
   argmax_merge(gv, gi, b.m, b.idx);
@@ -249,247 +269,211 @@ __device__ void reduce_argmax(VerifySmem& sm, int slot, float& gv, int& gi, int&
   flags |= __reduce_or_sync(0xffffffffu, a.flags | b.flags);
 }
 
-// ------------------------------------------------------------------------------------------------
-// sweeps over staged slices
-// ------------------------------------------------------------------------------------------------
-// Slice max -> warp partial (the cluster max M is reduced from these first).
-__device__ WarpPart slice_max(const Slice& s, const float* lbuf, int lflags) {
+// Per-thread state of a node at T > 0.
+struct RunState {
+  float f;    // 2^((m_t - M) k): e(y) = e_t(y) f over the thread's run
+  DF tot;     // the thread's total of the current sampling weights (e(y) scale)
+  float cw;   // current weights max(0, e_t(y) - cw p(y)) f; cw = 0: w = e (p not read)
+};
+
+// Warp totals (two per lane) of the current sampling weights -> sm.wtot (warp 0 writes).
+template <int CL>
+__device__ __forceinline__ void store_wtot(VerifySmem& sm, DF wa, DF wb) {
+  if (threadIdx.x < 32) {
+    const int l = threadIdx.x;
+    if (2 * l < CL * kVWarps) sm.wtot[2 * l] = wa;
+    if (2 * l + 1 < CL * kVWarps) sm.wtot[2 * l + 1] = wb;
+  }
+}
+
+// T > 0: e_t(y) replaces the logits; returns M, S (cluster-wide) and the thread's state.  The warp
+// totals of e(y) go to sm.wtot.
+template <int CL>
+__device__ void cluster_stats(const Slice& s, float* lbuf, float k, int lflags, int rank,
+                              int& slot, float& M, DF& S, RunState& rs, int& flags,
+                              VerifySmem& sm) {
+  float4* L4 = reinterpret_cast<float4*>(lbuf + threadIdx.x * s.ch);
+  const RunWalk rw(s.ch);
   float m = -INFINITY;
-  bool bad = false;
-  for_slice4(s, [&](int idx, int n) {
-    float v[4];
-    load_run(lbuf, idx, n, v);
-    for (int k = 0; k < n; ++k) {
-      bad |= bad_value(v[k]);
-      m = fmaxf(m, v[k]);
-    }
-  });
-  m = warp_max_f(m);
-  const int f = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0) | lflags;
-  return WarpPart{m, 0, 0.f, 0.f, f, {0, 0, 0}};
-}
-
-// e(y) = exp((l_y - M) / T) written over the logits, and summed -> warp partial.
-__device__ WarpPart slice_exp_sum(const Slice& s, float* lbuf, float M, float invT) {
+  for (int c = 0; c < rw.n4; ++c) {
+    const float4 v = L4[rw.at(c)];
+    m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+  }
+  const float mm = (m == -INFINITY) ? 0.f : m;  // NaN / +Inf reach S and are flagged there
   CompSum acc;
-  for_slice4(s, [&](int idx, int n) {
-    float v[4];
-    load_run(lbuf, idx, n, v);
-    float sum = 0.f;
-    for (int k = 0; k < n; ++k) {
-      v[k] = (M == -INFINITY) ? 0.f : scaled_exp(v[k], M, invT);
-      sum = __fadd_rn(sum, v[k]);
-    }
-    store_run(lbuf, idx, n, v);
-    acc.add(sum);
-  });
-  const DF S = warp_sum_df(df_from(acc));
-  return WarpPart{M, 0, S.hi, S.lo, 0, {0, 0, 0}};
-}
-
-// Cluster max of the published slice maxima.
-template <int CL>
-__device__ float reduce_max(VerifySmem& sm, int slot, int& flags) {
-  const int l = threadIdx.x & 31;
-  const WarpPart fill{-INFINITY, 0, 0.f, 0.f, 0, {0, 0, 0}};
-  const WarpPart a = entry<CL>(sm, slot, 2 * l, fill), b = entry<CL>(sm, slot, 2 * l + 1, fill);
+  for (int c = 0; c < rw.n4; ++c) {
+    const int q = rw.at(c);
+    float4 v = L4[q];
+    v.x = ex2f(__fmul_rn(__fsub_rn(v.x, mm), k));
+    v.y = ex2f(__fmul_rn(__fsub_rn(v.y, mm), k));
+    v.z = ex2f(__fmul_rn(__fsub_rn(v.z, mm), k));
+    v.w = ex2f(__fmul_rn(__fsub_rn(v.w, mm), k));
+    L4[q] = v;
+    acc.add(__fadd_rn(__fadd_rn(v.x, v.y), __fadd_rn(v.z, v.w)));
+  }
+  const DF st = df_from(acc);
+  const float mw = warp_max_f(m);
+  const float g = (m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(m, mw), k));
+  const DF sw = warp_sum_df(df_scale(st, g));
+  publish<CL>(sm, slot, rank, WarpPart{mw, 0, sw.hi, sw.lo, lflags, {0, 0, 0}});
+  WarpPart a, b;
+  entries<CL>(sm, slot, WarpPart{-INFINITY, 0, 0.f, 0.f, 0, {0, 0, 0}}, a, b);
+  slot ^= 1;
+  M = warp_max_f(fmaxf(a.m, b.m));
+  const float ga = (a.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(a.m, M), k));
+  const float gb = (b.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(b.m, M), k));
+  const DF wa = df_scale(DF{a.s_hi, a.s_lo}, ga), wb = df_scale(DF{b.s_hi, b.s_lo}, gb);
+  S = warp_sum_df(df_add(wa, wb));
   flags |= __reduce_or_sync(0xffffffffu, a.flags | b.flags);
-  return warp_max_f(fmaxf(a.m, b.m));
+  store_wtot<CL>(sm, wa, wb);
+  const float gM = (mw == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(mw, M), k));
+  rs.f = __fmul_rn(g, gM);
+  rs.tot = df_scale(st, rs.f);
+  rs.cw = 0.f;
+  if (!(S.hi > 0.f) || !(S.hi <= FLT_MAX)) flags |= SPEC_ST_NONFINITE;
 }
 
-// Statistics of softmax(l / T) over the cluster's row: M = max, S = sum exp((l - M)/T); e(y)
-// replaces the logits in lbuf.  Two cluster exchanges (max, then sum).
+// Residual round: returns D = sum_y max(0, e(y) - c p(y)) (cluster-wide; c_t = c / f).  check_p:
+// flag bad draft values.  The thread's total of the new weights goes to `tot`, the warp totals
+// (entries 2 * lane, 2 * lane + 1) to wta, wtb.
 template <int CL>
-__device__ void cluster_exp_stats(const Slice& s, float* lbuf, float invT, int lflags, int rank,
-                                  int& slot, float& M, DF& S, int& flags, VerifySmem& sm) {
-  publish<CL>(sm, slot, rank, slice_max(s, lbuf, lflags));
-  M = reduce_max<CL>(sm, slot, flags);
-  slot ^= 1;
-  publish<CL>(sm, slot, rank, slice_exp_sum(s, lbuf, M, invT));
-  S = reduce_sum<CL>(sm, slot, flags);
-  slot ^= 1;
-}
-
-__device__ WarpPart slice_argmax(const Slice& s, const float* lbuf, int lflags) {
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
-  bool bad = false;
-  for_slice4(s, [&](int idx, int n) {
-    float v[4];
-    load_run(lbuf, idx, n, v);
-    for (int k = 0; k < n; ++k) {
-      bad |= bad_value(v[k]);
-      argmax_merge(bv, bi, v[k], idx + k + s.sbase);
-    }
-  });
-  warp_argmax(bv, bi);
-  const int f = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0) | lflags;
-  return WarpPart{bv, bi, 0.f, 0.f, f, {0, 0, 0}};
-}
-
-// q^(t)(y) from scratch: q^(0) = e(y) * c0 (c0 = 1/S), then t residual rounds (rounds whose
-// normaliser was zero keep q).  Used only after a zero normaliser.
-__device__ __forceinline__ float chain_q(float e, float p, float c0, const float* inv_beta, int t) {
-  float q = __fmul_rn(e, c0);
-  for (int i = 0; i < t; ++i)
-    if (inv_beta[i] > 0.f) q = __fmul_rn(fmaxf(__fsub_rn(q, p), 0.f), inv_beta[i]);
-  return q;
-}
-
-struct RoundArgs {
-  float c0;               // 1 / S: q^(0) = e * c0
-  const float* inv_beta;  // [rounds so far]
-  int k;                  // this round (1-based): residual of q^(k-1)
-  bool chain;             // a normaliser was zero: recompute q^(k-1) from e
-};
-
-// Residual round k: rbuf[y] = max(0, q^(k-1)(y) - p(y)) -> warp partial of sum_y rbuf[y].
-// q^(0) = e * c0; q^(k-1) for k > 1 is the previous residual times 1/beta_{k-1}.
-__device__ WarpPart residual_round(const Slice& s, const float* ebuf, const float* pbuf,
-                                   float* rbuf, const RoundArgs& ra, int lflags) {
+__device__ DF cluster_residual(const Slice& s, const float* ebuf, const float* pbuf, float c_t,
+                               float f, bool check_p, int lflags, int rank, int& slot, DF& tot,
+                               DF& wta, DF& wtb, int& flags, VerifySmem& sm) {
+  const float4* E4 = reinterpret_cast<const float4*>(ebuf + threadIdx.x * s.ch);
+  const float4* P4 = reinterpret_cast<const float4*>(pbuf + threadIdx.x * s.ch);
   CompSum acc;
-  bool bad = false;
-  const float invb = (ra.k > 1) ? ra.inv_beta[ra.k - 2] : 0.f;
-  for_slice4(s, [&](int idx, int n) {
-    float p[4], q[4];
-    load_run(pbuf, idx, n, p);
-    if (ra.k == 1 || ra.chain) {
-      load_run(ebuf, idx, n, q);
-    } else {
-      load_run(rbuf, idx, n, q);
+  float pmin = 0.f, psum = 0.f;
+  const RunWalk rw(s.ch);
+  for (int c = 0; c < rw.n4; ++c) {
+    const int q = rw.at(c);
+    const float4 e = E4[q], p = P4[q];
+    const float r0 = fmaxf(fmaf(-c_t, p.x, e.x), 0.f);
+    const float r1 = fmaxf(fmaf(-c_t, p.y, e.y), 0.f);
+    const float r2 = fmaxf(fmaf(-c_t, p.z, e.z), 0.f);
+    const float r3 = fmaxf(fmaf(-c_t, p.w, e.w), 0.f);
+    acc.add(__fadd_rn(__fadd_rn(r0, r1), __fadd_rn(r2, r3)));
+    if (check_p) {
+      pmin = fminf(pmin, fminf(fminf(p.x, p.y), fminf(p.z, p.w)));
+      psum += (p.x + p.y) + (p.z + p.w);
     }
-    float sum = 0.f;
-    for (int k = 0; k < n; ++k) {
-      bad |= !(p[k] >= 0.f && p[k] <= FLT_MAX);
-      float qq;
-      if (ra.chain) {
-        qq = chain_q(q[k], p[k], ra.c0, ra.inv_beta, ra.k - 1);
-      } else {
-        qq = __fmul_rn(q[k], ra.k == 1 ? ra.c0 : invb);
-      }
-      q[k] = fmaxf(__fsub_rn(qq, p[k]), 0.f);
-      sum = __fadd_rn(sum, q[k]);
-    }
-    store_run(rbuf, idx, n, q);
-    acc.add(sum);
-  });
-  const DF S = warp_sum_df(df_from(acc));
-  const int f = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0) | lflags;
-  return WarpPart{0.f, 0, S.hi, S.lo, f, {0, 0, 0}};
+  }
+  const bool bad = check_p && (pmin < 0.f || !(psum <= FLT_MAX));  // NaN, +Inf or negative p
+  tot = df_scale(df_from(acc), f);
+  const DF w = warp_sum_df(tot);
+  const int wf = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0) | lflags;
+  publish<CL>(sm, slot, rank, WarpPart{0.f, 0, w.hi, w.lo, wf, {0, 0, 0}});
+  WarpPart a, b;
+  entries<CL>(sm, slot, WarpPart{0.f, 0, 0.f, 0.f, 0, {0, 0, 0}}, a, b);
+  slot ^= 1;
+  flags |= __reduce_or_sync(0xffffffffu, a.flags | b.flags);
+  wta = DF{a.s_hi, a.s_lo};
+  wtb = DF{b.s_hi, b.s_lo};
+  return warp_sum_df(df_add(wta, wtb));
 }
 
 // ------------------------------------------------------------------------------------------------
-// inverse-CDF draw across the cluster
+// inverse-CDF draw: y = min{y : C(y) > u * total}, else the last y with a positive weight
 // ------------------------------------------------------------------------------------------------
-// Weights of the bonus draw, read from the staged buffers (element index idx = y - sbase).
-struct Weights {
-  enum Kind { kExp, kBuffer, kChain } kind;
-  const float* ebuf;  // e(y)
-  const float* pbuf;
-  const float* rbuf;
-  float c;            // kExp: 1 (weights e(y)); kChain: 1/S
-  const float* inv_beta;
-  int t;
-  __device__ __forceinline__ float operator()(int idx) const {
-    if (kind == kExp) return ebuf[idx];
-    if (kind == kBuffer) return rbuf[idx];
-    return chain_q(ebuf[idx], pbuf[idx], c, inv_beta, t);
+// Over the 32 lanes' values v (DF, in order; incl = their inclusive scan): the first lane whose
+// inclusive prefix exceeds t, with the prefix before it; if none does (or t < 0: "last positive"
+// mode), the last lane with a positive value (-1 if none), and t becomes -1.
+__device__ __forceinline__ int lane_crossing(DF v, DF incl, DF& t, DF& before) {
+  const int lane = threadIdx.x & 31;
+  DF excl{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+  if (lane == 0) excl = DF{0.f, 0.f};
+  const unsigned cross = __ballot_sync(0xffffffffu, t.hi >= 0.f && df_gt(incl, t));
+  if (cross) {
+    const int L = __ffs(cross) - 1;
+    before = DF{__shfl_sync(0xffffffffu, excl.hi, L), __shfl_sync(0xffffffffu, excl.lo, L)};
+    return L;
   }
-};
+  const unsigned pos = __ballot_sync(0xffffffffu, v.hi > 0.f);
+  t = DF{-1.f, 0.f};
+  before = DF{0.f, 0.f};
+  return pos ? 31 - __clz(pos) : -1;
+}
 
-// y = min{y : C(y) > u * S} over the whole row.  Each CTA owns its slice, each thread a contiguous
-// chunk of it, so (rank, warp, lane) order is element order.  Returns the token (the same in every
-// CTA of the cluster), or -1 when the weights sum to zero.  If rounding leaves no crossing, the
-// last positive weight is taken.
+// Weight of buffer position i under the state (cw, f) (e(y) scale).
+__device__ __forceinline__ float weight_at(const float* ebuf, const float* pbuf, int i, float cw,
+                                          float f) {
+  const float e = ebuf[i];
+  const float w = (cw == 0.f) ? e : fmaxf(fmaf(-cw, pbuf[i], e), 0.f);
+  return __fmul_rn(w, f);
+}
+
+// The drawn token, valid in rank 0 (other CTAs: unspecified), or -1 when every weight is zero.
+// Warp totals come from sm.wtot, thread totals and weights from rs.  Ends with a cluster barrier.
 template <int CL>
-__device__ int cluster_sample(const Weights& w, const Slice& s, int rank, float u, int& slot,
-                              int& flags, VerifySmem& sm) {
+__device__ int cluster_draw(const Slice& s, const float* ebuf, const float* pbuf,
+                            const RunState& rs, float u, int rank, VerifySmem& sm) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int chunk = (s.hi - s.lo + kVThreads - 1) / kVThreads;
-  const int c_lo = min(s.lo + (int)threadIdx.x * chunk, s.hi), c_hi = min(c_lo + chunk, s.hi);
-  CompSum acc;
-  int last_nz = -1;
-  bool bad = false;
-  for (int y = c_lo; y < c_hi; ++y) {
-    const float x = w(y - s.sbase);
-    bad |= !(x >= 0.f && x <= FLT_MAX);
-    if (x > 0.f) last_nz = y;
-    acc.add(x);
+  __syncthreads();  // sm.wtot (written by warp 0) is visible
+  const DF a = (2 * lane < CL * kVWarps) ? sm.wtot[2 * lane] : DF{0.f, 0.f};
+  const DF b = (2 * lane + 1 < CL * kVWarps) ? sm.wtot[2 * lane + 1] : DF{0.f, 0.f};
+  // level 1: warp of the cluster, two entries per lane (every CTA takes the same decisions)
+  const DF pair = df_add(a, b);
+  const DF incl = warp_scan_df(pair);
+  const DF tot{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+  DF t = (tot.hi > 0.f) ? df_scale(tot, u) : DF{-1.f, 0.f};
+  DF before;
+  const int L = lane_crossing(pair, incl, t, before);
+  if (L < 0) {  // nothing positive anywhere
+    cluster_barrier<CL>();
+    return -1;
   }
-  const DF lane_incl = warp_scan_df(df_from(acc));
-  const DF wtot{__shfl_sync(0xffffffffu, lane_incl.hi, 31),
-                __shfl_sync(0xffffffffu, lane_incl.lo, 31)};
-  int wlnz = last_nz;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wlnz = max(wlnz, __shfl_xor_sync(0xffffffffu, wlnz, o));
-  const int wf = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0);
-  publish<CL>(sm, slot, rank, WarpPart{0.f, wlnz, wtot.hi, wtot.lo, wf, {0, 0, 0}});
-
-  // every warp: prefix over the CL * 8 warp totals in element order (lane l: entries 2l, 2l + 1)
-  const WarpPart fill{0.f, -1, 0.f, 0.f, 0, {0, 0, 0}};
-  const WarpPart ea = entry<CL>(sm, slot, 2 * lane, fill);
-  const WarpPart eb = entry<CL>(sm, slot, 2 * lane + 1, fill);
-  slot ^= 1;
-  flags |= __reduce_or_sync(0xffffffffu, ea.flags | eb.flags);
-  int g_lnz = max(ea.idx, eb.idx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) g_lnz = max(g_lnz, __shfl_xor_sync(0xffffffffu, g_lnz, o));
-  const DF a{ea.s_hi, ea.s_lo}, b{eb.s_hi, eb.s_lo};
-  const DF pincl = warp_scan_df(df_add(a, b));
-  DF pexcl{__shfl_up_sync(0xffffffffu, pincl.hi, 1), __shfl_up_sync(0xffffffffu, pincl.lo, 1)};
-  if (lane == 0) pexcl = DF{0.f, 0.f};
-  const DF Stot{__shfl_sync(0xffffffffu, pincl.hi, 31), __shfl_sync(0xffffffffu, pincl.lo, 31)};
-  if (!(Stot.hi > 0.f)) return -1;
-  const DF tgt = df_scale(Stot, u);
-  const DF incl_a = df_add(pexcl, a);
-  const bool ca = df_gt(incl_a, tgt);
-  const bool cb = !ca && df_gt(pincl, tgt);
-  const unsigned cross = __ballot_sync(0xffffffffu, ca || cb);
-  if (cross == 0) return g_lnz;  // rounding left no crossing
-  const int L = __ffs(cross) - 1;
-  const bool at_a = __shfl_sync(0xffffffffu, ca, L);
-  const int estar = 2 * L + (at_a ? 0 : 1);
-  const DF pe{__shfl_sync(0xffffffffu, pexcl.hi, L), __shfl_sync(0xffffffffu, pexcl.lo, L)};
-  const DF pa{__shfl_sync(0xffffffffu, incl_a.hi, L), __shfl_sync(0xffffffffu, incl_a.lo, L)};
-  const DF before = at_a ? pe : pa;
-  const int rstar = estar / kVWarps, wstar = estar % kVWarps;
-
-  if (rank == rstar && wid == wstar) {
-    // the crossing warp: find the crossing lane, then rescan that lane's chunk 32 at a time
-    const DF t_loc = df_add(tgt, DF{-before.hi, -before.lo});
-    DF lexcl{__shfl_up_sync(0xffffffffu, lane_incl.hi, 1),
-             __shfl_up_sync(0xffffffffu, lane_incl.lo, 1)};
-    if (lane == 0) lexcl = DF{0.f, 0.f};
-    const unsigned lb = __ballot_sync(0xffffffffu, df_gt(lane_incl, t_loc));
-    int y = wlnz;
-    if (lb) {
-      const int Lc = __ffs(lb) - 1;
-      const int tc = wid * 32 + Lc;
-      const int r_lo = min(s.lo + tc * chunk, s.hi), r_hi = min(r_lo + chunk, s.hi);
-      DF carry{__shfl_sync(0xffffffffu, lexcl.hi, Lc), __shfl_sync(0xffffffffu, lexcl.lo, Lc)};
-      y = __shfl_sync(0xffffffffu, last_nz, Lc);
-      for (int base = r_lo; base < r_hi; base += 32) {
-        const int yy = base + lane;
-        const float x = (yy < r_hi) ? w(yy - s.sbase) : 0.f;
-        const DF run = df_add(carry, warp_scan_df(DF{x, 0.f}));
-        const unsigned hb = __ballot_sync(0xffffffffu, yy < r_hi && df_gt(run, t_loc));
-        if (hb) {
-          y = base + __ffs(hb) - 1;
-          break;
-        }
-        carry = DF{__shfl_sync(0xffffffffu, run.hi, 31), __shfl_sync(0xffffffffu, run.lo, 31)};
-      }
-    }
-    if constexpr (CL > 1) {
-      if (lane < CL) dsmem_store_u32(dsmem_addr(&sm.found[slot], lane), (uint32_t)y);
+  const DF aL{__shfl_sync(0xffffffffu, a.hi, L), __shfl_sync(0xffffffffu, a.lo, L)};
+  const float bL = __shfl_sync(0xffffffffu, b.hi, L);
+  int e;
+  if (t.hi >= 0.f) {
+    const DF after_a = df_add(before, aL);
+    if (df_gt(after_a, t)) {
+      e = 2 * L;
     } else {
-      if (lane == 0) sm.found[slot] = y;
+      e = 2 * L + 1;
+      before = after_a;
+    }
+  } else {
+    e = (bL > 0.f) ? 2 * L + 1 : 2 * L;
+  }
+  if (rank == e / kVWarps && wid == e % kVWarps) {
+    // level 2: the thread of the crossing warp
+    DF tl = (t.hi >= 0.f) ? df_add(t, DF{-before.hi, -before.lo}) : t;
+    DF before2;
+    int Lc = lane_crossing(rs.tot, warp_scan_df(rs.tot), tl, before2);
+    if (Lc < 0) Lc = 31;  // cannot happen with a positive warp total; keeps the index valid
+    // level 3: the elements of that thread's run, 32 at a time, by the whole warp
+    const float fL = __shfl_sync(0xffffffffu, rs.f, Lc);
+    const float cwL = __shfl_sync(0xffffffffu, rs.cw, Lc);
+    const int i0 = (wid * 32 + Lc) * s.ch;
+    const DF t3 = (tl.hi >= 0.f) ? df_add(tl, DF{-before2.hi, -before2.lo}) : tl;
+    int y = -1, last_pos = -1;
+    DF carry{0.f, 0.f};
+    for (int base = 0; base < s.ch; base += 32) {
+      const int i = base + lane;
+      const float w = (i < s.ch) ? weight_at(ebuf, pbuf, i0 + i, cwL, fL) : 0.f;
+      const DF run = df_add(carry, warp_scan_df(DF{w, 0.f}));
+      const unsigned pos = __ballot_sync(0xffffffffu, w > 0.f);
+      if (pos) last_pos = base + 31 - __clz(pos);
+      const unsigned hb = __ballot_sync(0xffffffffu, t3.hi >= 0.f && df_gt(run, t3));
+      if (hb) {
+        y = base + __ffs(hb) - 1;
+        break;
+      }
+      carry = DF{__shfl_sync(0xffffffffu, run.hi, 31), __shfl_sync(0xffffffffu, run.lo, 31)};
+    }
+    if (y < 0) y = last_pos;
+    const int tok = (y >= 0) ? i0 + y + s.sbase : -1;
+    if (lane == 0) {  // exactly one warp of the cluster writes rank 0's result
+      if constexpr (CL > 1) {
+        dsmem_store_u32(dsmem_addr(&sm.found, 0), (uint32_t)tok);
+      } else {
+        sm.found = tok;
+      }
     }
   }
   cluster_barrier<CL>();
-  const int y = sm.found[slot];
-  slot ^= 1;
-  return y;
+  return sm.found;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -544,9 +528,8 @@ __device__ __forceinline__ double child_numerator(float lx, float M, DF invT) {
 }
 
 struct NodeBufs {
-  float* lbuf;  // logits, then e(y) at T > 0
+  float* lbuf;  // logits, then e_t(y) at T > 0
   float* pbuf;  // draft probabilities
-  float* rbuf;  // residual
   uint32_t bar_l, bar_p;
 };
 
@@ -554,9 +537,10 @@ struct NodeBufs {
 // one node: statistics, sibling tests, residual rounds, bonus if the walk can stop here
 // ------------------------------------------------------------------------------------------------
 // logits_staged: the kernel already issued the copy of this node's logit slice into nb.lbuf.
+// The bonus of the returned record is valid in rank 0.
 template <int CL>
 __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, const NodeBufs& nb,
-                                 bool eager_probs, bool logits_staged, DF invT_df, int& slot,
+                                 bool logits_staged, DF invT_df, float k2, int& slot,
                                  VerifySmem& sm) {
   const int N = a.N, V = a.V;
   list_children(j, N, sm);
@@ -566,18 +550,15 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   const float* prow = a.probs ? a.probs + row_off : nullptr;
   const Slice s = make_slice(lrow, V, rank, CL);  // the draft row has the same alignment
   const bool sampling = a.T > 0.f;
-  if (!logits_staged) stage_slice(lrow, s, nb.lbuf, nb.bar_l);
-  bool probs_staged = false, probs_ready = false;
-  if (sampling && nk > 0 && eager_probs) {
-    stage_slice(prow, s, nb.pbuf, nb.bar_p);
-    probs_staged = true;
-  }
+  if (!logits_staged) stage_slice(lrow, s, nb.lbuf, nb.bar_l, -INFINITY);
+  const bool probs_staged = sampling && nk > 0;
+  if (probs_staged) stage_slice(prow, s, nb.pbuf, nb.bar_p, 0.f);
   if ((int)threadIdx.x < nk) {  // gathers for the tests, overlapping the bulk copies
-    const int k = sm.kids[threadIdx.x];
-    const int x = sm.tokens[k];
+    const int kid = sm.kids[threadIdx.x];
+    const int x = sm.tokens[kid];
     sm.g_lx[threadIdx.x] = __ldg(lrow + x);
     sm.g_px[threadIdx.x] = sampling ? __ldg(prow + x) : 0.f;
-    sm.g_r[threadIdx.x] = __ldg(a.uniforms + (size_t)b * N + k);
+    sm.g_r[threadIdx.x] = __ldg(a.uniforms + (size_t)b * N + kid);
   }
   const float u_bonus = __ldg(a.uniforms + (size_t)b * N);
   const int lflags0 = wait_slice(nb.bar_l);
@@ -587,12 +568,10 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   st.s = 0.0;
 
   if (!sampling) {
-    publish<CL>(sm, slot, rank, slice_argmax(s, nb.lbuf, lflags0));
     float gv;
     int gi;
-    reduce_argmax<CL>(sm, slot, gv, gi, flags);
-    slot ^= 1;
-    if (gi == 0x7fffffff) gi = 0;  // every value NaN: flagged
+    cluster_argmax<CL>(s, nb.lbuf, lflags0, rank, slot, gv, gi, flags, sm);
+    if (gi < 0 || gi >= V) gi = 0;  // every value NaN: flagged
     int first = -1, nrej = nk;
     for (int t = 0; t < nk; ++t)
       if (sm.tokens[sm.kids[t]] == gi) {
@@ -601,9 +580,9 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
         break;
       }
     if (rank == 0 && a.child_q && (int)threadIdx.x < nk) {
-      const int k = sm.kids[threadIdx.x];
-      a.child_q[(size_t)b * N + k] =
-          (int)threadIdx.x <= nrej ? (sm.tokens[k] == gi ? 1.f : 0.f) : -1.f;
+      const int kid = sm.kids[threadIdx.x];
+      a.child_q[(size_t)b * N + kid] =
+          (int)threadIdx.x <= nrej ? (sm.tokens[kid] == gi ? 1.f : 0.f) : -1.f;
     }
     st.m = gv;
     st.argmax = gi;
@@ -614,15 +593,14 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     return st;
   }
 
-  // ---- T > 0: statistics of q_j = softmax(l_j / T); e(y) replaces the logits in lbuf
-  const float invT = 1.f / a.T;
+  // ---- T > 0: statistics of q_j = softmax(l_j / T); e_t(y) replaces the logits in lbuf
   float M;
   DF S;
-  cluster_exp_stats<CL>(s, nb.lbuf, invT, lflags0, rank, slot, M, S, flags, sm);
-  if (!(S.hi > 0.f) || !(S.hi <= FLT_MAX)) flags |= SPEC_ST_NONFINITE;
-  const float invS = __fdiv_rn(1.f, S.hi);
-  const float c0 = invS;
-  double D = df_to_double(S);
+  RunState rs;
+  cluster_stats<CL>(s, nb.lbuf, k2, lflags0, rank, slot, M, S, rs, flags, sm);
+  // Scalars every thread holds stay double-float: fp64 here is only for the few threads that
+  // take a decision or update a numerator.
+  DF D = S;
   if ((int)threadIdx.x < nk)
     sm.g_n[threadIdx.x] = child_numerator(sm.g_lx[threadIdx.x], M, invT_df);
   if (__syncthreads_or((int)threadIdx.x < nk && !(sm.g_px[threadIdx.x] >= 0.f &&
@@ -630,77 +608,58 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     flags |= SPEC_ST_NONFINITE;
 
   int first = -1, nrej = nk;
-  bool chain = false;
-  Weights wt;
-  wt.ebuf = nb.lbuf;
-  wt.pbuf = nb.pbuf;
-  wt.rbuf = nb.rbuf;
-  wt.inv_beta = sm.inv_beta;
-  wt.t = 0;
-  if (nk == 0 && !(flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT))) {
-    // leaf (small problems): the bonus when the walk ends here is drawn from q_j
-    wt.kind = Weights::kExp;
-    wt.c = 1.f;
-    st.bonus = cluster_sample<CL>(wt, s, rank, u_bonus, slot, flags, sm);
-  }
+  bool all_rejected = nk > 0;
+  DF c{0.f, 0.f};  // current weights: max(0, e - c p)
+  bool frozen = false, p_waited = false;
+  int pflags = 0;
   for (int t = 0; t < nk; ++t) {
-    const int k = sm.kids[t];
+    const int kid = sm.kids[t];
     if ((int)threadIdx.x == t) {
       const double px = (double)sm.g_px[t];
       const double r = (double)sm.g_r[t];
       const double n = sm.g_n[t];
-      sm.decision = (r * px * D < n) ? 1 : 0;  // r < min(1, q/p) with q = n / D
-      if (rank == 0 && a.child_q) {
-        const float df = (float)D;
-        a.child_q[(size_t)b * N + k] = df > 1e-30f ? __fdiv_rn((float)n, df) : (float)(n / D);
-      }
+      const double Dd = df_to_double(D);
+      sm.decision = (r * px * Dd < n) ? 1 : 0;  // r < min(1, q/p) with q = n / D
+      if (rank == 0 && a.child_q)
+        a.child_q[(size_t)b * N + kid] = D.hi > 1e-30f ? __fdiv_rn((float)n, D.hi) : (float)(n / Dd);
     }
     __syncthreads();
     if (sm.decision) {
-      first = k;
+      first = kid;
       nrej = t;
+      all_rejected = false;
       break;
     }
-    // rejected: residual round t + 1 (needed by the next sibling or by the bonus draw)
-    int lflags = 0;  // CTA-local events; they reach every CTA through the published partial
-    if (!probs_ready) {
-      if (!probs_staged) stage_slice(prow, s, nb.pbuf, nb.bar_p);
-      lflags |= wait_slice(nb.bar_p);
-      probs_staged = probs_ready = true;
+    if (frozen) continue;  // a zero residual keeps the distribution: nothing to compute
+    // rejected: residual of the current distribution (needed by the next sibling or the draw)
+    if (!p_waited) {
+      pflags = wait_slice(nb.bar_p);  // CTA-local: reaches the cluster through the partials
+      p_waited = true;
     }
-    const RoundArgs ra{c0, sm.inv_beta, t + 1, chain};
-    publish<CL>(sm, slot, rank, residual_round(s, nb.lbuf, nb.pbuf, nb.rbuf, ra, lflags));
-    const DF beta = reduce_sum<CL>(sm, slot, flags);
-    slot ^= 1;
-    const double beta_d = df_to_double(beta);
-    if (threadIdx.x == 0) {
-      sm.inv_beta[t] = beta.hi > 0.f ? __fdiv_rn(1.f, beta.hi) : 0.f;
-      if (rank == 0) a.beta[((size_t)b * N + j) * kMaxNodes + t] = beta_d;
-    }
-    if (t == nk - 1) {  // every child rejected: the bonus comes from the last residual
-      __syncthreads();
-      if (!(flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT))) {
-        wt.kind = Weights::kBuffer;
-        st.bonus = cluster_sample<CL>(wt, s, rank, u_bonus, slot, flags, sm);
-        if (st.bonus < 0) {  // the last residual is all zero: keep the distribution it came from
-          wt.kind = Weights::kChain;
-          wt.c = c0;
-          wt.t = t;
-          st.bonus = cluster_sample<CL>(wt, s, rank, u_bonus, slot, flags, sm);
-        }
-      }
-      break;
-    }
-    if (beta_d > 0.0) {
+    const DF c_next = df_add(c, D);
+    const float c_t = rs.f > 0.f ? __fdiv_rn(__fadd_rn(c_next.hi, c_next.lo), rs.f) : 0.f;
+    DF tot, wta, wtb;
+    const DF G = cluster_residual<CL>(s, nb.lbuf, nb.pbuf, c_t, rs.f, t == 0, pflags, rank, slot,
+                                      tot, wta, wtb, flags, sm);
+    pflags = 0;
+    if (G.hi > 0.f) {
       if ((int)threadIdx.x > t && (int)threadIdx.x < nk)
-        sm.g_n[threadIdx.x] = fmax(fma(-(double)sm.g_px[threadIdx.x], D, sm.g_n[threadIdx.x]), 0.0);
-      D *= beta_d;
+        sm.g_n[threadIdx.x] =
+            fmax(fma(-(double)sm.g_px[threadIdx.x], df_to_double(D), sm.g_n[threadIdx.x]), 0.0);
+      D = G;
+      c = c_next;
+      rs.tot = tot;
+      rs.cw = c_t;
+      store_wtot<CL>(sm, wta, wtb);
     } else {
-      chain = true;  // q stays: later rounds recompute it from e
+      frozen = true;
     }
     __syncthreads();
   }
-  if (probs_staged && !probs_ready) flags |= wait_slice(nb.bar_p);  // no copy left in flight
+  if (probs_staged && !p_waited) wait_slice(nb.bar_p);  // no copy left in flight (not needed)
+  const bool bad = (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) != 0;
+  if ((nk == 0 || all_rejected) && !bad)  // the walk can stop here: draw its bonus
+    st.bonus = cluster_draw<CL>(s, nb.lbuf, nb.pbuf, rs, u_bonus, rank, sm);
   if (rank == 0 && a.child_q && (int)threadIdx.x > nrej && (int)threadIdx.x < nk)
     a.child_q[(size_t)b * N + sm.kids[threadIdx.x]] = -1.f;
   st.m = M;
@@ -709,30 +668,24 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   st.first_acc = first;
   st.nrej = nrej;
   st.flags = flags;
-  if (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) st.bonus = -1;
+  if (bad) st.bonus = -1;
   return st;
 }
 
 // ------------------------------------------------------------------------------------------------
-// the walk (run by the last cluster of the sequence to finish)
+// the walk (by the last cluster of the sequence to finish)
 // ------------------------------------------------------------------------------------------------
-// bar_l_used: whether this CTA already staged a row on nb.bar_l in this launch.
-template <int CL>
-__device__ void walk_sequence(const VerifyArgs& a, int b, int rank, const NodeBufs& nb,
-                              bool leaves_done, bool bar_l_used, int& slot, VerifySmem& sm) {
-  const int N = a.N, V = a.V;
-  // every node record written in this call (L2: bypass L1), flags of the internal rows
+// Reads every node record written in this call (L2: bypass L1) and follows the accepted children;
+// leaves sm.path, sm.path_len, sm.terminal and the OR of the internal nodes' flags in sm.flags.
+__device__ void walk_path(const VerifyArgs& a, int b, bool leaves_done, VerifySmem& sm) {
+  const int N = a.N;
   int f = 0;
   if ((int)threadIdx.x < N) {
     const int i = threadIdx.x;
     if (sm.internal[i] || leaves_done) {
       const NodeStat* src = a.stats + (size_t)b * N + i;
       NodeStat st;
-      st.m = __ldcg(&src->m);
-      st.argmax = __ldcg(&src->argmax);
-      st.s = __ldcg(&src->s);
       st.first_acc = __ldcg(&src->first_acc);
-      st.nrej = __ldcg(&src->nrej);
       st.flags = __ldcg(&src->flags);
       st.bonus = __ldcg(&src->bonus);
       sm.st[i] = st;
@@ -754,59 +707,60 @@ __device__ void walk_sequence(const VerifyArgs& a, int b, int rank, const NodeBu
     sm.terminal = c;
   }
   __syncthreads();
+}
+
+// Writes the outputs of sequence b (one CTA).
+__device__ void write_outputs(const VerifyArgs& a, int b, int bonus, int flags, VerifySmem& sm) {
+  const int N = a.N;
+  if (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) bonus = -1;
+  const int len = sm.path_len;
+  const bool ok = bonus >= 0;
+  if (threadIdx.x == 0) {
+    a.accept_len[b] = ok ? len : -1;
+    a.bonus[b] = ok ? bonus : -1;
+    if (a.status && flags) atomicOr(a.status + b, flags);
+    if (a.child_q) a.child_q[(size_t)b * N] = -1.f;
+  }
+  for (int i = threadIdx.x; i < N; i += kVThreads) {
+    const int node = (ok && i < len) ? sm.path[i] : -1;
+    a.acc_tokens[(size_t)b * N + i] = node >= 0 ? sm.tokens[node] : -1;
+    if (a.acc_nodes) a.acc_nodes[(size_t)b * N + i] = node;
+  }
+}
+
+// Leaves not processed (large problems): the whole cluster walks and draws the bonus at a leaf
+// terminal.  bar_l_used: whether this CTA already staged a row on nb.bar_l in this launch.
+template <int CL>
+__device__ void walk_sequence_cluster(const VerifyArgs& a, int b, int rank, const NodeBufs& nb,
+                                      bool bar_l_used, float k2, int& slot, VerifySmem& sm) {
+  walk_path(a, b, false, sm);
   const int c = sm.terminal;
   int flags = sm.flags;
   int bonus = -1;
   if (sm.internal[c]) {
     bonus = sm.st[c].bonus;
-  } else if (leaves_done) {
-    flags |= sm.st[c].flags;
-    bonus = sm.st[c].bonus;
   } else {
-    // leaf terminal of a large problem: sweep its row here
-    const size_t row_off = ((size_t)b * N + c) * (size_t)V;
+    const size_t row_off = ((size_t)b * a.N + c) * (size_t)a.V;
     const float* lrow = a.logits + row_off;
-    const Slice s = make_slice(lrow, V, rank, CL);
-    stage_slice(lrow, s, nb.lbuf, nb.bar_l);
+    const Slice s = make_slice(lrow, a.V, rank, CL);
+    stage_slice(lrow, s, nb.lbuf, nb.bar_l, -INFINITY);
     const int lflags = wait_slice(nb.bar_l, bar_l_used ? 1 : 0);  // CTA-local: published below
     if (a.T == 0.f) {
-      publish<CL>(sm, slot, rank, slice_argmax(s, nb.lbuf, lflags));
       float gv;
       int gi;
-      reduce_argmax<CL>(sm, slot, gv, gi, flags);
-      slot ^= 1;
-      bonus = (gi == 0x7fffffff) ? 0 : gi;
+      cluster_argmax<CL>(s, nb.lbuf, lflags, rank, slot, gv, gi, flags, sm);
+      bonus = (gi < 0 || gi >= a.V) ? 0 : gi;
     } else {
-      const float invT = 1.f / a.T;
       float M;
       DF S;
-      cluster_exp_stats<CL>(s, nb.lbuf, invT, lflags, rank, slot, M, S, flags, sm);
-      Weights wt;
-      wt.kind = Weights::kExp;
-      wt.ebuf = nb.lbuf;
-      wt.c = 1.f;
-      const float u = __ldg(a.uniforms + (size_t)b * N);
+      RunState rs;
+      cluster_stats<CL>(s, nb.lbuf, k2, lflags, rank, slot, M, S, rs, flags, sm);
+      const float u = __ldg(a.uniforms + (size_t)b * a.N);
       if (!(flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)))
-        bonus = cluster_sample<CL>(wt, s, rank, u, slot, flags, sm);
+        bonus = cluster_draw<CL>(s, nb.lbuf, nb.pbuf, rs, u, rank, sm);
     }
   }
-  if (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) bonus = -1;
-
-  if (rank == 0) {
-    const int len = sm.path_len;
-    const bool ok = bonus >= 0;
-    if (threadIdx.x == 0) {
-      a.accept_len[b] = ok ? len : -1;
-      a.bonus[b] = ok ? bonus : -1;
-      if (a.status && flags) atomicOr(a.status + b, flags);
-      if (a.child_q) a.child_q[(size_t)b * N] = -1.f;
-    }
-    for (int i = threadIdx.x; i < N; i += kVThreads) {
-      const int node = (ok && i < len) ? sm.path[i] : -1;
-      a.acc_tokens[(size_t)b * N + i] = node >= 0 ? sm.tokens[node] : -1;
-      if (a.acc_nodes) a.acc_nodes[(size_t)b * N + i] = node;
-    }
-  }
+  if (rank == 0) write_outputs(a, b, bonus, flags, sm);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -824,10 +778,13 @@ __device__ __forceinline__ void claim_counter(unsigned long long* ctr, unsigned 
   for (int it = 0; it < 4 && (old >> 16) != g; ++it) old = atomicCAS(ctr, old, g << 16);
 }
 
-// Returns true for the last of the N arrivals.
+// Returns true for the last of the N arrivals.  Release: this thread's earlier global writes (the
+// node record) are visible to whoever sees the count; acquire: the last arriver sees every other
+// cluster's record.
 __device__ __forceinline__ bool arrive(unsigned long long* ctr, unsigned long long gen, int N) {
   const unsigned long long g = gen & 0xFFFFFFFFFFFFull;
-  const unsigned long long old = atomicAdd(ctr, 1ull);
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
   if ((old >> 16) == g && (old & 0xFFFFull) + 1 == (unsigned long long)N) {
     atomicExch(ctr, g << 16);
     return true;
@@ -840,12 +797,12 @@ __device__ __forceinline__ bool arrive(unsigned long long* ctr, unsigned long lo
 // ------------------------------------------------------------------------------------------------
 template <int CL>
 __global__ void __launch_bounds__(kVThreads)
-    verify_kernel(const VerifyArgs a, int cap, int eager_probs, int do_leaves, float invT_hi,
-                  float invT_lo) {
+    verify_kernel(const VerifyArgs a, int cap, int do_leaves, float invT_hi, float invT_lo,
+                  float k2) {
   extern __shared__ __align__(16) float dyn[];
   __shared__ VerifySmem sm;
   __shared__ __align__(8) uint64_t bars[2];
-  const NodeBufs nb{dyn, dyn + cap, dyn + 2 * cap, smem_u32(&bars[0]), smem_u32(&bars[1])};
+  const NodeBufs nb{dyn, dyn + cap, smem_u32(&bars[0]), smem_u32(&bars[1])};
   const int rank = (CL > 1) ? int(cg::this_cluster().block_rank()) : 0;
   const int j = blockIdx.y, b = blockIdx.z;
   const int N = a.N;
@@ -861,7 +818,7 @@ __global__ void __launch_bounds__(kVThreads)
   const bool early = do_leaves != 0;
   if (early) {
     const float* lrow = a.logits + ((size_t)b * N + j) * (size_t)a.V;
-    stage_slice(lrow, make_slice(lrow, a.V, rank, CL), nb.lbuf, nb.bar_l);
+    stage_slice(lrow, make_slice(lrow, a.V, rank, CL), nb.lbuf, nb.bar_l, -INFINITY);
   }
   if (rank == 0 && threadIdx.x == 0) claim_counter(a.counters + b, a.gen);
   const int bad = load_tree(a, b, sm);  // uniform across the cluster: same tree everywhere
@@ -884,16 +841,27 @@ __global__ void __launch_bounds__(kVThreads)
   int slot = 0;
   const bool work = sm.internal[j] || do_leaves;
   NodeStat st;
-  if (work)
-    st = process_node<CL>(a, b, j, rank, nb, eager_probs != 0, early, DF{invT_hi, invT_lo}, slot,
-                          sm);
+  if (work) st = process_node<CL>(a, b, j, rank, nb, early, DF{invT_hi, invT_lo}, k2, slot, sm);
 
-  // arrival: the last cluster of the sequence walks the tree
+  // arrival: the last cluster of the sequence to finish walks the tree
+  if (do_leaves) {
+    // every possible stop already has its bonus, so rank 0 finishes alone (this cluster's
+    // exchanges are complete: the other CTAs may leave)
+    if (rank != 0) return;
+    if (threadIdx.x == 0) {
+      a.stats[(size_t)b * N + j] = st;
+      sm.is_last = arrive(a.counters + b, a.gen, N) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!sm.is_last) return;
+    walk_path(a, b, true, sm);
+    const int c = sm.terminal;
+    write_outputs(a, b, sm.st[c].bonus, sm.flags | (sm.internal[c] ? 0 : sm.st[c].flags), sm);
+    return;
+  }
   if (rank == 0 && threadIdx.x == 0) {
     if (work) a.stats[(size_t)b * N + j] = st;
-    __threadfence();
     const int last = arrive(a.counters + b, a.gen, N) ? 1 : 0;
-    __threadfence();
     if constexpr (CL > 1) {
       for (int r = 0; r < CL; ++r) dsmem_store_u32(dsmem_addr(&sm.is_last, r), (uint32_t)last);
     } else {
@@ -902,7 +870,7 @@ __global__ void __launch_bounds__(kVThreads)
   }
   cluster_barrier<CL>();
   if (!sm.is_last) return;
-  walk_sequence<CL>(a, b, rank, nb, do_leaves != 0, work, slot, sm);
+  walk_sequence_cluster<CL>(a, b, rank, nb, work, k2, slot, sm);
   cluster_barrier<CL>();  // keep shared memory alive for remote stores
 }
 
@@ -911,8 +879,7 @@ __global__ void __launch_bounds__(kVThreads)
 // ------------------------------------------------------------------------------------------------
 size_t verify_workspace_bytes(int B, int N, int V) {
   (void)V;
-  return (size_t)B * N * sizeof(NodeStat) + (size_t)B * N * kMaxNodes * sizeof(double) +
-         (size_t)B * sizeof(unsigned long long);
+  return (size_t)B * N * sizeof(NodeStat) + (size_t)B * sizeof(unsigned long long);
 }
 
 template <class... Params, class... Args>
@@ -937,8 +904,8 @@ static cudaError_t launch_ex(void (*kern)(Params...), dim3 grid, int cl, size_t 
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Per-buffer slice limit (floats): three buffers plus the static state must fit in a CTA's 227 KB.
-constexpr int kMaxSliceFloats = 16 * 1024 + 64;
+// Per-buffer slice limit (floats): two buffers plus the static state fit in a CTA's 227 KB.
+constexpr int kMaxSliceFloats = 26 * 1024;
 
 // Cluster size: large enough that the slice buffers fit; for latency-bound (small) problems as
 // large as slices of >= 1024 elements allow; otherwise aim for about one wave of CTAs.
@@ -957,21 +924,21 @@ bool verify_supported(int V) { return slice_capacity(V, 8) <= kMaxSliceFloats; }
 
 cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s) {
   const bool small = (long long)a.B * a.N * a.V * 4 <= (64ll << 20);
-  // small problems are latency-bound: stage the draft rows eagerly and process leaves speculatively
-  const int eager = small ? 1 : 0;
+  // small problems are latency-bound: process leaves speculatively too
   const int leaves = small ? 1 : 0;
   const long long units = (long long)a.B * (leaves ? a.N : (a.N + 1) / 2);
   const int cl = pick_cluster(units, a.V, num_sms, small);
   const int cap = slice_capacity(a.V, cl);
-  const size_t smem = (size_t)(a.T > 0.f ? 3 : 1) * cap * sizeof(float);
+  const size_t smem = (size_t)(a.T > 0.f ? 2 : 1) * cap * sizeof(float);
   const double invTd = a.T > 0.f ? 1.0 / (double)a.T : 0.0;
   const float invT_hi = (float)invTd, invT_lo = (float)(invTd - (double)invT_hi);
+  const float k2 = (float)(invTd * 1.4426950408889634);  // log2(e) / T
   const dim3 g(cl, a.N, a.B);
   switch (cl) {
-    case 1: return launch_ex(verify_kernel<1>, g, 1, smem, s, a, cap, eager, leaves, invT_hi, invT_lo);
-    case 2: return launch_ex(verify_kernel<2>, g, 2, smem, s, a, cap, eager, leaves, invT_hi, invT_lo);
-    case 4: return launch_ex(verify_kernel<4>, g, 4, smem, s, a, cap, eager, leaves, invT_hi, invT_lo);
-    default: return launch_ex(verify_kernel<8>, g, 8, smem, s, a, cap, eager, leaves, invT_hi, invT_lo);
+    case 1: return launch_ex(verify_kernel<1>, g, 1, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
+    case 2: return launch_ex(verify_kernel<2>, g, 2, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
+    case 4: return launch_ex(verify_kernel<4>, g, 4, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
+    default: return launch_ex(verify_kernel<8>, g, 8, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
   }
 }
 

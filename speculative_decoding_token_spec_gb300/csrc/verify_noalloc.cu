@@ -3,11 +3,11 @@
 // Some callers cannot hand the library device scratch memory.  Examples: a serving engine that
 // reserves all free GPU memory for its KV cache at start-up and forbids cudaMalloc afterwards, or
 // a plugin host that passes a kernel only its input and output buffers.  For them this entry point
-// keeps the per-node statistics and residual normalisers that spec_tree_verify otherwise writes to
-// its workspace in one fixed, file-scope device array instead.
+// keeps the per-node statistics and arrival counters that spec_tree_verify otherwise writes to its
+// workspace in one fixed, file-scope device array instead.
 //
 // Properties of that array:
-//   * Size: room for B * N <= SPEC_NOALLOC_MAX_NODES tree nodes per call (about 2.3 MB).  Every
+//   * Size: room for B * N <= SPEC_NOALLOC_MAX_NODES tree nodes per call (160 KB).  Every
 //     GPU on which the library is loaded holds it until the process exits.
 //   * Set-up: the first call on a device looks up the array's device address (cudaGetSymbolAddress)
 //     with that device current and caches it; make that first call before any stream capture.
@@ -29,9 +29,8 @@ using namespace spectree;
 
 namespace {
 
-// per node: its statistics record and residual normalisers; per sequence (B <= B * N): one
-// arrival counter
-constexpr size_t kPerNode = sizeof(NodeStat) + kMaxNodes * sizeof(double) + sizeof(unsigned long long);
+// per node: its statistics record; per sequence (B <= B * N): one arrival counter
+constexpr size_t kPerNode = sizeof(NodeStat) + sizeof(unsigned long long);
 constexpr size_t kScratchBytes = (size_t)SPEC_NOALLOC_MAX_NODES * kPerNode;
 
 // The fixed scratch.  In host code `g_verify_scratch` names a host-side stand-in, not device
