@@ -66,6 +66,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return false;
 }
 
+// Wait with cluster-scope acquire (data delivered by other CTAs of the cluster, e.g. st.async
+// completing on this barrier); false if it did not complete within kSpinLimit polls.
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
 // ------------------------------------------------------------------------------------------------
 // TMA (tensor) loads
 // ------------------------------------------------------------------------------------------------
@@ -214,6 +230,17 @@ __device__ __forceinline__ DF warp_scan_df(DF v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
+    DF w{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+    if (lane >= o) v = df_add(w, v);
+  }
+  return v;
+}
+
+// Inclusive scan within each group of 8 lanes (same association as warp_scan_df on lanes 0..7).
+__device__ __forceinline__ DF warp_scan8_df(DF v) {
+  const int lane = threadIdx.x & 7;
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
     DF w{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
     if (lane >= o) v = df_add(w, v);
   }

@@ -11,7 +11,8 @@ namespace spectree {
 struct NodeStat {
   float m;        // max target logit of the row (raw logit units)
   int argmax;     // lowest index attaining the max
-  double s;       // sum_y exp((l_y - m) / T)
+  float s_hi;     // sum_y exp((l_y - m) / T), as a double-float
+  float s_lo;
   int first_acc;  // accepted child, or -1 when every child was rejected
   int nrej;       // children rejected before first_acc (all of them if none was accepted)
   int flags;      // SPEC_ST_NONFINITE / SPEC_ST_TIMEOUT met while processing the node

@@ -32,9 +32,11 @@
 //
 // Precision.  Element weights are fp32 (hardware 2^x on an argument formed as (l - m) * k).  Every
 // sum is a compensated fp32 sum per thread and a double-float (pair of fp32) sum across threads and
-// CTAs (fp64 arithmetic on this part costs 64 cycles per dependent operation, 1 us per division).
-// The accept decisions compare in fp64: n(x) starts as exp((l_x - M)/T) with the argument formed
-// exactly as a double-float, and after a rejection n <- max(0, n - p(x) D), D <- D_k.
+// CTAs.  No fp64 arithmetic: this part's fp64 pipe is narrow (a dependent operation costs 64
+// cycles, a division about 1 us) and shared by every CTA on the SM.
+// The accept decisions compare double-floats (relative error about 2^-44): n(x) starts as
+// exp((l_x - M)/T) with the argument formed exactly as a double-float, and after a rejection
+// n <- max(0, n - p(x) D), D <- D_k.
 #include <cooperative_groups.h>
 #include <float.h>
 
@@ -47,10 +49,11 @@ namespace spectree {
 
 constexpr int kVThreads = 256;
 constexpr int kVWarps = kVThreads / 32;
+static_assert(kVWarps == 8, "exchanges and draws combine 8 warps (and at most 8 CTAs) in 8 lanes");
 constexpr uint32_t kBulkChunk = 32768;  // bytes per bulk copy instruction
 
-// One warp's partial result, published to the whole cluster (32 bytes: two 16-byte stores).
-struct __align__(16) WarpPart {
+// A warp's or a CTA's partial result in an exchange (32 bytes: two 16-byte stores).
+struct __align__(16) Entry {
   float m;     // max (statistics) / value (argmax)
   int idx;     // argmax index
   float s_hi;  // sum (double-float)
@@ -58,7 +61,7 @@ struct __align__(16) WarpPart {
   int flags;
   int pad[3];
 };
-static_assert(sizeof(WarpPart) == 32, "WarpPart layout");
+static_assert(sizeof(Entry) == 32, "Entry layout");
 
 struct VerifySmem {
   int parent[kMaxNodes];
@@ -76,10 +79,14 @@ struct VerifySmem {
   float g_r[kMaxNodes];         // children's test uniforms
   float g_lx[kMaxNodes];        // gathered target logit / draft probability of each child's token
   float g_px[kMaxNodes];
-  double g_n[kMaxNodes];        // numerators n(x~) of the children's current q values
-  WarpPart wp[2][8 * kVWarps];  // ping-pong: every warp partial of the cluster, pushed here
-  DF wtot[8 * kVWarps];         // warp totals of the current sampling weights (e(y) scale)
+  DF g_n[kMaxNodes];            // numerators n(x~) of the children's current q values
+  Entry wpart[kVWarps];         // this CTA's warp entries of the current exchange
+  Entry cpart[2][8];            // every CTA's entry, per exchange slot (sent here by st.async)
+  DF wcur[kVWarps];             // totals of the current sampling weights: this CTA's warps,
+  DF ccur[8];                   // and every CTA of the cluster (e(y) scale)
   NodeStat st[kMaxNodes];
+  Entry xres;                     // result of the current exchange (written by warp 0)
+  __align__(8) uint64_t xbar[2];  // transaction barriers of the exchange slots
 };
 
 __device__ __forceinline__ float ex2f(float x) {  // hardware 2^x
@@ -155,9 +162,14 @@ __device__ __forceinline__ int wait_slice(uint32_t bar, uint32_t parity = 0) {
   return st;
 }
 
-// ------------------------------------------------------------------------------------------------
-// cluster exchanges: warp partial -> every warp of every CTA reads all CL * 8 partials
-// ------------------------------------------------------------------------------------------------
+// argmax with lowest index on ties (indices compared unsigned); NaN never wins.
+__device__ __forceinline__ void argmax_merge(float& bv, int& bi, float v, int i) {
+  if (v > bv || (v == bv && (unsigned)i < (unsigned)bi)) {
+    bv = v;
+    bi = i;
+  }
+}
+
 template <int CL>
 __device__ __forceinline__ void cluster_barrier() {
   if constexpr (CL > 1) {
@@ -167,49 +179,120 @@ __device__ __forceinline__ void cluster_barrier() {
   }
 }
 
-// p must be warp-uniform.  Lane L < CL of every warp pushes it into CTA L's copy of the partial
-// table (entry rank * 8 + warp); after the barrier every CTA holds all CL * 8 partials locally.
-template <int CL>
-__device__ __forceinline__ void publish(VerifySmem& sm, int slot, int rank, const WarpPart& p) {
-  const int lane = threadIdx.x & 31;
-  WarpPart* dst = &sm.wp[slot][rank * kVWarps + (threadIdx.x >> 5)];
-  if constexpr (CL > 1) {
-    if (lane < CL) {
-      const uint32_t a = dsmem_addr(dst, lane);
-      const uint4* v = reinterpret_cast<const uint4*>(&p);
-      dsmem_store_v4(a, v[0]);
-      dsmem_store_v4(a + 16, v[1]);
-    }
+// ------------------------------------------------------------------------------------------------
+// cluster exchanges
+// ------------------------------------------------------------------------------------------------
+// An exchange combines one entry per warp into a cluster-wide result.  The warps' entries are first
+// combined inside the CTA; warp 0 then sends the CTA's entry to every CTA of the cluster with
+// st.async, whose completion is counted on the receiver's transaction mbarrier (a one-way trip,
+// no cluster barrier).  Every CTA then combines the CL entries in rank order.  Two slots alternate;
+// slot s of exchange x waits for phase (x / 2) & 1 of its barrier.  A CTA can send exchange x + 2
+// only after exchange x + 1 completed everywhere it reads from, and every CTA passes a
+// __syncthreads (step 1) after reading exchange x, so slots are never overwritten early.
+enum XKind { kXSum = 0, kXMaxSum = 1, kXArgmax = 2 };
+
+__device__ __forceinline__ Entry entry_identity(int kind) {
+  return kind == kXArgmax ? Entry{-INFINITY, 0x7fffffff, 0.f, 0.f, 0, {0, 0, 0}}
+                          : Entry{-INFINITY, 0, 0.f, 0.f, 0, {0, 0, 0}};
+}
+
+// a then b (a holds the lower lanes / ranks): sums in that order, max-sums rescaled to the larger
+// max (k = log2(e) / T), argmax with the lower index on ties.
+__device__ __forceinline__ Entry entry_combine(const Entry& a, const Entry& b, int kind, float k) {
+  Entry r = a;
+  r.flags = a.flags | b.flags;
+  if (kind == kXArgmax) {
+    argmax_merge(r.m, r.idx, b.m, b.idx);
+  } else if (kind == kXSum) {
+    const DF s = df_add(DF{a.s_hi, a.s_lo}, DF{b.s_hi, b.s_lo});
+    r.s_hi = s.hi;
+    r.s_lo = s.lo;
   } else {
-    if (lane == 0) *dst = p;
+    const float m = fmaxf(a.m, b.m);
+    const float fa = (a.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(a.m, m), k));
+    const float fb = (b.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(b.m, m), k));
+    const DF s = df_add(df_scale(DF{a.s_hi, a.s_lo}, fa), df_scale(DF{b.s_hi, b.s_lo}, fb));
+    r.m = m;
+    r.s_hi = s.hi;
+    r.s_lo = s.lo;
   }
-  cluster_barrier<CL>();
+  return r;
 }
 
-// Partials 2 * lane and 2 * lane + 1 (entries past CL * 8 read as `fill`).
-template <int CL>
-__device__ __forceinline__ void entries(const VerifySmem& sm, int slot, const WarpPart& fill,
-                                        WarpPart& a, WarpPart& b) {
-  const int l = threadIdx.x & 31;
-  a = (2 * l < CL * kVWarps) ? sm.wp[slot][2 * l] : fill;
-  b = (2 * l + 1 < CL * kVWarps) ? sm.wp[slot][2 * l + 1] : fill;
+__device__ __forceinline__ Entry shfl_entry(const Entry& e, int o) {
+  Entry f;
+  f.m = __shfl_xor_sync(0xffffffffu, e.m, o);
+  f.idx = __shfl_xor_sync(0xffffffffu, e.idx, o);
+  f.s_hi = __shfl_xor_sync(0xffffffffu, e.s_hi, o);
+  f.s_lo = __shfl_xor_sync(0xffffffffu, e.s_lo, o);
+  f.flags = __shfl_xor_sync(0xffffffffu, e.flags, o);
+  return f;
 }
 
-// argmax with lowest index on ties (indices compared unsigned); NaN never wins.
-__device__ __forceinline__ void argmax_merge(float& bv, int& bi, float v, int i) {
-  if (v > bv || (v == bv && (unsigned)i < (unsigned)bi)) {
-    bv = v;
-    bi = i;
-  }
-}
-
-__device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
+// Combination of the entries held by lanes 0..7 (in lane order), in every one of those lanes.
+// Max-sums take the max first and rescale each lane's sum once.
+__device__ __forceinline__ Entry lanes8_combine(Entry e, int kind, float k) {
+  const int lane = threadIdx.x & 31;
+  if (kind == kXMaxSum) {
+    float M = e.m;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    argmax_merge(bv, bi, ov, oi);
+    for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float f = (e.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(e.m, M), k));
+    const DF sc = df_scale(DF{e.s_hi, e.s_lo}, f);
+    e.m = M;
+    e.s_hi = sc.hi;
+    e.s_lo = sc.lo;
+    kind = kXSum;
   }
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) {
+    const Entry f = shfl_entry(e, o);
+    e = (lane & o) ? entry_combine(f, e, kind, k) : entry_combine(e, f, kind, k);
+  }
+  return e;
+}
+
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+      : "memory");
+}
+
+// One exchange; returns the cluster-wide combination (in every thread).  `mine` is this warp's
+// entry (warp-uniform).  Warp 0 combines the CTA's warps, sends, waits for the CL entries and
+// combines them; the others meet it at a __syncthreads.  After it, sm.cpart[slot][r] holds CTA
+// r's entry (slot returned through xslot).  A wait that gives up sets SPEC_ST_TIMEOUT.
+template <int CL>
+__device__ Entry exchange(VerifySmem& sm, int& xk, const Entry& mine, int kind, float k, int rank,
+                          int& xslot) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (lane == 0) sm.wpart[wid] = mine;
+  __syncthreads();
+  const int slot = xk & 1;
+  const uint32_t parity = (xk >> 1) & 1;
+  ++xk;
+  xslot = slot;
+  if (wid == 0) {
+    const uint32_t bar = smem_u32(&sm.xbar[slot]);
+    const Entry c = lanes8_combine(lane < kVWarps ? sm.wpart[lane] : entry_identity(kind), kind, k);
+    if (lane == 0) mbar_arrive_expect_tx(bar, CL * (uint32_t)sizeof(Entry));
+    if (lane < CL) {
+      const uint32_t dst = dsmem_addr(&sm.cpart[slot][rank], lane);
+      const uint32_t rbar = dsmem_addr(&sm.xbar[slot], lane);
+      const uint4* v = reinterpret_cast<const uint4*>(&c);
+      st_async_v4(dst, v[0], rbar);
+      st_async_v4(dst + 16, v[1], rbar);
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_acq_cluster(bar, parity));
+    Entry r = lanes8_combine(lane < CL ? sm.cpart[slot][lane] : entry_identity(kind), kind, k);
+    if (lane == 0) {
+      r.flags |= ok ? 0 : SPEC_ST_TIMEOUT;
+      sm.xres = r;
+    }
+  }
+  __syncthreads();
+  return sm.xres;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -233,9 +316,18 @@ struct RunWalk {
   }
 };
 
+__device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    argmax_merge(bv, bi, ov, oi);
+  }
+}
+
 // T = 0: argmax of the row (cluster-wide), NaN / +Inf flagged.
 template <int CL>
-__device__ void cluster_argmax(const Slice& s, const float* lbuf, int lflags, int rank, int& slot,
+__device__ void cluster_argmax(const Slice& s, const float* lbuf, int lflags, int rank, int& xk,
                                float& gv, int& gi, int& flags, VerifySmem& sm) {
   const float4* L4 = reinterpret_cast<const float4*>(lbuf + threadIdx.x * s.ch);
   const int y0 = threadIdx.x * s.ch + s.sbase;  // element of the run's first position
@@ -258,15 +350,12 @@ __device__ void cluster_argmax(const Slice& s, const float* lbuf, int lflags, in
   }
   warp_argmax(bv, bi);
   const int f = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0) | lflags;
-  publish<CL>(sm, slot, rank, WarpPart{bv, bi, 0.f, 0.f, f, {0, 0, 0}});
-  WarpPart a, b;
-  entries<CL>(sm, slot, WarpPart{-INFINITY, 0x7fffffff, 0.f, 0.f, 0, {0, 0, 0}}, a, b);
-  slot ^= 1;
-  gv = a.m;
-  gi = a.idx;
-  argmax_merge(gv, gi, b.m, b.idx);
-  warp_argmax(gv, gi);
-  flags |= __reduce_or_sync(0xffffffffu, a.flags | b.flags);
+  int xs;
+  const Entry r = exchange<CL>(sm, xk, Entry{bv, bi, 0.f, 0.f, f, {0, 0, 0}}, kXArgmax, 0.f,
+                               rank, xs);
+  gv = r.m;
+  gi = r.idx;
+  flags |= r.flags;
 }
 
 // Per-thread state of a node at T > 0.
@@ -276,22 +365,12 @@ struct RunState {
   float cw;   // current weights max(0, e_t(y) - cw p(y)) f; cw = 0: w = e (p not read)
 };
 
-// Warp totals (two per lane) of the current sampling weights -> sm.wtot (warp 0 writes).
+// T > 0: e_t(y) replaces the logits; returns M, S (cluster-wide) and the thread's state.  The
+// totals of e(y) per CTA of the cluster go to sm.ccur.
 template <int CL>
-__device__ __forceinline__ void store_wtot(VerifySmem& sm, DF wa, DF wb) {
-  if (threadIdx.x < 32) {
-    const int l = threadIdx.x;
-    if (2 * l < CL * kVWarps) sm.wtot[2 * l] = wa;
-    if (2 * l + 1 < CL * kVWarps) sm.wtot[2 * l + 1] = wb;
-  }
-}
-
-// T > 0: e_t(y) replaces the logits; returns M, S (cluster-wide) and the thread's state.  The warp
-// totals of e(y) go to sm.wtot.
-template <int CL>
-__device__ void cluster_stats(const Slice& s, float* lbuf, float k, int lflags, int rank,
-                              int& slot, float& M, DF& S, RunState& rs, int& flags,
-                              VerifySmem& sm) {
+__device__ void cluster_stats(const Slice& s, float* lbuf, float k, int lflags, int rank, int& xk,
+                              float& M, DF& S, RunState& rs, int& flags, VerifySmem& sm) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   float4* L4 = reinterpret_cast<float4*>(lbuf + threadIdx.x * s.ch);
   const RunWalk rw(s.ch);
   float m = -INFINITY;
@@ -315,31 +394,31 @@ __device__ void cluster_stats(const Slice& s, float* lbuf, float k, int lflags, 
   const float mw = warp_max_f(m);
   const float g = (m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(m, mw), k));
   const DF sw = warp_sum_df(df_scale(st, g));
-  publish<CL>(sm, slot, rank, WarpPart{mw, 0, sw.hi, sw.lo, lflags, {0, 0, 0}});
-  WarpPart a, b;
-  entries<CL>(sm, slot, WarpPart{-INFINITY, 0, 0.f, 0.f, 0, {0, 0, 0}}, a, b);
-  slot ^= 1;
-  M = warp_max_f(fmaxf(a.m, b.m));
-  const float ga = (a.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(a.m, M), k));
-  const float gb = (b.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(b.m, M), k));
-  const DF wa = df_scale(DF{a.s_hi, a.s_lo}, ga), wb = df_scale(DF{b.s_hi, b.s_lo}, gb);
-  S = warp_sum_df(df_add(wa, wb));
-  flags |= __reduce_or_sync(0xffffffffu, a.flags | b.flags);
-  store_wtot<CL>(sm, wa, wb);
-  const float gM = (mw == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(mw, M), k));
-  rs.f = __fmul_rn(g, gM);
+  int xs;
+  const Entry r = exchange<CL>(sm, xk, Entry{mw, 0, sw.hi, sw.lo, lflags, {0, 0, 0}}, kXMaxSum,
+                               k, rank, xs);
+  M = r.m;
+  S = DF{r.s_hi, r.s_lo};
+  flags |= r.flags;
+  // sampling state of q^(0): thread, warp and CTA totals of e(y)
+  rs.f = (m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(m, M), k));
   rs.tot = df_scale(st, rs.f);
   rs.cw = 0.f;
+  if (wid == 0 && lane < CL) {
+    const Entry& c = sm.cpart[xs][lane];
+    const float fc = (c.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(c.m, M), k));
+    sm.ccur[lane] = df_scale(DF{c.s_hi, c.s_lo}, fc);
+  }
   if (!(S.hi > 0.f) || !(S.hi <= FLT_MAX)) flags |= SPEC_ST_NONFINITE;
 }
 
 // Residual round: returns D = sum_y max(0, e(y) - c p(y)) (cluster-wide; c_t = c / f).  check_p:
-// flag bad draft values.  The thread's total of the new weights goes to `tot`, the warp totals
-// (entries 2 * lane, 2 * lane + 1) to wta, wtb.
+// flag bad draft values.  The thread's total of the new weights goes to `tot`, the warp's to
+// `wt`; `xs` is the slot whose sm.cpart holds the CTA totals.
 template <int CL>
 __device__ DF cluster_residual(const Slice& s, const float* ebuf, const float* pbuf, float c_t,
-                               float f, bool check_p, int lflags, int rank, int& slot, DF& tot,
-                               DF& wta, DF& wtb, int& flags, VerifySmem& sm) {
+                               float f, bool check_p, int lflags, int rank, int& xk, DF& tot,
+                               DF& wt, int& xs, int& flags, VerifySmem& sm) {
   const float4* E4 = reinterpret_cast<const float4*>(ebuf + threadIdx.x * s.ch);
   const float4* P4 = reinterpret_cast<const float4*>(pbuf + threadIdx.x * s.ch);
   CompSum acc;
@@ -360,22 +439,25 @@ __device__ DF cluster_residual(const Slice& s, const float* ebuf, const float* p
   }
   const bool bad = check_p && (pmin < 0.f || !(psum <= FLT_MAX));  // NaN, +Inf or negative p
   tot = df_scale(df_from(acc), f);
-  const DF w = warp_sum_df(tot);
+  wt = warp_sum_df(tot);
   const int wf = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0) | lflags;
-  publish<CL>(sm, slot, rank, WarpPart{0.f, 0, w.hi, w.lo, wf, {0, 0, 0}});
-  WarpPart a, b;
-  entries<CL>(sm, slot, WarpPart{0.f, 0, 0.f, 0.f, 0, {0, 0, 0}}, a, b);
-  slot ^= 1;
-  flags |= __reduce_or_sync(0xffffffffu, a.flags | b.flags);
-  wta = DF{a.s_hi, a.s_lo};
-  wtb = DF{b.s_hi, b.s_lo};
-  return warp_sum_df(df_add(wta, wtb));
+  const Entry r = exchange<CL>(sm, xk, Entry{0.f, 0, wt.hi, wt.lo, wf, {0, 0, 0}}, kXSum, 0.f,
+                               rank, xs);
+  flags |= r.flags;
+  return DF{r.s_hi, r.s_lo};
+}
+
+// The current weights became those of this round: record its CTA totals for a draw.
+template <int CL>
+__device__ __forceinline__ void commit_round_totals(VerifySmem& sm, int xs) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (wid == 0 && lane < CL) sm.ccur[lane] = DF{sm.cpart[xs][lane].s_hi, sm.cpart[xs][lane].s_lo};
 }
 
 // ------------------------------------------------------------------------------------------------
 // inverse-CDF draw: y = min{y : C(y) > u * total}, else the last y with a positive weight
 // ------------------------------------------------------------------------------------------------
-// Over the 32 lanes' values v (DF, in order; incl = their inclusive scan): the first lane whose
+// Over the lanes' values v (DF, in order; incl = their inclusive scan): the first lane whose
 // inclusive prefix exceeds t, with the prefix before it; if none does (or t < 0: "last positive"
 // mode), the last lane with a positive value (-1 if none), and t becomes -1.
 __device__ __forceinline__ int lane_crossing(DF v, DF incl, DF& t, DF& before) {
@@ -402,51 +484,47 @@ __device__ __forceinline__ float weight_at(const float* ebuf, const float* pbuf,
   return __fmul_rn(w, f);
 }
 
-// The drawn token, valid in rank 0 (other CTAs: unspecified), or -1 when every weight is zero.
-// Warp totals come from sm.wtot, thread totals and weights from rs.  Ends with a cluster barrier.
+// Result of a draw: every CTA of the cluster agrees on `writer`, the CTA that holds the crossing
+// (rank 0 if every weight is zero); `tok` is valid there (-1: every weight is zero).
+struct Draw {
+  int writer, tok;
+};
+
+// Levels: CTA of the cluster (sm.ccur, same in every CTA), warp of that CTA (sums of rs.tot),
+// thread of that warp (rs.tot), element of that thread's run.  No exchange: the writer CTA finds
+// the token alone and records the node itself.
 template <int CL>
-__device__ int cluster_draw(const Slice& s, const float* ebuf, const float* pbuf,
-                            const RunState& rs, float u, int rank, VerifySmem& sm) {
+__device__ Draw cluster_draw(const Slice& s, const float* ebuf, const float* pbuf,
+                             const RunState& rs, float u, int rank, VerifySmem& sm) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  __syncthreads();  // sm.wtot (written by warp 0) is visible
-  const DF a = (2 * lane < CL * kVWarps) ? sm.wtot[2 * lane] : DF{0.f, 0.f};
-  const DF b = (2 * lane + 1 < CL * kVWarps) ? sm.wtot[2 * lane + 1] : DF{0.f, 0.f};
-  // level 1: warp of the cluster, two entries per lane (every CTA takes the same decisions)
-  const DF pair = df_add(a, b);
-  const DF incl = warp_scan_df(pair);
-  const DF tot{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+  __syncthreads();  // sm.ccur / sm.wcur are visible
+  // level 1: CTA (lanes 0..7; lanes past CL hold zeros)
+  const DF cv = lane < CL ? sm.ccur[lane] : DF{0.f, 0.f};
+  const DF cincl = warp_scan8_df(cv);
+  const DF tot{__shfl_sync(0xffffffffu, cincl.hi, 7), __shfl_sync(0xffffffffu, cincl.lo, 7)};
   DF t = (tot.hi > 0.f) ? df_scale(tot, u) : DF{-1.f, 0.f};
   DF before;
-  const int L = lane_crossing(pair, incl, t, before);
-  if (L < 0) {  // nothing positive anywhere
-    cluster_barrier<CL>();
-    return -1;
-  }
-  const DF aL{__shfl_sync(0xffffffffu, a.hi, L), __shfl_sync(0xffffffffu, a.lo, L)};
-  const float bL = __shfl_sync(0xffffffffu, b.hi, L);
-  int e;
-  if (t.hi >= 0.f) {
-    const DF after_a = df_add(before, aL);
-    if (df_gt(after_a, t)) {
-      e = 2 * L;
-    } else {
-      e = 2 * L + 1;
-      before = after_a;
-    }
-  } else {
-    e = (bL > 0.f) ? 2 * L + 1 : 2 * L;
-  }
-  if (rank == e / kVWarps && wid == e % kVWarps) {
-    // level 2: the thread of the crossing warp
-    DF tl = (t.hi >= 0.f) ? df_add(t, DF{-before.hi, -before.lo}) : t;
-    DF before2;
-    int Lc = lane_crossing(rs.tot, warp_scan_df(rs.tot), tl, before2);
-    if (Lc < 0) Lc = 31;  // cannot happen with a positive warp total; keeps the index valid
-    // level 3: the elements of that thread's run, 32 at a time, by the whole warp
+  const int cstar = lane_crossing(cv, cincl, t, before);
+  if (cstar < 0) return Draw{0, -1};  // nothing positive anywhere
+  if (rank != cstar) return Draw{cstar, -1};
+  const DF wsum = warp_sum_df(rs.tot);
+  if (lane == 0) sm.wcur[wid] = wsum;
+  __syncthreads();
+  // level 2: warp of this CTA (every warp computes it; one acts)
+  if (t.hi >= 0.f) t = df_add(t, DF{-before.hi, -before.lo});
+  const DF wv = lane < kVWarps ? sm.wcur[lane] : DF{0.f, 0.f};
+  int wstar = lane_crossing(wv, warp_scan8_df(wv), t, before);
+  if (wstar < 0) wstar = kVWarps - 1;  // rounding: the CTA total was positive but no warp's is
+  if (wid == wstar) {
+    // level 3: thread of the crossing warp
+    if (t.hi >= 0.f) t = df_add(t, DF{-before.hi, -before.lo});
+    int Lc = lane_crossing(rs.tot, warp_scan_df(rs.tot), t, before);
+    if (Lc < 0) Lc = 31;
+    // level 4: the elements of that thread's run, 32 at a time, by the whole warp
     const float fL = __shfl_sync(0xffffffffu, rs.f, Lc);
     const float cwL = __shfl_sync(0xffffffffu, rs.cw, Lc);
     const int i0 = (wid * 32 + Lc) * s.ch;
-    const DF t3 = (tl.hi >= 0.f) ? df_add(tl, DF{-before2.hi, -before2.lo}) : tl;
+    const DF t3 = (t.hi >= 0.f) ? df_add(t, DF{-before.hi, -before.lo}) : t;
     int y = -1, last_pos = -1;
     DF carry{0.f, 0.f};
     for (int base = 0; base < s.ch; base += 32) {
@@ -463,17 +541,10 @@ __device__ int cluster_draw(const Slice& s, const float* ebuf, const float* pbuf
       carry = DF{__shfl_sync(0xffffffffu, run.hi, 31), __shfl_sync(0xffffffffu, run.lo, 31)};
     }
     if (y < 0) y = last_pos;
-    const int tok = (y >= 0) ? i0 + y + s.sbase : -1;
-    if (lane == 0) {  // exactly one warp of the cluster writes rank 0's result
-      if constexpr (CL > 1) {
-        dsmem_store_u32(dsmem_addr(&sm.found, 0), (uint32_t)tok);
-      } else {
-        sm.found = tok;
-      }
-    }
+    if (lane == 0) sm.found = (y >= 0) ? i0 + y + s.sbase : -1;
   }
-  cluster_barrier<CL>();
-  return sm.found;
+  __syncthreads();
+  return Draw{cstar, sm.found};
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -517,14 +588,15 @@ __device__ void list_children(int j, int N, VerifySmem& sm) {
   __syncthreads();
 }
 
-// Numerator e(x) = exp((l_x - M) / T) of a child's q^(0): the argument is formed exactly as a
-// double-float, exponentiated by expf on its high part and corrected by (1 + low part).
-__device__ __forceinline__ double child_numerator(float lx, float M, DF invT) {
+// Numerator e(x) = exp((l_x - M) / T) of a child's q^(0), as a double-float: the argument is
+// formed exactly as a double-float, exponentiated by expf on its high part and corrected by
+// (1 + low part).  Below expf's normal range (weights under 2^-126 of the row max) it is 0.
+__device__ __forceinline__ DF child_numerator(float lx, float M, DF invT) {
   const DF d = df_two_sum(lx, -M);
   const DF a = df_mul(d, invT);
-  if (a.hi < -80.f) return exp((double)a.hi + (double)a.lo);  // outside expf's normal range
-  const double e = (double)expf(a.hi);
-  return fma(e, (double)a.lo, e);
+  if (!(a.hi >= -87.f)) return DF{0.f, 0.f};
+  const float e = expf(a.hi);
+  return df_fast_two_sum(e, __fmul_rn(e, a.lo));
 }
 
 struct NodeBufs {
@@ -537,10 +609,10 @@ struct NodeBufs {
 // one node: statistics, sibling tests, residual rounds, bonus if the walk can stop here
 // ------------------------------------------------------------------------------------------------
 // logits_staged: the kernel already issued the copy of this node's logit slice into nb.lbuf.
-// The bonus of the returned record is valid in rank 0.
+// The returned record is complete in CTA `writer` (every CTA gets the same writer).
 template <int CL>
 __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, const NodeBufs& nb,
-                                 bool logits_staged, DF invT_df, float k2, int& slot,
+                                 bool logits_staged, DF invT_df, float k2, int& xk, int& writer,
                                  VerifySmem& sm) {
   const int N = a.N, V = a.V;
   list_children(j, N, sm);
@@ -563,14 +635,15 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   const float u_bonus = __ldg(a.uniforms + (size_t)b * N);
   const int lflags0 = wait_slice(nb.bar_l);
   int flags = 0;  // cluster-uniform: only ever updated from published partials
+  writer = 0;
   NodeStat st;
   st.bonus = -1;
-  st.s = 0.0;
+  st.s_hi = st.s_lo = 0.f;
 
   if (!sampling) {
     float gv;
     int gi;
-    cluster_argmax<CL>(s, nb.lbuf, lflags0, rank, slot, gv, gi, flags, sm);
+    cluster_argmax<CL>(s, nb.lbuf, lflags0, rank, xk, gv, gi, flags, sm);
     if (gi < 0 || gi >= V) gi = 0;  // every value NaN: flagged
     int first = -1, nrej = nk;
     for (int t = 0; t < nk; ++t)
@@ -597,7 +670,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   float M;
   DF S;
   RunState rs;
-  cluster_stats<CL>(s, nb.lbuf, k2, lflags0, rank, slot, M, S, rs, flags, sm);
+  cluster_stats<CL>(s, nb.lbuf, k2, lflags0, rank, xk, M, S, rs, flags, sm);
   // Scalars every thread holds stay double-float: fp64 here is only for the few threads that
   // take a decision or update a numerator.
   DF D = S;
@@ -615,13 +688,11 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   for (int t = 0; t < nk; ++t) {
     const int kid = sm.kids[t];
     if ((int)threadIdx.x == t) {
-      const double px = (double)sm.g_px[t];
-      const double r = (double)sm.g_r[t];
-      const double n = sm.g_n[t];
-      const double Dd = df_to_double(D);
-      sm.decision = (r * px * Dd < n) ? 1 : 0;  // r < min(1, q/p) with q = n / D
+      const DF n = sm.g_n[t];
+      const DF rpD = df_mul(df_two_prod(sm.g_r[t], sm.g_px[t]), D);
+      sm.decision = df_gt(n, rpD) ? 1 : 0;  // r < min(1, q/p) with q = n / D
       if (rank == 0 && a.child_q)
-        a.child_q[(size_t)b * N + kid] = D.hi > 1e-30f ? __fdiv_rn((float)n, D.hi) : (float)(n / Dd);
+        a.child_q[(size_t)b * N + kid] = D.hi > 0.f ? __fdiv_rn(__fadd_rn(n.hi, n.lo), D.hi) : 0.f;
     }
     __syncthreads();
     if (sm.decision) {
@@ -638,19 +709,22 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     }
     const DF c_next = df_add(c, D);
     const float c_t = rs.f > 0.f ? __fdiv_rn(__fadd_rn(c_next.hi, c_next.lo), rs.f) : 0.f;
-    DF tot, wta, wtb;
-    const DF G = cluster_residual<CL>(s, nb.lbuf, nb.pbuf, c_t, rs.f, t == 0, pflags, rank, slot,
-                                      tot, wta, wtb, flags, sm);
+    DF tot, wt;
+    int xs;
+    const DF G = cluster_residual<CL>(s, nb.lbuf, nb.pbuf, c_t, rs.f, t == 0, pflags, rank, xk,
+                                      tot, wt, xs, flags, sm);
     pflags = 0;
     if (G.hi > 0.f) {
-      if ((int)threadIdx.x > t && (int)threadIdx.x < nk)
-        sm.g_n[threadIdx.x] =
-            fmax(fma(-(double)sm.g_px[threadIdx.x], df_to_double(D), sm.g_n[threadIdx.x]), 0.0);
+      if ((int)threadIdx.x > t && (int)threadIdx.x < nk) {  // n <- max(0, n - p(x) D)
+        const DF pD = df_mul(DF{sm.g_px[threadIdx.x], 0.f}, D);
+        const DF nn = df_add(sm.g_n[threadIdx.x], DF{-pD.hi, -pD.lo});
+        sm.g_n[threadIdx.x] = nn.hi > 0.f ? nn : DF{0.f, 0.f};
+      }
       D = G;
       c = c_next;
       rs.tot = tot;
       rs.cw = c_t;
-      store_wtot<CL>(sm, wta, wtb);
+      commit_round_totals<CL>(sm, xs);
     } else {
       frozen = true;
     }
@@ -658,13 +732,17 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   }
   if (probs_staged && !p_waited) wait_slice(nb.bar_p);  // no copy left in flight (not needed)
   const bool bad = (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) != 0;
-  if ((nk == 0 || all_rejected) && !bad)  // the walk can stop here: draw its bonus
-    st.bonus = cluster_draw<CL>(s, nb.lbuf, nb.pbuf, rs, u_bonus, rank, sm);
+  if ((nk == 0 || all_rejected) && !bad) {  // the walk can stop here: draw its bonus
+    const Draw d = cluster_draw<CL>(s, nb.lbuf, nb.pbuf, rs, u_bonus, rank, sm);
+    writer = d.writer;
+    st.bonus = d.tok;
+  }
   if (rank == 0 && a.child_q && (int)threadIdx.x > nrej && (int)threadIdx.x < nk)
     a.child_q[(size_t)b * N + sm.kids[threadIdx.x]] = -1.f;
   st.m = M;
   st.argmax = -1;
-  st.s = df_to_double(S);
+  st.s_hi = S.hi;
+  st.s_lo = S.lo;
   st.first_acc = first;
   st.nrej = nrej;
   st.flags = flags;
@@ -732,11 +810,12 @@ __device__ void write_outputs(const VerifyArgs& a, int b, int bonus, int flags, 
 // terminal.  bar_l_used: whether this CTA already staged a row on nb.bar_l in this launch.
 template <int CL>
 __device__ void walk_sequence_cluster(const VerifyArgs& a, int b, int rank, const NodeBufs& nb,
-                                      bool bar_l_used, float k2, int& slot, VerifySmem& sm) {
+                                      bool bar_l_used, float k2, int& xk, VerifySmem& sm) {
   walk_path(a, b, false, sm);
   const int c = sm.terminal;
   int flags = sm.flags;
   int bonus = -1;
+  int writer = 0;
   if (sm.internal[c]) {
     bonus = sm.st[c].bonus;
   } else {
@@ -748,19 +827,22 @@ __device__ void walk_sequence_cluster(const VerifyArgs& a, int b, int rank, cons
     if (a.T == 0.f) {
       float gv;
       int gi;
-      cluster_argmax<CL>(s, nb.lbuf, lflags, rank, slot, gv, gi, flags, sm);
+      cluster_argmax<CL>(s, nb.lbuf, lflags, rank, xk, gv, gi, flags, sm);
       bonus = (gi < 0 || gi >= a.V) ? 0 : gi;
     } else {
       float M;
       DF S;
       RunState rs;
-      cluster_stats<CL>(s, nb.lbuf, k2, lflags, rank, slot, M, S, rs, flags, sm);
+      cluster_stats<CL>(s, nb.lbuf, k2, lflags, rank, xk, M, S, rs, flags, sm);
       const float u = __ldg(a.uniforms + (size_t)b * a.N);
-      if (!(flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)))
-        bonus = cluster_draw<CL>(s, nb.lbuf, nb.pbuf, rs, u, rank, sm);
+      if (!(flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT))) {
+        const Draw d = cluster_draw<CL>(s, nb.lbuf, nb.pbuf, rs, u, rank, sm);
+        writer = d.writer;
+        bonus = d.tok;
+      }
     }
   }
-  if (rank == 0) write_outputs(a, b, bonus, flags, sm);
+  if (rank == writer) write_outputs(a, b, bonus, flags, sm);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -809,8 +891,12 @@ __global__ void __launch_bounds__(kVThreads)
   if (threadIdx.x == 0) {
     mbar_init(nb.bar_l, 1);
     mbar_init(nb.bar_p, 1);
+    mbar_init(smem_u32(&sm.xbar[0]), 1);
+    mbar_init(smem_u32(&sm.xbar[1]), 1);
     mbar_fence_init();
   }
+  __syncthreads();
+  cluster_arrive_release();  // exchange barriers initialised (waited for before the first exchange)
   griddep_wait();  // the inputs may be produced by the preceding kernel in the stream
   griddep_launch_dependents();
   // small problems process every node: its logit row is needed whatever the tree looks like, so
@@ -820,7 +906,9 @@ __global__ void __launch_bounds__(kVThreads)
     const float* lrow = a.logits + ((size_t)b * N + j) * (size_t)a.V;
     stage_slice(lrow, make_slice(lrow, a.V, rank, CL), nb.lbuf, nb.bar_l, -INFINITY);
   }
-  if (rank == 0 && threadIdx.x == 0) claim_counter(a.counters + b, a.gen);
+  // the claim's round trip overlaps the tree loads (issued by the first threads) instead of
+  // delaying thread 0, which issues the copies
+  if (rank == 0 && threadIdx.x == kVThreads - 1) claim_counter(a.counters + b, a.gen);
   const int bad = load_tree(a, b, sm);  // uniform across the cluster: same tree everywhere
   if (bad) {
     if (j == 0 && rank == 0) {  // one writer per sequence
@@ -836,18 +924,21 @@ __global__ void __launch_bounds__(kVThreads)
       }
     }
     if (early) wait_slice(nb.bar_l);  // no copy left in flight
+    cluster_wait_acquire();
     return;
   }
-  int slot = 0;
+  cluster_wait_acquire();  // every CTA of the cluster can now receive exchanges
+  int xk = 0, writer = 0;
   const bool work = sm.internal[j] || do_leaves;
   NodeStat st;
-  if (work) st = process_node<CL>(a, b, j, rank, nb, early, DF{invT_hi, invT_lo}, k2, slot, sm);
+  if (work)
+    st = process_node<CL>(a, b, j, rank, nb, early, DF{invT_hi, invT_lo}, k2, xk, writer, sm);
 
   // arrival: the last cluster of the sequence to finish walks the tree
   if (do_leaves) {
-    // every possible stop already has its bonus, so rank 0 finishes alone (this cluster's
-    // exchanges are complete: the other CTAs may leave)
-    if (rank != 0) return;
+    // every possible stop already has its bonus, so the writer CTA finishes alone (this
+    // cluster's exchanges are complete: the other CTAs may leave)
+    if (rank != writer) return;
     if (threadIdx.x == 0) {
       a.stats[(size_t)b * N + j] = st;
       sm.is_last = arrive(a.counters + b, a.gen, N) ? 1 : 0;
@@ -859,7 +950,7 @@ __global__ void __launch_bounds__(kVThreads)
     write_outputs(a, b, sm.st[c].bonus, sm.flags | (sm.internal[c] ? 0 : sm.st[c].flags), sm);
     return;
   }
-  if (rank == 0 && threadIdx.x == 0) {
+  if (rank == writer && threadIdx.x == 0) {
     if (work) a.stats[(size_t)b * N + j] = st;
     const int last = arrive(a.counters + b, a.gen, N) ? 1 : 0;
     if constexpr (CL > 1) {
@@ -870,7 +961,7 @@ __global__ void __launch_bounds__(kVThreads)
   }
   cluster_barrier<CL>();
   if (!sm.is_last) return;
-  walk_sequence_cluster<CL>(a, b, rank, nb, work, k2, slot, sm);
+  walk_sequence_cluster<CL>(a, b, rank, nb, work, k2, xk, sm);
   cluster_barrier<CL>();  // keep shared memory alive for remote stores
 }
 
