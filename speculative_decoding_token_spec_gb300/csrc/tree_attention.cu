@@ -42,7 +42,7 @@
 
 namespace spectree {
 
-constexpr int kTileKeys = 64;
+constexpr int kChunkKeys = 128;  // keys per K/V chunk: one ring slot, one pipeline step
 constexpr int kMaxSplits = 8;  // portable cluster size
 
 struct AttnKParams {
@@ -81,22 +81,23 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 template <int D>
 struct TcCfg {
   static constexpr int NB = D / 64;               // 64-dim swizzle boxes per row
-  static constexpr int KEYS = kTileKeys;          // keys per tile
-  static constexpr int BOX = KEYS * 128;          // [64 keys x 64 dims] bf16 box: 8 KB
-  static constexpr int TILE = 2 * NB * BOX;       // K + V of one tile
+  static constexpr int KEYS = kChunkKeys;         // keys per chunk
+  static constexpr int BOX = KEYS * 128;          // [128 keys x 64 dims] bf16 box: 16 KB
+  static constexpr int TILE = 2 * NB * BOX;       // K + V of one chunk
   static constexpr int RING = 192 * 1024;         // K/V ring
-  static constexpr int SLOTS = RING / TILE;       // 6 (D = 128) or 12 (D = 64) tiles
+  static constexpr int SLOTS = RING / TILE;       // 3 (D = 128) or 6 (D = 64) chunks
   static constexpr int QBOX = 128 * 128;          // [128 rows x 64 dims] bf16: 16 KB
   static constexpr int OFF_Q = RING;
   static constexpr int OFF_BAR = OFF_Q + NB * QBOX;
   static constexpr int SMEM = 1024 /*alignment slack*/ + OFF_BAR + 512;
-  // TMEM columns: S[0] 0..127, S[1] 128..255, O 256..256+D, P[buffer][key group] 384 + 64 b + 32 g
-  // (64 bf16 keys packed in 32 columns)
+  // TMEM columns: S[0] 0..127, S[1] 128..255 (one chunk each: 128 keys in fp32); P of a chunk
+  // overwrites columns 0..63 of its S buffer (128 bf16 keys packed in pairs; key group g in
+  // columns 32 g..32 g + 31); O[parity] at 256 + 128 parity (the two softmax warp sets take
+  // alternate chunks, each with its own accumulator).
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COLS = 128;
   static constexpr uint32_t O_COL = 256;
-  static constexpr uint32_t P_COL = 384;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 320;
   static constexpr int RSTRIDE = D + 4;           // floats per exchanged row (padding: no bank clash)
   static constexpr int STAGE_OFF = RING / 2;      // in-CTA key-group exchange, after the combine
                                                   // receive area
@@ -112,7 +113,7 @@ __host__ __device__ inline int owned_rows(int kg, int splits) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) tree_attn_kernel(
+__global__ void __launch_bounds__(320, 1) tree_attn_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const AttnKParams p) {
   using C = TcCfg<D>;
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(192, 1) tree_attn_kernel(
   uint8_t* q_s = base + C::OFF_Q;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::OFF_BAR);
   const int B_FULL = 0, B_EMPTY = C::SLOTS, B_SFULL = 2 * C::SLOTS, B_SFREE = 2 * C::SLOTS + 2,
-            B_PFULL = 2 * C::SLOTS + 4, B_PV = 2 * C::SLOTS + 6, B_DONE = 2 * C::SLOTS + 7;
+            B_PFULL = 2 * C::SLOTS + 4, B_PV = 2 * C::SLOTS + 6, B_DONE = 2 * C::SLOTS + 8;
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -148,17 +149,41 @@ __global__ void __launch_bounds__(192, 1) tree_attn_kernel(
   }
   griddep_wait();  // every global access below may depend on the preceding kernel in the stream
   griddep_launch_dependents();
+  // The small inputs go out first: requests issued after a split's K/V stream wait behind it.
+  // Q: the CTA's distinct query rows (64 with key groups, else 128), two rows per warp instruction
+  // (coalesced); rows past R are zeros.
+  constexpr int QCH = D / 8;  // 16-byte chunks per row
+  constexpr int QIT = 128 * QCH / 256;  // per softmax thread
+  const int qrows = 128 / kg;
+  uint4 qv[QIT];
+  if (warp >= 2) {
+#pragma unroll
+    for (int k = 0; k < QIT; ++k) {
+      const int idx = (tid - 64) + k * 256, row = idx / QCH, ch = idx % QCH;
+      const int qrow = rb * 128 + row;
+      qv[k] = make_uint4(0, 0, 0, 0);
+      if (row < qrows && qrow < p.R) {
+        const int i = qrow / g, hl = qrow % g;
+        qv[k] = __ldg(reinterpret_cast<const uint4*>(
+                          p.q + (((size_t)b * N + i) * p.Hq + kvh * g + hl) * D) + ch);
+      }
+    }
+  }
+  int parent_i = 0;
+  if (tid >= 64 && tid < 64 + N) parent_i = __ldg(p.parent + (size_t)b * N + (tid - 64));
+  const int L = __ldg(p.prefix_lens + b);
+  if (warp != 1) named_bar_sync(2, 288);  // those loads are issued before the K/V copies
   if (tid == 0) {
     for (int i = 0; i < C::SLOTS; ++i) {
       mbar_init(bar(B_FULL + i), 1);
       mbar_init(bar(B_EMPTY + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 2; ++i) {  // [parity of the chunk]
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SFREE + i), 4);  // one arrival per softmax warp
+      mbar_init(bar(B_SFREE + i), 4);  // one arrival per softmax warp of that parity
       mbar_init(bar(B_PFULL + i), 4);
+      mbar_init(bar(B_PV + i), 1);
     }
-    mbar_init(bar(B_PV), 1);
     mbar_init(bar(B_DONE), 1);
     mbar_fence_init();
     abort_s = 0;
@@ -176,23 +201,24 @@ __global__ void __launch_bounds__(192, 1) tree_attn_kernel(
     }
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_s), C::TMEM_COLS);
-  if (tid >= 64 && tid < 64 + N) par_s[tid - 64] = __ldg(p.parent + (size_t)b * N + (tid - 64));
-  const int L = __ldg(p.prefix_lens + b);
+  if (tid >= 64 && tid < 64 + N) par_s[tid - 64] = parent_i;
 
   // softmax threads: MMA row r (TMEM lane r), key group gi, query row qrow of this KV head
   const int r = 32 * (warp & 3) + lane;
+  const int par = (warp - 2) >> 2;  // softmax warps: parity of the chunks this warp takes
   const int gi = (kg == 2) ? (r >> 6) : 0;
   const int qloc = (kg == 2) ? (r & 63) : r;  // row within this CTA's block of query rows
   const int qrow = rb * 128 + qloc;
   const bool live = qrow < p.R;
-  if (warp >= 2) {  // Q row -> swizzled shared memory (zeros for rows past R)
-    const int i = live ? qrow / g : 0, hl = live ? qrow % g : 0;
-    const uint4* src =
-        reinterpret_cast<const uint4*>(p.q + (((size_t)b * N + i) * p.Hq + kvh * g + hl) * D);
+  if (warp >= 2) {  // Q rows -> swizzled shared memory (key groups: rows r and r + 64 alike)
 #pragma unroll
-    for (int ch = 0; ch < D / 8; ++ch) {
-      const uint4 v = live ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(q_s + (ch >> 3) * C::QBOX + swz(r, ch & 7)) = v;
+    for (int k = 0; k < QIT; ++k) {
+      const int idx = (tid - 64) + k * 256, row = idx / QCH, ch = idx % QCH;
+      if (row < qrows) {
+        *reinterpret_cast<uint4*>(q_s + (ch >> 3) * C::QBOX + swz(row, ch & 7)) = qv[k];
+        if (kg == 2)
+          *reinterpret_cast<uint4*>(q_s + (ch >> 3) * C::QBOX + swz(row + 64, ch & 7)) = qv[k];
+      }
     }
     fence_async_smem();  // Q is read by the tensor cores (async proxy)
   }
@@ -225,7 +251,7 @@ __global__ void __launch_bounds__(192, 1) tree_attn_kernel(
   const int ntiles = (total_keys + C::KEYS - 1) / C::KEYS;
   const int t_end = min(ntiles, t_begin + tps);
   const int my_tiles = max(0, t_end - t_begin);
-  const int U = (my_tiles + kg - 1) / kg;  // pipeline steps (kg tiles each)
+  const int U = my_tiles;  // pipeline steps: one chunk each
 
   auto wait = [&](int i, uint32_t parity) -> bool {
     if (abort_s) return false;
@@ -260,9 +286,10 @@ __global__ void __launch_bounds__(192, 1) tree_attn_kernel(
           if (abort_s || it >= my_tiles) mbar_wait(bar(B_FULL + it % C::SLOTS), (it / C::SLOTS) & 1);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: QK of step u once its tiles landed and S[u % 2] is free (and
-    // the PV of step u - 2, which read the P buffer step u will rewrite, was issued before it);
-    // PV of step u once its P is written.  Whichever is ready goes first.
+    // ---------------- MMA issuer: QK of step u once its chunk landed and S[u % 2] is free (and
+    // the PV of step u - 2, which read the P that step u overwrites, was issued before it: the
+    // tensor pipe runs a CTA's MMAs in issue order); PV of step u once its P is written.
+    // Whichever is ready goes first.
     if (lane == 0 && my_tiles > 0) {
       constexpr uint32_t IQK = idesc_bf16_f32(128, C::KEYS, false);
       constexpr uint32_t IPV = idesc_bf16_f32(128, D, true);
@@ -272,23 +299,21 @@ __global__ void __launch_bounds__(192, 1) tree_attn_kernel(
       while (np < U) {
         bool progressed = false;
         if (nq < U && nq <= np + 1) {
-          const int t0 = nq * kg, nt = min(kg, my_tiles - t0);
-          bool rdy = nq < 2 || mbar_test(bar(B_SFREE + (nq & 1)), ((nq >> 1) - 1) & 1);
-          for (int k = 0; k < nt && rdy; ++k)
-            rdy = mbar_test(bar(B_FULL + (t0 + k) % C::SLOTS), ((t0 + k) / C::SLOTS) & 1);
+          const int sl = nq % C::SLOTS;
+          const bool rdy =
+              (nq < 2 || mbar_test(bar(B_SFREE + (nq & 1)), ((nq >> 1) - 1) & 1)) &&
+              mbar_test(bar(B_FULL + sl), (nq / C::SLOTS) & 1);
           if (rdy) {
             tc_fence_after();
-            for (int k = 0; k < nt; ++k) {
-              const uint32_t k_addr = smem_u32(ring + ((t0 + k) % C::SLOTS) * C::TILE);
-              const uint32_t d = tmem + (uint32_t)((nq & 1) * C::S_COLS + k * C::KEYS);
+            const uint32_t k_addr = smem_u32(ring + sl * C::TILE);
+            const uint32_t d = tmem + (uint32_t)((nq & 1) * C::S_COLS);
 #pragma unroll
-              for (int ks = 0; ks < D / 16; ++ks) {
-                const uint64_t ad =
-                    smem_desc_sw128(q_addr + (ks >> 2) * C::QBOX + (ks & 3) * 32, 16, 1024);
-                const uint64_t bd =
-                    smem_desc_sw128(k_addr + (ks >> 2) * C::BOX + (ks & 3) * 32, 16, 1024);
-                tc_mma_bf16(d, ad, bd, IQK, ks > 0 ? 1u : 0u);
-              }
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint64_t ad =
+                  smem_desc_sw128(q_addr + (ks >> 2) * C::QBOX + (ks & 3) * 32, 16, 1024);
+              const uint64_t bd =
+                  smem_desc_sw128(k_addr + (ks >> 2) * C::BOX + (ks & 3) * 32, 16, 1024);
+              tc_mma_bf16(d, ad, bd, IQK, ks > 0 ? 1u : 0u);
             }
             tc_commit(bar(B_SFULL + (nq & 1)));
             ++nq;
@@ -297,20 +322,17 @@ __global__ void __launch_bounds__(192, 1) tree_attn_kernel(
         }
         if (np < nq && mbar_test(bar(B_PFULL + (np & 1)), (np >> 1) & 1)) {
           tc_fence_after();
-          const int t0 = np * kg, nt = min(kg, my_tiles - t0);
-          const uint32_t p_tm = tmem + C::P_COL + (uint32_t)((np & 1) * 64);
-          for (int k = 0; k < nt; ++k) {
-            const int s = (t0 + k) % C::SLOTS;
-            const uint32_t v_addr = smem_u32(ring + s * C::TILE + C::NB * C::BOX);
+          const int sl = np % C::SLOTS;
+          const uint32_t p_tm = tmem + (uint32_t)((np & 1) * C::S_COLS);
+          const uint32_t o_tm = tmem + C::O_COL + (uint32_t)((np & 1) * 128);
+          const uint32_t v_addr = smem_u32(ring + sl * C::TILE + C::NB * C::BOX);
 #pragma unroll
-            for (int kk = 0; kk < C::KEYS / 16; ++kk) {
-              const uint64_t bd = smem_desc_sw128(v_addr + kk * 2048, C::BOX, 1024);
-              tc_mma_bf16_ts(tmem + C::O_COL, p_tm + (uint32_t)(k * 32 + kk * 8), bd, IPV,
-                             (np > 0 || k > 0 || kk > 0) ? 1u : 0u);
-            }
-            tc_commit(bar(B_EMPTY + s));  // the tile's slot is free once these MMAs complete
+          for (int kk = 0; kk < C::KEYS / 16; ++kk) {
+            const uint64_t bd = smem_desc_sw128(v_addr + kk * 2048, C::BOX, 1024);
+            tc_mma_bf16_ts(o_tm, p_tm + (uint32_t)(kk * 8), bd, IPV, (np > 1 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(bar(B_PV));
+          tc_commit(bar(B_EMPTY + sl));  // the chunk's slot is free once these MMAs complete
+          tc_commit(bar(B_PV + (np & 1)));
           ++np;
           progressed = true;
         }
@@ -327,47 +349,35 @@ __global__ void __launch_bounds__(192, 1) tree_attn_kernel(
       mbar_wait(bar(B_DONE), 0);
     }
   } else {
-    // ---------------- softmax: one MMA row per thread
+    // ---------------- softmax: one MMA row per thread; warps 2..5 take the even chunks and
+    // warps 6..9 the odd ones (each set covers all 128 TMEM lanes).  With key groups a row covers
+    // one 64-key half of each chunk (half gi); otherwise both halves (the second one is read twice:
+    // first for the max, then again for the exponentials, so only 64 scores are live at a time).
     const int node = min(qrow / g, N - 1);
     const unsigned long long anc = anc_s[node];
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t o_col = C::O_COL + (uint32_t)(par * 128);
     const float sc = p.scale_log2;
-    const int tg = (kg == 2) ? (r & 63) : r;  // thread index within the key group
-    const int gthreads = 128 / kg;
-    if (kg == 2) {  // the other key group's P columns of this row stay zero in both buffers
-      float z[32];
+    const int tp = 32 * ((warp - 2) & 3) + lane;  // 0..127 within this parity's warps
+    const int nh = 2 / kg;                        // 64-key halves per row per chunk
+    const int h0 = (kg == 2) ? gi : 0;
+    float zero32[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) z[c] = 0.f;
-      tmem_st32(lane_base + C::P_COL + (uint32_t)((1 - gi) * 32), z);
-      tmem_st32(lane_base + C::P_COL + (uint32_t)(64 + (1 - gi) * 32), z);
-      tmem_wait_st();
-    }
-    for (int u = 0; u < U; ++u) {
-      const int t = u * kg + gi;  // this row's tile (>= my_tiles: past the split, all masked)
-      if (!__all_sync(0xffffffffu, wait(B_SFULL + (u & 1), (u >> 1) & 1))) {
-        ok_rows = false;
-        break;
-      }
-      tc_fence_after();
-      float xa[32], xb[32];
-      const uint32_t scol = (uint32_t)((u & 1) * C::S_COLS + gi * C::KEYS);
+    for (int c = 0; c < 32; ++c) zero32[c] = 0.f;
+    // visibility of the 64 keys key0..key0+63 (bit c: key key0 + c): the prefix part, then the
+    // tree slots L + j of the node's ancestors j.  One code path for every chunk.
+    auto visible = [&](int key0) -> unsigned long long {
+      const int pre = L - key0;
+      unsigned long long vis = pre >= 64 ? ~0ull : (pre <= 0 ? 0ull : (1ull << pre) - 1ull);
+      const int j0 = key0 - L;
+      if (j0 > -64 && j0 < N) vis |= j0 >= 0 ? (anc >> j0) : (anc << -j0);
+      return vis;
+    };
+    auto load_masked = [&](uint32_t scol, unsigned long long vis, float (&xa)[32],
+                           float (&xb)[32]) -> float {
       tmem_ld32(lane_base + scol, xa);
       tmem_ld32(lane_base + scol + 32, xb);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SFREE + (u & 1)));  // S[u % 2] may be overwritten
-
-      // visibility of the tile's 64 keys (bit c: key key0 + c): the prefix part, then the
-      // tree slots L + j of the node's ancestors j.  One code path for every tile.
-      const int key0 = (t_begin + t) * C::KEYS;
-      unsigned long long vis = 0;
-      if (t < my_tiles) {
-        const int pre = L - key0;
-        vis = pre >= 64 ? ~0ull : (pre <= 0 ? 0ull : (1ull << pre) - 1ull);
-        const int j0 = key0 - L;
-        if (j0 > -64 && j0 < N) vis |= j0 >= 0 ? (anc >> j0) : (anc << -j0);
-      }
       const uint32_t vlo = (uint32_t)vis, vhi = (uint32_t)(vis >> 32);
       float mx = -INFINITY;
 #pragma unroll
@@ -376,6 +386,20 @@ __global__ void __launch_bounds__(192, 1) tree_attn_kernel(
         xb[c] = ((vhi >> c) & 1u) ? xb[c] : -INFINITY;
         mx = fmaxf(mx, fmaxf(xa[c], xb[c]));
       }
+      return mx;
+    };
+    for (int u = par; u < U; u += 2) {
+      if (!__all_sync(0xffffffffu, wait(B_SFULL + (u & 1), (u >> 1) & 1))) {
+        ok_rows = false;
+        break;
+      }
+      tc_fence_after();
+      const int ckey0 = (t_begin + u) * C::KEYS;
+      const uint32_t scol0 = (uint32_t)((u & 1) * C::S_COLS);
+      float xa[32], xb[32];
+      float mx = -INFINITY;
+      if (nh == 2) mx = load_masked(scol0 + 64, visible(ckey0 + 64), xa, xb);
+      mx = fmaxf(mx, load_masked(scol0 + 64 * h0, visible(ckey0 + 64 * h0), xa, xb));
       const float mt = mx * sc;  // scale > 0
       const bool raise = mt > m_used + 8.f;
       float factor = 1.f;
@@ -384,128 +408,179 @@ __global__ void __launch_bounds__(192, 1) tree_attn_kernel(
         m_used = mt;
       }
       const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-      float rs0 = 0.f, rs1 = 0.f;
-      float pk[32];  // P as bf16 pairs (bit patterns), key 2c in the low half of column c
+      float rs = 0.f;
+      for (int hh = 0; hh < nh; ++hh) {
+        if (hh == 1) load_masked(scol0 + 64, visible(ckey0 + 64), xa, xb);
+        float rs0 = 0.f, rs1 = 0.f;
+        float pk[32];  // P as bf16 pairs (bit patterns), key 2c in the low half of column c
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float a0 = ex2_approx(fmaf(xa[2 * c], sc, neg_m));
-        const float a1 = ex2_approx(fmaf(xa[2 * c + 1], sc, neg_m));
-        const float b0 = ex2_approx(fmaf(xb[2 * c], sc, neg_m));
-        const float b1 = ex2_approx(fmaf(xb[2 * c + 1], sc, neg_m));
-        rs0 += a0 + a1;
-        rs1 += b0 + b1;
-        pk[c] = __uint_as_float(pack_bf16(a0, a1));
-        pk[16 + c] = __uint_as_float(pack_bf16(b0, b1));
+        for (int c = 0; c < 16; ++c) {
+          const float a0 = ex2_approx(fmaf(xa[2 * c], sc, neg_m));
+          const float a1 = ex2_approx(fmaf(xa[2 * c + 1], sc, neg_m));
+          const float b0 = ex2_approx(fmaf(xb[2 * c], sc, neg_m));
+          const float b1 = ex2_approx(fmaf(xb[2 * c + 1], sc, neg_m));
+          rs0 += a0 + a1;
+          rs1 += b0 + b1;
+          pk[c] = __uint_as_float(pack_bf16(a0, a1));
+          pk[16 + c] = __uint_as_float(pack_bf16(b0, b1));
+        }
+        rs += rs0 + rs1;
+        // P over the scores already read (columns 0..63 of this lane; key group g at 32 g)
+        tmem_st32(lane_base + scol0 + (uint32_t)((h0 + hh) * 32), pk);
       }
-      l = l * factor + (rs0 + rs1);
-      tmem_st32(lane_base + C::P_COL + (uint32_t)((u & 1) * 64 + gi * 32), pk);
-      // The tile holding the last key L + N - 1: V rows past it hold whatever the cache holds
+      if (kg == 2) tmem_st32(lane_base + scol0 + (uint32_t)((1 - gi) * 32), zero32);
+      l = l * factor + rs;
+      // The chunk holding the last key L + N - 1: V rows past it hold whatever the cache holds
       // there (possibly NaN); their P is 0, but 0 * NaN is not, so zero those rows.
-      if (t < my_tiles && key0 + C::KEYS > total_keys) {
-        const int s = t % C::SLOTS;
-        if (__all_sync(0xffffffffu, wait(B_FULL + s, (t / C::SLOTS) & 1))) {
-          const int nv = total_keys - key0;  // 1..63 valid keys
+      if (ckey0 + C::KEYS > total_keys) {
+        const int sl = u % C::SLOTS;
+        if (__all_sync(0xffffffffu, wait(B_FULL + sl, (u / C::SLOTS) & 1))) {
+          const int nv = total_keys - ckey0;  // 1..127 valid keys
           const int units = C::NB * (C::KEYS - nv) * 8;
-          for (int w = tg; w < units; w += gthreads) {
+          for (int w = tp; w < units; w += 128) {
             const int bx = w / ((C::KEYS - nv) * 8), rem = w % ((C::KEYS - nv) * 8);
-            *reinterpret_cast<uint4*>(ring + s * C::TILE + (C::NB + bx) * C::BOX +
+            *reinterpret_cast<uint4*>(ring + sl * C::TILE + (C::NB + bx) * C::BOX +
                                       (nv + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_async_smem();  // the zeros are read by the tensor cores (async proxy)
         }
       }
-      // O rescale (only after the first step, only if some row of this warp raised its max)
-      if (u > 0 && __any_sync(0xffffffffu, raise)) {
-        if (__all_sync(0xffffffffu, wait(B_PV, (u - 1) & 1))) {
+      // O rescale (only if this parity accumulated before and some row of this warp raised its
+      // max): after the PV of step u - 2, the last one into O[parity], completed
+      if (u >= 2 && __any_sync(0xffffffffu, raise)) {
+        if (__all_sync(0xffffffffu, wait(B_PV + par, ((u >> 1) - 1) & 1))) {
           tc_fence_after();
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             float o[32];
-            tmem_ld32(lane_base + C::O_COL + c0, o);
+            tmem_ld32(lane_base + o_col + c0, o);
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] *= factor;
-            tmem_st32(lane_base + C::O_COL + c0, o);
+            tmem_st32(lane_base + o_col + c0, o);
           }
         }
       }
       tmem_wait_st();  // P (and a rescaled O) are in TMEM before the PV MMA reads them
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL + (u & 1)));
+      if (lane == 0) {
+        mbar_arrive(bar(B_SFREE + (u & 1)));  // QK of step u + 2 may overwrite S[u % 2] (and P
+                                              // once PV of step u, issued before it, has run)
+        mbar_arrive(bar(B_PFULL + (u & 1)));
+      }
     }
-    if (ok_rows && U > 0) ok_rows = __all_sync(0xffffffffu, wait(B_PV, (U - 1) & 1));
+    // the last PV into each accumulator has completed (the combine reads both)
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (ok_rows && U > q)
+        ok_rows = __all_sync(0xffffffffu, wait(B_PV + q, ((U - 1 - q) >> 1) & 1));
     if (ok_rows && U > 0) tc_fence_after();
   }
 
   // ---------------- combine across the cluster (all threads of every CTA take part)
-  // Partial of a row: (m, l, O) with m = NaN after a timeout and l = 0 when it saw no key.
+  // A lane's two accumulators (even and odd chunks) merge first; with key groups, lanes r and
+  // r + 64 (the same query over different keys) then merge too.  Partial: (m, l, O) with m = NaN
+  // after a timeout and l = 0 when it saw no key (its O is then never read).
   const int QO = owned_rows(kg, S);
   // [S][QO][RSTRIDE] partial rows, then one trash row that rows without data are pushed into (so
   // the push has no branch), then the (m, l) pairs [S][QO].  The ring is idle now.
   float* recv_o = reinterpret_cast<float*>(ring);
   float2* recv_ml = reinterpret_cast<float2*>(recv_o + ((size_t)S * QO + 1) * C::RSTRIDE);
-  // key groups (kg == 2): rows r and r + 64 hold the same query over different keys.  Each of the
-  // two threads combines and pushes half of the columns; the other half of its own O row goes to
-  // the partner through shared memory.
-  float* stage = reinterpret_cast<float*>(ring + C::STAGE_OFF);   // [64][RSTRIDE]
-  float2* stage_ml = reinterpret_cast<float2*>(stage + 64 * C::RSTRIDE);  // [2][64]
-  const bool pushes_o = ok_rows && U > 0;  // warp-uniform: TMEM loads are warp-collective
+  // in-CTA exchange: the key-group quarter rows [64][RSTRIDE], the per-(parity, lane) states
+  // [2][128] and the per-lane merged states [128]
+  float* stage = reinterpret_cast<float*>(ring + C::STAGE_OFF);
+  float2* stage_ml = reinterpret_cast<float2*>(stage + 64 * C::RSTRIDE);
+  float2* stage_lm = stage_ml + 256;
   const float m_own = ok_rows ? (l > 0.f ? m_used : -INFINITY) : NAN;
   const float l_own = (ok_rows && l > 0.f) ? l : 0.f;
   cluster_arrive_release();  // every CTA of the cluster is done with its ring (TMA copies drained)
   cluster_wait_acquire();    // and its MMAs
-  if (warp >= 2 && kg == 2) {
-    stage_ml[gi * 64 + qloc] = make_float2(m_own, l_own);
-    if (pushes_o) {
-      const int c_give = (1 - gi) * (D / 2);
-#pragma unroll 1
-      for (int c0 = c_give; c0 < c_give + D / 2; c0 += 32) {
-        float o[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + C::O_COL + c0, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 32; c += 4)
-          *reinterpret_cast<float4*>(stage + qloc * C::RSTRIDE + c0 + c) =
-              make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-      }
-    }
-    named_bar_sync(1, 128);  // the four softmax warps
-  }
   if (warp >= 2) {
-    // this CTA's partial of the row: both key groups merged (kg == 2) or the row itself
-    const float2 other = kg == 2 ? stage_ml[(1 - gi) * 64 + qloc] : make_float2(-INFINITY, 0.f);
-    const bool timeout = isnan(m_own) || isnan(other.x);
-    const float mc = fmaxf(l_own > 0.f ? m_own : -INFINITY, other.y > 0.f ? other.x : -INFINITY);
-    const float f_own = l_own > 0.f ? ex2_approx(m_own - mc) : 0.f;
-    const float f_oth = other.y > 0.f ? ex2_approx(other.x - mc) : 0.f;
-    const float lc = l_own * f_own + other.y * f_oth;
-    const bool has = !timeout && lc > 0.f;
+    stage_ml[par * 128 + r] = make_float2(m_own, l_own);
+    named_bar_sync(1, 256);  // the eight softmax warps
+    const uint32_t lane_tm = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const float2 s0 = stage_ml[r], s1 = stage_ml[128 + r];
+    const bool tmo = isnan(s0.x) || isnan(s1.x);
+    const bool use0 = s0.y > 0.f, use1 = s1.y > 0.f;
+    const float mc = fmaxf(use0 ? s0.x : -INFINITY, use1 ? s1.x : -INFINITY);
+    const float f0 = use0 ? ex2_approx(s0.x - mc) : 0.f;
+    const float f1 = use1 ? ex2_approx(s1.x - mc) : 0.f;
+    const float lc = s0.y * f0 + s1.y * f1;
+    // this lane's merged O over columns c0..c0+15 (an accumulator without keys is never read: it
+    // may hold anything)
+    auto merged16 = [&](int c0, float (&o)[16]) {
+      float a0[16], a1[16];
+      tmem_ld16(lane_tm + C::O_COL + (uint32_t)c0, a0);
+      tmem_ld16(lane_tm + C::O_COL + 128u + (uint32_t)c0, a1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 16; ++k) o[k] = (use0 ? a0[k] * f0 : 0.f) + (use1 ? a1[k] * f1 : 0.f);
+    };
     const int owner = qloc % S, ql = qloc / S;
-    if (live && gi == 0)
-      dsmem_store_v2(dsmem_addr(recv_ml + (size_t)split * QO + ql, owner),
-                     __float_as_uint(timeout ? NAN : (has ? mc : -INFINITY)),
-                     __float_as_uint(has ? lc : 0.f));
-    if (pushes_o) {
+    if (kg == 2) {
+      // columns in quarters: the thread of (key group g, parity p) merges and pushes quarter
+      // 2 g + p, and hands its lane's values of quarter 2 (1 - g) + p to the other group
+      constexpr int Q4 = D / 4;
+      const int my_q4 = 2 * gi + par, give_q4 = 2 * (1 - gi) + par;
+      if (par == 0) stage_lm[r] = make_float2(tmo ? NAN : mc, lc);
+#pragma unroll 1
+      for (int c0 = give_q4 * Q4; c0 < (give_q4 + 1) * Q4; c0 += 16) {
+        float o[16];
+        merged16(c0, o);
+#pragma unroll
+        for (int k = 0; k < 16; k += 4)
+          *reinterpret_cast<float4*>(stage + qloc * C::RSTRIDE + c0 + k) =
+              make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+      }
+      named_bar_sync(1, 256);
+      const float2 oth = stage_lm[(1 - gi) * 64 + qloc];
+      const bool tmo2 = tmo || isnan(oth.x);
+      const float M2 = fmaxf(lc > 0.f ? mc : -INFINITY, oth.y > 0.f ? oth.x : -INFINITY);
+      const float g_own = lc > 0.f ? ex2_approx(mc - M2) : 0.f;
+      const float g_oth = oth.y > 0.f ? ex2_approx(oth.x - M2) : 0.f;
+      const float L2 = lc * g_own + oth.y * g_oth;
+      const bool has = !tmo2 && L2 > 0.f;
+      if (live && gi == 0 && par == 0)
+        dsmem_store_v2(dsmem_addr(recv_ml + (size_t)split * QO + ql, owner),
+                       __float_as_uint(tmo2 ? NAN : (has ? M2 : -INFINITY)),
+                       __float_as_uint(has ? L2 : 0.f));
       const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
       const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE, owner);
-      const int c_lo = gi * (D / 2);  // kg == 1: gi == 0 and the whole row
 #pragma unroll 1
-      for (int c0 = c_lo; c0 < c_lo + D / kg; c0 += 32) {
-        float o[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + C::O_COL + c0, o);
-        tmem_wait_ld();
-        const float* st = stage + qloc * C::RSTRIDE + c0;  // not read when f_oth == 0
+      for (int c0 = my_q4 * Q4; c0 < (my_q4 + 1) * Q4; c0 += 16) {
+        float o[16];
+        merged16(c0, o);
+        const float* st = stage + qloc * C::RSTRIDE + c0;  // ignored when g_oth == 0
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 pv = f_oth != 0.f ? *reinterpret_cast<const float4*>(st + c)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-          dsmem_store_v4(dst + (c0 + c) * 4,
-                         make_uint4(__float_as_uint(fmaf(o[c], f_own, pv.x * f_oth)),
-                                    __float_as_uint(fmaf(o[c + 1], f_own, pv.y * f_oth)),
-                                    __float_as_uint(fmaf(o[c + 2], f_own, pv.z * f_oth)),
-                                    __float_as_uint(fmaf(o[c + 3], f_own, pv.w * f_oth))));
+        for (int k = 0; k < 16; k += 4) {
+          const float4 sv = *reinterpret_cast<const float4*>(st + k);
+          const float4 pv = g_oth != 0.f ? sv : make_float4(0.f, 0.f, 0.f, 0.f);
+          dsmem_store_v4(dst + (c0 + k) * 4,
+                         make_uint4(__float_as_uint(fmaf(o[k], g_own, pv.x * g_oth)),
+                                    __float_as_uint(fmaf(o[k + 1], g_own, pv.y * g_oth)),
+                                    __float_as_uint(fmaf(o[k + 2], g_own, pv.z * g_oth)),
+                                    __float_as_uint(fmaf(o[k + 3], g_own, pv.w * g_oth))));
         }
+      }
+    } else {
+      // no key groups: the thread of parity p pushes half p of its row's columns
+      const bool has = !tmo && lc > 0.f;
+      if (live && par == 0)
+        dsmem_store_v2(dsmem_addr(recv_ml + (size_t)split * QO + ql, owner),
+                       __float_as_uint(tmo ? NAN : (has ? mc : -INFINITY)),
+                       __float_as_uint(has ? lc : 0.f));
+      const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
+      const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE, owner);
+#pragma unroll 1
+      for (int c0 = par * (D / 2); c0 < (par + 1) * (D / 2); c0 += 16) {
+        float o[16];
+        merged16(c0, o);
+#pragma unroll
+        for (int k = 0; k < 16; k += 4)
+          dsmem_store_v4(dst + (c0 + k) * 4,
+                         make_uint4(__float_as_uint(o[k]), __float_as_uint(o[k + 1]),
+                                    __float_as_uint(o[k + 2]), __float_as_uint(o[k + 3])));
       }
     }
   }
@@ -591,7 +666,7 @@ static bool make_kv_map(CUtensorMap* m, const void* ptr, int D, long long rows) 
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, kTileKeys};
+  cuuint32_t box[2] = {64, kChunkKeys};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -664,7 +739,7 @@ bool attn_plan(int B, int N, int Hq, int Hkv, int D, int Lmax, int num_sms, Attn
   const int R = N * (Hq / Hkv);
   plan->kg = R <= 64 ? 2 : 1;
   plan->row_blocks = plan->kg == 2 ? 1 : (R + 127) / 128;
-  plan->tiles = (Lmax + kTileKeys - 1) / kTileKeys;
+  plan->tiles = (Lmax + kChunkKeys - 1) / kChunkKeys;
   const long long units = (long long)B * Hkv * plan->row_blocks;
   const int sms = num_sms > 0 ? num_sms : 148;
   // cost = waves x (pipeline steps + fixed set-up / combine cost of about three steps)
@@ -680,7 +755,7 @@ bool attn_plan(int B, int N, int Hq, int Hkv, int D, int Lmax, int num_sms, Attn
     if (per_wave < 1) per_wave = s == 1 ? sms : sms / (2 * s);  // conservative guess
     if (per_wave < 1) continue;
     const long long waves = (units + per_wave - 1) / per_wave;
-    const double cost = (double)waves * ((tps + plan->kg - 1) / plan->kg + 3.0);
+    const double cost = (double)waves * (tps + 3.0);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;

@@ -252,13 +252,6 @@ __device__ __forceinline__ Entry lanes8_combine(Entry e, int kind, float k) {
   return e;
 }
 
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t remote_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-      ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
-      : "memory");
-}
-
 // One exchange; returns the cluster-wide combination (in every thread).  `mine` is this warp's
 // entry (warp-uniform).  Warp 0 combines the CTA's warps, sends, waits for the CL entries and
 // combines them; the others meet it at a __syncthreads.  After it, sm.cpart[slot][r] holds CTA
