@@ -68,6 +68,12 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// V rows of a chunk are stored in the order the PV MMAs consume them: 32-key blocks 0, 2, 1, 3
+// (so that P of keys 0..31, 64..95, 32..63, 96..127 sits in TMEM columns 0, 16, 32, 48).  The map
+// is its own inverse: V row block j holds key block v_block_key(j), key block b sits in row block
+// v_block_key(b).
+__host__ __device__ constexpr int v_block_key(int j) { return ((j & 1) << 1) | (j >> 1); }
+
 __device__ __forceinline__ float ex2_approx(float x) {  // hardware 2^x (P is rounded to bf16)
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -91,9 +97,9 @@ struct TcCfg {
   static constexpr int OFF_BAR = OFF_Q + NB * QBOX;
   static constexpr int SMEM = 1024 /*alignment slack*/ + OFF_BAR + 512;
   // TMEM columns: S[0] 0..127, S[1] 128..255 (one chunk each: 128 keys in fp32); P of a chunk
-  // overwrites columns 0..63 of its S buffer (128 bf16 keys packed in pairs; key group g in
-  // columns 32 g..32 g + 31); O[parity] at 256 + 128 parity (the two softmax warp sets take
-  // alternate chunks, each with its own accumulator).
+  // overwrites columns 0..63 of its S buffer (128 bf16 keys packed in pairs, in the V row order:
+  // keys 0..31, 64..95, 32..63, 96..127 in columns 0, 16, 32, 48); O[key set] at 256 + 128 ks
+  // (the two softmax warp sets each accumulate their own keys).
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COLS = 128;
   static constexpr uint32_t O_COL = 256;
@@ -178,12 +184,12 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       mbar_init(bar(B_FULL + i), 1);
       mbar_init(bar(B_EMPTY + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {  // [parity of the chunk]
+    for (int i = 0; i < 2; ++i) {  // [S / P buffer]
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SFREE + i), 4);  // one arrival per softmax warp of that parity
-      mbar_init(bar(B_PFULL + i), 4);
-      mbar_init(bar(B_PV + i), 1);
+      mbar_init(bar(B_SFREE + i), 8);  // one arrival per softmax warp
+      mbar_init(bar(B_PFULL + i), 8);
     }
+    mbar_init(bar(B_PV), 1);
     mbar_init(bar(B_DONE), 1);
     mbar_fence_init();
     abort_s = 0;
@@ -196,7 +202,10 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
 #pragma unroll
       for (int bx = 0; bx < C::NB; ++bx) {
         tma_load_2d(smem_u32(st + bx * C::BOX), &tmap_k, bar(B_FULL + it), bx * 64, y);
-        tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX), &tmap_v, bar(B_FULL + it), bx * 64, y);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX + j * 32 * 128), &tmap_v,
+                      bar(B_FULL + it), bx * 64, y + 32 * v_block_key(j));
       }
     }
   }
@@ -205,7 +214,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
 
   // softmax threads: MMA row r (TMEM lane r), key group gi, query row qrow of this KV head
   const int r = 32 * (warp & 3) + lane;
-  const int par = (warp - 2) >> 2;  // softmax warps: parity of the chunks this warp takes
+  const int ks = (warp - 2) >> 2;  // softmax warps: key set (the first or second 32 keys of a half)
   const int gi = (kg == 2) ? (r >> 6) : 0;
   const int qloc = (kg == 2) ? (r & 63) : r;  // row within this CTA's block of query rows
   const int qrow = rb * 128 + qloc;
@@ -275,7 +284,10 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
 #pragma unroll
         for (int bx = 0; bx < C::NB; ++bx) {
           tma_load_2d(smem_u32(st + bx * C::BOX), &tmap_k, bar(B_FULL + s), bx * 64, y);
-          tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX), &tmap_v, bar(B_FULL + s), bx * 64, y);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX + j * 32 * 128), &tmap_v,
+                        bar(B_FULL + s), bx * 64, y + 32 * v_block_key(j));
         }
         issued = it + 1;
       }
@@ -323,16 +335,18 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
         if (np < nq && mbar_test(bar(B_PFULL + (np & 1)), (np >> 1) & 1)) {
           tc_fence_after();
           const int sl = np % C::SLOTS;
+          // V rows 0..63 (keys 0..31, 64..95) belong to key set 0, rows 64..127 to key set 1:
+          // each set accumulates into its own O
           const uint32_t p_tm = tmem + (uint32_t)((np & 1) * C::S_COLS);
-          const uint32_t o_tm = tmem + C::O_COL + (uint32_t)((np & 1) * 128);
           const uint32_t v_addr = smem_u32(ring + sl * C::TILE + C::NB * C::BOX);
 #pragma unroll
           for (int kk = 0; kk < C::KEYS / 16; ++kk) {
             const uint64_t bd = smem_desc_sw128(v_addr + kk * 2048, C::BOX, 1024);
-            tc_mma_bf16_ts(o_tm, p_tm + (uint32_t)(kk * 8), bd, IPV, (np > 1 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16_ts(tmem + C::O_COL + (uint32_t)((kk >> 2) * 128), p_tm + (uint32_t)(kk * 8),
+                           bd, IPV, (np > 0 || (kk & 3) > 0) ? 1u : 0u);
           }
           tc_commit(bar(B_EMPTY + sl));  // the chunk's slot is free once these MMAs complete
-          tc_commit(bar(B_PV + (np & 1)));
+          tc_commit(bar(B_PV));
           ++np;
           progressed = true;
         }
@@ -349,46 +363,29 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       mbar_wait(bar(B_DONE), 0);
     }
   } else {
-    // ---------------- softmax: one MMA row per thread; warps 2..5 take the even chunks and
-    // warps 6..9 the odd ones (each set covers all 128 TMEM lanes).  With key groups a row covers
-    // one 64-key half of each chunk (half gi); otherwise both halves (the second one is read twice:
-    // first for the max, then again for the exponentials, so only 64 scores are live at a time).
+    // ---------------- softmax: one MMA row per thread, two warps per row.  Key set ks (warps
+    // 2..5: ks = 0, warps 6..9: ks = 1) takes keys 32 ks..32 ks + 31 of each 64-key half of a chunk
+    // -- the half gi with key groups, both halves otherwise -- with its own running max, sum and O
+    // accumulator, so the two warps of a row never exchange anything.
     const int node = min(qrow / g, N - 1);
     const unsigned long long anc = anc_s[node];
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    const uint32_t o_col = C::O_COL + (uint32_t)(par * 128);
+    const uint32_t o_col = C::O_COL + (uint32_t)(ks * 128);
     const float sc = p.scale_log2;
-    const int tp = 32 * ((warp - 2) & 3) + lane;  // 0..127 within this parity's warps
-    const int nh = 2 / kg;                        // 64-key halves per row per chunk
-    const int h0 = (kg == 2) ? gi : 0;
-    float zero32[32];
+    const int tg = tid - 64;  // 0..255
+    float zero16[16];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) zero32[c] = 0.f;
-    // visibility of the 64 keys key0..key0+63 (bit c: key key0 + c): the prefix part, then the
+    for (int c = 0; c < 16; ++c) zero16[c] = 0.f;
+    // visibility of the 32 keys key0..key0+31 (bit c: key key0 + c): the prefix part, then the
     // tree slots L + j of the node's ancestors j.  One code path for every chunk.
-    auto visible = [&](int key0) -> unsigned long long {
+    auto visible32 = [&](int key0) -> uint32_t {
       const int pre = L - key0;
       unsigned long long vis = pre >= 64 ? ~0ull : (pre <= 0 ? 0ull : (1ull << pre) - 1ull);
       const int j0 = key0 - L;
       if (j0 > -64 && j0 < N) vis |= j0 >= 0 ? (anc >> j0) : (anc << -j0);
-      return vis;
+      return (uint32_t)vis;
     };
-    auto load_masked = [&](uint32_t scol, unsigned long long vis, float (&xa)[32],
-                           float (&xb)[32]) -> float {
-      tmem_ld32(lane_base + scol, xa);
-      tmem_ld32(lane_base + scol + 32, xb);
-      tmem_wait_ld();
-      const uint32_t vlo = (uint32_t)vis, vhi = (uint32_t)(vis >> 32);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        xa[c] = ((vlo >> c) & 1u) ? xa[c] : -INFINITY;
-        xb[c] = ((vhi >> c) & 1u) ? xb[c] : -INFINITY;
-        mx = fmaxf(mx, fmaxf(xa[c], xb[c]));
-      }
-      return mx;
-    };
-    for (int u = par; u < U; u += 2) {
+    for (int u = 0; u < U; ++u) {
       if (!__all_sync(0xffffffffu, wait(B_SFULL + (u & 1), (u >> 1) & 1))) {
         ok_rows = false;
         break;
@@ -396,10 +393,27 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       tc_fence_after();
       const int ckey0 = (t_begin + u) * C::KEYS;
       const uint32_t scol0 = (uint32_t)((u & 1) * C::S_COLS);
-      float xa[32], xb[32];
+      // this thread's 32-key blocks: half hf = gi (key groups) or 0 and 1; S columns
+      // 64 hf + 32 ks, P columns 32 ks + 16 hf (inside the S columns this warp has read)
+      float x[2][32];
       float mx = -INFINITY;
-      if (nh == 2) mx = load_masked(scol0 + 64, visible(ckey0 + 64), xa, xb);
-      mx = fmaxf(mx, load_masked(scol0 + 64 * h0, visible(ckey0 + 64 * h0), xa, xb));
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        if (hh == 1 && kg == 2) break;
+        const int hf = (kg == 2) ? gi : hh;
+        tmem_ld32(lane_base + scol0 + (uint32_t)(64 * hf + 32 * ks), x[hh]);
+        tmem_wait_ld();
+        const uint32_t vis = visible32(ckey0 + 64 * hf + 32 * ks);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) x[hh][c] = ((vis >> c) & 1u) ? x[hh][c] : -INFINITY;
+        float m0 = fmaxf(x[hh][0], x[hh][1]), m1 = fmaxf(x[hh][2], x[hh][3]);
+#pragma unroll
+        for (int c = 4; c < 32; c += 4) {
+          m0 = fmaxf(m0, fmaxf(x[hh][c], x[hh][c + 1]));
+          m1 = fmaxf(m1, fmaxf(x[hh][c + 2], x[hh][c + 3]));
+        }
+        mx = fmaxf(mx, fmaxf(m0, m1));
+      }
       const float mt = mx * sc;  // scale > 0
       const bool raise = mt > m_used + 8.f;
       float factor = 1.f;
@@ -409,26 +423,24 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       }
       const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
       float rs = 0.f;
-      for (int hh = 0; hh < nh; ++hh) {
-        if (hh == 1) load_masked(scol0 + 64, visible(ckey0 + 64), xa, xb);
-        float rs0 = 0.f, rs1 = 0.f;
-        float pk[32];  // P as bf16 pairs (bit patterns), key 2c in the low half of column c
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        if (hh == 1 && kg == 2) break;
+        const int hf = (kg == 2) ? gi : hh;
+        float r0 = 0.f, r1 = 0.f;
+        float pk[16];  // P as bf16 pairs (bit patterns), key 2c in the low half of column c
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float a0 = ex2_approx(fmaf(xa[2 * c], sc, neg_m));
-          const float a1 = ex2_approx(fmaf(xa[2 * c + 1], sc, neg_m));
-          const float b0 = ex2_approx(fmaf(xb[2 * c], sc, neg_m));
-          const float b1 = ex2_approx(fmaf(xb[2 * c + 1], sc, neg_m));
-          rs0 += a0 + a1;
-          rs1 += b0 + b1;
+          const float a0 = ex2_approx(fmaf(x[hh][2 * c], sc, neg_m));
+          const float a1 = ex2_approx(fmaf(x[hh][2 * c + 1], sc, neg_m));
+          if (c & 1) r1 += a0 + a1; else r0 += a0 + a1;
           pk[c] = __uint_as_float(pack_bf16(a0, a1));
-          pk[16 + c] = __uint_as_float(pack_bf16(b0, b1));
         }
-        rs += rs0 + rs1;
-        // P over the scores already read (columns 0..63 of this lane; key group g at 32 g)
-        tmem_st32(lane_base + scol0 + (uint32_t)((h0 + hh) * 32), pk);
+        rs += r0 + r1;
+        tmem_st16(lane_base + scol0 + (uint32_t)(32 * ks + 16 * hf), pk);
       }
-      if (kg == 2) tmem_st32(lane_base + scol0 + (uint32_t)((1 - gi) * 32), zero32);
+      // key groups: the other group's P columns of this set are zero for this row
+      if (kg == 2) tmem_st16(lane_base + scol0 + (uint32_t)(32 * ks + 16 * (1 - gi)), zero16);
       l = l * factor + rs;
       // The chunk holding the last key L + N - 1: V rows past it hold whatever the cache holds
       // there (possibly NaN); their P is 0, but 0 * NaN is not, so zero those rows.
@@ -437,18 +449,18 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
         if (__all_sync(0xffffffffu, wait(B_FULL + sl, (u / C::SLOTS) & 1))) {
           const int nv = total_keys - ckey0;  // 1..127 valid keys
           const int units = C::NB * (C::KEYS - nv) * 8;
-          for (int w = tp; w < units; w += 128) {
+          for (int w = tg; w < units; w += 256) {
             const int bx = w / ((C::KEYS - nv) * 8), rem = w % ((C::KEYS - nv) * 8);
-            *reinterpret_cast<uint4*>(ring + sl * C::TILE + (C::NB + bx) * C::BOX +
-                                      (nv + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+            const int key = nv + rem / 8, vrow = 32 * v_block_key(key >> 5) + (key & 31);
+            *reinterpret_cast<uint4*>(ring + sl * C::TILE + (C::NB + bx) * C::BOX + vrow * 128 +
+                                      (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_async_smem();  // the zeros are read by the tensor cores (async proxy)
         }
       }
-      // O rescale (only if this parity accumulated before and some row of this warp raised its
-      // max): after the PV of step u - 2, the last one into O[parity], completed
-      if (u >= 2 && __any_sync(0xffffffffu, raise)) {
-        if (__all_sync(0xffffffffu, wait(B_PV + par, ((u >> 1) - 1) & 1))) {
+      // O rescale (only after the first step, only if some row of this warp raised its max)
+      if (u > 0 && __any_sync(0xffffffffu, raise)) {
+        if (__all_sync(0xffffffffu, wait(B_PV, (u - 1) & 1))) {
           tc_fence_after();
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -470,16 +482,12 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
         mbar_arrive(bar(B_PFULL + (u & 1)));
       }
     }
-    // the last PV into each accumulator has completed (the combine reads both)
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-      if (ok_rows && U > q)
-        ok_rows = __all_sync(0xffffffffu, wait(B_PV + q, ((U - 1 - q) >> 1) & 1));
+    if (ok_rows && U > 0) ok_rows = __all_sync(0xffffffffu, wait(B_PV, (U - 1) & 1));
     if (ok_rows && U > 0) tc_fence_after();
   }
 
   // ---------------- combine across the cluster (all threads of every CTA take part)
-  // A lane's two accumulators (even and odd chunks) merge first; with key groups, lanes r and
+  // A lane's two accumulators (key sets 0 and 1) merge first; with key groups, lanes r and
   // r + 64 (the same query over different keys) then merge too.  Partial: (m, l, O) with m = NaN
   // after a timeout and l = 0 when it saw no key (its O is then never read).
   const int QO = owned_rows(kg, S);
@@ -497,7 +505,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   cluster_arrive_release();  // every CTA of the cluster is done with its ring (TMA copies drained)
   cluster_wait_acquire();    // and its MMAs
   if (warp >= 2) {
-    stage_ml[par * 128 + r] = make_float2(m_own, l_own);
+    stage_ml[ks * 128 + r] = make_float2(m_own, l_own);
     named_bar_sync(1, 256);  // the eight softmax warps
     const uint32_t lane_tm = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const float2 s0 = stage_ml[r], s1 = stage_ml[128 + r];
@@ -519,11 +527,11 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
     };
     const int owner = qloc % S, ql = qloc / S;
     if (kg == 2) {
-      // columns in quarters: the thread of (key group g, parity p) merges and pushes quarter
-      // 2 g + p, and hands its lane's values of quarter 2 (1 - g) + p to the other group
+      // columns in quarters: the thread of (key group g, key set k) merges and pushes quarter
+      // 2 g + k, and hands its lane's values of quarter 2 (1 - g) + k to the other group
       constexpr int Q4 = D / 4;
-      const int my_q4 = 2 * gi + par, give_q4 = 2 * (1 - gi) + par;
-      if (par == 0) stage_lm[r] = make_float2(tmo ? NAN : mc, lc);
+      const int my_q4 = 2 * gi + ks, give_q4 = 2 * (1 - gi) + ks;
+      if (ks == 0) stage_lm[r] = make_float2(tmo ? NAN : mc, lc);
 #pragma unroll 1
       for (int c0 = give_q4 * Q4; c0 < (give_q4 + 1) * Q4; c0 += 16) {
         float o[16];
@@ -541,7 +549,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       const float g_oth = oth.y > 0.f ? ex2_approx(oth.x - M2) : 0.f;
       const float L2 = lc * g_own + oth.y * g_oth;
       const bool has = !tmo2 && L2 > 0.f;
-      if (live && gi == 0 && par == 0)
+      if (live && gi == 0 && ks == 0)
         dsmem_store_v2(dsmem_addr(recv_ml + (size_t)split * QO + ql, owner),
                        __float_as_uint(tmo2 ? NAN : (has ? M2 : -INFINITY)),
                        __float_as_uint(has ? L2 : 0.f));
@@ -564,16 +572,16 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
         }
       }
     } else {
-      // no key groups: the thread of parity p pushes half p of its row's columns
+      // no key groups: the thread of key set k pushes half k of its row's columns
       const bool has = !tmo && lc > 0.f;
-      if (live && par == 0)
+      if (live && ks == 0)
         dsmem_store_v2(dsmem_addr(recv_ml + (size_t)split * QO + ql, owner),
                        __float_as_uint(tmo ? NAN : (has ? mc : -INFINITY)),
                        __float_as_uint(has ? lc : 0.f));
       const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
       const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE, owner);
 #pragma unroll 1
-      for (int c0 = par * (D / 2); c0 < (par + 1) * (D / 2); c0 += 16) {
+      for (int c0 = ks * (D / 2); c0 < (ks + 1) * (D / 2); c0 += 16) {
         float o[16];
         merged16(c0, o);
 #pragma unroll
@@ -661,12 +669,12 @@ static PFN_encodeTiled encode_fn() {
   return fn;
 }
 
-static bool make_kv_map(CUtensorMap* m, const void* ptr, int D, long long rows) {
+static bool make_kv_map(CUtensorMap* m, const void* ptr, int D, long long rows, int box_rows) {
   PFN_encodeTiled fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, kChunkKeys};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -781,7 +789,8 @@ static cudaError_t launch_d(const CUtensorMap& mk, const CUtensorMap& mv, const 
 cudaError_t launch_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream_t s) {
   CUtensorMap mk, mv;
   const long long rows = (long long)a.B * a.Hkv * a.Lmax;
-  if (!make_kv_map(&mk, a.k, a.D, rows) || !make_kv_map(&mv, a.v, a.D, rows))
+  // K in boxes of a whole chunk; V in 32-key boxes (stored in the PV order, see v_block_key)
+  if (!make_kv_map(&mk, a.k, a.D, rows, kChunkKeys) || !make_kv_map(&mv, a.v, a.D, rows, 32))
     return cudaErrorInvalidValue;
   AttnKParams kp;
   kp.q = static_cast<const __nv_bfloat16*>(a.q);
