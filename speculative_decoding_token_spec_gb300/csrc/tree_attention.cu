@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   __shared__ int par_s[kMaxNodes];
   __shared__ unsigned long long anc_s[kMaxNodes];
   __shared__ int abort_s;
+  __shared__ int bad_s;  // SPEC_ST_BAD_TREE / SPEC_ST_BAD_LEN found in the set-up
   __shared__ uint32_t tmem_s;
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -135,7 +136,8 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   uint8_t* q_s = base + C::OFF_Q;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::OFF_BAR);
   const int B_FULL = 0, B_EMPTY = C::SLOTS, B_SFULL = 2 * C::SLOTS, B_SFREE = 2 * C::SLOTS + 2,
-            B_PFULL = 2 * C::SLOTS + 4, B_PV = 2 * C::SLOTS + 6, B_DONE = 2 * C::SLOTS + 8;
+            B_PFULL = 2 * C::SLOTS + 4, B_PV = 2 * C::SLOTS + 6, B_DONE = 2 * C::SLOTS + 7,
+            B_SETUP = 2 * C::SLOTS + 8;
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -155,6 +157,23 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   }
   griddep_wait();  // every global access below may depend on the preceding kernel in the stream
   griddep_launch_dependents();
+  if (tid == 0) {
+    for (int i = 0; i < C::SLOTS; ++i) {
+      mbar_init(bar(B_FULL + i), 1);
+      mbar_init(bar(B_EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {  // [S / P buffer]
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_SFREE + i), 8);  // one arrival per softmax warp
+      mbar_init(bar(B_PFULL + i), 8);
+    }
+    mbar_init(bar(B_PV), 1);
+    mbar_init(bar(B_DONE), 1);
+    mbar_init(bar(B_SETUP), 1);
+    mbar_fence_init();
+    abort_s = 0;
+    bad_s = 0;
+  }
   // The small inputs go out first: requests issued after a split's K/V stream wait behind it.
   // Q: the CTA's distinct query rows (64 with key groups, else 128), two rows per warp instruction
   // (coalesced); rows past R are zeros.
@@ -178,23 +197,10 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   int parent_i = 0;
   if (tid >= 64 && tid < 64 + N) parent_i = __ldg(p.parent + (size_t)b * N + (tid - 64));
   const int L = __ldg(p.prefix_lens + b);
-  if (warp != 1) named_bar_sync(2, 288);  // those loads are issued before the K/V copies
+  __syncthreads();  // the barriers are initialised; the small loads are on their way
   if (tid == 0) {
-    for (int i = 0; i < C::SLOTS; ++i) {
-      mbar_init(bar(B_FULL + i), 1);
-      mbar_init(bar(B_EMPTY + i), 1);
-    }
-    for (int i = 0; i < 2; ++i) {  // [S / P buffer]
-      mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SFREE + i), 8);  // one arrival per softmax warp
-      mbar_init(bar(B_PFULL + i), 8);
-    }
-    mbar_init(bar(B_PV), 1);
-    mbar_init(bar(B_DONE), 1);
-    mbar_fence_init();
-    abort_s = 0;
-    // the split's first tiles do not depend on the prefix length: issue them now (a tile past
-    // L_b + N is simply not consumed)
+    // the split's first chunks do not depend on the prefix length: issue them now (a chunk past
+    // L_b + N is simply not consumed).  Nothing else waits for this issue.
     for (int it = 0; it < spec; ++it) {
       mbar_arrive_expect_tx(bar(B_FULL + it), C::TILE);
       uint8_t* st = ring + it * C::TILE;
@@ -210,7 +216,6 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
     }
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_s), C::TMEM_COLS);
-  if (tid >= 64 && tid < 64 + N) par_s[tid - 64] = parent_i;
 
   // softmax threads: MMA row r (TMEM lane r), key group gi, query row qrow of this KV head
   const int r = 32 * (warp & 3) + lane;
@@ -219,7 +224,9 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   const int qloc = (kg == 2) ? (r & 63) : r;  // row within this CTA's block of query rows
   const int qrow = rb * 128 + qloc;
   const bool live = qrow < p.R;
-  if (warp >= 2) {  // Q rows -> swizzled shared memory (key groups: rows r and r + 64 alike)
+  if (warp >= 2) {
+    if (tid < 64 + N) par_s[tid - 64] = parent_i;
+    // Q rows -> swizzled shared memory (key groups: rows r and r + 64 alike)
 #pragma unroll
     for (int k = 0; k < QIT; ++k) {
       const int idx = (tid - 64) + k * 256, row = idx / QCH, ch = idx % QCH;
@@ -231,29 +238,33 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
     }
     fence_async_smem();  // Q is read by the tensor cores (async proxy)
   }
-  __syncthreads();
-  // tree: every node validates its own parent and walks its ancestor chain (in parallel)
-  int st_bits = 0;
-  if (tid < N) {
-    const int pi = par_s[tid];
-    if (tid == 0 ? pi != -1 : (pi < 0 || pi >= tid)) st_bits = SPEC_ST_BAD_TREE;
-    unsigned long long m = 1ull << tid;
-    int k = pi;
-    for (int steps = 0; k >= 0 && k < N && steps < N; ++steps) {
-      m |= 1ull << k;
-      k = par_s[k];
+  if (warp >= 1) {  // warp 0 may still be issuing copies: it learns the outcome from B_SETUP
+    named_bar_sync(2, 288);
+    // tree: every node validates its own parent and walks its ancestor chain (in parallel)
+    if (tid >= 64 && tid < 64 + N) {
+      const int i = tid - 64;
+      const int pi = par_s[i];
+      if (i == 0 ? pi != -1 : (pi < 0 || pi >= i)) atomicOr(&bad_s, SPEC_ST_BAD_TREE);
+      unsigned long long m = 1ull << i;
+      int k = pi;
+      for (int steps = 0; k >= 0 && k < N && steps < N; ++steps) {
+        m |= 1ull << k;
+        k = par_s[k];
+      }
+      anc_s[i] = m;
     }
-    anc_s[tid] = m;
+    if (tid == 64 && (L < 0 || L + N > p.Lmax)) atomicOr(&bad_s, SPEC_ST_BAD_LEN);
+    tc_fence_before();
+    named_bar_sync(2, 288);
+    tc_fence_after();
+    if (tid == 64) mbar_arrive(bar(B_SETUP));
+  } else if (!mbar_wait(bar(B_SETUP), 0)) {
+    abort_s = 1;
   }
-  if (tid == 0 && (L < 0 || L + N > p.Lmax)) st_bits |= SPEC_ST_BAD_LEN;
-  const int bad_tree = __syncthreads_or(st_bits & SPEC_ST_BAD_TREE);
-  const int bad_len = __syncthreads_or(st_bits & SPEC_ST_BAD_LEN);
-  const bool bad = (bad_tree | bad_len) != 0;
-  if (tid == 0 && bad && split == 0 && kvh == 0 && rb == 0 && p.status)
-    atomicOr(p.status + b, (bad_tree ? SPEC_ST_BAD_TREE : 0) | (bad_len ? SPEC_ST_BAD_LEN : 0));
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  const int bad_bits = bad_s;
+  const bool bad = bad_bits != 0;
+  if (tid == 64 && bad && split == 0 && kvh == 0 && rb == 0 && p.status)
+    atomicOr(p.status + b, bad_bits);
   const uint32_t tmem = tmem_s;
 
   const int total_keys = bad ? 0 : L + N;
