@@ -80,6 +80,9 @@ __device__ __forceinline__ float ex2_approx(float x) {  // hardware 2^x (P is ro
   return y;
 }
 
+__device__ __forceinline__ void tmem_ldq(uint32_t taddr, float (&v)[32]) { tmem_ld32(taddr, v); }
+__device__ __forceinline__ void tmem_ldq(uint32_t taddr, float (&v)[16]) { tmem_ld16(taddr, v); }
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -498,108 +501,128 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   }
 
   // ---------------- combine across the cluster (all threads of every CTA take part)
-  // A lane's two accumulators (key sets 0 and 1) merge first; with key groups, lanes r and
-  // r + 64 (the same query over different keys) then merge too.  Partial: (m, l, O) with m = NaN
-  // after a timeout and l = 0 when it saw no key (its O is then never read).
+  // A query's partials inside the CTA -- the two accumulators (key sets 0 and 1) of its lane and,
+  // with key groups, of lane r + 64 too (the same query over different keys) -- merge into one,
+  // which goes to the cluster CTA that owns the row.  Partial: (m, l, O) with m = NaN after a
+  // timeout and l = 0 when it saw no key (its O is then never read).
   const int QO = owned_rows(kg, S);
   // [S][QO][RSTRIDE] partial rows, then one trash row that rows without data are pushed into (so
   // the push has no branch), then the (m, l) pairs [S][QO].  The ring is idle now.
   float* recv_o = reinterpret_cast<float*>(ring);
   float2* recv_ml = reinterpret_cast<float2*>(recv_o + ((size_t)S * QO + 1) * C::RSTRIDE);
-  // in-CTA exchange: the key-group quarter rows [64][RSTRIDE], the per-(parity, lane) states
-  // [2][128] and the per-lane merged states [128]
-  float* stage = reinterpret_cast<float*>(ring + C::STAGE_OFF);
-  float2* stage_ml = reinterpret_cast<float2*>(stage + 64 * C::RSTRIDE);
-  float2* stage_lm = stage_ml + 256;
+  // in-CTA exchange: the (m, l) of every (key set, lane) [2][128], then the raw accumulator
+  // values a lane hands to the other key group, [2 accumulators][64 rows][RSTRIDE]
+  float2* stage_ml = reinterpret_cast<float2*>(ring + C::STAGE_OFF);
+  float* stage_o = reinterpret_cast<float*>(stage_ml + 256);
   const float m_own = ok_rows ? (l > 0.f ? m_used : -INFINITY) : NAN;
   const float l_own = (ok_rows && l > 0.f) ? l : 0.f;
   cluster_arrive_release();  // every CTA of the cluster is done with its ring (TMA copies drained)
   cluster_wait_acquire();    // and its MMAs
   if (warp >= 2) {
-    stage_ml[ks * 128 + r] = make_float2(m_own, l_own);
-    named_bar_sync(1, 256);  // the eight softmax warps
     const uint32_t lane_tm = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    const float2 s0 = stage_ml[r], s1 = stage_ml[128 + r];
-    const bool tmo = isnan(s0.x) || isnan(s1.x);
-    const bool use0 = s0.y > 0.f, use1 = s1.y > 0.f;
-    const float mc = fmaxf(use0 ? s0.x : -INFINITY, use1 ? s1.x : -INFINITY);
-    const float f0 = use0 ? ex2_approx(s0.x - mc) : 0.f;
-    const float f1 = use1 ? ex2_approx(s1.x - mc) : 0.f;
-    const float lc = s0.y * f0 + s1.y * f1;
-    // this lane's merged O over columns c0..c0+15 (an accumulator without keys is never read: it
-    // may hold anything)
-    auto merged16 = [&](int c0, float (&o)[16]) {
-      float a0[16], a1[16];
-      tmem_ld16(lane_tm + C::O_COL + (uint32_t)c0, a0);
-      tmem_ld16(lane_tm + C::O_COL + 128u + (uint32_t)c0, a1);
-      tmem_wait_ld();
-#pragma unroll
-      for (int k = 0; k < 16; ++k) o[k] = (use0 ? a0[k] * f0 : 0.f) + (use1 ? a1[k] * f1 : 0.f);
-    };
     const int owner = qloc % S, ql = qloc / S;
+    stage_ml[ks * 128 + r] = make_float2(m_own, l_own);
+    auto sel = [](float w, float v) { return w != 0.f ? w * v : 0.f; };  // v may be garbage
+    auto push_ml = [&](bool tmo, bool has, float m, float lsum) {
+      dsmem_store_v2(dsmem_addr(recv_ml + (size_t)split * QO + ql, owner),
+                     __float_as_uint(tmo ? NAN : (has ? m : -INFINITY)),
+                     __float_as_uint(has ? lsum : 0.f));
+    };
     if (kg == 2) {
-      // columns in quarters: the thread of (key group g, key set k) merges and pushes quarter
-      // 2 g + k, and hands its lane's values of quarter 2 (1 - g) + k to the other group
+      // Query qloc has four partials: (key group g, key set k) = lane 64 g + qloc, accumulator k.
+      // The thread of (g, k) combines columns quarter 2 g + k of all four and pushes them; it
+      // hands its lane's raw values of quarter 2 (1 - g) + k to the other group first.  One
+      // barrier covers the states and the hand-over.
       constexpr int Q4 = D / 4;
-      const int my_q4 = 2 * gi + ks, give_q4 = 2 * (1 - gi) + ks;
-      if (ks == 0) stage_lm[r] = make_float2(tmo ? NAN : mc, lc);
-#pragma unroll 1
-      for (int c0 = give_q4 * Q4; c0 < (give_q4 + 1) * Q4; c0 += 16) {
-        float o[16];
-        merged16(c0, o);
+      const int my_c = (2 * gi + ks) * Q4, give_c = (2 * (1 - gi) + ks) * Q4;
+      {
+        float g0[Q4], g1[Q4];
+        tmem_ldq(lane_tm + C::O_COL + (uint32_t)give_c, g0);
+        tmem_ldq(lane_tm + C::O_COL + 128u + (uint32_t)give_c, g1);
+        tmem_wait_ld();
+        float* s0 = stage_o + qloc * C::RSTRIDE + give_c;
+        float* s1 = stage_o + (64 + qloc) * C::RSTRIDE + give_c;
 #pragma unroll
-        for (int k = 0; k < 16; k += 4)
-          *reinterpret_cast<float4*>(stage + qloc * C::RSTRIDE + c0 + k) =
-              make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
-      }
-      named_bar_sync(1, 256);
-      const float2 oth = stage_lm[(1 - gi) * 64 + qloc];
-      const bool tmo2 = tmo || isnan(oth.x);
-      const float M2 = fmaxf(lc > 0.f ? mc : -INFINITY, oth.y > 0.f ? oth.x : -INFINITY);
-      const float g_own = lc > 0.f ? ex2_approx(mc - M2) : 0.f;
-      const float g_oth = oth.y > 0.f ? ex2_approx(oth.x - M2) : 0.f;
-      const float L2 = lc * g_own + oth.y * g_oth;
-      const bool has = !tmo2 && L2 > 0.f;
-      if (live && gi == 0 && ks == 0)
-        dsmem_store_v2(dsmem_addr(recv_ml + (size_t)split * QO + ql, owner),
-                       __float_as_uint(tmo2 ? NAN : (has ? M2 : -INFINITY)),
-                       __float_as_uint(has ? L2 : 0.f));
-      const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
-      const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE, owner);
-#pragma unroll 1
-      for (int c0 = my_q4 * Q4; c0 < (my_q4 + 1) * Q4; c0 += 16) {
-        float o[16];
-        merged16(c0, o);
-        const float* st = stage + qloc * C::RSTRIDE + c0;  // ignored when g_oth == 0
-#pragma unroll
-        for (int k = 0; k < 16; k += 4) {
-          const float4 sv = *reinterpret_cast<const float4*>(st + k);
-          const float4 pv = g_oth != 0.f ? sv : make_float4(0.f, 0.f, 0.f, 0.f);
-          dsmem_store_v4(dst + (c0 + k) * 4,
-                         make_uint4(__float_as_uint(fmaf(o[k], g_own, pv.x * g_oth)),
-                                    __float_as_uint(fmaf(o[k + 1], g_own, pv.y * g_oth)),
-                                    __float_as_uint(fmaf(o[k + 2], g_own, pv.z * g_oth)),
-                                    __float_as_uint(fmaf(o[k + 3], g_own, pv.w * g_oth))));
+        for (int k = 0; k < Q4; k += 4) {
+          *reinterpret_cast<float4*>(s0 + k) = make_float4(g0[k], g0[k + 1], g0[k + 2], g0[k + 3]);
+          *reinterpret_cast<float4*>(s1 + k) = make_float4(g1[k], g1[k + 1], g1[k + 2], g1[k + 3]);
         }
       }
+      float o0[Q4], o1[Q4];
+      tmem_ldq(lane_tm + C::O_COL + (uint32_t)my_c, o0);  // in flight across the barrier
+      tmem_ldq(lane_tm + C::O_COL + 128u + (uint32_t)my_c, o1);
+      named_bar_sync(1, 256);  // the eight softmax warps
+      float2 st[2][2];         // [group][key set]
+#pragma unroll
+      for (int g2 = 0; g2 < 2; ++g2)
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) st[g2][k2] = stage_ml[k2 * 128 + g2 * 64 + qloc];
+      bool tmo = false;
+      float M = -INFINITY;
+#pragma unroll
+      for (int g2 = 0; g2 < 2; ++g2)
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+          tmo |= isnan(st[g2][k2].x);
+          M = st[g2][k2].y > 0.f ? fmaxf(M, st[g2][k2].x) : M;
+        }
+      float w[2][2], Lsum = 0.f;
+#pragma unroll
+      for (int g2 = 0; g2 < 2; ++g2)
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+          w[g2][k2] = st[g2][k2].y > 0.f ? ex2_approx(st[g2][k2].x - M) : 0.f;
+          Lsum = fmaf(w[g2][k2], st[g2][k2].y, Lsum);
+        }
+      const bool has = !tmo && Lsum > 0.f;
+      if (live && gi == 0 && ks == 0) push_ml(tmo, has, M, Lsum);
+      const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
+      const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE + my_c, owner);
+      const float* r0 = stage_o + qloc * C::RSTRIDE + my_c;
+      const float* r1 = stage_o + (64 + qloc) * C::RSTRIDE + my_c;
+      const float wo0 = gi ? w[1][0] : w[0][0], wo1 = gi ? w[1][1] : w[0][1];  // own lane
+      const float wx0 = gi ? w[0][0] : w[1][0], wx1 = gi ? w[0][1] : w[1][1];  // the other lane
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < Q4; k += 4) {
+        const float4 x0 = *reinterpret_cast<const float4*>(r0 + k);
+        const float4 x1 = *reinterpret_cast<const float4*>(r1 + k);
+        const float xa[4] = {x0.x, x0.y, x0.z, x0.w}, xb[4] = {x1.x, x1.y, x1.z, x1.w};
+        uint32_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          v[j] = __float_as_uint(sel(wo0, o0[k + j]) + sel(wo1, o1[k + j]) + sel(wx0, xa[j]) +
+                                 sel(wx1, xb[j]));
+        dsmem_store_v4(dst + k * 4, make_uint4(v[0], v[1], v[2], v[3]));
+      }
     } else {
-      // no key groups: the thread of key set k pushes half k of its row's columns
-      const bool has = !tmo && lc > 0.f;
-      if (live && ks == 0)
-        dsmem_store_v2(dsmem_addr(recv_ml + (size_t)split * QO + ql, owner),
-                       __float_as_uint(tmo ? NAN : (has ? mc : -INFINITY)),
-                       __float_as_uint(has ? lc : 0.f));
+      // no key groups: the two accumulators of this lane; the thread of key set k pushes half k
+      // of the columns, 32 at a time
+      named_bar_sync(1, 256);
+      const float2 s0 = stage_ml[r], s1 = stage_ml[128 + r];
+      const bool tmo = isnan(s0.x) || isnan(s1.x);
+      const float M = fmaxf(s0.y > 0.f ? s0.x : -INFINITY, s1.y > 0.f ? s1.x : -INFINITY);
+      const float w0 = s0.y > 0.f ? ex2_approx(s0.x - M) : 0.f;
+      const float w1 = s1.y > 0.f ? ex2_approx(s1.x - M) : 0.f;
+      const float Lsum = s0.y * w0 + s1.y * w1;
+      const bool has = !tmo && Lsum > 0.f;
+      if (live && ks == 0) push_ml(tmo, has, M, Lsum);
       const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
       const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE, owner);
+      constexpr int HC = D / 2 < 32 ? D / 2 : 32;
 #pragma unroll 1
-      for (int c0 = ks * (D / 2); c0 < (ks + 1) * (D / 2); c0 += 16) {
-        float o[16];
-        merged16(c0, o);
+      for (int c0 = ks * (D / 2); c0 < (ks + 1) * (D / 2); c0 += HC) {
+        float a0[HC], a1[HC];
+        tmem_ldq(lane_tm + C::O_COL + (uint32_t)c0, a0);
+        tmem_ldq(lane_tm + C::O_COL + 128u + (uint32_t)c0, a1);
+        tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 16; k += 4)
+        for (int k = 0; k < HC; k += 4)
           dsmem_store_v4(dst + (c0 + k) * 4,
-                         make_uint4(__float_as_uint(o[k]), __float_as_uint(o[k + 1]),
-                                    __float_as_uint(o[k + 2]), __float_as_uint(o[k + 3])));
+                         make_uint4(__float_as_uint(sel(w0, a0[k]) + sel(w1, a1[k])),
+                                    __float_as_uint(sel(w0, a0[k + 1]) + sel(w1, a1[k + 1])),
+                                    __float_as_uint(sel(w0, a0[k + 2]) + sel(w1, a1[k + 2])),
+                                    __float_as_uint(sel(w0, a0[k + 3]) + sel(w1, a1[k + 3]))));
       }
     }
   }
