@@ -23,7 +23,8 @@ from typing import Optional, Sequence
 import numpy as np
 
 __all__ = [
-    "AttnCase", "VerifyCase", "CONFIGS", "make_tree", "chain_tree", "make_attention_case",
+    "AttnCase", "VerifyCase", "PagedAttnCase", "CompactCase", "CONFIGS", "make_tree",
+    "chain_tree", "make_attention_case", "make_paged_attention_case", "make_compaction_case",
     "make_verify_case", "bf16_bits", "bf16_to_f64", "config",
 ]
 
@@ -186,6 +187,76 @@ def make_attention_case(cfg: Config, seed: int = 0, lmax_pad: int = 0,
         v[b] = bf16_bits(rng.standard_normal((Hkv, Lmax, D), dtype=np.float32))
         par[b] = _tree(cfg, seed, b)
     return AttnCase(q, k, v, lens, par, 1.0 / float(np.sqrt(D)), Lmax)
+
+
+@dataclasses.dataclass
+class PagedAttnCase:
+    q: np.ndarray             # uint16 bf16 bits [B, N, Hq, D]
+    k_pages: np.ndarray       # uint16 bf16 bits [num_pages, Hkv, page_size, D]
+    v_pages: np.ndarray       # uint16 bf16 bits [num_pages, Hkv, page_size, D]
+    block_table: np.ndarray   # int32 [B, max_pages]: physical page of each logical page
+    page_size: int
+    prefix_lens: np.ndarray   # int32 [B]
+    tree_parent: np.ndarray   # int32 [B, N]
+    scale: float
+
+
+def make_paged_attention_case(cfg: Config, page_size: int, seed: int = 0, spare_pages: int = 3,
+                              prefix_lens: Optional[Sequence[int]] = None) -> PagedAttnCase:
+    """Pages of N(0, 1) bf16 values and a block table that hands every sequence distinct physical
+    pages in a random order (plus a few pages nobody uses).  Table entries past the pages a
+    sequence needs are -1."""
+    B, N, Hq, Hkv, D = cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.D
+    lens = (np.asarray(prefix_lens, dtype=np.int32) if prefix_lens is not None
+            else _prefix_lens(cfg, seed))
+    need = [(int(L) + N + page_size - 1) // page_size for L in lens]
+    max_pages = max(need) + 1
+    num_pages = sum(need) + int(spare_pages)
+    rng = _rng(seed, cfg.cfg_id, 20_000, 3)
+    perm = rng.permutation(num_pages).astype(np.int32)
+    table = np.full((B, max_pages), -1, dtype=np.int32)
+    at = 0
+    for b in range(B):
+        table[b, :need[b]] = perm[at:at + need[b]]
+        at += need[b]
+    k = bf16_bits(rng.standard_normal((num_pages, Hkv, page_size, D), dtype=np.float32))
+    v = bf16_bits(rng.standard_normal((num_pages, Hkv, page_size, D), dtype=np.float32))
+    q = np.empty((B, N, Hq, D), dtype=np.uint16)
+    par = np.empty((B, N), dtype=np.int32)
+    for b in range(B):
+        q[b] = bf16_bits(_rng(seed, cfg.cfg_id, b, 2).standard_normal((N, Hq, D), dtype=np.float32))
+        par[b] = _tree(cfg, seed, b)
+    return PagedAttnCase(q, k, v, table, page_size, lens, par, 1.0 / float(np.sqrt(D)))
+
+
+@dataclasses.dataclass
+class CompactCase:
+    k_cache: np.ndarray       # uint16 bf16 bits [B, Hkv, Lmax, D]
+    v_cache: np.ndarray
+    prefix_lens: np.ndarray   # int32 [B]
+    accept_len: np.ndarray    # int32 [B]: -1 (verification failed), 0 .. N-1
+    accepted_nodes: np.ndarray  # int32 [B, N]: the accepted node ids, -1 padded
+
+
+def make_compaction_case(B: int, N: int, Hkv: int, D: int, seed: int = 0,
+                         prefix_range=(0, 200), lmax_pad: int = 5,
+                         lens: Optional[Sequence[int]] = None) -> CompactCase:
+    """Random caches and random accepted paths: for each sequence a length in -1 .. N-1 (or the
+    given ``lens``) and that many distinct node ids in 1 .. N-1, increasing (the numbering of a
+    root-to-node path when parents precede children)."""
+    rng = np.random.default_rng([int(seed), 30_000, B, N])
+    prefix = rng.integers(prefix_range[0], prefix_range[1] + 1, size=B).astype(np.int32)
+    Lmax = int(prefix.max()) + N + int(lmax_pad)
+    k = bf16_bits(rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32))
+    v = bf16_bits(rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32))
+    acc = (np.asarray(lens, dtype=np.int32) if lens is not None
+           else rng.integers(-1, N, size=B).astype(np.int32))
+    nodes = np.full((B, N), -1, dtype=np.int32)
+    for b in range(B):
+        ln = int(acc[b])
+        if ln > 0:
+            nodes[b, :ln] = np.sort(rng.choice(np.arange(1, N), size=ln, replace=False))
+    return CompactCase(k, v, prefix, acc, nodes)
 
 
 # ----------------------------------------------------------------------------------------------
