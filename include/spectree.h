@@ -58,6 +58,8 @@ typedef enum {
 #define SPEC_ST_BAD_TOKEN 4  /* a draft token tree_tokens[b][i >= 1] outside [0, V)                */
 #define SPEC_ST_NONFINITE 8  /* NaN or +Inf in a target-logit row that was read, or a bad p value  */
 #define SPEC_ST_TIMEOUT 16   /* a bounded device-side wait gave up                                 */
+#define SPEC_ST_BAD_PAGE 32  /* paged cache: a block-table entry a call needs is outside [0, pages) */
+#define SPEC_ST_BAD_PATH 64  /* compaction: accepted nodes not increasing in [1, N), or L+1+len>Lmax */
 
 /* ------------------------------------------------------------------------------------------------
  * Tree attention
@@ -163,6 +165,63 @@ int spec_tree_verify_noalloc(const float* target_logits, const float* draft_prob
                              int32_t* out_accept_len, int32_t* out_accepted_tokens,
                              int32_t* out_bonus_token, int32_t* out_accepted_nodes,
                              float* out_child_q, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * Tree attention over a paged KV cache
+ * ------------------------------------------------------------------------------------------------
+ * Survey explainer, "vLLMでの実装状況" section: serving stacks run speculative decoding on
+ * PagedAttention; EAGLE explainer, vLLM usage section: the tree's nodes take extra KV-cache slots.
+ * Layout (a reading; the pages give none): the cache is cut into pages of page_size slots,
+ *   k_pages, v_pages  bf16 [num_pages, Hkv, page_size, D]
+ *   block_table       int32 [B, max_pages]: slot s of sequence b lives in page
+ *                     block_table[b][s / page_size], row s % page_size
+ * Lmax = max_pages * page_size.  The other arguments, the visibility rule and the outputs are those
+ * of spec_tree_attention (node i's key and value at slot L_b + i, written by the caller).  Every
+ * page holding a slot below L_b + N must be a real page; otherwise the sequence gets
+ * SPEC_ST_BAD_PAGE and unspecified output rows (no out-of-bounds access happens: such pages read as
+ * zeros).  Table entries past the pages a sequence uses are never read for keys.
+ * Supported: page_size a power of two in [16, 1024]; num_pages * Hkv * page_size < 2^31.
+ * No workspace.  Returns SPEC_OK or a negative spec_err_t before any launch.
+ */
+int spec_tree_attention_paged(const void* q, const void* k_pages, const void* v_pages,
+                              const int32_t* block_table, int page_size, int max_pages,
+                              int num_pages, const int32_t* prefix_lens,
+                              const int32_t* tree_parent, void* out, float* out_lse, int B, int N,
+                              int Hq, int Hkv, int D, float softmax_scale, int32_t* status,
+                              void* stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * Post-accept KV compaction
+ * ------------------------------------------------------------------------------------------------
+ * After spec_tree_verify accepted the path accepted_nodes[b][0 .. accept_len[b] - 1] (node ids,
+ * root excluded), commit it: the root stays at slot L_b, and slot L_b + 1 + k receives, for every
+ * KV head, the key and value that slot L_b + accepted_nodes[b][k] held before the call (in place;
+ * overlapping moves read the old values).  Other slots are untouched.
+ *   k_cache, v_cache  bf16 [B, Hkv, Lmax, D], updated in place
+ *   prefix_lens       int32 [B]  L_b
+ *   accept_len        int32 [B]  from spec_tree_verify: -1 (verification failed) leaves the
+ *                                sequence alone, 0 commits the root only
+ *   accepted_nodes    int32 [B, N] from spec_tree_verify (out_accepted_nodes)
+ *   new_prefix_lens   int32 [B] or NULL: L_b + 1 + accept_len[b] (L_b if nothing was committed);
+ *                     must not alias prefix_lens (other CTAs of the call still read it)
+ *   status            int32 [B] or NULL: SPEC_ST_BAD_PATH when the node ids are not strictly
+ *                     increasing inside [1, N) or L_b + 1 + accept_len > Lmax (the sequence is
+ *                     then left unchanged); OR-ed
+ * Supported: D in {64, 128}, N <= 64, B * Hkv * Lmax < 2^31; k_cache and v_cache 16-byte aligned.
+ */
+int spec_kv_compact(void* k_cache, void* v_cache, const int32_t* prefix_lens,
+                    const int32_t* accept_len, const int32_t* accepted_nodes,
+                    int32_t* new_prefix_lens, int B, int N, int Hkv, int D, int Lmax,
+                    int32_t* status, void* stream);
+
+/* The same moves on the paged layout of spec_tree_attention_paged (any page_size >= 1 here); a
+ * sequence whose table maps a moved slot outside [0, num_pages) gets SPEC_ST_BAD_PAGE and is left
+ * unchanged.  Destination pages must not be shared with another sequence of the call. */
+int spec_kv_compact_paged(void* k_pages, void* v_pages, const int32_t* block_table, int page_size,
+                          int max_pages, int num_pages, const int32_t* prefix_lens,
+                          const int32_t* accept_len, const int32_t* accepted_nodes,
+                          int32_t* new_prefix_lens, int B, int N, int Hkv, int D,
+                          int32_t* status, void* stream);
 
 /* Human-readable text for a spec_err_t return value or a SPEC_ST_* bit. */
 const char* spec_status_string(int code);

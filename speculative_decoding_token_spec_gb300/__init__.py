@@ -8,12 +8,19 @@ Two calls make up the hot path, both hand-written CUDA for sm_103a behind a C AB
 * ``spec_tree_verify`` -- speculative-sampling accept/reject over the tree, the walk to the accepted
   path and the bonus-token resample (greedy argmax matching at temperature 0).
 
+Beside them: ``spec_tree_attention_paged`` (the same attention over a paged KV cache) and
+``spec_kv_compact`` / ``spec_kv_compact_paged`` (after verification, the accepted path's keys and
+values move next to the root).
+
 The Python functions of the same names only marshal torch tensors into pointers and the current
 CUDA stream.  There is no CPU fallback: a missing library raises.
 """
 from ._binding import (  # noqa: F401
     SpecError,
+    spec_kv_compact,
+    spec_kv_compact_paged,
     spec_tree_attention,
+    spec_tree_attention_paged,
     spec_tree_attention_workspace,
     spec_tree_verify,
     spec_tree_verify_workspace,

@@ -22,6 +22,7 @@ SPEC_OK = 0
 ERRORS = {-1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_UNSUPPORTED", -3: "SPEC_ERR_WORKSPACE",
           -4: "SPEC_ERR_CUDA"}
 ST_BAD_TREE, ST_BAD_LEN, ST_BAD_TOKEN, ST_NONFINITE, ST_TIMEOUT = 1, 2, 4, 8, 16
+ST_BAD_PAGE, ST_BAD_PATH = 32, 64
 
 
 class SpecError(RuntimeError):
@@ -39,6 +40,11 @@ _SIGNATURES = {
     "spec_tree_verify_workspace": (_c_size, [_c_int] * 3),
     "spec_tree_verify": (_c_int, [_vp] * 5 + [_c_float] + [_c_int] * 3 + [_vp] * 5
                          + [_vp, _c_size, _vp, _vp]),
+    "spec_tree_attention_paged": (_c_int, [_vp] * 4 + [_c_int] * 3 + [_vp] * 4 + [_c_int] * 5
+                                  + [_c_float, _vp, _vp]),
+    "spec_kv_compact": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_vp, _vp]),
+    "spec_kv_compact_paged": (_c_int, [_vp] * 3 + [_c_int] * 3 + [_vp] * 4 + [_c_int] * 4
+                              + [_vp, _vp]),
     "spec_status_string": (ctypes.c_char_p, [_c_int]),
 }
 
@@ -139,6 +145,89 @@ def spec_tree_attention(q, k_cache, v_cache, prefix_lens, tree_parent, softmax_s
     if rc != SPEC_OK:
         raise SpecError("spec_tree_attention", rc)
     return out, out_lse, status
+
+
+def spec_tree_attention_paged(q, k_pages, v_pages, block_table, prefix_lens, tree_parent,
+                              softmax_scale=None, out=None, out_lse=None, want_lse=True,
+                              status=None, stream=None):
+    """Tree attention over a paged cache (pages [num_pages, Hkv, P, D], block_table [B,
+    max_pages]); returns (out, lse or None, status) like spec_tree_attention."""
+    torch = _torch()
+    B, N, Hq, D = q.shape
+    num_pages, Hkv, P, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    dev = q.device
+    _check(q, "q", torch.bfloat16, (B, N, Hq, D), dev)
+    _check(k_pages, "k_pages", torch.bfloat16, (num_pages, Hkv, P, D), dev)
+    _check(v_pages, "v_pages", torch.bfloat16, (num_pages, Hkv, P, D), dev)
+    _check(block_table, "block_table", torch.int32, (B, max_pages), dev)
+    _check(prefix_lens, "prefix_lens", torch.int32, (B,), dev)
+    _check(tree_parent, "tree_parent", torch.int32, (B, N), dev)
+    if out is None:
+        out = torch.empty((B, N, Hq, D), dtype=torch.bfloat16, device=dev)
+    if out_lse is None and want_lse:
+        out_lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    if status is None:
+        status = torch.zeros((B,), dtype=torch.int32, device=dev)
+    scale = (1.0 / math.sqrt(D)) if softmax_scale is None else float(softmax_scale)
+    rc = lib().spec_tree_attention_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), P, max_pages, num_pages,
+        _ptr(prefix_lens), _ptr(tree_parent), _ptr(out), _ptr(out_lse), B, N, Hq, Hkv, D, scale,
+        _ptr(status), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_tree_attention_paged", rc)
+    return out, out_lse, status
+
+
+def spec_kv_compact(k_cache, v_cache, prefix_lens, accept_len, accepted_nodes,
+                    new_prefix_lens=None, status=None, stream=None):
+    """Commit the accepted path in place (contiguous cache); returns (new_prefix_lens, status)."""
+    torch = _torch()
+    B, Hkv, Lmax, D = k_cache.shape
+    N = accepted_nodes.shape[1]
+    dev = k_cache.device
+    _check(k_cache, "k_cache", torch.bfloat16, (B, Hkv, Lmax, D), dev)
+    _check(v_cache, "v_cache", torch.bfloat16, (B, Hkv, Lmax, D), dev)
+    _check(prefix_lens, "prefix_lens", torch.int32, (B,), dev)
+    _check(accept_len, "accept_len", torch.int32, (B,), dev)
+    _check(accepted_nodes, "accepted_nodes", torch.int32, (B, N), dev)
+    if new_prefix_lens is None:
+        new_prefix_lens = torch.empty((B,), dtype=torch.int32, device=dev)
+    if status is None:
+        status = torch.zeros((B,), dtype=torch.int32, device=dev)
+    rc = lib().spec_kv_compact(
+        _ptr(k_cache), _ptr(v_cache), _ptr(prefix_lens), _ptr(accept_len), _ptr(accepted_nodes),
+        _ptr(new_prefix_lens), B, N, Hkv, D, Lmax, _ptr(status), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_kv_compact", rc)
+    return new_prefix_lens, status
+
+
+def spec_kv_compact_paged(k_pages, v_pages, block_table, prefix_lens, accept_len, accepted_nodes,
+                          new_prefix_lens=None, status=None, stream=None):
+    """Commit the accepted path in place (paged cache); returns (new_prefix_lens, status)."""
+    torch = _torch()
+    num_pages, Hkv, P, D = k_pages.shape
+    B, max_pages = block_table.shape
+    N = accepted_nodes.shape[1]
+    dev = k_pages.device
+    _check(k_pages, "k_pages", torch.bfloat16, (num_pages, Hkv, P, D), dev)
+    _check(v_pages, "v_pages", torch.bfloat16, (num_pages, Hkv, P, D), dev)
+    _check(block_table, "block_table", torch.int32, (B, max_pages), dev)
+    _check(prefix_lens, "prefix_lens", torch.int32, (B,), dev)
+    _check(accept_len, "accept_len", torch.int32, (B,), dev)
+    _check(accepted_nodes, "accepted_nodes", torch.int32, (B, N), dev)
+    if new_prefix_lens is None:
+        new_prefix_lens = torch.empty((B,), dtype=torch.int32, device=dev)
+    if status is None:
+        status = torch.zeros((B,), dtype=torch.int32, device=dev)
+    rc = lib().spec_kv_compact_paged(
+        _ptr(k_pages), _ptr(v_pages), _ptr(block_table), P, max_pages, num_pages,
+        _ptr(prefix_lens), _ptr(accept_len), _ptr(accepted_nodes), _ptr(new_prefix_lens),
+        B, N, Hkv, D, _ptr(status), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_kv_compact_paged", rc)
+    return new_prefix_lens, status
 
 
 def spec_tree_verify(target_logits, draft_probs, tree_tokens, tree_parent, uniforms, temperature,

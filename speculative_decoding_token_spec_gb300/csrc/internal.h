@@ -56,6 +56,10 @@ struct AttnArgs {
   int32_t* status;
   void* workspace;
   size_t ws_bytes;
+  // paged cache (page_size > 0): k / v are pages [num_pages][Hkv][page_size][D], Lmax =
+  // max_pages * page_size, block_table [B][max_pages]
+  int page_size = 0, max_pages = 0, num_pages = 0;
+  const int32_t* block_table = nullptr;
 };
 
 struct AttnPlan {
@@ -69,5 +73,20 @@ struct AttnPlan {
 
 bool attn_plan(int B, int N, int Hq, int Hkv, int D, int Lmax, int num_sms, AttnPlan* plan);
 cudaError_t launch_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream_t s);
+
+// post-accept compaction (contiguous when page_size == 0)
+struct CompactArgs {
+  void* k;
+  void* v;
+  const int32_t* prefix_lens;
+  const int32_t* accept_len;
+  const int32_t* accepted_nodes;
+  int32_t* new_prefix_lens;
+  int32_t* status;
+  int B, N, Hkv, D, Lmax;
+  int page_size = 0, max_pages = 0, num_pages = 0;
+  const int32_t* block_table = nullptr;
+};
+cudaError_t launch_compact(const CompactArgs& a, cudaStream_t s);
 
 }  // namespace spectree

@@ -66,6 +66,105 @@ int spec_tree_attention(const void* q, const void* k_cache, const void* v_cache,
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+static bool page_size_ok(int P) { return P >= 16 && P <= 1024 && (P & (P - 1)) == 0; }
+
+int spec_tree_attention_paged(const void* q, const void* k_pages, const void* v_pages,
+                              const int32_t* block_table, int page_size, int max_pages,
+                              int num_pages, const int32_t* prefix_lens,
+                              const int32_t* tree_parent, void* out, float* out_lse, int B, int N,
+                              int Hq, int Hkv, int D, float softmax_scale, int32_t* status,
+                              void* stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !prefix_lens || !tree_parent || !out)
+    return SPEC_ERR_INVALID_ARG;
+  if (B < 1 || B > 65535 || N < 1 || N > kMaxNodes || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 ||
+      max_pages < 1 || num_pages < 1 || !std::isfinite(softmax_scale) || !(softmax_scale > 0.f))
+    return SPEC_ERR_INVALID_ARG;
+  if (!page_size_ok(page_size)) return SPEC_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
+  const long long lmax = (long long)max_pages * page_size;
+  if (lmax < N) return SPEC_ERR_INVALID_ARG;
+  if (lmax >= (1ll << 31) || (long long)num_pages * Hkv * page_size >= (1ll << 31))
+    return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+    return SPEC_ERR_INVALID_ARG;
+  const int sms = sm_count();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  AttnPlan plan;
+  if (!attn_plan(B, N, Hq, Hkv, D, (int)lmax, sms, &plan)) return SPEC_ERR_INVALID_ARG;
+  if (plan.ws_bytes > 0) return SPEC_ERR_UNSUPPORTED;  // this path takes no workspace
+  AttnArgs a{q, k_pages, v_pages, prefix_lens, tree_parent, out, out_lse, B, N, Hq, Hkv, D,
+             (int)lmax, softmax_scale, status, nullptr, 0};
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.block_table = block_table;
+  cudaError_t e = launch_attention(a, plan, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+static int compact_common(CompactArgs& a, void* stream) {
+  if (!a.k || !a.v || !a.prefix_lens || !a.accept_len || !a.accepted_nodes)
+    return SPEC_ERR_INVALID_ARG;
+  if (a.new_prefix_lens && a.new_prefix_lens == a.prefix_lens) return SPEC_ERR_INVALID_ARG;
+  if (a.B < 1 || a.B > 65535 || a.N < 1 || a.N > kMaxNodes || a.Hkv < 1 || a.Hkv > 65535 ||
+      a.Lmax < 1)
+    return SPEC_ERR_INVALID_ARG;
+  if (a.D != 64 && a.D != 128) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(a.k) || !aligned16(a.v)) return SPEC_ERR_INVALID_ARG;
+  cudaError_t e = launch_compact(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+int spec_kv_compact(void* k_cache, void* v_cache, const int32_t* prefix_lens,
+                    const int32_t* accept_len, const int32_t* accepted_nodes,
+                    int32_t* new_prefix_lens, int B, int N, int Hkv, int D, int Lmax,
+                    int32_t* status, void* stream) {
+  if ((long long)B * Hkv * (long long)Lmax >= (1ll << 31)) return SPEC_ERR_UNSUPPORTED;
+  CompactArgs a;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.prefix_lens = prefix_lens;
+  a.accept_len = accept_len;
+  a.accepted_nodes = accepted_nodes;
+  a.new_prefix_lens = new_prefix_lens;
+  a.status = status;
+  a.B = B;
+  a.N = N;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.Lmax = Lmax;
+  return compact_common(a, stream);
+}
+
+int spec_kv_compact_paged(void* k_pages, void* v_pages, const int32_t* block_table, int page_size,
+                          int max_pages, int num_pages, const int32_t* prefix_lens,
+                          const int32_t* accept_len, const int32_t* accepted_nodes,
+                          int32_t* new_prefix_lens, int B, int N, int Hkv, int D,
+                          int32_t* status, void* stream) {
+  if (!block_table || page_size < 1 || max_pages < 1 || num_pages < 1) return SPEC_ERR_INVALID_ARG;
+  const long long lmax = (long long)max_pages * page_size;
+  if (lmax >= (1ll << 31) || (long long)num_pages * Hkv * page_size >= (1ll << 31))
+    return SPEC_ERR_UNSUPPORTED;
+  CompactArgs a;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.prefix_lens = prefix_lens;
+  a.accept_len = accept_len;
+  a.accepted_nodes = accepted_nodes;
+  a.new_prefix_lens = new_prefix_lens;
+  a.status = status;
+  a.B = B;
+  a.N = N;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.Lmax = (int)lmax;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.block_table = block_table;
+  return compact_common(a, stream);
+}
+
 size_t spec_tree_verify_workspace(int B, int N, int V) {
   if (B < 1 || N < 1 || N > kMaxNodes || V < 1) return 0;
   return verify_workspace_bytes(B, N, V);
@@ -129,6 +228,9 @@ const char* spec_status_string(int code) {
     case SPEC_ST_BAD_TOKEN: return "draft token outside [0, V)";
     case SPEC_ST_NONFINITE: return "NaN/Inf in a target-logit row or a bad draft probability";
     case SPEC_ST_TIMEOUT: return "a bounded device-side wait gave up";
+    case SPEC_ST_BAD_PAGE: return "block-table entry outside [0, num_pages) for a slot the call uses";
+    case SPEC_ST_BAD_PATH:
+      return "accepted nodes not increasing inside [1, N), or L_b + 1 + accept_len > Lmax";
     default: return "unknown status code";
   }
 }

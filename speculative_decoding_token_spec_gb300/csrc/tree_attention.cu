@@ -56,6 +56,10 @@ struct AttnKParams {
   int kg;  // key groups per MMA row block: 2 when R <= 64, else 1
   int row_blocks, splits, tiles_per_split, tiles_total;
   float scale_log2;  // softmax_scale * log2(e)
+  // paged cache (page_size > 0): slot s of sequence b in page block_table[b * max_pages + s / P],
+  // row s % P, pages [num_pages][Hkv][P][D]; 0: contiguous [B][Hkv][Lmax][D]
+  int page_size, max_pages, num_pages;
+  const int32_t* block_table;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -152,7 +156,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   // ---- set-up, with the first K/V tiles in flight as early as possible
   const int tps = p.tiles_per_split;
   const int t_begin = split * tps;
-  const int row0 = (b * p.Hkv + kvh) * p.Lmax;
+  const int row0 = p.page_size ? 0 : (b * p.Hkv + kvh) * p.Lmax;  // contiguous cache
   const int spec = max(0, min(C::SLOTS, min(tps, p.tiles_total - t_begin)));  // before L is known
   if (tid == 0) {
     prefetch_tmap(&tmap_k);
@@ -201,22 +205,66 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   if (tid >= 64 && tid < 64 + N) parent_i = __ldg(p.parent + (size_t)b * N + (tid - 64));
   const int L = __ldg(p.prefix_lens + b);
   __syncthreads();  // the barriers are initialised; the small loads are on their way
-  if (tid == 0) {
+  // One chunk (keys 128 ci .. 128 ci + 127 of this sequence and KV head) into ring slot sl; warp 0
+  // calls it with every lane, lane 0 issues.  Contiguous cache: rows of the [B Hkv Lmax, D] view.
+  // Paged cache: the lanes read the block-table entries of the chunk's pages; an entry outside
+  // [0, num_pages) (or past the table) aims its boxes past the tensor, which reads zeros (the
+  // set-up flags it when a slot the call needs is there).  K boxes of min(P, 128) rows, V boxes of
+  // min(P, 32) rows in the PV block order (see v_block_key).
+  auto issue_chunk = [&](int sl, int ci) {
+    uint8_t* st = ring + sl * C::TILE;
+    const uint32_t fb = bar(B_FULL + sl);
+    if (lane == 0) mbar_arrive_expect_tx(fb, C::TILE);
+    const int P = p.page_size;
+    if (P == 0) {
+      const int y = row0 + ci * C::KEYS;
+      if (lane == 0) {
+#pragma unroll
+        for (int bx = 0; bx < C::NB; ++bx) {
+          tma_load_2d(smem_u32(st + bx * C::BOX), &tmap_k, fb, bx * 64, y);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX + j * 32 * 128), &tmap_v, fb, bx * 64,
+                        y + 32 * v_block_key(j));
+        }
+      }
+      return;
+    }
+    const int lp0 = (ci * C::KEYS) / P;
+    const int past = p.num_pages * p.Hkv * P;  // first row past the tensor
+    int yl = past;                             // lane l: first row of the chunk's l-th page
+    if (lane < (P >= C::KEYS ? 1 : C::KEYS / P) && lp0 + lane < p.max_pages) {
+      const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + lp0 + lane);
+      if (pg >= 0 && pg < p.num_pages) yl = (pg * p.Hkv + kvh) * P;
+    }
+    auto row_of = [&](int key) {  // every lane calls this (shuffle)
+      const int y = __shfl_sync(0xffffffffu, yl, key / P - lp0);
+      return y >= past ? past : y + key % P;
+    };
+    const int kb_rows = P < C::KEYS ? P : C::KEYS, vb_rows = P < 32 ? P : 32;
+#pragma unroll 1
+    for (int i = 0; i < C::KEYS / kb_rows; ++i) {
+      const int y = row_of(ci * C::KEYS + i * kb_rows);
+      if (lane == 0)
+#pragma unroll
+        for (int bx = 0; bx < C::NB; ++bx)
+          tma_load_2d(smem_u32(st + bx * C::BOX + i * kb_rows * 128), &tmap_k, fb, bx * 64, y);
+    }
+#pragma unroll 1
+    for (int i = 0; i < C::KEYS / vb_rows; ++i) {
+      const int j = (i * vb_rows) >> 5, t = (i * vb_rows) & 31;  // V row block j, row t in it
+      const int y = row_of(ci * C::KEYS + 32 * v_block_key(j) + t);
+      if (lane == 0)
+#pragma unroll
+        for (int bx = 0; bx < C::NB; ++bx)
+          tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX + (32 * j + t) * 128), &tmap_v, fb,
+                      bx * 64, y);
+    }
+  };
+  if (warp == 0) {
     // the split's first chunks do not depend on the prefix length: issue them now (a chunk past
     // L_b + N is simply not consumed).  Nothing else waits for this issue.
-    for (int it = 0; it < spec; ++it) {
-      mbar_arrive_expect_tx(bar(B_FULL + it), C::TILE);
-      uint8_t* st = ring + it * C::TILE;
-      const int y = row0 + (t_begin + it) * C::KEYS;
-#pragma unroll
-      for (int bx = 0; bx < C::NB; ++bx) {
-        tma_load_2d(smem_u32(st + bx * C::BOX), &tmap_k, bar(B_FULL + it), bx * 64, y);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX + j * 32 * 128), &tmap_v,
-                      bar(B_FULL + it), bx * 64, y + 32 * v_block_key(j));
-      }
-    }
+    for (int it = 0; it < spec; ++it) issue_chunk(it, t_begin + it);
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_s), C::TMEM_COLS);
 
@@ -257,6 +305,16 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       anc_s[i] = m;
     }
     if (tid == 64 && (L < 0 || L + N > p.Lmax)) atomicOr(&bad_s, SPEC_ST_BAD_LEN);
+    if (p.page_size > 0 && L >= 0 && L + N <= p.Lmax) {
+      // paged: every page holding a slot this split reads must be a real page
+      const int P = p.page_size;
+      const int k_lo = t_begin * C::KEYS, k_hi = min((t_begin + tps) * C::KEYS, L + N);
+      if (k_hi > k_lo)
+        for (int lp = k_lo / P + (tid - 32); lp <= (k_hi - 1) / P; lp += 288) {
+          const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + lp);
+          if (pg < 0 || pg >= p.num_pages) atomicOr(&bad_s, SPEC_ST_BAD_PAGE);
+        }
+    }
     tc_fence_before();
     named_bar_sync(2, 288);
     tc_fence_after();
@@ -266,7 +324,8 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   }
   const int bad_bits = bad_s;
   const bool bad = bad_bits != 0;
-  if (tid == 64 && bad && split == 0 && kvh == 0 && rb == 0 && p.status)
+  if (tid == 64 && bad && p.status &&
+      ((bad_bits & SPEC_ST_BAD_PAGE) || (split == 0 && kvh == 0 && rb == 0)))
     atomicOr(p.status + b, bad_bits);
   const uint32_t tmem = tmem_s;
 
@@ -286,25 +345,16 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   float m_used = -INFINITY, l = 0.f;  // softmax threads: running max (log2 units) and sum
   bool ok_rows = true;                // softmax warps: every step completed (no timeout)
   if (warp == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer (the whole warp: it reads block-table entries in parallel)
+    int issued = spec;
+    for (int it = spec; it < my_tiles; ++it) {
+      const int s = it % C::SLOTS;
+      if (it >= C::SLOTS && !__all_sync(0xffffffffu, wait(B_EMPTY + s, ((it / C::SLOTS) - 1) & 1)))
+        break;
+      issue_chunk(s, t_begin + it);
+      issued = it + 1;
+    }
     if (lane == 0) {
-      int issued = spec;
-      for (int it = spec; it < my_tiles; ++it) {
-        const int s = it % C::SLOTS;
-        if (it >= C::SLOTS && !wait(B_EMPTY + s, ((it / C::SLOTS) - 1) & 1)) break;
-        uint8_t* st = ring + s * C::TILE;
-        mbar_arrive_expect_tx(bar(B_FULL + s), C::TILE);
-        const int y = row0 + (t_begin + it) * C::KEYS;
-#pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx) {
-          tma_load_2d(smem_u32(st + bx * C::BOX), &tmap_k, bar(B_FULL + s), bx * 64, y);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX + j * 32 * 128), &tmap_v,
-                        bar(B_FULL + s), bx * 64, y + 32 * v_block_key(j));
-        }
-        issued = it + 1;
-      }
       // never leave with a copy in flight: speculative tiles nobody consumed, or an abort
       // (bounded waits)
       if (abort_s || my_tiles < spec)
@@ -822,9 +872,12 @@ static cudaError_t launch_d(const CUtensorMap& mk, const CUtensorMap& mv, const 
 
 cudaError_t launch_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream_t s) {
   CUtensorMap mk, mv;
-  const long long rows = (long long)a.B * a.Hkv * a.Lmax;
-  // K in boxes of a whole chunk; V in 32-key boxes (stored in the PV order, see v_block_key)
-  if (!make_kv_map(&mk, a.k, a.D, rows, kChunkKeys) || !make_kv_map(&mv, a.v, a.D, rows, 32))
+  const int P = a.page_size;
+  const long long rows =
+      P > 0 ? (long long)a.num_pages * a.Hkv * P : (long long)a.B * a.Hkv * a.Lmax;
+  // K in boxes of a whole chunk (or page); V in 32-key boxes (or pages), stored in the PV order
+  const int kb = P > 0 && P < kChunkKeys ? P : kChunkKeys, vb = P > 0 && P < 32 ? P : 32;
+  if (!make_kv_map(&mk, a.k, a.D, rows, kb) || !make_kv_map(&mv, a.v, a.D, rows, vb))
     return cudaErrorInvalidValue;
   AttnKParams kp;
   kp.q = static_cast<const __nv_bfloat16*>(a.q);
@@ -846,6 +899,10 @@ cudaError_t launch_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream
   kp.tiles_per_split = plan.tiles_per_split;
   kp.tiles_total = plan.tiles;
   kp.scale_log2 = a.scale * 1.4426950408889634f;
+  kp.page_size = P;
+  kp.max_pages = a.max_pages;
+  kp.num_pages = a.num_pages;
+  kp.block_table = a.block_table;
   return a.D == 128 ? launch_d<128>(mk, mv, kp, s) : launch_d<64>(mk, mv, kp, s);
 }
 

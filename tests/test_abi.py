@@ -32,7 +32,8 @@ def lib():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("spec_tree_attention", "spec_tree_verify", "spec_tree_attention_workspace",
-              "spec_tree_verify_workspace", "spec_status_string"):
+              "spec_tree_verify_workspace", "spec_status_string", "spec_tree_attention_paged",
+              "spec_kv_compact", "spec_kv_compact_paged"):
         assert n in names
 
 
@@ -42,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, 1, 2, 4, 8, 16):
+    for code in (0, -1, -2, -3, -4, 1, 2, 4, 8, 16, 32, 64):
         assert lib.spec_status_string(code)
     assert b"unknown" in lib.spec_status_string(12345)
 
@@ -100,3 +101,44 @@ def test_argument_errors_are_synchronous(lib):
         rc = lib.spec_tree_attention(*args, fake, null, 1, 5, 8, 8, 128, 200, scale, fake,
                                      1 << 20, null, null)
         assert rc == -1
+
+
+def test_paged_and_compaction_argument_errors(lib):
+    """The new entry points reject bad arguments before any CUDA call (works without a GPU)."""
+    fake = ctypes.c_void_p(256)
+    null = None
+    # paged attention: q, k_pages, v_pages, block_table, P, max_pages, num_pages, lens, parent,
+    # out, lse, B, N, Hq, Hkv, D, scale, status, stream
+    def attn(P=16, max_pages=8, num_pages=10, N=5, D=128, table=fake, scale=0.1):
+        return lib.spec_tree_attention_paged(fake, fake, fake, table, P, max_pages, num_pages,
+                                             fake, fake, fake, null, 1, N, 8, 8, D, scale, null,
+                                             null)
+    for P in (8, 24, 2048):            # page size: a power of two in [16, 1024]
+        assert attn(P=P) == -2
+    assert attn(table=null) == -1
+    assert attn(max_pages=0) == -1
+    assert attn(num_pages=0) == -1
+    assert attn(D=96) == -2
+    assert attn(N=65) == -1
+    assert attn(P=16, max_pages=1, N=20) == -1        # Lmax = 16 < N
+    assert attn(scale=float("nan")) == -1
+    assert attn(P=1024, num_pages=1 << 20) == -2       # num_pages * Hkv * P >= 2^31
+    # compaction: k, v, lens, accept_len, nodes, new_lens, B, N, Hkv, D, Lmax, status, stream
+    lens = ctypes.c_void_p(512)
+    def comp(new_lens=fake, k=fake, B=1, N=5, D=128, Lmax=100):
+        return lib.spec_kv_compact(k, fake, lens, fake, fake, new_lens, B, N, 8, D, Lmax, null,
+                                   null)
+    assert comp(new_lens=lens) == -1                   # new lengths may not alias prefix_lens
+    assert comp(k=null) == -1
+    assert comp(N=65) == -1
+    assert comp(D=80) == -2
+    assert comp(B=0) == -1
+    assert comp(Lmax=1 << 30, B=8) == -2               # B * Hkv * Lmax >= 2^31
+    # paged compaction: k, v, table, P, max_pages, num_pages, lens, accept_len, nodes, new_lens,
+    # B, N, Hkv, D, status, stream
+    rc = lib.spec_kv_compact_paged(fake, fake, null, 16, 4, 4, lens, fake, fake, fake, 1, 5, 8,
+                                   128, null, null)
+    assert rc == -1
+    rc = lib.spec_kv_compact_paged(fake, fake, fake, 0, 4, 4, lens, fake, fake, fake, 1, 5, 8,
+                                   128, null, null)
+    assert rc == -1
