@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip the paged-attention and KV-compaction measurements")
     ap.add_argument("--cpu-child", default=None, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -431,6 +433,8 @@ def run_ours(args):
 
     if rank != 0:
         return
+    nxt = None if args.no_next else measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs,
+                                                      attn_ms, timed, dev, L2)
     # ---- CPU oracle baseline (bounded sample)
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
@@ -474,8 +478,95 @@ def run_ours(args):
         "gpu_launches": launches_per_step * K,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "next_rows": nxt,
     }
     print(json.dumps(line))
+
+
+def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev, L2):
+    """Paged-cache attention (16-slot pages) and post-accept KV compaction on this workload.
+
+    Paged attention: the same queries, tree and prefix over pages in a random physical order,
+    rotated over device copies larger than 2 x L2, timed per call from CUDA graphs; its
+    algorithmic bytes are those of the contiguous call.  Compaction: the accepted paths that the
+    verification kernel produced in this run, applied to each copy's contiguous cache (in place,
+    after every other measurement), timed the same way; algorithmic bytes = the moved rows read
+    and written.
+    """
+    import numpy as np
+    import torch
+    import speculative_decoding_token_spec_gb300 as st
+    from speculative_decoding_token_spec_gb300 import workloads as W
+    page = 16
+    pc = W.make_paged_attention_case(cfg, page, seed=args.seed)
+    per_copy = pc.k_pages.nbytes * 2 + pc.q.nbytes
+    ncp = max(2, math.ceil(2 * L2 / per_copy))
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    pcs = [{"q": to_dev(pc.q).view(torch.bfloat16), "k": to_dev(pc.k_pages).view(torch.bfloat16),
+            "v": to_dev(pc.v_pages).view(torch.bfloat16), "t": to_dev(pc.block_table),
+            "lens": to_dev(pc.prefix_lens), "par": to_dev(pc.tree_parent),
+            "out": torch.empty(pc.q.shape, dtype=torch.bfloat16, device=dev),
+            "lse": torch.empty((pc.q.shape[0], pc.q.shape[2], pc.q.shape[1]),
+                               dtype=torch.float32, device=dev),
+            "st": torch.zeros((pc.q.shape[0],), dtype=torch.int32, device=dev)}
+           for _ in range(ncp)]
+
+    def paged(c):
+        st.spec_tree_attention_paged(c["q"], c["k"], c["v"], c["t"], c["lens"], c["par"],
+                                     softmax_scale=pc.scale, out=c["out"], out_lse=c["lse"],
+                                     status=c["st"])
+
+    def compact(c):
+        st.spec_kv_compact(c["k"], c["v"], c["lens"], c["vout"]["accept_len"],
+                           c["vout"]["accepted_nodes"], new_prefix_lens=c["new_lens"],
+                           status=c["st_c"])
+
+    for c in bufs:
+        c["new_lens"] = torch.empty_like(c["lens"])
+        c["st_c"] = torch.zeros_like(c["lens"])
+    for _ in range(3):
+        for c in pcs:
+            paged(c)
+        for c in bufs:
+            compact(c)
+    torch.cuda.synchronize()
+    assert all(int(c["st"].sum()) == 0 for c in pcs) and all(int(c["st_c"].sum()) == 0 for c in bufs)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+
+    def capture(fn, items):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for c in items:
+                    fn(c)
+        return g
+
+    g_p, g_c = capture(paged, pcs), capture(compact, bufs)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        g_p.replay()
+        g_c.replay()
+    torch.cuda.synchronize()
+    reps = max(1, 600 // ncp)
+    p_ms = timed(lambda: [g_p.replay() for _ in range(reps)]) / (reps * ncp)
+    reps_c = max(1, 600 // len(bufs))
+    c_ms = timed(lambda: [g_c.replay() for _ in range(reps_c)]) / (reps_c * len(bufs))
+    _, Hkv, _, D = bufs[0]["k"].shape
+    lens = bufs[0]["vout"]["accept_len"].cpu().numpy()
+    moved = int(np.maximum(lens, 0).sum()) * Hkv * D * 2 * 2 * 2  # K and V rows, read + write
+    p_gbs = attn_bytes / (p_ms * 1e-3) / 1e9
+    return {
+        "paged_attention": {"page_size": page, "us_per_call": p_ms * 1e3, "achieved_gbs": p_gbs,
+                            "frac": p_gbs / hbm_gbs, "contiguous_us_per_call": attn_ms * 1e3,
+                            "algorithmic_bytes": attn_bytes, "copies": ncp,
+                            "kernel": "tree_attn_kernel, boxes addressed through the block table"},
+        "kv_compact": {"us_per_call": c_ms * 1e3, "accept_len": lens.tolist(),
+                       "algorithmic_bytes": moved,
+                       "achieved_gbs": moved / (c_ms * 1e-3) / 1e9,
+                       "note": "latency-bound: a few KB to a few hundred KB per call"},
+        "peak_gbs": hbm_gbs,
+    }
 
 
 def profiled_traffic(kernel):

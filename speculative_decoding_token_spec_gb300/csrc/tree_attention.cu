@@ -125,7 +125,9 @@ __host__ __device__ inline int owned_rows(int kg, int splits) {
   return (128 / kg + splits - 1) / splits;
 }
 
-template <int D>
+// PAGED: the cache is paged (p.page_size > 0); a separate instantiation so that the contiguous
+// kernel carries none of the page-table code.
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const AttnKParams p) {
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   // ---- set-up, with the first K/V tiles in flight as early as possible
   const int tps = p.tiles_per_split;
   const int t_begin = split * tps;
-  const int row0 = p.page_size ? 0 : (b * p.Hkv + kvh) * p.Lmax;  // contiguous cache
+  const int row0 = PAGED ? 0 : (b * p.Hkv + kvh) * p.Lmax;  // contiguous cache
   const int spec = max(0, min(C::SLOTS, min(tps, p.tiles_total - t_begin)));  // before L is known
   if (tid == 0) {
     prefetch_tmap(&tmap_k);
@@ -206,19 +208,30 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   const int L = __ldg(p.prefix_lens + b);
   __syncthreads();  // the barriers are initialised; the small loads are on their way
   // One chunk (keys 128 ci .. 128 ci + 127 of this sequence and KV head) into ring slot sl; warp 0
-  // calls it with every lane, lane 0 issues.  Contiguous cache: rows of the [B Hkv Lmax, D] view.
-  // Paged cache: the lanes read the block-table entries of the chunk's pages; an entry outside
-  // [0, num_pages) (or past the table) aims its boxes past the tensor, which reads zeros (the
-  // set-up flags it when a slot the call needs is there).  K boxes of min(P, 128) rows, V boxes of
-  // min(P, 32) rows in the PV block order (see v_block_key).
-  auto issue_chunk = [&](int sl, int ci) {
+  // calls it with every lane.  Contiguous cache: ten boxes (rows of the [B Hkv Lmax, D] view) from
+  // lane 0.  Paged cache: up to 32 boxes, one per lane, so that one instruction sends the whole
+  // chunk (a copy issued by one thread costs about 100 cycles); `yl` is page_rows(ci) of this
+  // lane; an entry outside [0, num_pages) (or past the table) aims its boxes past the tensor,
+  // which reads zeros (the set-up flags it when a slot the call needs is there).  K boxes of
+  // min(P, 128) rows, V boxes of min(P, 32) rows in the PV block order (see v_block_key).
+  const int P = PAGED ? p.page_size : 0;
+  const int past = p.num_pages * p.Hkv * P;  // paged: first row past the tensor
+  auto page_rows = [&](int ci) -> int {     // lane l: first row of the chunk's l-th page
+    int yl = past;
+    const int lp0 = (ci * C::KEYS) / P;
+    if (lane < (P >= C::KEYS ? 1 : C::KEYS / P) && lp0 + lane < p.max_pages) {
+      const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + lp0 + lane);
+      if (pg >= 0 && pg < p.num_pages) yl = (pg * p.Hkv + kvh) * P;
+    }
+    return yl;
+  };
+  auto issue_chunk = [&](int sl, int ci, int yl) {
     uint8_t* st = ring + sl * C::TILE;
     const uint32_t fb = bar(B_FULL + sl);
     if (lane == 0) mbar_arrive_expect_tx(fb, C::TILE);
-    const int P = p.page_size;
-    if (P == 0) {
-      const int y = row0 + ci * C::KEYS;
+    if (P == 0) {  // contiguous: ten boxes, issued in order by one lane (K first) measured faster
       if (lane == 0) {
+        const int y = row0 + ci * C::KEYS;
 #pragma unroll
         for (int bx = 0; bx < C::NB; ++bx) {
           tma_load_2d(smem_u32(st + bx * C::BOX), &tmap_k, fb, bx * 64, y);
@@ -230,41 +243,47 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       }
       return;
     }
-    const int lp0 = (ci * C::KEYS) / P;
-    const int past = p.num_pages * p.Hkv * P;  // first row past the tensor
-    int yl = past;                             // lane l: first row of the chunk's l-th page
-    if (lane < (P >= C::KEYS ? 1 : C::KEYS / P) && lp0 + lane < p.max_pages) {
-      const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + lp0 + lane);
-      if (pg >= 0 && pg < p.num_pages) yl = (pg * p.Hkv + kvh) * P;
-    }
-    auto row_of = [&](int key) {  // every lane calls this (shuffle)
-      const int y = __shfl_sync(0xffffffffu, yl, key / P - lp0);
-      return y >= past ? past : y + key % P;
-    };
-    const int kb_rows = P < C::KEYS ? P : C::KEYS, vb_rows = P < 32 ? P : 32;
-#pragma unroll 1
-    for (int i = 0; i < C::KEYS / kb_rows; ++i) {
-      const int y = row_of(ci * C::KEYS + i * kb_rows);
-      if (lane == 0)
-#pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx)
-          tma_load_2d(smem_u32(st + bx * C::BOX + i * kb_rows * 128), &tmap_k, fb, bx * 64, y);
-    }
-#pragma unroll 1
-    for (int i = 0; i < C::KEYS / vb_rows; ++i) {
+    __syncwarp();
+    const int kb_rows = (P == 0 || P >= C::KEYS) ? C::KEYS : P;
+    const int vb_rows = (P == 0 || P >= 32) ? 32 : P;
+    const int nk = C::NB * (C::KEYS / kb_rows), nv = C::NB * (C::KEYS / vb_rows);
+    int key = ci * C::KEYS, dst = 0, bx = 0;  // this lane's box: list of K boxes, then V boxes
+    const bool is_v = lane >= nk;
+    if (!is_v) {
+      const int i = lane % (C::KEYS / kb_rows);
+      bx = lane / (C::KEYS / kb_rows);
+      key += i * kb_rows;
+      dst = bx * C::BOX + i * kb_rows * 128;
+    } else if (lane < nk + nv) {
+      const int m = lane - nk, i = m % (C::KEYS / vb_rows);
+      bx = m / (C::KEYS / vb_rows);
       const int j = (i * vb_rows) >> 5, t = (i * vb_rows) & 31;  // V row block j, row t in it
-      const int y = row_of(ci * C::KEYS + 32 * v_block_key(j) + t);
-      if (lane == 0)
-#pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx)
-          tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX + (32 * j + t) * 128), &tmap_v, fb,
-                      bx * 64, y);
+      key += 32 * v_block_key(j) + t;
+      dst = (C::NB + bx) * C::BOX + (32 * j + t) * 128;
     }
+    int y;
+    if (P == 0) {
+      y = row0 + key;
+    } else {
+      y = __shfl_sync(0xffffffffu, yl, key / P - (ci * C::KEYS) / P);
+      y = y >= past ? past : y + key % P;
+    }
+    if (lane < nk + nv) tma_load_2d(smem_u32(st + dst), is_v ? &tmap_v : &tmap_k, fb, bx * 64, y);
   };
   if (warp == 0) {
     // the split's first chunks do not depend on the prefix length: issue them now (a chunk past
-    // L_b + N is simply not consumed).  Nothing else waits for this issue.
-    for (int it = 0; it < spec; ++it) issue_chunk(it, t_begin + it);
+    // L_b + N is simply not consumed).  Nothing else waits for this issue.  Paged: every page
+    // entry first (independent loads), then the copies.
+    if constexpr (PAGED) {
+      int yl[C::SLOTS];
+#pragma unroll
+      for (int it = 0; it < C::SLOTS; ++it) yl[it] = it < spec ? page_rows(t_begin + it) : 0;
+#pragma unroll
+      for (int it = 0; it < C::SLOTS; ++it)
+        if (it < spec) issue_chunk(it, t_begin + it, yl[it]);
+    } else {
+      for (int it = 0; it < spec; ++it) issue_chunk(it, t_begin + it, 0);
+    }
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_s), C::TMEM_COLS);
 
@@ -305,7 +324,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       anc_s[i] = m;
     }
     if (tid == 64 && (L < 0 || L + N > p.Lmax)) atomicOr(&bad_s, SPEC_ST_BAD_LEN);
-    if (p.page_size > 0 && L >= 0 && L + N <= p.Lmax) {
+    if (PAGED && L >= 0 && L + N <= p.Lmax) {
       // paged: every page holding a slot this split reads must be a real page
       const int P = p.page_size;
       const int k_lo = t_begin * C::KEYS, k_hi = min((t_begin + tps) * C::KEYS, L + N);
@@ -349,9 +368,10 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
     int issued = spec;
     for (int it = spec; it < my_tiles; ++it) {
       const int s = it % C::SLOTS;
+      const int yl = P > 0 ? page_rows(t_begin + it) : 0;  // in flight during the wait
       if (it >= C::SLOTS && !__all_sync(0xffffffffu, wait(B_EMPTY + s, ((it / C::SLOTS) - 1) & 1)))
         break;
-      issue_chunk(s, t_begin + it);
+      issue_chunk(s, t_begin + it, yl);
       issued = it + 1;
     }
     if (lane == 0) {
@@ -785,7 +805,7 @@ static cudaLaunchConfig_t launch_config(int splits, dim3 grid, cudaStream_t s,
 }
 
 // Opt the kernel into its shared-memory size on the current device (once per device).
-template <int D>
+template <int D, bool PAGED>
 static cudaError_t prepare_kernel() {
   constexpr int kDev = 64;
   static std::mutex mu;
@@ -796,7 +816,7 @@ static cudaError_t prepare_kernel() {
   if (dev < 0 || dev >= kDev) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (!done[dev]) {
-    e = cudaFuncSetAttribute(tree_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tree_attn_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              TcCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     done[dev] = true;
@@ -812,13 +832,13 @@ static int clusters_per_wave(int splits) {
   static int cache[kDev][kMaxSplits + 1] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDev) return 0;
-  if (prepare_kernel<D>() != cudaSuccess) return 0;
+  if (prepare_kernel<D, false>() != cudaSuccess) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (cache[dev][splits] == 0) {
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config<D>(splits, dim3(splits, 1, 1), nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tree_attn_kernel<D>, &cfg) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveClusters(&n, tree_attn_kernel<D, false>, &cfg) != cudaSuccess || n < 1)
       return 0;
     cache[dev][splits] = n;
   }
@@ -859,15 +879,15 @@ bool attn_plan(int B, int N, int Hq, int Hkv, int D, int Lmax, int num_sms, Attn
   return true;
 }
 
-template <int D>
+template <int D, bool PAGED>
 static cudaError_t launch_d(const CUtensorMap& mk, const CUtensorMap& mv, const AttnKParams& kp,
                             cudaStream_t s) {
-  cudaError_t e = prepare_kernel<D>();
+  cudaError_t e = prepare_kernel<D, PAGED>();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg =
       launch_config<D>(kp.splits, dim3(kp.splits, kp.Hkv * kp.row_blocks, kp.B), s, attr);
-  return cudaLaunchKernelEx(&cfg, tree_attn_kernel<D>, mk, mv, kp);
+  return cudaLaunchKernelEx(&cfg, tree_attn_kernel<D, PAGED>, mk, mv, kp);
 }
 
 cudaError_t launch_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream_t s) {
@@ -903,7 +923,9 @@ cudaError_t launch_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream
   kp.max_pages = a.max_pages;
   kp.num_pages = a.num_pages;
   kp.block_table = a.block_table;
-  return a.D == 128 ? launch_d<128>(mk, mv, kp, s) : launch_d<64>(mk, mv, kp, s);
+  if (P > 0)
+    return a.D == 128 ? launch_d<128, true>(mk, mv, kp, s) : launch_d<64, true>(mk, mv, kp, s);
+  return a.D == 128 ? launch_d<128, false>(mk, mv, kp, s) : launch_d<64, false>(mk, mv, kp, s);
 }
 
 }  // namespace spectree
