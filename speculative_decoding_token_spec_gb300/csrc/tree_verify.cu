@@ -63,6 +63,8 @@ struct __align__(16) Entry {
 };
 static_assert(sizeof(Entry) == 32, "Entry layout");
 
+constexpr int kMaxCluster = 8;  // the portable cluster size
+
 struct VerifySmem {
   int parent[kMaxNodes];
   int tokens[kMaxNodes];
@@ -81,9 +83,9 @@ struct VerifySmem {
   float g_px[kMaxNodes];
   DF g_n[kMaxNodes];            // numerators n(x~) of the children's current q values
   Entry wpart[kVWarps];         // this CTA's warp entries of the current exchange
-  Entry cpart[2][8];            // every CTA's entry, per exchange slot (sent here by st.async)
+  Entry cpart[2][kMaxCluster];  // every CTA's entry, per exchange slot (sent here by st.async)
   DF wcur[kVWarps];             // totals of the current sampling weights: this CTA's warps,
-  DF ccur[8];                   // and every CTA of the cluster (e(y) scale)
+  DF ccur[kMaxCluster];         // and every CTA of the cluster (e(y) scale)
   NodeStat st[kMaxNodes];
   Entry xres;                     // result of the current exchange (written by warp 0)
   __align__(8) uint64_t xbar[2];  // transaction barriers of the exchange slots
@@ -229,14 +231,15 @@ __device__ __forceinline__ Entry shfl_entry(const Entry& e, int o) {
   return f;
 }
 
-// Combination of the entries held by lanes 0..7 (in lane order), in every one of those lanes.
+// Combination of the entries held by lanes 0..W-1 (in lane order), in every one of those lanes.
 // Max-sums take the max first and rescale each lane's sum once.
-__device__ __forceinline__ Entry lanes8_combine(Entry e, int kind, float k) {
+template <int W = 8>
+__device__ __forceinline__ Entry lanes_combine(Entry e, int kind, float k) {
   const int lane = threadIdx.x & 31;
   if (kind == kXMaxSum) {
     float M = e.m;
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int o = W / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float f = (e.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(e.m, M), k));
     const DF sc = df_scale(DF{e.s_hi, e.s_lo}, f);
     e.m = M;
@@ -245,7 +248,7 @@ __device__ __forceinline__ Entry lanes8_combine(Entry e, int kind, float k) {
     kind = kXSum;
   }
 #pragma unroll
-  for (int o = 4; o > 0; o >>= 1) {
+  for (int o = W / 2; o > 0; o >>= 1) {
     const Entry f = shfl_entry(e, o);
     e = (lane & o) ? entry_combine(f, e, kind, k) : entry_combine(e, f, kind, k);
   }
@@ -268,7 +271,7 @@ __device__ Entry exchange(VerifySmem& sm, int& xk, const Entry& mine, int kind, 
   xslot = slot;
   if (wid == 0) {
     const uint32_t bar = smem_u32(&sm.xbar[slot]);
-    const Entry c = lanes8_combine(lane < kVWarps ? sm.wpart[lane] : entry_identity(kind), kind, k);
+    const Entry c = lanes_combine<8>(lane < kVWarps ? sm.wpart[lane] : entry_identity(kind), kind, k);
     if (lane == 0) mbar_arrive_expect_tx(bar, CL * (uint32_t)sizeof(Entry));
     if (lane < CL) {
       const uint32_t dst = dsmem_addr(&sm.cpart[slot][rank], lane);
@@ -278,7 +281,7 @@ __device__ Entry exchange(VerifySmem& sm, int& xk, const Entry& mine, int kind, 
       st_async_v4(dst + 16, v[1], rbar);
     }
     const bool ok = __all_sync(0xffffffffu, mbar_wait_acq_cluster(bar, parity));
-    Entry r = lanes8_combine(lane < CL ? sm.cpart[slot][lane] : entry_identity(kind), kind, k);
+    Entry r = lanes_combine<8>(lane < CL ? sm.cpart[slot][lane] : entry_identity(kind), kind, k);
     if (lane == 0) {
       r.flags |= ok ? 0 : SPEC_ST_TIMEOUT;
       sm.xres = r;
@@ -992,8 +995,12 @@ static cudaError_t launch_ex(void (*kern)(Params...), dim3 grid, int cl, size_t 
 constexpr int kMaxSliceFloats = 26 * 1024;
 
 // Cluster size: large enough that the slice buffers fit; for latency-bound (small) problems as
-// large as slices of >= 1024 elements allow; otherwise aim for about one wave of CTAs.
-static int pick_cluster(long long units, int V, int num_sms, bool small) {
+// large as slices of >= 1024 elements allow; otherwise aim for about one wave of CTAs, then grow
+// (up to 8) until a CTA's buffers take at most ~72 KB, so that three CTAs share an SM: each node
+// is a chain of dependent steps, and one CTA per SM leaves the SM idle between them.
+constexpr size_t kLargeCtaBytes = 72 * 1024;
+
+static int pick_cluster(long long units, int V, int num_sms, bool small, int nbuf) {
   int cl = 1;
   while (cl < 8 && slice_capacity(V, cl) > kMaxSliceFloats) cl *= 2;
   if (small) {
@@ -1001,6 +1008,8 @@ static int pick_cluster(long long units, int V, int num_sms, bool small) {
     return cl;
   }
   while (cl < 8 && units * (cl * 2) <= (long long)num_sms * 3 / 2 && V / (cl * 2) >= 2048) cl *= 2;
+  while (cl < kMaxCluster && (size_t)nbuf * slice_capacity(V, cl) * sizeof(float) > kLargeCtaBytes)
+    cl *= 2;
   return cl;
 }
 
@@ -1011,7 +1020,7 @@ cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s) {
   // small problems are latency-bound: process leaves speculatively too
   const int leaves = small ? 1 : 0;
   const long long units = (long long)a.B * (leaves ? a.N : (a.N + 1) / 2);
-  const int cl = pick_cluster(units, a.V, num_sms, small);
+  const int cl = pick_cluster(units, a.V, num_sms, small, a.T > 0.f ? 2 : 1);
   const int cap = slice_capacity(a.V, cl);
   const size_t smem = (size_t)(a.T > 0.f ? 2 : 1) * cap * sizeof(float);
   const double invTd = a.T > 0.f ? 1.0 / (double)a.T : 0.0;
