@@ -37,6 +37,7 @@ struct VerifyArgs {
   NodeStat* stats;  // [B, N]
   unsigned long long* counters;  // [B] arrival counters: (call generation << 16) | arrivals
   unsigned long long gen;        // this call's generation (48 bits)
+  int p_global = 0;  // set by launch_verify: draft rows read from global memory, not staged
 };
 
 size_t verify_workspace_bytes(int B, int N, int V);

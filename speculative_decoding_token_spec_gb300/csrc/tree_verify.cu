@@ -124,6 +124,37 @@ __device__ __forceinline__ Slice make_slice(const float* row, int V, int rank, i
   return s;
 }
 
+// The draft probabilities of a slice, at the positions of the logit buffer: either staged in
+// shared memory (sbuf) or read from the row in global memory (through L2) -- positions outside
+// [lo, hi) - sbase are pads and read as 0, as the staged pads do.  row + sbase is 16-byte aligned
+// (make_slice keeps it so), so whole float4s inside the slice load as float4.
+template <bool GLOBAL>
+struct DraftSlice;
+
+template <>
+struct DraftSlice<false> {  // staged
+  const float* sbuf;
+  __device__ __forceinline__ float4 load4(int pos) const {
+    return *reinterpret_cast<const float4*>(sbuf + pos);
+  }
+  __device__ __forceinline__ float at(int pos) const { return sbuf[pos]; }
+};
+
+template <>
+struct DraftSlice<true> {  // read from the row in global memory
+  const float* grow;
+  int sbase, lo, hi;
+  __device__ __forceinline__ float at(int pos) const {
+    const int y = sbase + pos;
+    return (y >= lo && y < hi) ? __ldg(grow + y) : 0.f;
+  }
+  __device__ __forceinline__ float4 load4(int pos) const {
+    const int y = sbase + pos;
+    if (y >= lo && y + 4 <= hi) return __ldg(reinterpret_cast<const float4*>(grow + y));
+    return make_float4(at(pos), at(pos + 1), at(pos + 2), at(pos + 3));
+  }
+};
+
 // Floats of shared memory one slice buffer needs for (V, CL): the widest slice (with its ragged
 // ends) rounded up to whole runs.
 static inline int slice_capacity(int V, int cl) {
@@ -411,18 +442,18 @@ __device__ void cluster_stats(const Slice& s, float* lbuf, float k, int lflags, 
 // Residual round: returns D = sum_y max(0, e(y) - c p(y)) (cluster-wide; c_t = c / f).  check_p:
 // flag bad draft values.  The thread's total of the new weights goes to `tot`, the warp's to
 // `wt`; `xs` is the slot whose sm.cpart holds the CTA totals.
-template <int CL>
-__device__ DF cluster_residual(const Slice& s, const float* ebuf, const float* pbuf, float c_t,
+template <int CL, class PD>
+__device__ DF cluster_residual(const Slice& s, const float* ebuf, const PD& pd, float c_t,
                                float f, bool check_p, int lflags, int rank, int& xk, DF& tot,
                                DF& wt, int& xs, int& flags, VerifySmem& sm) {
   const float4* E4 = reinterpret_cast<const float4*>(ebuf + threadIdx.x * s.ch);
-  const float4* P4 = reinterpret_cast<const float4*>(pbuf + threadIdx.x * s.ch);
+  const int p0 = threadIdx.x * s.ch;
   CompSum acc;
   float pmin = 0.f, psum = 0.f;
   const RunWalk rw(s.ch);
   for (int c = 0; c < rw.n4; ++c) {
     const int q = rw.at(c);
-    const float4 e = E4[q], p = P4[q];
+    const float4 e = E4[q], p = pd.load4(p0 + 4 * q);
     const float r0 = fmaxf(fmaf(-c_t, p.x, e.x), 0.f);
     const float r1 = fmaxf(fmaf(-c_t, p.y, e.y), 0.f);
     const float r2 = fmaxf(fmaf(-c_t, p.z, e.z), 0.f);
@@ -473,10 +504,11 @@ __device__ __forceinline__ int lane_crossing(DF v, DF incl, DF& t, DF& before) {
 }
 
 // Weight of buffer position i under the state (cw, f) (e(y) scale).
-__device__ __forceinline__ float weight_at(const float* ebuf, const float* pbuf, int i, float cw,
+template <class PD>
+__device__ __forceinline__ float weight_at(const float* ebuf, const PD& pd, int i, float cw,
                                           float f) {
   const float e = ebuf[i];
-  const float w = (cw == 0.f) ? e : fmaxf(fmaf(-cw, pbuf[i], e), 0.f);
+  const float w = (cw == 0.f) ? e : fmaxf(fmaf(-cw, pd.at(i), e), 0.f);
   return __fmul_rn(w, f);
 }
 
@@ -489,8 +521,8 @@ struct Draw {
 // Levels: CTA of the cluster (sm.ccur, same in every CTA), warp of that CTA (sums of rs.tot),
 // thread of that warp (rs.tot), element of that thread's run.  No exchange: the writer CTA finds
 // the token alone and records the node itself.
-template <int CL>
-__device__ Draw cluster_draw(const Slice& s, const float* ebuf, const float* pbuf,
+template <int CL, class PD>
+__device__ Draw cluster_draw(const Slice& s, const float* ebuf, const PD& pd,
                              const RunState& rs, float u, int rank, VerifySmem& sm) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   __syncthreads();  // sm.ccur / sm.wcur are visible
@@ -525,7 +557,7 @@ __device__ Draw cluster_draw(const Slice& s, const float* ebuf, const float* pbu
     DF carry{0.f, 0.f};
     for (int base = 0; base < s.ch; base += 32) {
       const int i = base + lane;
-      const float w = (i < s.ch) ? weight_at(ebuf, pbuf, i0 + i, cwL, fL) : 0.f;
+      const float w = (i < s.ch) ? weight_at(ebuf, pd, i0 + i, cwL, fL) : 0.f;
       const DF run = df_add(carry, warp_scan_df(DF{w, 0.f}));
       const unsigned pos = __ballot_sync(0xffffffffu, w > 0.f);
       if (pos) last_pos = base + 31 - __clz(pos);
@@ -606,7 +638,7 @@ struct NodeBufs {
 // ------------------------------------------------------------------------------------------------
 // logits_staged: the kernel already issued the copy of this node's logit slice into nb.lbuf.
 // The returned record is complete in CTA `writer` (every CTA gets the same writer).
-template <int CL>
+template <int CL, bool PGLOBAL>
 __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, const NodeBufs& nb,
                                  bool logits_staged, DF invT_df, float k2, int& xk, int& writer,
                                  VerifySmem& sm) {
@@ -619,8 +651,14 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   const Slice s = make_slice(lrow, V, rank, CL);  // the draft row has the same alignment
   const bool sampling = a.T > 0.f;
   if (!logits_staged) stage_slice(lrow, s, nb.lbuf, nb.bar_l, -INFINITY);
-  const bool probs_staged = sampling && nk > 0;
+  const bool probs_staged = sampling && nk > 0 && !PGLOBAL;
   if (probs_staged) stage_slice(prow, s, nb.pbuf, nb.bar_p, 0.f);
+  DraftSlice<PGLOBAL> pd;
+  if constexpr (PGLOBAL) {
+    pd = DraftSlice<true>{prow, s.sbase, s.lo, s.hi};
+  } else {
+    pd = DraftSlice<false>{nb.pbuf};
+  }
   if ((int)threadIdx.x < nk) {  // gathers for the tests, overlapping the bulk copies
     const int kid = sm.kids[threadIdx.x];
     const int x = sm.tokens[kid];
@@ -700,14 +738,15 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     if (frozen) continue;  // a zero residual keeps the distribution: nothing to compute
     // rejected: residual of the current distribution (needed by the next sibling or the draw)
     if (!p_waited) {
-      pflags = wait_slice(nb.bar_p);  // CTA-local: reaches the cluster through the partials
+      // CTA-local: reaches the cluster through the partials
+      pflags = probs_staged ? wait_slice(nb.bar_p) : 0;
       p_waited = true;
     }
     const DF c_next = df_add(c, D);
     const float c_t = rs.f > 0.f ? __fdiv_rn(__fadd_rn(c_next.hi, c_next.lo), rs.f) : 0.f;
     DF tot, wt;
     int xs;
-    const DF G = cluster_residual<CL>(s, nb.lbuf, nb.pbuf, c_t, rs.f, t == 0, pflags, rank, xk,
+    const DF G = cluster_residual<CL>(s, nb.lbuf, pd, c_t, rs.f, t == 0, pflags, rank, xk,
                                       tot, wt, xs, flags, sm);
     pflags = 0;
     if (G.hi > 0.f) {
@@ -729,7 +768,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   if (probs_staged && !p_waited) wait_slice(nb.bar_p);  // no copy left in flight (not needed)
   const bool bad = (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) != 0;
   if ((nk == 0 || all_rejected) && !bad) {  // the walk can stop here: draw its bonus
-    const Draw d = cluster_draw<CL>(s, nb.lbuf, nb.pbuf, rs, u_bonus, rank, sm);
+    const Draw d = cluster_draw<CL>(s, nb.lbuf, pd, rs, u_bonus, rank, sm);
     writer = d.writer;
     st.bonus = d.tok;
   }
@@ -832,7 +871,8 @@ __device__ void walk_sequence_cluster(const VerifyArgs& a, int b, int rank, cons
       cluster_stats<CL>(s, nb.lbuf, k2, lflags, rank, xk, M, S, rs, flags, sm);
       const float u = __ldg(a.uniforms + (size_t)b * a.N);
       if (!(flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT))) {
-        const Draw d = cluster_draw<CL>(s, nb.lbuf, nb.pbuf, rs, u, rank, sm);
+        // a leaf's q: the current weights are e (cw = 0), p is never read
+        const Draw d = cluster_draw<CL>(s, nb.lbuf, DraftSlice<false>{nb.pbuf}, rs, u, rank, sm);
         writer = d.writer;
         bonus = d.tok;
       }
@@ -873,7 +913,8 @@ __device__ __forceinline__ bool arrive(unsigned long long* ctr, unsigned long lo
 // ------------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------------
-template <int CL>
+// PGLOBAL: draft rows read from global memory instead of staged (large problems with V ~ 128K).
+template <int CL, bool PGLOBAL>
 __global__ void __launch_bounds__(kVThreads)
     verify_kernel(const VerifyArgs a, int cap, int do_leaves, float invT_hi, float invT_lo,
                   float k2) {
@@ -928,7 +969,8 @@ __global__ void __launch_bounds__(kVThreads)
   const bool work = sm.internal[j] || do_leaves;
   NodeStat st;
   if (work)
-    st = process_node<CL>(a, b, j, rank, nb, early, DF{invT_hi, invT_lo}, k2, xk, writer, sm);
+    st = process_node<CL, PGLOBAL>(a, b, j, rank, nb, early, DF{invT_hi, invT_lo}, k2, xk, writer,
+                                   sm);
 
   // arrival: the last cluster of the sequence to finish walks the tree
   if (do_leaves) {
@@ -1013,6 +1055,14 @@ static int pick_cluster(long long units, int V, int num_sms, bool small, int nbu
   return cl;
 }
 
+template <int CL>
+static cudaError_t launch_cl(const VerifyArgs& a, dim3 g, size_t smem, cudaStream_t s, int cap,
+                             int leaves, float invT_hi, float invT_lo, float k2) {
+  if (a.p_global)
+    return launch_ex(verify_kernel<CL, true>, g, CL, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
+  return launch_ex(verify_kernel<CL, false>, g, CL, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
+}
+
 bool verify_supported(int V) { return slice_capacity(V, 8) <= kMaxSliceFloats; }
 
 cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s) {
@@ -1022,16 +1072,20 @@ cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s) {
   const long long units = (long long)a.B * (leaves ? a.N : (a.N + 1) / 2);
   const int cl = pick_cluster(units, a.V, num_sms, small, a.T > 0.f ? 2 : 1);
   const int cap = slice_capacity(a.V, cl);
-  const size_t smem = (size_t)(a.T > 0.f ? 2 : 1) * cap * sizeof(float);
+  // large problems whose two slices would still leave one CTA per SM read the draft row from
+  // global memory (L2) instead of staging it
+  VerifyArgs ak = a;
+  ak.p_global = (!small && a.T > 0.f && 2 * (size_t)cap * sizeof(float) > kLargeCtaBytes) ? 1 : 0;
+  const size_t smem = (size_t)(a.T > 0.f && !ak.p_global ? 2 : 1) * cap * sizeof(float);
   const double invTd = a.T > 0.f ? 1.0 / (double)a.T : 0.0;
   const float invT_hi = (float)invTd, invT_lo = (float)(invTd - (double)invT_hi);
   const float k2 = (float)(invTd * 1.4426950408889634);  // log2(e) / T
   const dim3 g(cl, a.N, a.B);
   switch (cl) {
-    case 1: return launch_ex(verify_kernel<1>, g, 1, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
-    case 2: return launch_ex(verify_kernel<2>, g, 2, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
-    case 4: return launch_ex(verify_kernel<4>, g, 4, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
-    default: return launch_ex(verify_kernel<8>, g, 8, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
+    case 1: return launch_cl<1>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2);
+    case 2: return launch_cl<2>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2);
+    case 4: return launch_cl<4>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2);
+    default: return launch_cl<8>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2);
   }
 }
 
