@@ -11,6 +11,9 @@ published definitions:
   s % P) and post-accept compaction (the accepted path's keys and values move next to the root).
   Survey explainer, "vLLMでの実装状況" section (speculative decoding on PagedAttention); EAGLE
   explainer, vLLM usage section (the tree's extra KV-cache memory).
+* ``oracle.filtering`` -- top-k / top-p filtered target distributions (the filtered logits feed
+  ``oracle.verify`` unchanged).  Survey explainer, verification taxonomy (speculative sampling
+  with top-k / top-p).
 * ``oracle.verify`` -- speculative-sampling accept/reject over the tree, the walk to the accepted
   path and the resample of the bonus token from norm(max(0, q - p)); temperature 0 is greedy
   argmax matching.  Survey explainer, "Formal Definition" (draft / verify / accept-reject
@@ -22,4 +25,4 @@ It shares no code with the CUDA path and imports nothing from it.
 Parity pins: every function here is pinned by ``tests/test_oracle_*.py`` against library routines,
 closed forms, exact rational enumeration and brute force (none re-types the oracle's formulas).
 """
-from . import attention, paged, verify  # noqa: F401
+from . import attention, filtering, paged, verify  # noqa: F401
