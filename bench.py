@@ -484,7 +484,8 @@ def run_ours(args):
 
 
 def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev, L2):
-    """Paged-cache attention (16-slot pages) and post-accept KV compaction on this workload.
+    """Paged-cache attention (16-slot pages), post-accept KV compaction and filtered verification
+    on this workload.
 
     Paged attention: the same queries, tree and prefix over pages in a random physical order,
     rotated over device copies larger than 2 x L2, timed per call from CUDA graphs; its
@@ -542,14 +543,46 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
                     fn(c)
         return g
 
+    # filtered verification (top-k 50, top-p 0.9) on the same rotated copies as verification
+    B, N, V = bufs[0]["logits"].shape
+    T = args.temperature if args.temperature > 0 else 1.0
+    top_k, top_p = 50, 0.9
+    ws_f = st.spec_tree_verify_filtered_workspace(B, N, V)
+    for c in bufs:
+        c["ws_f"] = torch.empty((ws_f,), dtype=torch.uint8, device=dev)
+        c["st_f"] = torch.zeros_like(c["lens"])
+        c["fout"] = {k: torch.empty_like(v) for k, v in c["vout"].items()}
+
+    def filtered(c):
+        st.spec_tree_verify_filtered(c["logits"], c["probs"], c["tokens"], c["parent"],
+                                     c["unif"], T, top_k=top_k, top_p=top_p, outputs=c["fout"],
+                                     workspace=c["ws_f"], status=c["st_f"])
+
+    def plain(c):
+        st.spec_tree_verify(c["logits"], c["probs"], c["tokens"], c["parent"], c["unif"], T,
+                            outputs=c["fout"], workspace=c["ws_f"], status=c["st_f"])
+
+    for _ in range(3):
+        for c in bufs:
+            filtered(c)
+    torch.cuda.synchronize()
+    assert all(int(c["st_f"].sum()) == 0 for c in bufs)
     g_p, g_c = capture(paged, pcs), capture(compact, bufs)
+    g_f, g_v = capture(filtered, bufs), capture(plain, bufs)
     torch.cuda.current_stream().wait_stream(s)
     for _ in range(2):
         g_p.replay()
         g_c.replay()
+        g_f.replay()
+        g_v.replay()
     torch.cuda.synchronize()
     reps = max(1, 600 // ncp)
     p_ms = timed(lambda: [g_p.replay() for _ in range(reps)]) / (reps * ncp)
+    reps_f = max(1, 600 // len(bufs))
+    f_ms = timed(lambda: [g_f.replay() for _ in range(reps_f)]) / (reps_f * len(bufs))
+    v_ms = timed(lambda: [g_v.replay() for _ in range(reps_f)]) / (reps_f * len(bufs))
+    filt_bytes = 2 * B * N * V * 4  # the logits read once, the filtered logits written once
+    fil_gbs = filt_bytes / ((f_ms - v_ms) * 1e-3) / 1e9 if f_ms > v_ms else None
     reps_c = max(1, 600 // len(bufs))
     c_ms = timed(lambda: [g_c.replay() for _ in range(reps_c)]) / (reps_c * len(bufs))
     _, Hkv, _, D = bufs[0]["k"].shape
@@ -565,6 +598,14 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
                        "algorithmic_bytes": moved,
                        "achieved_gbs": moved / (c_ms * 1e-3) / 1e9,
                        "note": "latency-bound: a few KB to a few hundred KB per call"},
+        "filtered_verify": {"top_k": top_k, "top_p": top_p, "temperature": T,
+                            "us_per_call": f_ms * 1e3, "plain_verify_us_per_call": v_ms * 1e3,
+                            "filter_us_per_call": (f_ms - v_ms) * 1e3,
+                            "filter_algorithmic_bytes": filt_bytes, "filter_achieved_gbs": fil_gbs,
+                            "filter_frac": fil_gbs / hbm_gbs if fil_gbs else None,
+                            "note": "filter kernel time = filtered call - plain call (same "
+                                    "copies, same temperature); rows are re-read from L2 by "
+                                    "the radix passes"},
         "peak_gbs": hbm_gbs,
     }
 

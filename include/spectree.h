@@ -167,6 +167,42 @@ int spec_tree_verify_noalloc(const float* target_logits, const float* draft_prob
                              float* out_child_q, int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------------------------------
+ * Verification against a top-k / top-p filtered target distribution
+ * ------------------------------------------------------------------------------------------------
+ * Survey explainer, verification taxonomy (sampling paragraph): speculative sampling carries over
+ * to top-k and top-p sampling when the accept/reject test and the residual use the filtered target
+ * distribution.  Reading (the pages give no procedure): per target row, temperature first, then
+ * top-k on the logits (every token whose logit is >= the k-th largest is kept, ties included), then
+ * top-p on the renormalised top-k distribution (token y is kept when the probability mass of the
+ * tokens strictly more probable than y is < top_p; ties are kept or dropped together, the most
+ * probable token always stays).  The filtered target q'_j = softmax(l_j / T) over the kept tokens,
+ * renormalised, replaces q_j everywhere in spec_tree_verify's rule.  draft_probs is the drafter's
+ * own distribution (filtered or not, as it sampled).
+ *
+ *   top_k  >= 0; 0 or >= V: no top-k filter
+ *   top_p  in (0, 1]; 1: no top-p filter
+ * Top-p masses come from single-precision exponentials summed exactly in 2^-40 fixed point
+ * (relative error a few 1e-7), so a top_p within about 2e-6 of the mass above a tie group may
+ * keep or drop that group; top-k decisions are exact.
+ * At temperature 0 both filters keep the argmax, and the call is spec_tree_verify (greedy); with
+ * both filters off it is spec_tree_verify as well, and needs only spec_tree_verify_workspace
+ * bytes.  Otherwise the workspace must hold spec_tree_verify_filtered_workspace(B, N, V) bytes:
+ * the verification scratch followed by the filtered logits (B * N * V fp32, -inf outside the kept
+ * sets), written by one kernel and read by the verification kernel on the same stream.  A row of
+ * target_logits holding NaN or +Inf is passed through unfiltered (verification flags it
+ * SPEC_ST_NONFINITE when it reads it).
+ * The other arguments, outputs and the status bits are spec_tree_verify's.
+ */
+size_t spec_tree_verify_filtered_workspace(int B, int N, int V);
+int spec_tree_verify_filtered(const float* target_logits, const float* draft_probs,
+                              const int32_t* tree_tokens, const int32_t* tree_parent,
+                              const float* uniforms, float temperature, int top_k, float top_p,
+                              int B, int N, int V, int32_t* out_accept_len,
+                              int32_t* out_accepted_tokens, int32_t* out_bonus_token,
+                              int32_t* out_accepted_nodes, float* out_child_q, void* workspace,
+                              size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------------------------------
  * Tree attention over a paged KV cache
  * ------------------------------------------------------------------------------------------------
  * Survey explainer, "vLLMでの実装状況" section: serving stacks run speculative decoding on

@@ -43,13 +43,16 @@ def keep_mask(logits_row, T: float, top_k: int, top_p: float):
         order = np.argsort(-q, kind="stable")
         qs = q[order]
         csum = np.cumsum(qs)
-        gt = np.empty(V)
+        gt = np.full(V, np.inf)
         i = 0
         while i < V:
+            above = csum[i - 1] if i > 0 else 0.0
+            if above >= top_p:   # masses above only grow along the order: the rest is dropped
+                break
             j = i
             while j + 1 < V and qs[j + 1] == qs[i]:
                 j += 1
-            gt[order[i:j + 1]] = csum[i - 1] if i > 0 else 0.0
+            gt[order[i:j + 1]] = above
             i = j + 1
         keep &= gt < top_p
     return keep

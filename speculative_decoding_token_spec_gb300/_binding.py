@@ -45,6 +45,9 @@ _SIGNATURES = {
     "spec_kv_compact": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_vp, _vp]),
     "spec_kv_compact_paged": (_c_int, [_vp] * 3 + [_c_int] * 3 + [_vp] * 4 + [_c_int] * 4
                               + [_vp, _vp]),
+    "spec_tree_verify_filtered_workspace": (_c_size, [_c_int] * 3),
+    "spec_tree_verify_filtered": (_c_int, [_vp] * 5 + [_c_float, _c_int, _c_float] + [_c_int] * 3
+                                  + [_vp] * 5 + [_vp, _c_size, _vp, _vp]),
     "spec_status_string": (ctypes.c_char_p, [_c_int]),
 }
 
@@ -230,14 +233,12 @@ def spec_kv_compact_paged(k_pages, v_pages, block_table, prefix_lens, accept_len
     return new_prefix_lens, status
 
 
-def spec_tree_verify(target_logits, draft_probs, tree_tokens, tree_parent, uniforms, temperature,
-                     outputs=None, workspace=None, status=None, want_nodes=True,
-                     want_child_q=False, stream=None):
-    """Speculative-sampling verification; returns a dict of device tensors.
+def spec_tree_verify_filtered_workspace(B, N, V) -> int:
+    return int(lib().spec_tree_verify_filtered_workspace(B, N, V))
 
-    Keys: accept_len [B], accepted_tokens [B,N], bonus [B], accepted_nodes [B,N] (if want_nodes),
-    child_q [B,N] (if want_child_q), status [B].
-    """
+
+def _verify_outputs(target_logits, draft_probs, tree_tokens, tree_parent, uniforms, outputs,
+                    status, want_nodes, want_child_q):
     torch = _torch()
     B, N, V = target_logits.shape
     dev = target_logits.device
@@ -257,6 +258,22 @@ def spec_tree_verify(target_logits, draft_probs, tree_tokens, tree_parent, unifo
     if want_child_q:
         o.setdefault("child_q", torch.empty((B, N), dtype=torch.float32, device=dev))
     o["status"] = status if status is not None else torch.zeros((B,), **i32)  # bits are OR-ed in
+    return o
+
+
+def spec_tree_verify(target_logits, draft_probs, tree_tokens, tree_parent, uniforms, temperature,
+                     outputs=None, workspace=None, status=None, want_nodes=True,
+                     want_child_q=False, stream=None):
+    """Speculative-sampling verification; returns a dict of device tensors.
+
+    Keys: accept_len [B], accepted_tokens [B,N], bonus [B], accepted_nodes [B,N] (if want_nodes),
+    child_q [B,N] (if want_child_q), status [B].
+    """
+    torch = _torch()
+    o = _verify_outputs(target_logits, draft_probs, tree_tokens, tree_parent, uniforms, outputs,
+                        status, want_nodes, want_child_q)
+    B, N, V = target_logits.shape
+    dev = target_logits.device
     ws_bytes = spec_tree_verify_workspace(B, N, V)
     if workspace is None:
         workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
@@ -268,6 +285,30 @@ def spec_tree_verify(target_logits, draft_probs, tree_tokens, tree_parent, unifo
         _stream(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_tree_verify", rc)
+    return o
+
+
+def spec_tree_verify_filtered(target_logits, draft_probs, tree_tokens, tree_parent, uniforms,
+                              temperature, top_k=0, top_p=1.0, outputs=None, workspace=None,
+                              status=None, want_nodes=True, want_child_q=False, stream=None):
+    """Verification against the top-k / top-p filtered target distribution (top_k 0 and top_p 1
+    switch a filter off); same outputs as spec_tree_verify."""
+    torch = _torch()
+    o = _verify_outputs(target_logits, draft_probs, tree_tokens, tree_parent, uniforms, outputs,
+                        status, want_nodes, want_child_q)
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    ws_bytes = spec_tree_verify_filtered_workspace(B, N, V)
+    if workspace is None:
+        workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
+    rc = lib().spec_tree_verify_filtered(
+        _ptr(target_logits), _ptr(draft_probs), _ptr(tree_tokens), _ptr(tree_parent),
+        _ptr(uniforms), float(temperature), int(top_k), float(top_p), B, N, V,
+        _ptr(o["accept_len"]), _ptr(o["accepted_tokens"]), _ptr(o["bonus"]),
+        _ptr(o.get("accepted_nodes")), _ptr(o.get("child_q")), _ptr(workspace),
+        workspace.numel(), _ptr(o["status"]), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_tree_verify_filtered", rc)
     return o
 
 

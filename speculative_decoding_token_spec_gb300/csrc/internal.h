@@ -43,6 +43,10 @@ struct VerifyArgs {
 size_t verify_workspace_bytes(int B, int N, int V);
 bool verify_supported(int V);  // the row slices of a cluster fit in shared memory
 cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s);
+// rows of V target logits -> the same rows with -inf outside the top-k / top-p set (T > 0)
+bool filter_supported(int V);  // a row fits the filter kernel's clusters
+cudaError_t launch_filter(const float* in, float* out, int rows, int V, float T, int top_k,
+                          float top_p, cudaStream_t s);
 
 struct AttnArgs {
   const void* q;

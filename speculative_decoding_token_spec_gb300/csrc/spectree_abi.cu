@@ -31,6 +31,28 @@ int sm_count() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Argument checks shared by the verification entry points (everything but the workspace).
+int verify_check(const float* target_logits, const float* draft_probs, const int32_t* tree_tokens,
+                 const int32_t* tree_parent, const float* uniforms, float temperature, int B,
+                 int N, int V, const int32_t* out_accept_len, const int32_t* out_accepted_tokens,
+                 const int32_t* out_bonus_token) {
+  if (!target_logits || !tree_tokens || !tree_parent || !uniforms || !out_accept_len ||
+      !out_accepted_tokens || !out_bonus_token)
+    return SPEC_ERR_INVALID_ARG;
+  if (!std::isfinite(temperature) || temperature < 0.f) return SPEC_ERR_INVALID_ARG;
+  if (temperature > 0.f && !draft_probs) return SPEC_ERR_INVALID_ARG;
+  if (B < 1 || B > 65535 || N < 1 || N > kMaxNodes || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (!verify_supported(V)) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(target_logits) || (draft_probs && !aligned16(draft_probs)))
+    return SPEC_ERR_INVALID_ARG;
+  return SPEC_OK;
+}
+
+// The filtered logits follow the verification scratch in the filtered entry's workspace.
+size_t filtered_logits_offset(int B, int N, int V) {
+  return (verify_workspace_bytes(B, N, V) + 15) & ~size_t(15);
+}
+
 }  // namespace
 
 extern "C" {
@@ -176,15 +198,10 @@ int spec_tree_verify(const float* target_logits, const float* draft_probs,
                      int32_t* out_accept_len, int32_t* out_accepted_tokens,
                      int32_t* out_bonus_token, int32_t* out_accepted_nodes, float* out_child_q,
                      void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
-  if (!target_logits || !tree_tokens || !tree_parent || !uniforms || !out_accept_len ||
-      !out_accepted_tokens || !out_bonus_token)
-    return SPEC_ERR_INVALID_ARG;
-  if (!std::isfinite(temperature) || temperature < 0.f) return SPEC_ERR_INVALID_ARG;
-  if (temperature > 0.f && !draft_probs) return SPEC_ERR_INVALID_ARG;
-  if (B < 1 || B > 65535 || N < 1 || N > kMaxNodes || V < 1) return SPEC_ERR_INVALID_ARG;
-  if (!verify_supported(V)) return SPEC_ERR_UNSUPPORTED;
-  if (!aligned16(target_logits) || (draft_probs && !aligned16(draft_probs)))
-    return SPEC_ERR_INVALID_ARG;
+  const int rc = verify_check(target_logits, draft_probs, tree_tokens, tree_parent, uniforms,
+                              temperature, B, N, V, out_accept_len, out_accepted_tokens,
+                              out_bonus_token);
+  if (rc != SPEC_OK) return rc;
   const size_t need = verify_workspace_bytes(B, N, V);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SPEC_ERR_WORKSPACE;
   const int sms = sm_count();
@@ -212,6 +229,44 @@ int spec_tree_verify(const float* target_logits, const float* draft_probs,
   a.gen = call_gen.fetch_add(1) & 0xFFFFFFFFFFFFull;
   cudaError_t e = launch_verify(a, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+size_t spec_tree_verify_filtered_workspace(int B, int N, int V) {
+  if (B < 1 || N < 1 || N > kMaxNodes || V < 1) return 0;
+  return filtered_logits_offset(B, N, V) + (size_t)B * N * V * sizeof(float);
+}
+
+int spec_tree_verify_filtered(const float* target_logits, const float* draft_probs,
+                              const int32_t* tree_tokens, const int32_t* tree_parent,
+                              const float* uniforms, float temperature, int top_k, float top_p,
+                              int B, int N, int V, int32_t* out_accept_len,
+                              int32_t* out_accepted_tokens, int32_t* out_bonus_token,
+                              int32_t* out_accepted_nodes, float* out_child_q, void* workspace,
+                              size_t workspace_bytes, int32_t* status, void* stream) {
+  const int rc = verify_check(target_logits, draft_probs, tree_tokens, tree_parent, uniforms,
+                              temperature, B, N, V, out_accept_len, out_accepted_tokens,
+                              out_bonus_token);
+  if (rc != SPEC_OK) return rc;
+  if (top_k < 0 || !(top_p > 0.f && top_p <= 1.f)) return SPEC_ERR_INVALID_ARG;
+  if (!filter_supported(V)) return SPEC_ERR_UNSUPPORTED;
+  const bool active = temperature > 0.f && ((top_k > 0 && top_k < V) || top_p < 1.f);
+  if (!active)
+    return spec_tree_verify(target_logits, draft_probs, tree_tokens, tree_parent, uniforms,
+                            temperature, B, N, V, out_accept_len, out_accepted_tokens,
+                            out_bonus_token, out_accepted_nodes, out_child_q, workspace,
+                            workspace_bytes, status, stream);
+  const size_t off = filtered_logits_offset(B, N, V);
+  if (!workspace || workspace_bytes < off + (size_t)B * N * V * sizeof(float) ||
+      !aligned16(workspace))
+    return SPEC_ERR_WORKSPACE;
+  float* filtered = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + off);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_filter(target_logits, filtered, B * N, V, temperature, top_k, top_p, s) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return spec_tree_verify(filtered, draft_probs, tree_tokens, tree_parent, uniforms, temperature,
+                          B, N, V, out_accept_len, out_accepted_tokens, out_bonus_token,
+                          out_accepted_nodes, out_child_q, workspace, off, status, stream);
 }
 
 const char* spec_status_string(int code) {

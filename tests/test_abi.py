@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("spec_tree_attention", "spec_tree_verify", "spec_tree_attention_workspace",
               "spec_tree_verify_workspace", "spec_status_string", "spec_tree_attention_paged",
-              "spec_kv_compact", "spec_kv_compact_paged"):
+              "spec_kv_compact", "spec_kv_compact_paged", "spec_tree_verify_filtered",
+              "spec_tree_verify_filtered_workspace"):
         assert n in names
 
 
@@ -142,3 +143,25 @@ def test_paged_and_compaction_argument_errors(lib):
     rc = lib.spec_kv_compact_paged(fake, fake, fake, 0, 4, 4, lens, fake, fake, fake, 1, 5, 8,
                                    128, null, null)
     assert rc == -1
+
+
+def test_filtered_verify_arguments(lib):
+    """Filtered verification: workspace query and argument errors, all before any CUDA call."""
+    base = lib.spec_tree_verify_workspace(2, 60, 32000)
+    full = lib.spec_tree_verify_filtered_workspace(2, 60, 32000)
+    assert full >= base + 2 * 60 * 32000 * 4 and full % 16 == 0
+    assert lib.spec_tree_verify_filtered_workspace(1, 65, 100) == 0
+    fake = ctypes.c_void_p(256)
+    null = None
+
+    def call(T=1.0, k=5, p=0.9, ws=1 << 30, probs=fake, N=5, V=1000):
+        return lib.spec_tree_verify_filtered(fake, probs, fake, fake, fake, T, k, p, 1, N, V,
+                                             fake, fake, fake, null, null, fake, ws, null, null)
+    for k, p in ((-1, 0.9), (5, 0.0), (5, -0.2), (5, 1.5), (5, float("nan"))):
+        assert call(k=k, p=p) == -1
+    assert call(T=-1.0) == -1
+    assert call(probs=null) == -1                    # T > 0 needs the draft distribution
+    assert call(N=65) == -1
+    need = lib.spec_tree_verify_filtered_workspace(1, 5, 1000)
+    assert call(ws=need - 16) == -3                  # the filtered logits do not fit
+    assert call(k=0, p=0.5, ws=need - 16) == -3      # top-p alone also filters
