@@ -603,9 +603,9 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
                             "filter_us_per_call": (f_ms - v_ms) * 1e3,
                             "filter_algorithmic_bytes": filt_bytes, "filter_achieved_gbs": fil_gbs,
                             "filter_frac": fil_gbs / hbm_gbs if fil_gbs else None,
+                            "kernel": "filter_kernel (cluster per row, row in shared memory)",
                             "note": "filter kernel time = filtered call - plain call (same "
-                                    "copies, same temperature); rows are re-read from L2 by "
-                                    "the radix passes"},
+                                    "copies, same temperature); latency-bound"},
         "peak_gbs": hbm_gbs,
     }
 
