@@ -11,6 +11,10 @@ published definitions:
   s % P) and post-accept compaction (the accepted path's keys and values move next to the root).
   Survey explainer, "vLLMでの実装状況" section (speculative decoding on PagedAttention); EAGLE
   explainer, vLLM usage section (the tree's extra KV-cache memory).
+* ``oracle.dyntree`` -- dynamic (EAGLE-2-style) draft-tree construction: level-by-level expansion
+  of the best frontier nodes by their top draft tokens, then the best candidates by cumulative
+  draft log-probability.  EAGLE-3 explainer, 背景と動機 / EAGLE-2との統合 (EAGLE-2's dynamic
+  tree).
 * ``oracle.filtering`` -- top-k / top-p filtered target distributions (the filtered logits feed
   ``oracle.verify`` unchanged).  Survey explainer, verification taxonomy (speculative sampling
   with top-k / top-p).
@@ -25,4 +29,4 @@ It shares no code with the CUDA path and imports nothing from it.
 Parity pins: every function here is pinned by ``tests/test_oracle_*.py`` against library routines,
 closed forms, exact rational enumeration and brute force (none re-types the oracle's formulas).
 """
-from . import attention, filtering, paged, verify  # noqa: F401
+from . import attention, dyntree, filtering, paged, verify  # noqa: F401
