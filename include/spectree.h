@@ -203,6 +203,69 @@ int spec_tree_verify_filtered(const float* target_logits, const float* draft_pro
                               size_t workspace_bytes, int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------------------------------
+ * Dynamic draft-tree construction
+ * ------------------------------------------------------------------------------------------------
+ * EAGLE-3 explainer, 背景と動機 and EAGLE-2との統合: EAGLE-2 builds the draft tree at inference
+ * time from the draft head's outputs instead of using a fixed shape.  The pages give no procedure;
+ * this follows EAGLE-2's expand-then-rerank construction (a reading):
+ *   - a drafted node's value is the sum of the draft log-probabilities log softmax(l)[token] along
+ *     its path from the root, under each parent's draft logits l (root value 0);
+ *   - level d expands the frontier (the root at level 1): frontier slot i's K highest draft logits
+ *     (ties: lower token id) become candidates, candidate order i K + r; the K candidates of the
+ *     level with the highest values (ties: lower order) are the next frontier, best first;
+ *   - spec_tree_finalize returns the root plus the N - 1 best candidates of all levels (ties:
+ *     shallower, then lower order), numbered by depth then candidate order, so every parent comes
+ *     before its children: the tree_parent / tree_tokens that spec_tree_verify and
+ *     spec_tree_attention take.
+ * The draft model runs between the levels: after level d the caller drafts the frontier nodes
+ * (their tokens and the slot of the row they came from are returned) and passes their logits as
+ * level d + 1.
+ *
+ * Workspace: spec_tree_build_workspace(B, K, D) bytes, 16-byte aligned, holding each sequence's
+ * construction state; level 1 starts a new construction in it.  0 if the shape is unsupported.
+ * Supported: 1 <= K <= SPEC_TREE_MAX_K, 1 <= D <= 16, 1 + K + (D - 1) K^2 <= SPEC_TREE_MAX_POOL.
+ */
+#define SPEC_TREE_MAX_K 16
+#define SPEC_TREE_MAX_POOL 2048
+size_t spec_tree_build_workspace(int B, int K, int D);
+
+/*
+ * One level of the construction.
+ *   draft_logits  fp32 [B, R, V], R = 1 at level 1 (the root's draft logits), else K (row i: the
+ *                 draft logits at frontier slot i of the previous level).  -inf entries are
+ *                 allowed (masked tokens); V >= K.
+ *   level         1 .. D, called in order for each construction (a call out of order sets
+ *                 SPEC_ST_BAD_TREE for every sequence and leaves the state unchanged)
+ *   out_frontier_tokens       int32 [B, K] or NULL: the new frontier's tokens, best first
+ *   out_frontier_parent_slot  int32 [B, K] or NULL: the row i of this level each came from
+ *   status        int32 [B] or NULL: SPEC_ST_NONFINITE (NaN or +Inf in one of the sequence's rows:
+ *                 its construction stops, spec_tree_finalize returns the root alone),
+ *                 SPEC_ST_BAD_TREE (out-of-order level); OR-ed in
+ * Draft row numbering across levels (node_row below): row 0 is the root's, row 1 + (d - 2) K + i
+ * is frontier slot i's at level d >= 2.
+ */
+int spec_tree_expand(const float* draft_logits, int B, int V, int K, int D, int level,
+                     void* workspace, size_t workspace_bytes, int32_t* out_frontier_tokens,
+                     int32_t* out_frontier_parent_slot, int32_t* status, void* stream);
+
+/*
+ * The tree of the root and the N - 1 best candidates (1 <= N <= 64, N <= 1 + K + (D - 1) K^2).
+ *   root_tokens     int32 [B]: token of node 0 (the last committed token)
+ *   out_tree_tokens int32 [B, N], out_tree_parent int32 [B, N]: the tree, parents first; entries
+ *                   past the nodes a construction produced (fewer levels run than D, or a stopped
+ *                   construction) are -1
+ *   out_node_row    int32 [B, N] or NULL: node j's own draft row (numbering above) if it was
+ *                   expanded, else -1 -- a node with children always has one; gather those rows
+ *                   for spec_tree_verify's draft_probs
+ *   out_node_value  fp32 [B, N] or NULL: node values (fp32 arithmetic; log-sum-exp from a
+ *                   compensated fp32 sum), NaN past the produced nodes
+ */
+int spec_tree_finalize(const void* workspace, size_t workspace_bytes, const int32_t* root_tokens,
+                       int B, int K, int D, int N, int32_t* out_tree_tokens,
+                       int32_t* out_tree_parent, int32_t* out_node_row, float* out_node_value,
+                       int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------------------------------
  * Tree attention over a paged KV cache
  * ------------------------------------------------------------------------------------------------
  * Survey explainer, "vLLMでの実装状況" section: serving stacks run speculative decoding on

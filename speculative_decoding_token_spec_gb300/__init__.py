@@ -10,8 +10,9 @@ Two calls make up the hot path, both hand-written CUDA for sm_103a behind a C AB
 
 Beside them: ``spec_tree_attention_paged`` (the same attention over a paged KV cache) and
 ``spec_kv_compact`` / ``spec_kv_compact_paged`` (after verification, the accepted path's keys and
-values move next to the root), and ``spec_tree_verify_filtered`` (verification against the top-k /
-top-p filtered target distribution).
+values move next to the root), ``spec_tree_verify_filtered`` (verification against the top-k /
+top-p filtered target distribution), and ``spec_tree_expand`` / ``spec_tree_finalize`` (dynamic
+draft-tree construction, one level per drafter step).
 
 The Python functions of the same names only marshal torch tensors into pointers and the current
 CUDA stream.  There is no CPU fallback: a missing library raises.
@@ -23,6 +24,9 @@ from ._binding import (  # noqa: F401
     spec_tree_attention,
     spec_tree_attention_paged,
     spec_tree_attention_workspace,
+    spec_tree_build_workspace,
+    spec_tree_expand,
+    spec_tree_finalize,
     spec_tree_verify,
     spec_tree_verify_filtered,
     spec_tree_verify_filtered_workspace,

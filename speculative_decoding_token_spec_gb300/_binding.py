@@ -48,6 +48,9 @@ _SIGNATURES = {
     "spec_tree_verify_filtered_workspace": (_c_size, [_c_int] * 3),
     "spec_tree_verify_filtered": (_c_int, [_vp] * 5 + [_c_float, _c_int, _c_float] + [_c_int] * 3
                                   + [_vp] * 5 + [_vp, _c_size, _vp, _vp]),
+    "spec_tree_build_workspace": (_c_size, [_c_int] * 3),
+    "spec_tree_expand": (_c_int, [_vp] + [_c_int] * 5 + [_vp, _c_size] + [_vp] * 4),
+    "spec_tree_finalize": (_c_int, [_vp, _c_size, _vp] + [_c_int] * 4 + [_vp] * 6),
     "spec_status_string": (ctypes.c_char_p, [_c_int]),
 }
 
@@ -350,4 +353,57 @@ def spec_tree_verify_noalloc(target_logits, draft_probs, tree_tokens, tree_paren
             _ptr(o.get("child_q")), _ptr(o["status"]), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_tree_verify_noalloc", rc)
+    return o
+
+
+# ----------------------------------------------------------------------------------------------
+# dynamic tree construction
+# ----------------------------------------------------------------------------------------------
+def spec_tree_build_workspace(B, K, D) -> int:
+    return int(lib().spec_tree_build_workspace(B, K, D))
+
+
+def spec_tree_expand(draft_logits, K, D, level, workspace, frontier_tokens=None,
+                     frontier_parent_slot=None, status=None, stream=None):
+    """One level: draft_logits [B, 1, V] at level 1, else [B, K, V] (the frontier's draft rows).
+    Returns (frontier_tokens [B, K], frontier_parent_slot [B, K], status [B])."""
+    torch = _torch()
+    B, R, V = draft_logits.shape
+    dev = draft_logits.device
+    _check(draft_logits, "draft_logits", torch.float32, (B, 1 if level == 1 else K, V), dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    if frontier_tokens is None:
+        frontier_tokens = torch.empty((B, K), **i32)
+    if frontier_parent_slot is None:
+        frontier_parent_slot = torch.empty((B, K), **i32)
+    if status is None:
+        status = torch.zeros((B,), **i32)
+    rc = lib().spec_tree_expand(_ptr(draft_logits), B, V, K, D, level, _ptr(workspace),
+                                workspace.numel() * workspace.element_size(),
+                                _ptr(frontier_tokens), _ptr(frontier_parent_slot), _ptr(status),
+                                _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_tree_expand", rc)
+    return frontier_tokens, frontier_parent_slot, status
+
+
+def spec_tree_finalize(workspace, root_tokens, K, D, N, outputs=None, status=None, stream=None):
+    """The tree of the root and the N - 1 best candidates; returns a dict of device tensors:
+    tree_tokens, tree_parent, node_row [B, N] int32, node_value [B, N] fp32, status [B]."""
+    torch = _torch()
+    B = root_tokens.shape[0]
+    dev = root_tokens.device
+    _check(root_tokens, "root_tokens", torch.int32, (B,), dev)
+    o = dict(outputs or {})
+    i32 = dict(dtype=torch.int32, device=dev)
+    for k in ("tree_tokens", "tree_parent", "node_row"):
+        o.setdefault(k, torch.empty((B, N), **i32))
+    o.setdefault("node_value", torch.empty((B, N), dtype=torch.float32, device=dev))
+    o["status"] = status if status is not None else torch.zeros((B,), **i32)
+    rc = lib().spec_tree_finalize(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _ptr(root_tokens), B, K, D, N, _ptr(o["tree_tokens"]),
+                                  _ptr(o["tree_parent"]), _ptr(o["node_row"]),
+                                  _ptr(o["node_value"]), _ptr(o["status"]), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_tree_finalize", rc)
     return o

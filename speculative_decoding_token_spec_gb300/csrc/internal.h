@@ -44,6 +44,18 @@ size_t verify_workspace_bytes(int B, int N, int V);
 bool verify_supported(int V);  // the row slices of a cluster fit in shared memory
 cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s);
 // rows of V target logits -> the same rows with -inf outside the top-k / top-p set (T > 0)
+// dynamic tree construction (tree_build.cu)
+constexpr int kMaxTreeK = 16;       // candidates per expanded node, frontier size
+constexpr int kMaxTreePool = 2048;  // drafted nodes per sequence: 1 + K + (D - 1) K^2
+size_t tree_build_stride(int K, int D);  // workspace bytes per sequence
+cudaError_t launch_tree_expand(const float* logits, int B, int R, int V, int K, int D, int level,
+                               void* state, int32_t* ftok, int32_t* fslot, int32_t* status,
+                               cudaStream_t s);
+cudaError_t launch_tree_finalize(const void* state, int B, int K, int D, const int32_t* root_tokens,
+                                 int N, int32_t* tree_tokens, int32_t* tree_parent,
+                                 int32_t* node_row, float* node_value, int32_t* status,
+                                 cudaStream_t s);
+
 bool filter_supported(int V);  // a row fits the filter kernel's clusters
 cudaError_t launch_filter(const float* in, float* out, int rows, int V, float T, int top_k,
                           float top_p, cudaStream_t s);

@@ -269,6 +269,49 @@ int spec_tree_verify_filtered(const float* target_logits, const float* draft_pro
                           out_accepted_nodes, out_child_q, workspace, off, status, stream);
 }
 
+// ---- dynamic tree construction
+namespace {
+bool tree_shape_ok(int B, int K, int D) {
+  if (B < 1 || K < 1 || K > kMaxTreeK || D < 1 || D > 16) return false;
+  return 1 + K + (long long)(D - 1) * K * K <= kMaxTreePool;
+}
+}  // namespace
+
+size_t spec_tree_build_workspace(int B, int K, int D) {
+  if (!tree_shape_ok(B, K, D)) return 0;
+  return (size_t)B * tree_build_stride(K, D);
+}
+
+int spec_tree_expand(const float* draft_logits, int B, int V, int K, int D, int level,
+                     void* workspace, size_t workspace_bytes, int32_t* out_frontier_tokens,
+                     int32_t* out_frontier_parent_slot, int32_t* status, void* stream) {
+  if (!draft_logits || !tree_shape_ok(B, K, D) || V < K || level < 1 || level > D)
+    return SPEC_ERR_INVALID_ARG;
+  const int R = level == 1 ? 1 : K;
+  if ((long long)B * R > 0x7fffffffLL) return SPEC_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < spec_tree_build_workspace(B, K, D) || !aligned16(workspace))
+    return SPEC_ERR_WORKSPACE;
+  const cudaError_t e =
+      launch_tree_expand(draft_logits, B, R, V, K, D, level, workspace, out_frontier_tokens,
+                         out_frontier_parent_slot, status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+int spec_tree_finalize(const void* workspace, size_t workspace_bytes, const int32_t* root_tokens,
+                       int B, int K, int D, int N, int32_t* out_tree_tokens,
+                       int32_t* out_tree_parent, int32_t* out_node_row, float* out_node_value,
+                       int32_t* status, void* stream) {
+  if (!root_tokens || !out_tree_tokens || !out_tree_parent || !tree_shape_ok(B, K, D))
+    return SPEC_ERR_INVALID_ARG;
+  if (N < 1 || N > kMaxNodes || N > 1 + K + (D - 1) * K * K) return SPEC_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < spec_tree_build_workspace(B, K, D) || !aligned16(workspace))
+    return SPEC_ERR_WORKSPACE;
+  const cudaError_t e = launch_tree_finalize(workspace, B, K, D, root_tokens, N, out_tree_tokens,
+                                             out_tree_parent, out_node_row, out_node_value, status,
+                                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 const char* spec_status_string(int code) {
   switch (code) {
     case SPEC_OK: return "ok";

@@ -328,3 +328,33 @@ def make_verify_case(cfg: Config, T: float, seed: int = 0, sigma_d: Optional[flo
                 rank[j] += 1
         uni[b] = rng.integers(0, 1 << 24, size=N).astype(np.float32) / np.float32(1 << 24)
     return VerifyCase(tl, dp, tok, par, uni, float(T))
+
+
+@dataclasses.dataclass
+class TreeBuildCase:
+    """Inputs of a dynamic tree construction: every level's draft rows, in the order the levels
+    consume them (row 0: the root's; row 1 + (d - 2) K + i: frontier slot i's at level d)."""
+    draft_rows: np.ndarray   # fp32 [B, 1 + (D - 1) K, V]
+    root_tokens: np.ndarray  # int32 [B]
+    K: int
+    D: int
+
+    def level_rows(self, d: int) -> np.ndarray:
+        """Level d's rows, [B, 1, V] at d = 1, else [B, K, V] (a contiguous copy)."""
+        if d == 1:
+            return np.ascontiguousarray(self.draft_rows[:, :1])
+        s = 1 + (d - 2) * self.K
+        return np.ascontiguousarray(self.draft_rows[:, s:s + self.K])
+
+
+def make_tree_build_case(B: int, K: int, D: int, V: int, seed: int = 0,
+                         sigma: float = 3.0) -> TreeBuildCase:
+    """Draft logits ~ N(0, sigma^2) per row, independent across rows (the draft model's rows for
+    the frontier nodes; the construction does not depend on where they come from)."""
+    rows = np.empty((B, 1 + (D - 1) * K, V), dtype=np.float32)
+    roots = np.empty(B, dtype=np.int32)
+    for b in range(B):
+        rng = _rng(seed, 7, b, 11)
+        rows[b] = rng.standard_normal((rows.shape[1], V), dtype=np.float32) * np.float32(sigma)
+        roots[b] = int(rng.integers(V))
+    return TreeBuildCase(rows, roots, K, D)

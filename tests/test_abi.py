@@ -34,7 +34,8 @@ def test_header_declares_the_entry_points():
     for n in ("spec_tree_attention", "spec_tree_verify", "spec_tree_attention_workspace",
               "spec_tree_verify_workspace", "spec_status_string", "spec_tree_attention_paged",
               "spec_kv_compact", "spec_kv_compact_paged", "spec_tree_verify_filtered",
-              "spec_tree_verify_filtered_workspace"):
+              "spec_tree_verify_filtered_workspace", "spec_tree_build_workspace",
+              "spec_tree_expand", "spec_tree_finalize"):
         assert n in names
 
 
@@ -165,3 +166,31 @@ def test_filtered_verify_arguments(lib):
     need = lib.spec_tree_verify_filtered_workspace(1, 5, 1000)
     assert call(ws=need - 16) == -3                  # the filtered logits do not fit
     assert call(k=0, p=0.5, ws=need - 16) == -3      # top-p alone also filters
+
+
+def test_tree_construction_arguments(lib):
+    """Workspace query and argument errors of the tree construction, before any CUDA call."""
+    assert lib.spec_tree_build_workspace(4, 10, 6) >= 4 * (128 + 16 * (1 + 10 + 5 * 100))
+    assert lib.spec_tree_build_workspace(4, 17, 2) == 0       # K above SPEC_TREE_MAX_K
+    assert lib.spec_tree_build_workspace(4, 16, 10) == 0      # pool above SPEC_TREE_MAX_POOL
+    assert lib.spec_tree_build_workspace(0, 4, 2) == 0
+    fake = ctypes.c_void_p(256)
+    null = None
+    ws = lib.spec_tree_build_workspace(2, 4, 3)
+
+    def expand(V=100, K=4, D=3, level=1, logits=fake, nbytes=ws):
+        return lib.spec_tree_expand(logits, 2, V, K, D, level, fake, nbytes, null, null, null,
+                                    null)
+    assert expand(logits=null) == -1
+    assert expand(V=3) == -1                  # fewer tokens than K
+    assert expand(level=0) == -1 and expand(level=4) == -1
+    assert expand(K=0) == -1
+    assert expand(nbytes=ws - 16) == -3
+
+    def fin(N=10, K=4, D=3, nbytes=ws, out=fake):
+        return lib.spec_tree_finalize(fake, nbytes, fake, 2, K, D, N, out, fake, null, null, null,
+                                      null)
+    assert fin(N=0) == -1 and fin(N=65) == -1
+    assert fin(N=1 + 4 + 2 * 16 + 1) == -1    # more nodes than the construction can draft
+    assert fin(out=null) == -1
+    assert fin(nbytes=16) == -3
