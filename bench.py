@@ -484,8 +484,8 @@ def run_ours(args):
 
 
 def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev, L2):
-    """Paged-cache attention (16-slot pages), post-accept KV compaction and filtered verification
-    on this workload.
+    """Paged-cache attention (16-slot pages), post-accept KV compaction, filtered verification and
+    dynamic tree construction on this workload.
 
     Paged attention: the same queries, tree and prefix over pages in a random physical order,
     rotated over device copies larger than 2 x L2, timed per call from CUDA graphs; its
@@ -567,14 +567,53 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
             filtered(c)
     torch.cuda.synchronize()
     assert all(int(c["st_f"].sum()) == 0 for c in bufs)
+
+    # dynamic tree construction: K = 10 candidates per expanded node, depth 6, this workload's
+    # vocabulary and tree size, rows rotated over copies larger than 2 x L2
+    tK, tD = 10, 6
+    tcase = W.make_tree_build_case(B, tK, tD, V, seed=args.seed)
+    ncp_t = max(2, math.ceil(2 * L2 / tcase.draft_rows.nbytes))
+    ws_t = st.spec_tree_build_workspace(B, tK, tD)
+    i32 = dict(dtype=torch.int32, device=dev)
+    tcs = [{"levels": [to_dev(tcase.level_rows(d)) for d in range(1, tD + 1)],
+            "roots": to_dev(tcase.root_tokens), "ws": torch.empty((ws_t,), dtype=torch.uint8,
+                                                                 device=dev),
+            "ft": torch.empty((B, tK), **i32), "fs": torch.empty((B, tK), **i32),
+            "st": torch.zeros((B,), **i32),
+            "out": {k: torch.empty((B, N), **i32) for k in ("tree_tokens", "tree_parent",
+                                                            "node_row")}}
+           for _ in range(ncp_t)]
+    for c in tcs:
+        c["out"]["node_value"] = torch.empty((B, N), dtype=torch.float32, device=dev)
+
+    def expand_all(c):
+        for d in range(1, tD + 1):
+            st.spec_tree_expand(c["levels"][d - 1], tK, tD, d, c["ws"], frontier_tokens=c["ft"],
+                                frontier_parent_slot=c["fs"], status=c["st"])
+
+    def finalize(c):
+        st.spec_tree_finalize(c["ws"], c["roots"], tK, tD, N, outputs=c["out"], status=c["st"])
+
+    def build(c):
+        expand_all(c)
+        finalize(c)
+
+    for _ in range(3):
+        for c in tcs:
+            build(c)
+    torch.cuda.synchronize()
+    assert all(int(c["st"].sum()) == 0 for c in tcs)
     g_p, g_c = capture(paged, pcs), capture(compact, bufs)
     g_f, g_v = capture(filtered, bufs), capture(plain, bufs)
+    g_tb, g_tx = capture(build, tcs), capture(expand_all, tcs)
     torch.cuda.current_stream().wait_stream(s)
     for _ in range(2):
         g_p.replay()
         g_c.replay()
         g_f.replay()
         g_v.replay()
+        g_tb.replay()
+        g_tx.replay()
     torch.cuda.synchronize()
     reps = max(1, 600 // ncp)
     p_ms = timed(lambda: [g_p.replay() for _ in range(reps)]) / (reps * ncp)
@@ -582,6 +621,10 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
     f_ms = timed(lambda: [g_f.replay() for _ in range(reps_f)]) / (reps_f * len(bufs))
     v_ms = timed(lambda: [g_v.replay() for _ in range(reps_f)]) / (reps_f * len(bufs))
     filt_bytes = 2 * B * N * V * 4  # the logits read once, the filtered logits written once
+    reps_t = max(1, 300 // ncp_t)
+    tb_ms = timed(lambda: [g_tb.replay() for _ in range(reps_t)]) / (reps_t * ncp_t)
+    tx_ms = timed(lambda: [g_tx.replay() for _ in range(reps_t)]) / (reps_t * ncp_t)
+    tree_bytes = tcase.draft_rows.nbytes  # every draft row read once
     fil_gbs = filt_bytes / ((f_ms - v_ms) * 1e-3) / 1e9 if f_ms > v_ms else None
     reps_c = max(1, 600 // len(bufs))
     c_ms = timed(lambda: [g_c.replay() for _ in range(reps_c)]) / (reps_c * len(bufs))
@@ -606,6 +649,14 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
                             "kernel": "filter_kernel (cluster per row, row in shared memory)",
                             "note": "filter kernel time = filtered call - plain call (same "
                                     "copies, same temperature); latency-bound"},
+        "tree_build": {"K": tK, "depth": tD, "nodes": N, "rows_per_sequence": 1 + (tD - 1) * tK,
+                       "us_per_tree": tb_ms * 1e3, "expand_us_all_levels": tx_ms * 1e3,
+                       "finalize_us": (tb_ms - tx_ms) * 1e3, "algorithmic_bytes": tree_bytes,
+                       "achieved_gbs": tree_bytes / (tx_ms * 1e-3) / 1e9,
+                       "frac": tree_bytes / (tx_ms * 1e-3) / 1e9 / hbm_gbs, "copies": ncp_t,
+                       "kernel": "expand_kernel (one CTA per draft row, six launches), "
+                                 "finalize_kernel",
+                       "note": "expand rate = draft-row bytes / time of the six expand launches"},
         "peak_gbs": hbm_gbs,
     }
 

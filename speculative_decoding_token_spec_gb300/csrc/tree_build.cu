@@ -15,11 +15,13 @@
 // State (the caller's workspace, per sequence): a 128-byte header (levels done, pool size, arrival
 // counter, status bits, frontier) and the pool, one 16-byte entry per drafted node.
 //
-// expand_kernel: one CTA per draft row of the level.  A pass over the row keeps each thread's best K
-// entries; K rounds of a CTA-wide argmax merge them; a second pass (L2) sums exp(x - m) with a
-// compensated sum for the log-sum-exp.  The CTA appends its K candidates to the pool; the last CTA
-// of the sequence to arrive (counter + fences, no waiting) ranks the level's candidates and writes
-// the frontier.  finalize_kernel: one CTA per sequence ranks the pool by counting and writes the tree.
+// expand_kernel: one CTA per draft row of the level.  A pass over the row (32 elements per thread
+// in flight) finds each warp's best entry; L, the K-th best of those, bounds the row's K best from
+// below.  A second pass (L2) sums exp(x - m) with a compensated sum for the log-sum-exp and
+// collects the few entries >= L, which are ranked exactly.  The CTA appends its K candidates to
+// the pool; the last CTA of the sequence to arrive (counter + fences, no waiting) ranks the
+// level's candidates and writes the frontier.  finalize_kernel: one CTA per sequence sorts the
+// pool (bitonic, by value then pool index) and writes the tree.
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,8 +29,11 @@ namespace spectree {
 
 namespace {
 
-constexpr int kBThreads = 256;
+constexpr int kBThreads = 512;
 constexpr int kFinThreads = 512;
+constexpr int kChunk = 32;  // row elements per thread in flight
+
+typedef unsigned long long u64;
 
 struct BuildHeader {
   int32_t level;    // levels expanded so far
@@ -51,14 +56,33 @@ __device__ __forceinline__ uint32_t meta_of(int depth, int row1, int order) {
   return (uint32_t(depth) << 24) | (uint32_t(row1) << 12) | uint32_t(order);
 }
 
+__device__ __forceinline__ uint32_t order_key(float x) {  // larger float <-> larger key
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;  // -0 and +0 are equal logits: one key
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_float(uint32_t k) {  // inverse of order_key (-0 -> +0)
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// An element's key: a larger key is a larger value, then a lower token id; every key is > 0.
+__device__ __forceinline__ unsigned long long elem_key(float x, int y) {
+  return ((unsigned long long)order_key(x) << 32) | (0xffffffffu - (uint32_t)y);
+}
+
 // (x, y) ranks before (v, z): larger value, then lower index
 __device__ __forceinline__ bool before(float x, int y, float v, int z) {
   return x > v || (x == v && y < z);
 }
 
+constexpr int kCandCap = 2048;  // keys at or above the threshold a CTA collects
+
 struct ExpandSmem {
-  float lv[kMaxTreeK][kBThreads];  // each thread's best entries (value), best first
-  int li[kMaxTreeK][kBThreads];    // and their token ids
+  unsigned long long wkey[kBThreads / 32];  // each warp's best key
+  unsigned long long ckey[kCandCap];        // the keys >= L
+  unsigned long long mkey, lkey;
+  int nc;
   float wv[kBThreads / 32];
   int wi[kBThreads / 32], wt[kBThreads / 32];
   float best_v[kMaxTreeK];
@@ -77,6 +101,10 @@ __global__ void __launch_bounds__(kBThreads) expand_kernel(const float* __restri
                                                            size_t stride, int32_t* ftok,
                                                            int32_t* fslot, int32_t* status) {
   __shared__ ExpandSmem sm;
+  // each thread's best K entries, best first: value lv[k * 512 + t], token id li[k * 512 + t]
+  extern __shared__ float4 lists_raw[];
+  float* lv = reinterpret_cast<float*>(lists_raw);
+  int* li = reinterpret_cast<int*>(lv + K * kBThreads);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int b = blockIdx.x / R, i = blockIdx.x % R;
   BuildHeader* hdr = reinterpret_cast<BuildHeader*>(state + (size_t)b * stride);
@@ -100,88 +128,92 @@ __global__ void __launch_bounds__(kBThreads) expand_kernel(const float* __restri
   }
   const float* row = logits + ((size_t)b * R + i) * (size_t)V;
 
-  // ---- pass 1: each thread's best K entries (insertion into its column of the lists)
-  for (int k = 0; k < K; ++k) {
-    sm.lv[k][tid] = -INFINITY;
-    sm.li[k][tid] = 0x7fffffff;
+  if (tid == 0) {
+    if (level == 1) {  // a new construction (one CTA per sequence at level 1)
+      hdr->flags = 0;
+      hdr->arrived = 0;
+    }
+    sm.lkey = 0ull;  // below every element's key: all elements, if fewer than K threads hold one
+    sm.nc = 0;
   }
-  if (tid == 0 && level == 1) {  // a new construction (one CTA per sequence at level 1)
-    hdr->flags = 0;
-    hdr->arrived = 0;
-  }
-  __syncthreads();
+  // rows 16-byte aligned (V % 4 == 0): float4 loads; thread t's chunk elements are
+  // base + 4 (t + 512 j) + e (vector) or base + t + 512 j (scalar)
+  const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  auto elem = [&](int base, int j) -> int {  // the row index of element j of a chunk
+    return vec ? base + 4 * (tid + kBThreads * (j >> 2)) + (j & 3) : base + tid + kBThreads * j;
+  };
+  auto load_chunk = [&](int base, float (&v)[kChunk]) {
+    if (vec) {
+#pragma unroll
+      for (int j = 0; j < kChunk / 4; ++j) {
+        const int y = base + 4 * (tid + kBThreads * j);
+        float4 q = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (y < V) q = __ldg(reinterpret_cast<const float4*>(row + y));
+        v[4 * j] = q.x;
+        v[4 * j + 1] = q.y;
+        v[4 * j + 2] = q.z;
+        v[4 * j + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        const int y = base + tid + kBThreads * j;
+        v[j] = y < V ? __ldg(row + y) : -INFINITY;
+      }
+    }
+  };
+  // ---- pass 1: each warp's best key (larger value, then lower token id); NaN / +Inf check
   bool bad = false;
-  float worst_v = -INFINITY;
-  int worst_i = 0x7fffffff;
-  for (int y = tid; y < V; y += kBThreads) {
-    const float x = __ldg(row + y);
-    if (isnan(x) || x == INFINITY) {
-      bad = true;
-      continue;
+  u64 best = 0ull;
+  for (int base = 0; base < V; base += kBThreads * kChunk) {
+    float v[kChunk];
+    load_chunk(base, v);
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const int y = elem(base, j);
+      if (y >= V) continue;
+      if (isnan(v[j]) || v[j] == INFINITY) bad = true;
+      else best = max(best, elem_key(v[j], y));
     }
-    if (!before(x, y, worst_v, worst_i)) continue;
-    int p = K - 1;  // shift the worse entries down, insert
-    while (p > 0 && before(x, y, sm.lv[p - 1][tid], sm.li[p - 1][tid])) {
-      sm.lv[p][tid] = sm.lv[p - 1][tid];
-      sm.li[p][tid] = sm.li[p - 1][tid];
-      --p;
-    }
-    sm.lv[p][tid] = x;
-    sm.li[p][tid] = y;
-    worst_v = sm.lv[K - 1][tid];
-    worst_i = sm.li[K - 1][tid];
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+  if (lane == 0) sm.wkey[w] = best;  // the warp's best key
   if (__syncthreads_or(bad)) {
     if (tid == 0) atomicOr(&hdr->flags, SPEC_ST_NONFINITE);
     bad = true;
   }
-  // ---- merge: K rounds of a CTA-wide argmax over the threads' heads
-  int head = 0;
-  if (!bad) {
-    for (int k = 0; k < K; ++k) {
-      float v = head < K ? sm.lv[head][tid] : -INFINITY;
-      int y = head < K ? sm.li[head][tid] : 0x7fffffff;
-      int t = tid;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-        const int y2 = __shfl_xor_sync(0xffffffffu, y, o);
-        const int t2 = __shfl_xor_sync(0xffffffffu, t, o);
-        if (before(v2, y2, v, y)) {
-          v = v2;
-          y = y2;
-          t = t2;
-        }
-      }
-      if (lane == 0) {
-        sm.wv[w] = v;
-        sm.wi[w] = y;
-        sm.wt[w] = t;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        float bv = sm.wv[0];
-        int bi = sm.wi[0], bt = sm.wt[0];
-        for (int q = 1; q < kBThreads / 32; ++q)
-          if (before(sm.wv[q], sm.wi[q], bv, bi)) {
-            bv = sm.wv[q];
-            bi = sm.wi[q];
-            bt = sm.wt[q];
-          }
-        sm.best_v[k] = bv;
-        sm.best_i[k] = bi;
-        sm.win_t = bt;
-      }
-      __syncthreads();
-      if (tid == sm.win_t) ++head;
-    }
+  // ---- the row max and L, the K-th best of the warps' bests (K <= 16 warps): at least K
+  // elements are >= L, so the K best elements all are
+  if (!bad && tid < kBThreads / 32 && sm.wkey[tid] != 0ull) {
+    const u64 mine = sm.wkey[tid];
+    int r = 0;
+    for (int t = 0; t < kBThreads / 32; ++t) r += sm.wkey[t] > mine ? 1 : 0;
+    if (r == 0) sm.mkey = mine;
+    if (r == K - 1) sm.lkey = mine;
   }
-  // ---- pass 2: log-sum-exp (compensated sum of exp(x - m), m = the row max)
+  __syncthreads();
+  // ---- pass 2 (L2): log-sum-exp (compensated sum of exp(x - m)), and the keys >= L
   float lse = 0.f;
   if (!bad) {
-    const float m = sm.best_v[0];
+    const float m = key_float((uint32_t)(sm.mkey >> 32));
+    const u64 L = sm.lkey;
     CompSum acc;
-    for (int y = tid; y < V; y += kBThreads) acc.add(__expf(__fsub_rn(__ldg(row + y), m)));
+    for (int base = 0; base < V; base += kBThreads * kChunk) {
+      float v[kChunk];
+      load_chunk(base, v);
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        const int y = elem(base, j);
+        if (y >= V) continue;
+        acc.add(__expf(__fsub_rn(v[j], m)));
+        const u64 k = elem_key(v[j], y);
+        if (k >= L) {
+          const int slot = atomicAdd(&sm.nc, 1);
+          if (slot < kCandCap) sm.ckey[slot] = k;
+        }
+      }
+    }
     float hi = acc.hi, lo = acc.lo;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {  // warp sum of the (hi, lo) pairs in two-float arithmetic
@@ -204,7 +236,86 @@ __global__ void __launch_bounds__(kBThreads) expand_kernel(const float* __restri
     }
     // log(S) for S = sh + sl (sh >= 1: the max contributes exp(0))
     lse = __fadd_rn(m, __fadd_rn(logf(sh), __fdiv_rn(sl, sh)));
+    // ---- the K best: rank the candidates
+    const int nc = sm.nc;
+    if (nc <= kCandCap) {
+      for (int c = tid; c < nc; c += kBThreads) {
+        const u64 kc = sm.ckey[c];
+        int r = 0;
+        for (int o = 0; o < nc; ++o) r += sm.ckey[o] > kc ? 1 : 0;
+        if (r < K) {
+          sm.best_v[r] = key_float((uint32_t)(kc >> 32));
+          sm.best_i[r] = (int)(0xffffffffu - (uint32_t)kc);
+        }
+      }
+    } else {
+      // more than kCandCap keys reach L (ties or values placed to defeat the warps' bests): each
+      // thread keeps its best K in shared memory, then K rounds of a CTA-wide argmax
+      for (int k = 0; k < K; ++k) {
+        lv[k * kBThreads + tid] = -INFINITY;
+        li[k * kBThreads + tid] = 0x7fffffff;
+      }
+      for (int base = 0; base < V; base += kBThreads * kChunk) {
+        float v[kChunk];
+        load_chunk(base, v);
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          const int y = elem(base, j);
+          if (y >= V || !before(v[j], y, lv[(K - 1) * kBThreads + tid],
+                                li[(K - 1) * kBThreads + tid]))
+            continue;
+          int p = K - 1;  // shift the worse entries down, insert
+          while (p > 0 && before(v[j], y, lv[(p - 1) * kBThreads + tid],
+                                 li[(p - 1) * kBThreads + tid])) {
+            lv[p * kBThreads + tid] = lv[(p - 1) * kBThreads + tid];
+            li[p * kBThreads + tid] = li[(p - 1) * kBThreads + tid];
+            --p;
+          }
+          lv[p * kBThreads + tid] = v[j];
+          li[p * kBThreads + tid] = y;
+        }
+      }
+      int head = 0;
+      for (int k = 0; k < K; ++k) {
+        float v = head < K ? lv[head * kBThreads + tid] : -INFINITY;
+        int y = head < K ? li[head * kBThreads + tid] : 0x7fffffff;
+        int t = tid;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+          const int y2 = __shfl_xor_sync(0xffffffffu, y, o);
+          const int t2 = __shfl_xor_sync(0xffffffffu, t, o);
+          if (before(v2, y2, v, y)) {
+            v = v2;
+            y = y2;
+            t = t2;
+          }
+        }
+        if (lane == 0) {
+          sm.wv[w] = v;
+          sm.wi[w] = y;
+          sm.wt[w] = t;
+        }
+        __syncthreads();
+        if (tid == 0) {
+          float bv = sm.wv[0];
+          int bi = sm.wi[0], bt = sm.wt[0];
+          for (int q = 1; q < kBThreads / 32; ++q)
+            if (before(sm.wv[q], sm.wi[q], bv, bi)) {
+              bv = sm.wv[q];
+              bi = sm.wi[q];
+              bt = sm.wt[q];
+            }
+          sm.best_v[k] = bv;
+          sm.best_i[k] = bi;
+          sm.win_t = bt;
+        }
+        __syncthreads();
+        if (tid == sm.win_t) ++head;
+      }
+    }
   }
+  __syncthreads();
   // ---- this row's candidates into the pool
   if (!bad && tid < K) {
     const float lp = fminf(__fsub_rn(sm.best_v[tid], lse), 0.f);  // a log-probability is <= 0
@@ -266,6 +377,13 @@ __global__ void __launch_bounds__(kBThreads) expand_kernel(const float* __restri
   }
 }
 
+__device__ __forceinline__ uint32_t value_key(float v) {  // larger value <-> smaller key
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // order-preserving
+  return ~u;
+}
+
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const uint8_t* __restrict__ state,
                                                                size_t stride,
                                                                const int32_t* root_tokens, int N,
@@ -274,10 +392,12 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const uint8_t* __
                                                                int32_t* node_row,
                                                                float* node_value,
                                                                int32_t* status) {
-  __shared__ float sv[kMaxTreePool];
-  __shared__ uint32_t smeta[kMaxTreePool];
-  __shared__ short spos[kMaxTreePool];
-  const int tid = threadIdx.x, b = blockIdx.x;
+  // (value, pool index) keys, sorted ascending = best first; a node's pool index orders it by
+  // (depth, candidate order), the tie rule
+  __shared__ unsigned long long key[kMaxTreePool];
+  __shared__ short spos[kMaxTreePool];  // chosen: tree position; else -1
+  __shared__ int wscan[kFinThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, b = blockIdx.x;
   const BuildHeader* hdr = reinterpret_cast<const BuildHeader*>(state + (size_t)b * stride);
   const PoolEntry* pool =
       reinterpret_cast<const PoolEntry*>(state + (size_t)b * stride + sizeof(BuildHeader));
@@ -286,33 +406,53 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const uint8_t* __
   const int level = __ldcg(&hdr->level), flags = __ldcg(&hdr->flags);
   const int n = (level >= 1 && !(flags & SPEC_ST_NONFINITE)) ? __ldcg(&hdr->count) : 1;
   if (tid == 0 && status && (flags & SPEC_ST_NONFINITE)) atomicOr(status + b, SPEC_ST_NONFINITE);
-  for (int c = tid; c < n; c += kFinThreads) {
-    sv[c] = c ? __ldcg(&pool[c].value) : 0.f;
-    smeta[c] = c ? __ldcg(&pool[c].meta) : 0u;
-    spos[c] = -1;
+  int np2 = 1;
+  while (np2 < n) np2 <<= 1;
+  for (int c = tid; c < np2; c += kFinThreads) {
+    // the root sorts first (it is always in the tree); padding last
+    key[c] = c == 0 ? 0ull
+             : c < n ? ((unsigned long long)value_key(__ldcg(&pool[c].value)) << 32) | (unsigned)c
+                     : ~0ull;
+    if (c < n) spos[c] = -1;
   }
   __syncthreads();
-  const int nsel = min(N - 1, n - 1);
-  // rank among the candidates: larger value, then shallower, then lower order
-  for (int c = 1 + tid; c < n; c += kFinThreads) {
-    const float v = sv[c];
-    const uint32_t k = smeta[c] & 0xff000fffu;  // depth and order
-    int r = 0;
-    for (int o = 1; o < n; ++o) {
-      const float v2 = sv[o];
-      r += (v2 > v || (v2 == v && (smeta[o] & 0xff000fffu) < k)) ? 1 : 0;
+  for (int k = 2; k <= np2; k <<= 1) {  // bitonic sort, ascending
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int a = tid; a < np2; a += kFinThreads) {
+        const int p = a ^ j;
+        if (p > a) {
+          const unsigned long long x = key[a], y = key[p];
+          const bool up = (a & k) == 0;
+          if ((x > y) == up) {
+            key[a] = y;
+            key[p] = x;
+          }
+        }
+      }
+      __syncthreads();
     }
-    spos[c] = r < nsel ? 0 : -1;  // chosen (position below)
   }
+  const int nsel = min(N - 1, n - 1);  // the chosen candidates: key[1 .. nsel]
+  for (int r = 1 + tid; r <= nsel; r += kFinThreads) spos[(int)(key[r] & 0xffffffffu)] = 0;
   __syncthreads();
-  // position: 1 + the chosen nodes before it in (depth, order)
-  for (int c = 1 + tid; c < n; c += kFinThreads) {
-    if (spos[c] < 0) continue;
-    const uint32_t k = smeta[c] & 0xff000fffu;
-    int p = 1;
-    for (int o = 1; o < n; ++o) p += (spos[o] >= 0 && (smeta[o] & 0xff000fffu) < k) ? 1 : 0;
-    spos[c] = (short)p;  // (other threads only test spos >= 0, which this keeps)
+  // tree position of a chosen node: 1 + chosen nodes with a lower pool index (block scan)
+  int run = 0;  // chosen nodes below this thread's range
+  const int per = (n + kFinThreads - 1) / kFinThreads;
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  int mine = 0;
+  for (int c = max(lo, 1); c < hi; ++c) mine += spos[c] >= 0 ? 1 : 0;
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
   }
+  if (lane == 31) wscan[w] = incl;
+  __syncthreads();
+  for (int q = 0; q < w; ++q) run += wscan[q];
+  run += incl - mine;
+  for (int c = max(lo, 1); c < hi; ++c)
+    if (spos[c] >= 0) spos[c] = (short)(1 + run++);
   __syncthreads();
   int32_t* tt = tree_tokens + (size_t)b * N;
   int32_t* tp = tree_parent + (size_t)b * N;
@@ -332,14 +472,14 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const uint8_t* __
     if (tr) tr[0] = level >= 1 ? 0 : -1;
     if (tv) tv[0] = 0.f;
   }
-  for (int c = 1 + tid; c < n; c += kFinThreads) {
+  for (int r = 1 + tid; r <= nsel; r += kFinThreads) {
+    const int c = (int)(key[r] & 0xffffffffu);
     const int j = spos[c];
-    if (j < 0) continue;
-    const int par = __ldcg(&pool[c].parent);
-    tt[j] = __ldcg(&pool[c].token);
-    tp[j] = par == 0 ? 0 : spos[par];
-    if (tr) tr[j] = int((smeta[c] >> 12) & 0xfffu) - 1;
-    if (tv) tv[j] = sv[c];
+    const PoolEntry e = pool[c];
+    tt[j] = e.token;
+    tp[j] = e.parent == 0 ? 0 : spos[e.parent];
+    if (tr) tr[j] = int((e.meta >> 12) & 0xfffu) - 1;
+    if (tv) tv[j] = e.value;
   }
 }
 
@@ -353,9 +493,16 @@ size_t tree_build_stride(int K, int D) {
 cudaError_t launch_tree_expand(const float* logits, int B, int R, int V, int K, int D, int level,
                                void* state, int32_t* ftok, int32_t* fslot, int32_t* status,
                                cudaStream_t s) {
+  const size_t lists = (size_t)K * kBThreads * (sizeof(float) + sizeof(int));
+  if (lists + sizeof(ExpandSmem) > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lists);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(B * R));
   cfg.blockDim = dim3(kBThreads);
+  cfg.dynamicSmemBytes = lists;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
