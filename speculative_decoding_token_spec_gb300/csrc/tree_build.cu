@@ -95,7 +95,156 @@ struct ExpandSmem {
   int rank[kMaxTreeK * kMaxTreeK];
 };
 
-__global__ void __launch_bounds__(kBThreads) expand_kernel(const float* __restrict__ logits, int R,
+__device__ __forceinline__ uint32_t cluster_atom_add_u32(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.relaxed.cluster.shared::cluster.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Exact top K of a whole row by per-thread insertion lists (lv / li, K x 512) and K rounds of a
+// CTA-wide argmax; for rows whose threshold admits more than kCandCap keys.  Every thread calls it.
+__device__ void slow_topk(ExpandSmem& sm, float* lv, int* li, const float* row, int V, int K) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  for (int k = 0; k < K; ++k) {
+    lv[k * kBThreads + tid] = -INFINITY;
+    li[k * kBThreads + tid] = 0x7fffffff;
+  }
+  for (int y = tid; y < V; y += kBThreads) {
+    const float x = __ldg(row + y);
+    if (!before(x, y, lv[(K - 1) * kBThreads + tid], li[(K - 1) * kBThreads + tid])) continue;
+    int p = K - 1;  // shift the worse entries down, insert
+    while (p > 0 && before(x, y, lv[(p - 1) * kBThreads + tid], li[(p - 1) * kBThreads + tid])) {
+      lv[p * kBThreads + tid] = lv[(p - 1) * kBThreads + tid];
+      li[p * kBThreads + tid] = li[(p - 1) * kBThreads + tid];
+      --p;
+    }
+    lv[p * kBThreads + tid] = x;
+    li[p * kBThreads + tid] = y;
+  }
+  int head = 0;
+  for (int k = 0; k < K; ++k) {
+    float v = head < K ? lv[head * kBThreads + tid] : -INFINITY;
+    int y = head < K ? li[head * kBThreads + tid] : 0x7fffffff;
+    int t = tid;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+      const int y2 = __shfl_xor_sync(0xffffffffu, y, o);
+      const int t2 = __shfl_xor_sync(0xffffffffu, t, o);
+      if (before(v2, y2, v, y)) {
+        v = v2;
+        y = y2;
+        t = t2;
+      }
+    }
+    if (lane == 0) {
+      sm.wv[w] = v;
+      sm.wi[w] = y;
+      sm.wt[w] = t;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float bv = sm.wv[0];
+      int bi = sm.wi[0], bt = sm.wt[0];
+      for (int q = 1; q < kBThreads / 32; ++q)
+        if (before(sm.wv[q], sm.wi[q], bv, bi)) {
+          bv = sm.wv[q];
+          bi = sm.wi[q];
+          bt = sm.wt[q];
+        }
+      sm.best_v[k] = bv;
+      sm.best_i[k] = bi;
+      sm.win_t = bt;
+    }
+    __syncthreads();
+    if (tid == sm.win_t) ++head;
+  }
+}
+
+// Ranks the collected keys (sm.ckey[0 .. nc)) into sm.best_v / sm.best_i (every thread calls it).
+__device__ void rank_candidates(ExpandSmem& sm, int nc, int K) {
+  for (int c = threadIdx.x; c < nc; c += kBThreads) {
+    const u64 kc = sm.ckey[c];
+    int r = 0;
+    for (int o = 0; o < nc; ++o) r += sm.ckey[o] > kc ? 1 : 0;
+    if (r < K) {
+      sm.best_v[r] = key_float((uint32_t)(kc >> 32));
+      sm.best_i[r] = (int)(0xffffffffu - (uint32_t)kc);
+    }
+  }
+}
+
+// The end of a row's expansion (every thread of the CTA): the row's K candidates into the pool,
+// the arrival, and for the last row of the sequence to arrive, the level's ranking and frontier.
+__device__ void finish_row(ExpandSmem& sm, BuildHeader* hdr, PoolEntry* pool, int b, int i, int R,
+                           int K, int level, int count, int f, float vf, float lse, bool bad,
+                           int32_t* ftok, int32_t* fslot, int32_t* status) {
+  const int tid = threadIdx.x;
+  // ---- this row's candidates into the pool
+  if (!bad && tid < K) {
+    const float lp = fminf(__fsub_rn(sm.best_v[tid], lse), 0.f);  // a log-probability is <= 0
+    PoolEntry e;
+    e.token = sm.best_i[tid];
+    e.parent = f;
+    e.value = __fadd_rn(vf, lp);
+    e.meta = meta_of(level, 0, i * K + tid);
+    pool[count + i * K + tid] = e;
+  }
+  if (tid == 0) {
+    const int row_idx = level == 1 ? 0 : 1 + (level - 2) * K + i;
+    if (level == 1) {
+      PoolEntry r;
+      r.token = -1;
+      r.parent = -1;
+      r.value = 0.f;
+      r.meta = meta_of(0, 1, 0);
+      pool[0] = r;
+    } else {
+      pool[f].meta = __ldcg(&pool[f].meta) | (uint32_t(row_idx + 1) << 12);
+    }
+  }
+  __threadfence();  // this CTA's pool writes before its arrival
+  __syncthreads();
+  if (tid == 0) sm.last = (atomicAdd(&hdr->arrived, 1) == R - 1);
+  __syncthreads();
+  if (!sm.last) return;
+  // ---- the last CTA of the sequence: rank the level's candidates, write the frontier
+  __threadfence();
+  const int nc = R * K;
+  const bool failed = (__ldcg(&hdr->flags) & SPEC_ST_NONFINITE) != 0;
+  if (!failed) {
+    for (int c = tid; c < nc; c += kBThreads) sm.cv[c] = __ldcg(&pool[count + c].value);
+    __syncthreads();
+    for (int c = tid; c < nc; c += kBThreads) {
+      const float v = sm.cv[c];
+      int r = 0;
+      for (int o = 0; o < nc; ++o) r += before(sm.cv[o], o, v, c) ? 1 : 0;
+      sm.rank[c] = r;
+    }
+    __syncthreads();
+    for (int c = tid; c < nc; c += kBThreads) {
+      const int r = sm.rank[c];
+      if (r < K) {
+        hdr->frontier[r] = count + c;
+        if (ftok) ftok[(size_t)b * K + r] = __ldcg(&pool[count + c].token);
+        if (fslot) fslot[(size_t)b * K + r] = c / K;
+      }
+    }
+  } else if (status && tid == 0) {
+    atomicOr(status + b, SPEC_ST_NONFINITE);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    hdr->count = count + (failed ? 0 : nc);
+    hdr->level = level;
+    hdr->arrived = 0;
+  }
+}
+
+__global__ void __launch_bounds__(kBThreads) expand_rows_kernel(const float* __restrict__ logits, int R,
                                                            int V, int K, int level,
                                                            uint8_t* __restrict__ state,
                                                            size_t stride, int32_t* ftok,
@@ -236,145 +385,214 @@ __global__ void __launch_bounds__(kBThreads) expand_kernel(const float* __restri
     }
     // log(S) for S = sh + sl (sh >= 1: the max contributes exp(0))
     lse = __fadd_rn(m, __fadd_rn(logf(sh), __fdiv_rn(sl, sh)));
-    // ---- the K best: rank the candidates
+    // ---- the K best: rank the candidates (or, if too many reach L, the slow exact way)
     const int nc = sm.nc;
-    if (nc <= kCandCap) {
-      for (int c = tid; c < nc; c += kBThreads) {
-        const u64 kc = sm.ckey[c];
-        int r = 0;
-        for (int o = 0; o < nc; ++o) r += sm.ckey[o] > kc ? 1 : 0;
-        if (r < K) {
-          sm.best_v[r] = key_float((uint32_t)(kc >> 32));
-          sm.best_i[r] = (int)(0xffffffffu - (uint32_t)kc);
-        }
-      }
-    } else {
-      // more than kCandCap keys reach L (ties or values placed to defeat the warps' bests): each
-      // thread keeps its best K in shared memory, then K rounds of a CTA-wide argmax
-      for (int k = 0; k < K; ++k) {
-        lv[k * kBThreads + tid] = -INFINITY;
-        li[k * kBThreads + tid] = 0x7fffffff;
-      }
-      for (int base = 0; base < V; base += kBThreads * kChunk) {
-        float v[kChunk];
-        load_chunk(base, v);
-#pragma unroll
-        for (int j = 0; j < kChunk; ++j) {
-          const int y = elem(base, j);
-          if (y >= V || !before(v[j], y, lv[(K - 1) * kBThreads + tid],
-                                li[(K - 1) * kBThreads + tid]))
-            continue;
-          int p = K - 1;  // shift the worse entries down, insert
-          while (p > 0 && before(v[j], y, lv[(p - 1) * kBThreads + tid],
-                                 li[(p - 1) * kBThreads + tid])) {
-            lv[p * kBThreads + tid] = lv[(p - 1) * kBThreads + tid];
-            li[p * kBThreads + tid] = li[(p - 1) * kBThreads + tid];
-            --p;
-          }
-          lv[p * kBThreads + tid] = v[j];
-          li[p * kBThreads + tid] = y;
-        }
-      }
-      int head = 0;
-      for (int k = 0; k < K; ++k) {
-        float v = head < K ? lv[head * kBThreads + tid] : -INFINITY;
-        int y = head < K ? li[head * kBThreads + tid] : 0x7fffffff;
-        int t = tid;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-          const int y2 = __shfl_xor_sync(0xffffffffu, y, o);
-          const int t2 = __shfl_xor_sync(0xffffffffu, t, o);
-          if (before(v2, y2, v, y)) {
-            v = v2;
-            y = y2;
-            t = t2;
-          }
-        }
-        if (lane == 0) {
-          sm.wv[w] = v;
-          sm.wi[w] = y;
-          sm.wt[w] = t;
-        }
-        __syncthreads();
-        if (tid == 0) {
-          float bv = sm.wv[0];
-          int bi = sm.wi[0], bt = sm.wt[0];
-          for (int q = 1; q < kBThreads / 32; ++q)
-            if (before(sm.wv[q], sm.wi[q], bv, bi)) {
-              bv = sm.wv[q];
-              bi = sm.wi[q];
-              bt = sm.wt[q];
-            }
-          sm.best_v[k] = bv;
-          sm.best_i[k] = bi;
-          sm.win_t = bt;
-        }
-        __syncthreads();
-        if (tid == sm.win_t) ++head;
-      }
-    }
+    if (nc <= kCandCap) rank_candidates(sm, nc, K);
+    else slow_topk(sm, lv, li, row, V, K);
   }
   __syncthreads();
-  // ---- this row's candidates into the pool
-  if (!bad && tid < K) {
-    const float lp = fminf(__fsub_rn(sm.best_v[tid], lse), 0.f);  // a log-probability is <= 0
-    PoolEntry e;
-    e.token = sm.best_i[tid];
-    e.parent = f;
-    e.value = __fadd_rn(vf, lp);
-    e.meta = meta_of(level, 0, i * K + tid);
-    pool[count + i * K + tid] = e;
+  finish_row(sm, hdr, pool, b, i, R, K, level, count, f, vf, lse, bad, ftok, fslot, status);
+}
+
+// Cluster form: the CL CTAs of a row each hold E elements per thread in registers (thread t of rank
+// r: elements r * 512 E + t + 512 j), so the row is read once and the log-sum-exp pass reads
+// registers.  Two DSMEM exchanges: every CTA's warp-best keys and non-finite flag to every CTA
+// (each derives the max and L), then every CTA's exp-sum and keys >= L to rank 0, which finishes
+// the row.
+template <int CL, int E>
+__global__ void __launch_bounds__(kBThreads) expand_cluster_kernel(
+    const float* __restrict__ logits, int R, int V, int K, int level, uint8_t* __restrict__ state,
+    size_t stride, int32_t* ftok, int32_t* fslot, int32_t* status) {
+  __shared__ ExpandSmem sm;
+  __shared__ unsigned long long xkey[CL][kBThreads / 32];  // every CTA's warp-best keys
+  __shared__ int xbad[CL];
+  __shared__ float xs_hi[CL], xs_lo[CL];  // every CTA's exp-sum (rank 0)
+  extern __shared__ float4 lists_raw[];   // slow_topk's lists (rank 0)
+  float* lv = reinterpret_cast<float*>(lists_raw);
+  int* li = reinterpret_cast<int*>(lv + K * kBThreads);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int rank = CL > 1 ? int(blockIdx.x % CL) : 0;
+  const int rowid = blockIdx.x / CL, b = rowid / R, i = rowid % R;
+  BuildHeader* hdr = reinterpret_cast<BuildHeader*>(state + (size_t)b * stride);
+  PoolEntry* pool = reinterpret_cast<PoolEntry*>(state + (size_t)b * stride + sizeof(BuildHeader));
+  griddep_wait();  // the rows and the state come from preceding work in the stream
+  griddep_launch_dependents();
+  int count = 1, f = 0;
+  float vf = 0.f;
+  if (level > 1) {  // the same header for every CTA of the cluster: they leave together
+    const int lv0 = __ldcg(&hdr->level), fl = __ldcg(&hdr->flags);
+    if (fl & SPEC_ST_NONFINITE) return;
+    if (lv0 != level - 1) {
+      if (tid == 0 && i == 0 && rank == 0 && status) atomicOr(status + b, SPEC_ST_BAD_TREE);
+      return;
+    }
+    count = __ldcg(&hdr->count);
+    f = __ldcg(&hdr->frontier[i]);
+    vf = __ldcg(&pool[f].value);
   }
   if (tid == 0) {
-    const int row_idx = level == 1 ? 0 : 1 + (level - 2) * K + i;
-    if (level == 1) {
-      PoolEntry r;
-      r.token = -1;
-      r.parent = -1;
-      r.value = 0.f;
-      r.meta = meta_of(0, 1, 0);
-      pool[0] = r;
-    } else {
-      pool[f].meta = __ldcg(&pool[f].meta) | (uint32_t(row_idx + 1) << 12);
+    if (level == 1 && rank == 0) {
+      hdr->flags = 0;
+      hdr->arrived = 0;
     }
+    sm.nc = 0;
+    sm.lkey = 0ull;
   }
-  __threadfence();  // this CTA's pool writes before its arrival
-  __syncthreads();
-  if (tid == 0) sm.last = (atomicAdd(&hdr->arrived, 1) == R - 1);
-  __syncthreads();
-  if (!sm.last) return;
-  // ---- the last CTA of the sequence: rank the level's candidates, write the frontier
-  __threadfence();
-  const int nc = R * K;
-  const bool failed = (__ldcg(&hdr->flags) & SPEC_ST_NONFINITE) != 0;
-  if (!failed) {
-    for (int c = tid; c < nc; c += kBThreads) sm.cv[c] = __ldcg(&pool[count + c].value);
+  if constexpr (CL > 1) cluster_arrive_release();  // this CTA has started and zeroed its counter
+  const float* row = logits + ((size_t)b * R + i) * (size_t)V;
+  const int y0 = rank * kBThreads * E + tid;
+  float x[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const int y = y0 + j * kBThreads;
+    x[j] = y < V ? __ldg(row + y) : -INFINITY;
+  }
+  bool bad = false;
+  u64 best = 0ull;
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const int y = y0 + j * kBThreads;
+    if (y >= V) continue;
+    if (isnan(x[j]) || x[j] == INFINITY) bad = true;
+    else best = max(best, elem_key(x[j], y));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+  bad = __syncthreads_or(bad);
+  // ---- exchange 1: warp-best keys and the non-finite flag to every CTA
+  if constexpr (CL > 1) {
+    cluster_wait_acquire();  // every CTA has started: its shared memory may be written
+    if (lane == 0)
+      for (int r = 0; r < CL; ++r)
+        dsmem_store_v2(dsmem_addr(&xkey[rank][w], r), (uint32_t)best, (uint32_t)(best >> 32));
+    if (tid == 0)
+      for (int r = 0; r < CL; ++r) dsmem_store_u32(dsmem_addr(&xbad[rank], r), bad ? 1u : 0u);
+    cluster_arrive_release();
+    cluster_wait_acquire();
+  } else {
+    if (lane == 0) xkey[0][w] = best;
+    if (tid == 0) xbad[0] = bad;
     __syncthreads();
-    for (int c = tid; c < nc; c += kBThreads) {
-      const float v = sm.cv[c];
+  }
+  bool anybad = false;
+  for (int r = 0; r < CL; ++r) anybad |= xbad[r] != 0;
+  if (anybad) {
+    if (rank != 0) return;
+    if (tid == 0) atomicOr(&hdr->flags, SPEC_ST_NONFINITE);
+    finish_row(sm, hdr, pool, b, i, R, K, level, count, f, vf, 0.f, true, ftok, fslot, status);
+    return;
+  }
+  // ---- the row max and L, the K-th best of the CL x 16 warp-best keys (>= K elements reach it)
+  constexpr int NX = CL * (kBThreads / 32);
+  if (tid < NX) {
+    const u64 mine = xkey[tid / (kBThreads / 32)][tid % (kBThreads / 32)];
+    if (mine != 0ull) {
       int r = 0;
-      for (int o = 0; o < nc; ++o) r += before(sm.cv[o], o, v, c) ? 1 : 0;
-      sm.rank[c] = r;
+      for (int t = 0; t < NX; ++t) r += xkey[t / (kBThreads / 32)][t % (kBThreads / 32)] > mine;
+      if (r == 0) sm.mkey = mine;
+      if (r == K - 1) sm.lkey = mine;
     }
-    __syncthreads();
-    for (int c = tid; c < nc; c += kBThreads) {
-      const int r = sm.rank[c];
-      if (r < K) {
-        hdr->frontier[r] = count + c;
-        if (ftok) ftok[(size_t)b * K + r] = __ldcg(&pool[count + c].token);
-        if (fslot) fslot[(size_t)b * K + r] = c / K;
+  }
+  __syncthreads();
+  const float m = key_float((uint32_t)(sm.mkey >> 32));
+  const u64 L = sm.lkey;
+  // ---- this CTA's exp-sum and keys >= L, to rank 0
+  CompSum acc;
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const int y = y0 + j * kBThreads;
+    if (y >= V) continue;
+    acc.add(__expf(__fsub_rn(x[j], m)));
+    const u64 k = elem_key(x[j], y);
+    if (k >= L) {
+      if constexpr (CL > 1) {
+        const uint32_t slot = cluster_atom_add_u32(dsmem_addr(&sm.nc, 0), 1u);
+        if (slot < (uint32_t)kCandCap)
+          dsmem_store_v2(dsmem_addr(&sm.ckey[slot], 0), (uint32_t)k, (uint32_t)(k >> 32));
+      } else {
+        const int slot = atomicAdd(&sm.nc, 1);
+        if (slot < kCandCap) sm.ckey[slot] = k;
       }
     }
-  } else if (status && tid == 0) {
-    atomicOr(status + b, SPEC_ST_NONFINITE);
+  }
+  float hi = acc.hi, lo = acc.lo;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {  // warp sum of the (hi, lo) pairs in two-float arithmetic
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    const DF d = df_two_sum(hi, h2);
+    hi = d.hi;
+    lo = __fadd_rn(__fadd_rn(lo, l2), d.lo);
+  }
+  if (lane == 0) {
+    sm.wsum_hi[w] = hi;
+    sm.wsum_lo[w] = lo;
   }
   __syncthreads();
   if (tid == 0) {
-    hdr->count = count + (failed ? 0 : nc);
-    hdr->level = level;
-    hdr->arrived = 0;
+    float sh = sm.wsum_hi[0], sl = sm.wsum_lo[0];
+    for (int q = 1; q < kBThreads / 32; ++q) {
+      const DF d = df_two_sum(sh, sm.wsum_hi[q]);
+      sh = d.hi;
+      sl = __fadd_rn(__fadd_rn(sl, sm.wsum_lo[q]), d.lo);
+    }
+    if constexpr (CL > 1) {
+      dsmem_store_u32(dsmem_addr(&xs_hi[rank], 0), __float_as_uint(sh));
+      dsmem_store_u32(dsmem_addr(&xs_lo[rank], 0), __float_as_uint(sl));
+    } else {
+      xs_hi[0] = sh;
+      xs_lo[0] = sl;
+    }
   }
+  if constexpr (CL > 1) {
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (rank != 0) return;  // nothing reads another CTA's shared memory after this point
+  } else {
+    __syncthreads();
+  }
+  // ---- rank 0: the log-sum-exp, the K best, the row's end
+  float sh = xs_hi[0], sl = xs_lo[0];
+  for (int r = 1; r < CL; ++r) {
+    const DF d = df_two_sum(sh, xs_hi[r]);
+    sh = d.hi;
+    sl = __fadd_rn(__fadd_rn(sl, xs_lo[r]), d.lo);
+  }
+  const float lse = __fadd_rn(m, __fadd_rn(logf(sh), __fdiv_rn(sl, sh)));
+  const int nc = sm.nc;
+  if (nc <= kCandCap) rank_candidates(sm, nc, K);
+  else slow_topk(sm, lv, li, row, V, K);
+  __syncthreads();
+  finish_row(sm, hdr, pool, b, i, R, K, level, count, f, vf, lse, false, ftok, fslot, status);
+}
+
+template <int CL, int E>
+cudaError_t launch_expand_cluster(const float* logits, int B, int R, int V, int K, int D, int level,
+                                  void* state, int32_t* ftok, int32_t* fslot, int32_t* status,
+                                  cudaStream_t s) {
+  const size_t lists = (size_t)K * kBThreads * (sizeof(float) + sizeof(int));
+  if (lists > 48 * 1024 - 24 * 1024) {  // with the static part above the default: opt in
+    const cudaError_t e = cudaFuncSetAttribute(
+        expand_cluster_kernel<CL, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lists);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(B * R * CL));
+  cfg.blockDim = dim3(kBThreads);
+  cfg.dynamicSmemBytes = lists;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, expand_cluster_kernel<CL, E>, logits, R, V, K, level,
+                            static_cast<uint8_t*>(state), tree_build_stride(K, D), ftok, fslot,
+                            status);
 }
 
 __device__ __forceinline__ uint32_t value_key(float v) {  // larger value <-> smaller key
@@ -493,10 +711,28 @@ size_t tree_build_stride(int K, int D) {
 cudaError_t launch_tree_expand(const float* logits, int B, int R, int V, int K, int D, int level,
                                void* state, int32_t* ftok, int32_t* fslot, int32_t* status,
                                cudaStream_t s) {
+  // a cluster per row with the row in registers (up to 8 CTAs x 512 threads x 32 elements) while
+  // the launch stays within 2048 CTAs: it shortens a row's latency, and with more rows than that
+  // one CTA per row already fills the GPU
+  const int per16 = kBThreads * 16;
+  const long long need = V <= per16 ? 1 : V <= 2 * per16 ? 2 : V <= 4 * per16 ? 4 : 8;
+  if ((long long)B * R * need <= 2048 || (need == 1 && (long long)B * R <= 0x7fffffffLL)) {
+    if (V <= per16) return launch_expand_cluster<1, 16>(logits, B, R, V, K, D, level, state, ftok,
+                                                        fslot, status, s);
+    if (V <= 2 * per16) return launch_expand_cluster<2, 16>(logits, B, R, V, K, D, level, state,
+                                                            ftok, fslot, status, s);
+    if (V <= 4 * per16) return launch_expand_cluster<4, 16>(logits, B, R, V, K, D, level, state,
+                                                            ftok, fslot, status, s);
+    if (V <= 8 * per16) return launch_expand_cluster<8, 16>(logits, B, R, V, K, D, level, state,
+                                                            ftok, fslot, status, s);
+    if (V <= 16 * per16) return launch_expand_cluster<8, 32>(logits, B, R, V, K, D, level, state,
+                                                             ftok, fslot, status, s);
+  }
+  // larger rows: one CTA per row, two passes over it
   const size_t lists = (size_t)K * kBThreads * (sizeof(float) + sizeof(int));
   if (lists + sizeof(ExpandSmem) > 48 * 1024) {
     const cudaError_t e =
-        cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lists);
+        cudaFuncSetAttribute(expand_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lists);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -509,7 +745,7 @@ cudaError_t launch_tree_expand(const float* logits, int B, int R, int V, int K, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, expand_kernel, logits, R, V, K, level,
+  return cudaLaunchKernelEx(&cfg, expand_rows_kernel, logits, R, V, K, level,
                             static_cast<uint8_t*>(state), tree_build_stride(K, D), ftok, fslot,
                             status);
 }

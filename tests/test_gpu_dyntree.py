@@ -197,3 +197,20 @@ def test_built_tree_drives_greedy_verification(dev):
     assert np.array_equal(res["accepted_tokens"].cpu().numpy(), ref["accepted_tokens"])
     assert np.array_equal(res["bonus"].cpu().numpy(), ref["bonus"])
     assert ref["accept_len"].max() >= 1
+
+
+def test_slow_exact_path_and_large_vocab(dev):
+    """A tie group of 2560 entries held by five warps puts more than 2048 keys at or above the
+    warp-best threshold (the exact per-thread path takes over); V = 150000 takes the one-CTA-per-
+    row kernel."""
+    case = W.make_tree_build_case(2, 10, 3, 32000, seed=12)
+    y = np.arange(32000)
+    case.draft_rows[:, :, (y < 8192) & (y % 512 < 160)] = np.float32(100.0)  # warps 0-4, rank 0
+    got = _compare(case, dev, 30)
+    assert list(np.sort(got["tree_tokens"][0, 1:11])) == list(range(10))  # lowest ids of the ties
+    _compare(W.make_tree_build_case(2, 4, 3, 150000, seed=13), dev, 20)
+
+
+def test_many_rows_take_one_cta_per_row(dev):
+    """80 sequences x 8 rows x 4-CTA clusters would exceed 2048 CTAs: one CTA per row instead."""
+    _compare(W.make_tree_build_case(80, 8, 3, 20000, seed=14), dev, 40, max_near=12)
