@@ -15,6 +15,9 @@ published definitions:
   of the best frontier nodes by their top draft tokens, then the best candidates by cumulative
   draft log-probability.  EAGLE-3 explainer, 背景と動機 / EAGLE-2との統合 (EAGLE-2's dynamic
   tree).
+* ``oracle.lmhead`` -- the LM head reduced to what verification reads: per row the max, the sum of
+  exp((l - max) / T), the argmax and the logits of tested tokens.  EAGLE explainer (the target
+  forward over the tree); survey explainer, Formal Definition (q_j and q_j(x~)).
 * ``oracle.filtering`` -- top-k / top-p filtered target distributions (the filtered logits feed
   ``oracle.verify`` unchanged).  Survey explainer, verification taxonomy (speculative sampling
   with top-k / top-p).
@@ -29,4 +32,4 @@ It shares no code with the CUDA path and imports nothing from it.
 Parity pins: every function here is pinned by ``tests/test_oracle_*.py`` against library routines,
 closed forms, exact rational enumeration and brute force (none re-types the oracle's formulas).
 """
-from . import attention, dyntree, filtering, paged, verify  # noqa: F401
+from . import attention, dyntree, filtering, lmhead, paged, verify  # noqa: F401
