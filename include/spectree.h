@@ -266,6 +266,32 @@ int spec_tree_finalize(const void* workspace, size_t workspace_bytes, const int3
                        int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------------------------------
+ * LM head fused with the statistics verification reads
+ * ------------------------------------------------------------------------------------------------
+ * EAGLE explainer (the target forward over the tree gives each node's next-token logits); survey
+ * explainer, Formal Definition, 検証フェーズ (q_j = softmax(l_j / T); a draft token x~ is tested
+ * against q_j(x~)).  Verification needs per row only m = max_y l_y, S = sum_y exp((l_y - m) / T),
+ * the argmax and the logits of the tokens it tests: q_j(x~) = exp((l_x~ - m) / T) / S.  This call
+ * computes logits = hidden @ weight^T on the tensor cores and reduces them on chip; the fp32 logit
+ * matrix is never written.
+ *   hidden      bf16 [M, H] (row-major; H a multiple of 8), 16-byte aligned
+ *   weight      bf16 [V, H] (the LM head, one row per vocabulary entry), 16-byte aligned
+ *   gather_idx  int32 [M, G] or NULL (G = 0): token ids whose logits to return (-1: none)
+ *   temperature > 0 (for the sum only; max and argmax do not depend on it)
+ *   out_max     fp32 [M] or NULL, out_sumexp fp32 [M] or NULL, out_argmax int32 [M] or NULL
+ *               (lowest index among equal maxima), out_gather fp32 [M, G] (entries whose id is -1
+ *               or outside [0, V) are left as they are)
+ *   workspace   spec_lm_head_stats_workspace(M, V) bytes, 16-byte aligned
+ *   status      int32 [1] or NULL: SPEC_ST_TIMEOUT if a bounded wait gave up (OR-ed in)
+ * Precision: bf16 products accumulated in fp32 over H.  NaN / Inf inputs give unspecified results.
+ */
+size_t spec_lm_head_stats_workspace(int M, int V);
+int spec_lm_head_stats(const void* hidden, const void* weight, const int32_t* gather_idx, int M,
+                       int H, int V, int G, float temperature, float* out_max, float* out_sumexp,
+                       int32_t* out_argmax, float* out_gather, void* workspace,
+                       size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------------------------------
  * Tree attention over a paged KV cache
  * ------------------------------------------------------------------------------------------------
  * Survey explainer, "vLLMでの実装状況" section: serving stacks run speculative decoding on

@@ -12,7 +12,8 @@ Beside them: ``spec_tree_attention_paged`` (the same attention over a paged KV c
 ``spec_kv_compact`` / ``spec_kv_compact_paged`` (after verification, the accepted path's keys and
 values move next to the root), ``spec_tree_verify_filtered`` (verification against the top-k /
 top-p filtered target distribution), and ``spec_tree_expand`` / ``spec_tree_finalize`` (dynamic
-draft-tree construction, one level per drafter step).
+draft-tree construction, one level per drafter step), and ``spec_lm_head_stats`` (the LM head
+fused with the per-row statistics verification reads).
 
 The Python functions of the same names only marshal torch tensors into pointers and the current
 CUDA stream.  There is no CPU fallback: a missing library raises.
@@ -20,6 +21,8 @@ CUDA stream.  There is no CPU fallback: a missing library raises.
 from ._binding import (  # noqa: F401
     SpecError,
     spec_kv_compact,
+    spec_lm_head_stats,
+    spec_lm_head_stats_workspace,
     spec_kv_compact_paged,
     spec_tree_attention,
     spec_tree_attention_paged,

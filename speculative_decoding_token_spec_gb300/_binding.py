@@ -51,6 +51,9 @@ _SIGNATURES = {
     "spec_tree_build_workspace": (_c_size, [_c_int] * 3),
     "spec_tree_expand": (_c_int, [_vp] + [_c_int] * 5 + [_vp, _c_size] + [_vp] * 4),
     "spec_tree_finalize": (_c_int, [_vp, _c_size, _vp] + [_c_int] * 4 + [_vp] * 6),
+    "spec_lm_head_stats_workspace": (_c_size, [_c_int] * 2),
+    "spec_lm_head_stats": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_c_float] + [_vp] * 5
+                           + [_c_size, _vp, _vp]),
     "spec_status_string": (ctypes.c_char_p, [_c_int]),
 }
 
@@ -406,4 +409,44 @@ def spec_tree_finalize(workspace, root_tokens, K, D, N, outputs=None, status=Non
                                   _ptr(o["node_value"]), _ptr(o["status"]), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_tree_finalize", rc)
+    return o
+
+
+# ----------------------------------------------------------------------------------------------
+# LM head fused with the verification statistics
+# ----------------------------------------------------------------------------------------------
+def spec_lm_head_stats_workspace(M, V) -> int:
+    return int(lib().spec_lm_head_stats_workspace(M, V))
+
+
+def spec_lm_head_stats(hidden, weight, temperature=1.0, gather_idx=None, outputs=None,
+                       workspace=None, status=None, stream=None):
+    """Per row of hidden [M, H] @ weight [V, H]^T (bf16): max, sum of exp((l - max) / T), argmax
+    and the logits at gather_idx [M, G]; returns a dict of device tensors."""
+    torch = _torch()
+    M, H = hidden.shape
+    V = weight.shape[0]
+    dev = hidden.device
+    _check(hidden, "hidden", torch.bfloat16, (M, H), dev)
+    _check(weight, "weight", torch.bfloat16, (V, H), dev)
+    G = 0 if gather_idx is None else gather_idx.shape[1]
+    if gather_idx is not None:
+        _check(gather_idx, "gather_idx", torch.int32, (M, G), dev)
+    o = dict(outputs or {})
+    o.setdefault("max", torch.empty((M,), dtype=torch.float32, device=dev))
+    o.setdefault("sumexp", torch.empty((M,), dtype=torch.float32, device=dev))
+    o.setdefault("argmax", torch.empty((M,), dtype=torch.int32, device=dev))
+    if G:
+        o.setdefault("gather", torch.full((M, G), float("nan"), dtype=torch.float32, device=dev))
+    o["status"] = status if status is not None else torch.zeros((1,), dtype=torch.int32,
+                                                                 device=dev)
+    if workspace is None:
+        workspace = torch.empty((max(spec_lm_head_stats_workspace(M, V), 16),), dtype=torch.uint8,
+                                device=dev)
+    rc = lib().spec_lm_head_stats(_ptr(hidden), _ptr(weight), _ptr(gather_idx), M, H, V, G,
+                                  float(temperature), _ptr(o["max"]), _ptr(o["sumexp"]),
+                                  _ptr(o["argmax"]), _ptr(o.get("gather")), _ptr(workspace),
+                                  workspace.numel(), _ptr(o["status"]), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_lm_head_stats", rc)
     return o

@@ -44,6 +44,18 @@ size_t verify_workspace_bytes(int B, int N, int V);
 bool verify_supported(int V);  // the row slices of a cluster fit in shared memory
 cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s);
 // rows of V target logits -> the same rows with -inf outside the top-k / top-p set (T > 0)
+// fused LM head (lm_head.cu)
+struct LmPartial {
+  float m, s;  // a vocabulary tile's max and sum of exp((l - m) / T)
+  int arg;     // its argmax (lowest index)
+  int pad;
+};
+size_t lm_head_workspace_bytes(int M, int V);
+cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t* gather_idx, int M,
+                           int H, int V, int G, float T, float* out_max, float* out_sumexp,
+                           int32_t* out_argmax, float* out_gather, void* workspace,
+                           int32_t* flag, cudaStream_t s);
+
 // dynamic tree construction (tree_build.cu)
 constexpr int kMaxTreeK = 16;       // candidates per expanded node, frontier size
 constexpr int kMaxTreePool = 2048;  // drafted nodes per sequence: 1 + K + (D - 1) K^2

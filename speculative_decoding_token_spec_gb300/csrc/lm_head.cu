@@ -1,0 +1,256 @@
+// The target model's LM head fused with the statistics verification reads (sm_103a).
+//
+// Method: EAGLE explainer (the target forward over the draft tree yields next-token logits per
+// node); survey explainer, Formal Definition, 検証フェーズ (q_j = softmax of node j's target logits;
+// each draft token x~ is tested against q_j(x~)).  Verification needs per row only the max m,
+// S = sum_y exp((l_y - m) / T), the argmax (T = 0) and the logits of the tokens it tests, so
+// q_j(x~) = exp((l_x~ - m) / T) / S.  Here logits = hidden @ W^T are computed on the tensor cores and
+// reduced in the epilogue: the fp32 logit matrix is never written or read.
+//
+// lm_head_kernel: one CTA per (128-row tile, 256-entry vocabulary tile).  Warp 0 streams the
+// 64-wide hidden slices of hidden [M, H] and W [V, H] (bf16, 128-byte swizzle) through a 4-stage
+// TMA ring; warp 1 issues tcgen05.mma (M = 128, N = 256, K = 16; fp32 accumulator in 256 TMEM
+// columns) over the whole hidden dimension; warps 4-7 read their row's 256 accumulators from TMEM
+// and write the tile's max, sum of exp and argmax.  Tested tokens are read from a copy of the tile
+// in the (then idle) stage memory.  lm_head_combine_kernel merges the tiles of each row.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace spectree {
+
+bool encode_bf16_2d(CUtensorMap* m, const void* ptr, long long inner, long long rows,
+                    int box_inner, int box_rows);
+
+namespace {
+
+constexpr int kLM = 128;                        // rows per tile (the MMA's M)
+constexpr int kLN = 256;                        // vocabulary entries per tile (the MMA's N)
+constexpr int kLK = 64;                         // hidden elements per stage: one 128-byte row
+constexpr int kStages = 4;
+constexpr int kABytes = kLM * kLK * 2;          // 16 KB
+constexpr int kBBytes = kLN * kLK * 2;          // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+constexpr int kTileStride = kLN + 1;            // fp32 tile copy: odd row stride, no conflicts
+constexpr int kLThreads = 256;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+static_assert(kLM * kTileStride * 4 <= kStages * kStageBytes, "tile copy fits the stages");
+
+__global__ void __launch_bounds__(kLThreads, 1)
+    lm_head_kernel(const __grid_constant__ CUtensorMap tmap_h,
+                   const __grid_constant__ CUtensorMap tmap_w, int M, int H, int V, int G,
+                   const int32_t* __restrict__ gather_idx, float k2, LmPartial* __restrict__ part,
+                   float* __restrict__ out_gather, int32_t* flag) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bars[2 * kStages + 1];  // full[s], empty[s], accumulator
+  __shared__ uint32_t tmem_s;
+  __shared__ int issued_s, timeout_s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m0 = blockIdx.x * kLM, v0 = blockIdx.y * kLN;
+  const int nk = (H + kLK - 1) / kLK;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  if (tid == 0) {
+    prefetch_tmap(&tmap_h);
+    prefetch_tmap(&tmap_w);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(s), 1);
+      mbar_init(bar(kStages + s), 1);
+    }
+    mbar_init(bar(2 * kStages), 1);
+    mbar_fence_init();
+    issued_s = 0;
+    timeout_s = 0;
+  }
+  griddep_wait();  // the hidden states may come from the preceding kernel
+  griddep_launch_dependents();
+  if (warp == 1) tmem_alloc(smem_u32(&tmem_s), kLN);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_s;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer
+      int kc = 0;
+      for (; kc < nk; ++kc) {
+        const int s = kc % kStages;
+        if (kc >= kStages && !mbar_wait(bar(kStages + s), ((kc / kStages) - 1) & 1)) {
+          timeout_s = 1;
+          break;
+        }
+        const uint32_t a = smem_u32(smem + s * kStageBytes);
+        mbar_arrive_expect_tx(bar(s), kStageBytes);
+        tma_load_2d(a, &tmap_h, bar(s), kc * kLK, m0);
+        tma_load_2d(a + kABytes, &tmap_w, bar(s), kc * kLK, v0);
+      }
+      issued_s = kc;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issuer
+      constexpr uint32_t IDESC = idesc_bf16_f32(kLM, kLN, false);
+      int kc = 0;
+      for (; kc < nk; ++kc) {
+        const int s = kc % kStages;
+        if (!mbar_wait(bar(s), (kc / kStages) & 1)) {
+          timeout_s = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a = smem_u32(smem + s * kStageBytes), b = a + kABytes;
+#pragma unroll
+        for (int ks = 0; ks < kLK / 16; ++ks)
+          tc_mma_bf16(tmem, smem_desc_sw128(a + ks * 32, 16, 1024),
+                      smem_desc_sw128(b + ks * 32, 16, 1024), IDESC, (kc > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(bar(kStages + s));  // the stage is free once these MMAs completed
+      }
+      tc_commit(bar(2 * kStages));  // the accumulator is final (or abandoned)
+    }
+  } else if (warp >= 4) {
+    // ---- epilogue: thread r holds row m0 + r (TMEM lane r)
+    const int r = 32 * (warp & 3) + lane, row = m0 + r;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const bool ok = mbar_wait(bar(2 * kStages), 0);
+    if (!ok) timeout_s = 1;
+    tc_fence_after();
+    float mx = -INFINITY;
+    int am = 0x7fffffff;
+    float sum = 0.f;
+    if (ok) {
+#pragma unroll 1
+      for (int c = 0; c < kLN / 32; ++c) {  // max and argmax (ascending columns: lowest index)
+        float v[32];
+        tmem_ld32(lane_base + (uint32_t)(32 * c), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int col = v0 + 32 * c + q;
+          if (col < V && v[q] > mx) {
+            mx = v[q];
+            am = col;
+          }
+        }
+      }
+      const float mk = __fmul_rn(mx, k2);
+      float* tile = reinterpret_cast<float*>(smem);  // the stages are idle now
+#pragma unroll 1
+      for (int c = 0; c < kLN / 32; ++c) {  // sum of exp((l - max) / T); copy for the gathers
+        float v[32];
+        tmem_ld32(lane_base + (uint32_t)(32 * c), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int col = v0 + 32 * c + q;
+          if (col < V) sum += exp2f(fmaf(v[q], k2, -mk));
+          if (G > 0) tile[r * kTileStride + 32 * c + q] = v[q];
+        }
+      }
+      if (row < M) {
+        LmPartial p;
+        p.m = mx;
+        p.s = sum;
+        p.arg = am;
+        p.pad = 0;
+        part[(size_t)blockIdx.y * M + row] = p;
+        if (G > 0 && out_gather) {
+          for (int g = 0; g < G; ++g) {
+            const int tok = __ldg(gather_idx + (size_t)row * G + g);
+            if (tok >= v0 && tok < v0 + kLN && tok < V)
+              out_gather[(size_t)row * G + g] = tile[r * kTileStride + (tok - v0)];
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (timeout_s && tid == 0) {
+    // wait (bounded) for the copies this CTA still has in flight before its memory goes away
+    const int issued = issued_s;
+    for (int s = 0; s < kStages; ++s) {
+      int last = -1;
+      for (int t = s; t < issued; t += kStages) last = t;
+      if (last >= 0) mbar_wait(bar(s), (last / kStages) & 1);
+    }
+    if (flag) atomicOr(flag, SPEC_ST_TIMEOUT);
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kLN);
+  }
+}
+
+// Per row: merge the vocabulary tiles' (max, sum of exp, argmax).
+__global__ void __launch_bounds__(256) lm_head_combine_kernel(const LmPartial* __restrict__ part,
+                                                              int M, int ntiles, float k2,
+                                                              float* out_max, float* out_sumexp,
+                                                              int32_t* out_argmax) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= M) return;
+  float m = -INFINITY;
+  int am = 0x7fffffff;
+  for (int t = 0; t < ntiles; ++t) {  // ascending tiles: the first tile with the max has the
+    const LmPartial p = part[(size_t)t * M + row];  // lowest index
+    if (p.m > m) {
+      m = p.m;
+      am = p.arg;
+    }
+  }
+  float s = 0.f;
+  const float mk = __fmul_rn(m, k2);
+  for (int t = 0; t < ntiles; ++t) {
+    const LmPartial p = part[(size_t)t * M + row];
+    if (p.m > -INFINITY) s += p.s * exp2f(fmaf(p.m, k2, -mk));
+  }
+  if (out_max) out_max[row] = m;
+  if (out_sumexp) out_sumexp[row] = s;
+  if (out_argmax) out_argmax[row] = am;
+}
+
+}  // namespace
+
+size_t lm_head_workspace_bytes(int M, int V) {
+  return (size_t)((V + kLN - 1) / kLN) * (size_t)M * sizeof(LmPartial);
+}
+
+cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t* gather_idx, int M,
+                           int H, int V, int G, float T, float* out_max, float* out_sumexp,
+                           int32_t* out_argmax, float* out_gather, void* workspace,
+                           int32_t* flag, cudaStream_t s) {
+  CUtensorMap mh, mw;
+  if (!encode_bf16_2d(&mh, hidden, H, M, kLK, kLM) || !encode_bf16_2d(&mw, weight, H, V, kLK, kLN))
+    return cudaErrorInvalidValue;
+  const float k2 = (float)(1.4426950408889634 / (double)T);
+  const int ntiles = (V + kLN - 1) / kLN;
+  cudaError_t e = cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((M + kLM - 1) / kLM), (unsigned)ntiles);
+  cfg.blockDim = dim3(kLThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  LmPartial* part = static_cast<LmPartial*>(workspace);
+  e = cudaLaunchKernelEx(&cfg, lm_head_kernel, mh, mw, M, H, V, G, gather_idx, k2, part, out_gather,
+                         flag);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t c2 = {};
+  c2.gridDim = dim3((unsigned)((M + 255) / 256));
+  c2.blockDim = dim3(256);
+  c2.stream = s;
+  c2.attrs = attr;
+  c2.numAttrs = 1;
+  return cudaLaunchKernelEx(&c2, lm_head_combine_kernel, (const LmPartial*)part, M, ntiles, k2,
+                            out_max, out_sumexp, out_argmax);
+}
+
+}  // namespace spectree

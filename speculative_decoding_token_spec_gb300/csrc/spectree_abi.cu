@@ -312,6 +312,32 @@ int spec_tree_finalize(const void* workspace, size_t workspace_bytes, const int3
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+// ---- fused LM head
+size_t spec_lm_head_stats_workspace(int M, int V) {
+  if (M < 1 || V < 1) return 0;
+  return lm_head_workspace_bytes(M, V);
+}
+
+int spec_lm_head_stats(const void* hidden, const void* weight, const int32_t* gather_idx, int M,
+                       int H, int V, int G, float temperature, float* out_max, float* out_sumexp,
+                       int32_t* out_argmax, float* out_gather, void* workspace,
+                       size_t workspace_bytes, int32_t* status, void* stream) {
+  if (!hidden || !weight || M < 1 || H < 8 || (H & 7) || V < 1 || G < 0)
+    return SPEC_ERR_INVALID_ARG;
+  if (!std::isfinite(temperature) || !(temperature > 0.f)) return SPEC_ERR_INVALID_ARG;
+  if (G > 0 && (!gather_idx || !out_gather)) return SPEC_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(weight)) return SPEC_ERR_INVALID_ARG;
+  if ((long long)(V + 255) / 256 > 65535 || (long long)M * V > (1ll << 40))
+    return SPEC_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < lm_head_workspace_bytes(M, V) || !aligned16(workspace))
+    return SPEC_ERR_WORKSPACE;
+  const cudaError_t e = launch_lm_head(hidden, weight, gather_idx, M, H, V, G, temperature, out_max,
+                                       out_sumexp, out_argmax, out_gather, workspace, status,
+                                       static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return SPEC_ERR_INVALID_ARG;  // tensor maps refused
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 const char* spec_status_string(int code) {
   switch (code) {
     case SPEC_OK: return "ok";

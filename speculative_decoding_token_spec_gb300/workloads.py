@@ -358,3 +358,23 @@ def make_tree_build_case(B: int, K: int, D: int, V: int, seed: int = 0,
         rows[b] = rng.standard_normal((rows.shape[1], V), dtype=np.float32) * np.float32(sigma)
         roots[b] = int(rng.integers(V))
     return TreeBuildCase(rows, roots, K, D)
+
+
+@dataclasses.dataclass
+class LmHeadCase:
+    hidden: np.ndarray      # bf16 bits [M, H]
+    weight: np.ndarray      # bf16 bits [V, H]
+    gather_idx: np.ndarray  # int32 [M, G] (-1: none)
+
+
+def make_lm_head_case(M: int, H: int, V: int, G: int = 0, seed: int = 0,
+                      sigma: float = 3.0) -> LmHeadCase:
+    """hidden ~ N(0, 1), weight ~ N(0, sigma^2 / H) (logits ~ N(0, sigma^2)), both rounded to
+    bf16; gather ids uniform in [0, V) with one in eight set to -1."""
+    rng = _rng(seed, 9, 0, 13)
+    hidden = bf16_bits(rng.standard_normal((M, H), dtype=np.float32))
+    weight = bf16_bits(rng.standard_normal((V, H), dtype=np.float32)
+                       * np.float32(sigma / np.sqrt(H)))
+    gi = rng.integers(0, V, size=(M, G)).astype(np.int32)
+    gi[rng.random((M, G)) < 0.125] = -1
+    return LmHeadCase(hidden, weight, gi)

@@ -35,7 +35,8 @@ def test_header_declares_the_entry_points():
               "spec_tree_verify_workspace", "spec_status_string", "spec_tree_attention_paged",
               "spec_kv_compact", "spec_kv_compact_paged", "spec_tree_verify_filtered",
               "spec_tree_verify_filtered_workspace", "spec_tree_build_workspace",
-              "spec_tree_expand", "spec_tree_finalize"):
+              "spec_tree_expand", "spec_tree_finalize", "spec_lm_head_stats",
+              "spec_lm_head_stats_workspace"):
         assert n in names
 
 
@@ -194,3 +195,21 @@ def test_tree_construction_arguments(lib):
     assert fin(N=1 + 4 + 2 * 16 + 1) == -1    # more nodes than the construction can draft
     assert fin(out=null) == -1
     assert fin(nbytes=16) == -3
+
+
+def test_lm_head_arguments(lib):
+    """Workspace query and argument errors of the fused LM head, before any CUDA call."""
+    assert lib.spec_lm_head_stats_workspace(60, 32000) == 125 * 60 * 16
+    assert lib.spec_lm_head_stats_workspace(0, 10) == 0
+    fake = ctypes.c_void_p(256)
+    null = None
+    ws = lib.spec_lm_head_stats_workspace(4, 1000)
+
+    def call(M=4, H=64, V=1000, G=0, T=1.0, gi=null, og=null, nbytes=ws, h=fake):
+        return lib.spec_lm_head_stats(h, fake, gi, M, H, V, G, T, fake, fake, fake, og, fake,
+                                      nbytes, null, null)
+    assert call(h=null) == -1
+    assert call(H=60) == -1                 # H not a multiple of 8
+    assert call(T=0.0) == -1 and call(T=float("nan")) == -1
+    assert call(G=3) == -1                  # gathers without ids / outputs
+    assert call(nbytes=ws - 16) == -3

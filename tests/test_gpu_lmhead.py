@@ -1,0 +1,98 @@
+"""GPU parity of the fused LM head (spec_lm_head_stats) against the fp64 oracle, through the C ABI.
+
+Max, log of the sum of exp and the gathered logits within 1e-3 (bf16 products, fp32 accumulation
+over H); the argmax exact except in rows whose two largest logits lie within 1e-3 (counted).
+Shapes: one ragged row tile (M = 60) and several (M = 300), H a multiple of 64 or not, V a whole
+number of 256-entry tiles or not, V = 128256; temperatures 1 and 0.7.  The statistics then drive
+greedy verification of a tree: the argmax gives the same walk as the full logits.
+"""
+import numpy as np
+import pytest
+
+from oracle import lmhead as OL
+from oracle import verify as OV
+from speculative_decoding_token_spec_gb300 import workloads as W
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def dev(cuda_lib):
+    import torch
+    return torch.device("cuda:0")
+
+
+def _run(case, dev, T):
+    import torch
+    import speculative_decoding_token_spec_gb300 as st
+    h = P.dev_tensor(case.hidden, dev).view(torch.bfloat16)
+    w = P.dev_tensor(case.weight, dev).view(torch.bfloat16)
+    gi = P.dev_tensor(case.gather_idx, dev) if case.gather_idx.shape[1] else None
+    out = st.spec_lm_head_stats(h, w, T, gather_idx=gi)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def _check(case, dev, T):
+    got = _run(case, dev, T)
+    ref = OL.lm_head_stats(W.bf16_to_f64(case.hidden), W.bf16_to_f64(case.weight), T,
+                           case.gather_idx if case.gather_idx.shape[1] else None)
+    assert got["status"][0] == 0
+    assert np.abs(got["max"] - ref["max"]).max() <= TOL
+    assert np.abs(np.log(got["sumexp"]) - np.log(ref["sumexp"])).max() <= TOL
+    near = ref["top_gap"] < TOL
+    assert np.array_equal(got["argmax"][~near], ref["argmax"][~near])
+    assert near.sum() <= max(1, len(near) // 50), near.sum()
+    if "gather" in ref:
+        ok = ~np.isnan(ref["gather"])
+        assert np.array_equal(ok, ~np.isnan(got["gather"]))
+        assert np.abs(got["gather"][ok] - ref["gather"][ok]).max() <= TOL
+    M, H = case.hidden.shape
+    print(f"M={M} H={H} V={case.weight.shape[0]} T={T}: max err "
+          f"{np.abs(got['max'] - ref['max']).max():.2e}, near-tie rows {int(near.sum())}")
+
+
+@pytest.mark.parametrize("M,H,V,G,T", [
+    (60, 4096, 32000, 10, 1.0),     # one 60-node tree, Vicuna-7B-sized head
+    (60, 512, 1000, 4, 0.7),        # a ragged vocabulary tile
+    (300, 520, 3000, 6, 1.0),       # three row tiles, a partial hidden slice
+    (20, 4096, 128256, 8, 0.7),     # 128K vocabulary
+])
+def test_matches_oracle(dev, M, H, V, G, T):
+    _check(W.make_lm_head_case(M, H, V, G, seed=M + V), dev, T)
+
+
+def test_statistics_drive_greedy_verification(dev):
+    """Fused argmax -> greedy walk equals the walk on the full fp64 logits (outside near ties)."""
+    B, N, H, V = 3, 24, 256, 2000
+    case = W.make_lm_head_case(B * N, H, V, 0, seed=5, sigma=4.0)
+    got = _run(case, dev, 1.0)
+    lg = OL.logits(W.bf16_to_f64(case.hidden), W.bf16_to_f64(case.weight)).reshape(B, N, V)
+    rng = np.random.default_rng(5)
+    par = np.stack([W.make_tree(rng, N, 4, 8) for _ in range(B)]).astype(np.int32)
+    am = got["argmax"].reshape(B, N)
+    # draft tokens: the target's argmax at the parent for most nodes, so the walk goes deep
+    tok = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for i in range(1, N):
+            tok[b, i] = am[b, par[b, i]] if rng.random() < 0.6 else int(rng.integers(V))
+    ref = OV.tree_verify(lg, None, tok, par, np.zeros((B, N), np.float32), 0.0)
+    near = OL.row_stats(lg.reshape(B * N, V), 1.0)["top_gap"].reshape(B, N) < TOL
+    for b in range(B):
+        if near[b].any():
+            continue
+        # the greedy walk from the fused argmax
+        path, j = [], 0
+        while True:
+            kids = [i for i in range(1, N) if par[b, i] == j]
+            nxt = next((i for i in kids if tok[b, i] == am[b, j]), None)
+            if nxt is None:
+                break
+            path.append(nxt)
+            j = nxt
+        assert len(path) == ref["accept_len"][b]
+        assert [int(tok[b, i]) for i in path] == list(ref["accepted_tokens"][b, :len(path)])
+        assert am[b, j] == ref["bonus"][b]
