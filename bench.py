@@ -434,7 +434,7 @@ def run_ours(args):
     if rank != 0:
         return
     nxt = None if args.no_next else measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs,
-                                                      attn_ms, timed, dev, L2)
+                                                      attn_ms, timed, dev, L2, tc_tflops)
     # ---- CPU oracle baseline (bounded sample)
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
@@ -483,9 +483,10 @@ def run_ours(args):
     print(json.dumps(line))
 
 
-def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev, L2):
-    """Paged-cache attention (16-slot pages), post-accept KV compaction, filtered verification and
-    dynamic tree construction on this workload.
+def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev, L2,
+                      tc_tflops):
+    """Paged-cache attention (16-slot pages), post-accept KV compaction, filtered verification,
+    dynamic tree construction and the fused LM head on this workload.
 
     Paged attention: the same queries, tree and prefix over pages in a random physical order,
     rotated over device copies larger than 2 x L2, timed per call from CUDA graphs; its
@@ -603,9 +604,35 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
             build(c)
     torch.cuda.synchronize()
     assert all(int(c["st"].sum()) == 0 for c in tcs)
+
+    # fused LM head: hidden [B N, H] (H = Hq D of this workload) times the head [V, H], reduced to
+    # the verification statistics; the head alone is larger than 2 x L2, so every call reads HBM
+    lm_h = cfg.Hq * cfg.D
+    lm_m = B * N
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed + 17)
+    lm_w = (torch.randn((V, lm_h), generator=gen, device=dev)
+            * (3.0 / math.sqrt(lm_h))).to(torch.bfloat16)
+    lm_x = torch.randn((lm_m, lm_h), generator=gen, device=dev).to(torch.bfloat16)
+    lm_out = {"max": torch.empty((lm_m,), dtype=torch.float32, device=dev),
+              "sumexp": torch.empty((lm_m,), dtype=torch.float32, device=dev),
+              "argmax": torch.empty((lm_m,), dtype=torch.int32, device=dev)}
+    lm_ws = torch.empty((st.spec_lm_head_stats_workspace(lm_m, V),), dtype=torch.uint8,
+                        device=dev)
+    lm_st = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    def lmhead(_c=None):
+        st.spec_lm_head_stats(lm_x, lm_w, T, outputs=lm_out, workspace=lm_ws, status=lm_st)
+
+    for _ in range(3):
+        lmhead()
+    torch.cuda.synchronize()
+    assert int(lm_st.item()) == 0
     g_p, g_c = capture(paged, pcs), capture(compact, bufs)
     g_f, g_v = capture(filtered, bufs), capture(plain, bufs)
     g_tb, g_tx = capture(build, tcs), capture(expand_all, tcs)
+    reps_lm = 20
+    g_lm = capture(lmhead, [None] * reps_lm)
     torch.cuda.current_stream().wait_stream(s)
     for _ in range(2):
         g_p.replay()
@@ -614,6 +641,7 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
         g_v.replay()
         g_tb.replay()
         g_tx.replay()
+        g_lm.replay()
     torch.cuda.synchronize()
     reps = max(1, 600 // ncp)
     p_ms = timed(lambda: [g_p.replay() for _ in range(reps)]) / (reps * ncp)
@@ -625,6 +653,9 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
     tb_ms = timed(lambda: [g_tb.replay() for _ in range(reps_t)]) / (reps_t * ncp_t)
     tx_ms = timed(lambda: [g_tx.replay() for _ in range(reps_t)]) / (reps_t * ncp_t)
     tree_bytes = tcase.draft_rows.nbytes  # every draft row read once
+    lm_ms = timed(lambda: [g_lm.replay() for _ in range(10)]) / (10 * reps_lm)
+    lm_bytes = lm_w.numel() * 2 + lm_x.numel() * 2 + lm_m * 12  # head, hidden, statistics
+    lm_flops = 2.0 * lm_m * lm_h * V
     fil_gbs = filt_bytes / ((f_ms - v_ms) * 1e-3) / 1e9 if f_ms > v_ms else None
     reps_c = max(1, 600 // len(bufs))
     c_ms = timed(lambda: [g_c.replay() for _ in range(reps_c)]) / (reps_c * len(bufs))
@@ -657,6 +688,15 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
                        "kernel": "expand_kernel (one CTA per draft row, six launches), "
                                  "finalize_kernel",
                        "note": "expand rate = draft-row bytes / time of the six expand launches"},
+        "lm_head": {"rows": lm_m, "hidden": lm_h, "vocab": V, "us_per_call": lm_ms * 1e3,
+                    "algorithmic_bytes": lm_bytes,
+                    "achieved_gbs": lm_bytes / (lm_ms * 1e-3) / 1e9,
+                    "frac": lm_bytes / (lm_ms * 1e-3) / 1e9 / hbm_gbs,
+                    "tflops": lm_flops / (lm_ms * 1e-3) / 1e12,
+                    "tensor_frac": lm_flops / (lm_ms * 1e-3) / 1e12 / tc_tflops,
+                    "kernel": "lm_head_kernel (tcgen05, 128 x 256 tiles) + lm_head_combine_kernel",
+                    "note": "weights generated on the device (seeded), bf16; the logit matrix is "
+                            "never written"},
         "peak_gbs": hbm_gbs,
     }
 

@@ -7,10 +7,10 @@
 // q_j(x~) = exp((l_x~ - m) / T) / S.  Here logits = hidden @ W^T are computed on the tensor cores and
 // reduced in the epilogue: the fp32 logit matrix is never written or read.
 //
-// lm_head_kernel: one CTA per (128-row tile, 256-entry vocabulary tile).  Warp 0 streams the
+// lm_head_kernel: one CTA per (128-row tile, vocabulary tile of 128..256 entries).  Warp 0 streams the
 // 64-wide hidden slices of hidden [M, H] and W [V, H] (bf16, 128-byte swizzle) through a 4-stage
-// TMA ring; warp 1 issues tcgen05.mma (M = 128, N = 256, K = 16; fp32 accumulator in 256 TMEM
-// columns) over the whole hidden dimension; warps 4-7 read their row's 256 accumulators from TMEM
+// TMA ring; warp 1 issues tcgen05.mma (M = 128, N = the tile width, K = 16; fp32 accumulator in
+// TMEM) over the whole hidden dimension; warps 4-7 read their row's accumulators from TMEM
 // and write the tile's max, sum of exp and argmax.  Tested tokens are read from a copy of the tile
 // in the (then idle) stage memory.  lm_head_combine_kernel merges the tiles of each row.
 #include <cuda.h>
@@ -26,7 +26,7 @@ bool encode_bf16_2d(CUtensorMap* m, const void* ptr, long long inner, long long 
 namespace {
 
 constexpr int kLM = 128;                        // rows per tile (the MMA's M)
-constexpr int kLN = 256;                        // vocabulary entries per tile (the MMA's N)
+constexpr int kLN = 256;                        // vocabulary entries per tile at most (MMA N)
 constexpr int kLK = 64;                         // hidden elements per stage: one 128-byte row
 constexpr int kStages = 4;
 constexpr int kABytes = kLM * kLK * 2;          // 16 KB
@@ -39,7 +39,7 @@ static_assert(kLM * kTileStride * 4 <= kStages * kStageBytes, "tile copy fits th
 
 __global__ void __launch_bounds__(kLThreads, 1)
     lm_head_kernel(const __grid_constant__ CUtensorMap tmap_h,
-                   const __grid_constant__ CUtensorMap tmap_w, int M, int H, int V, int G,
+                   const __grid_constant__ CUtensorMap tmap_w, int M, int H, int V, int G, int tn,
                    const int32_t* __restrict__ gather_idx, float k2, LmPartial* __restrict__ part,
                    float* __restrict__ out_gather, int32_t* flag) {
   extern __shared__ uint8_t smem_raw[];
@@ -49,7 +49,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
   __shared__ uint32_t tmem_s;
   __shared__ int issued_s, timeout_s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = blockIdx.x * kLM, v0 = blockIdx.y * kLN;
+  const int m0 = blockIdx.x * kLM, v0 = blockIdx.y * tn;  // tn: this launch's tile width
+  const int vend = min(V, v0 + tn);
   const int nk = (H + kLK - 1) / kLK;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   if (tid == 0) {
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
           break;
         }
         const uint32_t a = smem_u32(smem + s * kStageBytes);
-        mbar_arrive_expect_tx(bar(s), kStageBytes);
+        mbar_arrive_expect_tx(bar(s), kABytes + tn * kLK * 2);
         tma_load_2d(a, &tmap_h, bar(s), kc * kLK, m0);
         tma_load_2d(a + kABytes, &tmap_w, bar(s), kc * kLK, v0);
       }
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {  // ---- MMA issuer
-      constexpr uint32_t IDESC = idesc_bf16_f32(kLM, kLN, false);
+      const uint32_t IDESC = idesc_bf16_f32(kLM, tn, false);
       int kc = 0;
       for (; kc < nk; ++kc) {
         const int s = kc % kStages;
@@ -119,15 +120,16 @@ __global__ void __launch_bounds__(kLThreads, 1)
     int am = 0x7fffffff;
     float sum = 0.f;
     if (ok) {
+      const int nch = (tn + 31) / 32;  // 32-column chunks (the last may pass the tile: skipped)
 #pragma unroll 1
-      for (int c = 0; c < kLN / 32; ++c) {  // max and argmax (ascending columns: lowest index)
+      for (int c = 0; c < nch; ++c) {  // max and argmax (ascending columns: lowest index)
         float v[32];
         tmem_ld32(lane_base + (uint32_t)(32 * c), v);
         tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           const int col = v0 + 32 * c + q;
-          if (col < V && v[q] > mx) {
+          if (col < vend && v[q] > mx) {
             mx = v[q];
             am = col;
           }
@@ -136,14 +138,14 @@ __global__ void __launch_bounds__(kLThreads, 1)
       const float mk = __fmul_rn(mx, k2);
       float* tile = reinterpret_cast<float*>(smem);  // the stages are idle now
 #pragma unroll 1
-      for (int c = 0; c < kLN / 32; ++c) {  // sum of exp((l - max) / T); copy for the gathers
+      for (int c = 0; c < nch; ++c) {  // sum of exp((l - max) / T); copy for the gathers
         float v[32];
         tmem_ld32(lane_base + (uint32_t)(32 * c), v);
         tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           const int col = v0 + 32 * c + q;
-          if (col < V) sum += exp2f(fmaf(v[q], k2, -mk));
+          if (col < vend) sum += exp2f(fmaf(v[q], k2, -mk));
           if (G > 0) tile[r * kTileStride + 32 * c + q] = v[q];
         }
       }
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
         if (G > 0 && out_gather) {
           for (int g = 0; g < G; ++g) {
             const int tok = __ldg(gather_idx + (size_t)row * G + g);
-            if (tok >= v0 && tok < v0 + kLN && tok < V)
+            if (tok >= v0 && tok < vend)
               out_gather[(size_t)row * G + g] = tile[r * kTileStride + (tok - v0)];
           }
         }
@@ -213,19 +215,30 @@ __global__ void __launch_bounds__(256) lm_head_combine_kernel(const LmPartial* _
 
 }  // namespace
 
-size_t lm_head_workspace_bytes(int M, int V) {
-  return (size_t)((V + kLN - 1) / kLN) * (size_t)M * sizeof(LmPartial);
+// Tile width: 256 vocabulary entries.  Narrower tiles that spread a single row tile over every SM
+// (224 wide at V = 32000: 143 CTAs instead of 125) measured no faster: a CTA streams at about the
+// same rate either way (each box reads 128-byte pieces of rows 2 H bytes apart).
+static int tile_width(int M, int V, int num_sms) {
+  (void)M;
+  (void)V;
+  (void)num_sms;
+  return kLN;
+}
+
+size_t lm_head_workspace_bytes(int M, int V) {  // one partial per (tile, row); tiles >= 128 wide
+  return (size_t)((V + 127) / 128) * (size_t)M * sizeof(LmPartial);
 }
 
 cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t* gather_idx, int M,
                            int H, int V, int G, float T, float* out_max, float* out_sumexp,
                            int32_t* out_argmax, float* out_gather, void* workspace,
-                           int32_t* flag, cudaStream_t s) {
+                           int32_t* flag, int num_sms, cudaStream_t s) {
+  const int tn = tile_width(M, V, num_sms);
   CUtensorMap mh, mw;
-  if (!encode_bf16_2d(&mh, hidden, H, M, kLK, kLM) || !encode_bf16_2d(&mw, weight, H, V, kLK, kLN))
+  if (!encode_bf16_2d(&mh, hidden, H, M, kLK, kLM) || !encode_bf16_2d(&mw, weight, H, V, kLK, tn))
     return cudaErrorInvalidValue;
   const float k2 = (float)(1.4426950408889634 / (double)T);
-  const int ntiles = (V + kLN - 1) / kLN;
+  const int ntiles = (V + tn - 1) / tn;
   cudaError_t e = cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -240,8 +253,8 @@ cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   LmPartial* part = static_cast<LmPartial*>(workspace);
-  e = cudaLaunchKernelEx(&cfg, lm_head_kernel, mh, mw, M, H, V, G, gather_idx, k2, part, out_gather,
-                         flag);
+  e = cudaLaunchKernelEx(&cfg, lm_head_kernel, mh, mw, M, H, V, G, tn, gather_idx, k2, part,
+                         out_gather, flag);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t c2 = {};
   c2.gridDim = dim3((unsigned)((M + 255) / 256));

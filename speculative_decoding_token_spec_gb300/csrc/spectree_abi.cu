@@ -327,12 +327,14 @@ int spec_lm_head_stats(const void* hidden, const void* weight, const int32_t* ga
   if (!std::isfinite(temperature) || !(temperature > 0.f)) return SPEC_ERR_INVALID_ARG;
   if (G > 0 && (!gather_idx || !out_gather)) return SPEC_ERR_INVALID_ARG;
   if (!aligned16(hidden) || !aligned16(weight)) return SPEC_ERR_INVALID_ARG;
-  if ((long long)(V + 255) / 256 > 65535 || (long long)M * V > (1ll << 40))
+  if ((long long)(V + 127) / 128 > 65535 || (long long)M * V > (1ll << 40))
     return SPEC_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < lm_head_workspace_bytes(M, V) || !aligned16(workspace))
     return SPEC_ERR_WORKSPACE;
+  const int sms = sm_count();
+  if (sms <= 0) return SPEC_ERR_CUDA;
   const cudaError_t e = launch_lm_head(hidden, weight, gather_idx, M, H, V, G, temperature, out_max,
-                                       out_sumexp, out_argmax, out_gather, workspace, status,
+                                       out_sumexp, out_argmax, out_gather, workspace, status, sms,
                                        static_cast<cudaStream_t>(stream));
   if (e == cudaErrorInvalidValue) return SPEC_ERR_INVALID_ARG;  // tensor maps refused
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

@@ -199,7 +199,7 @@ def test_tree_construction_arguments(lib):
 
 def test_lm_head_arguments(lib):
     """Workspace query and argument errors of the fused LM head, before any CUDA call."""
-    assert lib.spec_lm_head_stats_workspace(60, 32000) == 125 * 60 * 16
+    assert lib.spec_lm_head_stats_workspace(60, 32000) == 250 * 60 * 16
     assert lib.spec_lm_head_stats_workspace(0, 10) == 0
     fake = ctypes.c_void_p(256)
     null = None
