@@ -621,7 +621,13 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
                         device=dev)
     lm_st = torch.zeros((1,), dtype=torch.int32, device=dev)
 
+    lm_p = st.spec_lm_head_pack(lm_w)  # the head in tile-major order, made once
+
     def lmhead(_c=None):
+        st.spec_lm_head_stats(lm_x, lm_p, T, outputs=lm_out, workspace=lm_ws, status=lm_st,
+                              packed_vocab=V)
+
+    def lmhead_rowmajor(_c=None):
         st.spec_lm_head_stats(lm_x, lm_w, T, outputs=lm_out, workspace=lm_ws, status=lm_st)
 
     for _ in range(3):
@@ -633,6 +639,7 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
     g_tb, g_tx = capture(build, tcs), capture(expand_all, tcs)
     reps_lm = 20
     g_lm = capture(lmhead, [None] * reps_lm)
+    g_lr = capture(lmhead_rowmajor, [None] * reps_lm)
     torch.cuda.current_stream().wait_stream(s)
     for _ in range(2):
         g_p.replay()
@@ -642,6 +649,7 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
         g_tb.replay()
         g_tx.replay()
         g_lm.replay()
+        g_lr.replay()
     torch.cuda.synchronize()
     reps = max(1, 600 // ncp)
     p_ms = timed(lambda: [g_p.replay() for _ in range(reps)]) / (reps * ncp)
@@ -654,6 +662,7 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
     tx_ms = timed(lambda: [g_tx.replay() for _ in range(reps_t)]) / (reps_t * ncp_t)
     tree_bytes = tcase.draft_rows.nbytes  # every draft row read once
     lm_ms = timed(lambda: [g_lm.replay() for _ in range(10)]) / (10 * reps_lm)
+    lr_ms = timed(lambda: [g_lr.replay() for _ in range(10)]) / (10 * reps_lm)
     lm_bytes = lm_w.numel() * 2 + lm_x.numel() * 2 + lm_m * 12  # head, hidden, statistics
     lm_flops = 2.0 * lm_m * lm_h * V
     fil_gbs = filt_bytes / ((f_ms - v_ms) * 1e-3) / 1e9 if f_ms > v_ms else None
@@ -694,7 +703,9 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
                     "frac": lm_bytes / (lm_ms * 1e-3) / 1e9 / hbm_gbs,
                     "tflops": lm_flops / (lm_ms * 1e-3) / 1e12,
                     "tensor_frac": lm_flops / (lm_ms * 1e-3) / 1e12 / tc_tflops,
-                    "kernel": "lm_head_kernel (tcgen05, 128 x 256 tiles) + lm_head_combine_kernel",
+                    "rowmajor_us_per_call": lr_ms * 1e3,
+                    "kernel": "lm_head_kernel (tcgen05, 128 x 256 tiles, tile-major head) + "
+                              "lm_head_combine_kernel",
                     "note": "weights generated on the device (seeded), bf16; the logit matrix is "
                             "never written"},
         "peak_gbs": hbm_gbs,

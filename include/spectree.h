@@ -291,6 +291,23 @@ int spec_lm_head_stats(const void* hidden, const void* weight, const int32_t* ga
                        int32_t* out_argmax, float* out_gather, void* workspace,
                        size_t workspace_bytes, int32_t* status, void* stream);
 
+/*
+ * The head in tile-major order, made once (it is a model weight): block (t, c) holds rows
+ * 256 t .. 256 t + 255 and hidden elements 64 c .. 64 c + 63, contiguous, zero past V and H, so
+ * that spec_lm_head_stats_packed reads every tile as one contiguous 32 KB block (the row-major head
+ * gives 128-byte pieces of 256 rows).  packed: spec_lm_head_packed_bytes(V, H) bytes, 16-byte
+ * aligned.  spec_lm_head_stats_packed: spec_lm_head_stats on a packed head, same results bit for
+ * bit.
+ */
+size_t spec_lm_head_packed_bytes(int V, int H);
+int spec_lm_head_pack(const void* weight, int V, int H, void* packed, size_t packed_bytes,
+                      void* stream);
+int spec_lm_head_stats_packed(const void* hidden, const void* packed, const int32_t* gather_idx,
+                              int M, int H, int V, int G, float temperature, float* out_max,
+                              float* out_sumexp, int32_t* out_argmax, float* out_gather,
+                              void* workspace, size_t workspace_bytes, int32_t* status,
+                              void* stream);
+
 /* ------------------------------------------------------------------------------------------------
  * Tree attention over a paged KV cache
  * ------------------------------------------------------------------------------------------------

@@ -21,6 +21,8 @@ CUDA stream.  There is no CPU fallback: a missing library raises.
 from ._binding import (  # noqa: F401
     SpecError,
     spec_kv_compact,
+    spec_lm_head_pack,
+    spec_lm_head_packed_bytes,
     spec_lm_head_stats,
     spec_lm_head_stats_workspace,
     spec_kv_compact_paged,

@@ -54,6 +54,10 @@ _SIGNATURES = {
     "spec_lm_head_stats_workspace": (_c_size, [_c_int] * 2),
     "spec_lm_head_stats": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_c_float] + [_vp] * 5
                            + [_c_size, _vp, _vp]),
+    "spec_lm_head_packed_bytes": (_c_size, [_c_int] * 2),
+    "spec_lm_head_pack": (_c_int, [_vp, _c_int, _c_int, _vp, _c_size, _vp]),
+    "spec_lm_head_stats_packed": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_c_float] + [_vp] * 5
+                                  + [_c_size, _vp, _vp]),
     "spec_status_string": (ctypes.c_char_p, [_c_int]),
 }
 
@@ -419,16 +423,41 @@ def spec_lm_head_stats_workspace(M, V) -> int:
     return int(lib().spec_lm_head_stats_workspace(M, V))
 
 
+def spec_lm_head_packed_bytes(V, H) -> int:
+    return int(lib().spec_lm_head_packed_bytes(V, H))
+
+
+def spec_lm_head_pack(weight, packed=None, stream=None):
+    """The head [V, H] (bf16) in tile-major order (a uint8 device tensor)."""
+    torch = _torch()
+    V, H = weight.shape
+    _check(weight, "weight", torch.bfloat16, (V, H), weight.device)
+    nbytes = spec_lm_head_packed_bytes(V, H)
+    if packed is None:
+        packed = torch.empty((nbytes,), dtype=torch.uint8, device=weight.device)
+    rc = lib().spec_lm_head_pack(_ptr(weight), V, H, _ptr(packed), packed.numel(),
+                                 _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_lm_head_pack", rc)
+    return packed
+
+
 def spec_lm_head_stats(hidden, weight, temperature=1.0, gather_idx=None, outputs=None,
-                       workspace=None, status=None, stream=None):
+                       workspace=None, status=None, stream=None, packed_vocab=None):
     """Per row of hidden [M, H] @ weight [V, H]^T (bf16): max, sum of exp((l - max) / T), argmax
-    and the logits at gather_idx [M, G]; returns a dict of device tensors."""
+    and the logits at gather_idx [M, G]; returns a dict of device tensors.  With packed_vocab = V,
+    `weight` is the head made by spec_lm_head_pack."""
     torch = _torch()
     M, H = hidden.shape
-    V = weight.shape[0]
     dev = hidden.device
     _check(hidden, "hidden", torch.bfloat16, (M, H), dev)
-    _check(weight, "weight", torch.bfloat16, (V, H), dev)
+    if packed_vocab is None:
+        V = weight.shape[0]
+        _check(weight, "weight", torch.bfloat16, (V, H), dev)
+    else:
+        V = int(packed_vocab)
+        if weight.numel() * weight.element_size() < spec_lm_head_packed_bytes(V, H):
+            raise ValueError("packed head too small")
     G = 0 if gather_idx is None else gather_idx.shape[1]
     if gather_idx is not None:
         _check(gather_idx, "gather_idx", torch.int32, (M, G), dev)
@@ -443,10 +472,10 @@ def spec_lm_head_stats(hidden, weight, temperature=1.0, gather_idx=None, outputs
     if workspace is None:
         workspace = torch.empty((max(spec_lm_head_stats_workspace(M, V), 16),), dtype=torch.uint8,
                                 device=dev)
-    rc = lib().spec_lm_head_stats(_ptr(hidden), _ptr(weight), _ptr(gather_idx), M, H, V, G,
-                                  float(temperature), _ptr(o["max"]), _ptr(o["sumexp"]),
-                                  _ptr(o["argmax"]), _ptr(o.get("gather")), _ptr(workspace),
-                                  workspace.numel(), _ptr(o["status"]), _stream(stream))
+    fn = lib().spec_lm_head_stats if packed_vocab is None else lib().spec_lm_head_stats_packed
+    rc = fn(_ptr(hidden), _ptr(weight), _ptr(gather_idx), M, H, V, G, float(temperature),
+            _ptr(o["max"]), _ptr(o["sumexp"]), _ptr(o["argmax"]), _ptr(o.get("gather")),
+            _ptr(workspace), workspace.numel(), _ptr(o["status"]), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_lm_head_stats", rc)
     return o

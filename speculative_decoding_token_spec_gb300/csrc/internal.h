@@ -54,7 +54,9 @@ size_t lm_head_workspace_bytes(int M, int V);
 cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t* gather_idx, int M,
                            int H, int V, int G, float T, float* out_max, float* out_sumexp,
                            int32_t* out_argmax, float* out_gather, void* workspace,
-                           int32_t* flag, int num_sms, cudaStream_t s);
+                           int32_t* flag, int num_sms, bool packed, cudaStream_t s);
+size_t lm_head_packed_bytes(int V, int H);
+cudaError_t launch_lm_head_pack(const void* weight, int V, int H, void* packed, cudaStream_t s);
 
 // dynamic tree construction (tree_build.cu)
 constexpr int kMaxTreeK = 16;       // candidates per expanded node, frontier size

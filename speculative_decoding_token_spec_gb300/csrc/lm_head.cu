@@ -40,6 +40,7 @@ static_assert(kLM * kTileStride * 4 <= kStages * kStageBytes, "tile copy fits th
 __global__ void __launch_bounds__(kLThreads, 1)
     lm_head_kernel(const __grid_constant__ CUtensorMap tmap_h,
                    const __grid_constant__ CUtensorMap tmap_w, int M, int H, int V, int G, int tn,
+                   int packed,
                    const int32_t* __restrict__ gather_idx, float k2, LmPartial* __restrict__ part,
                    float* __restrict__ out_gather, int32_t* flag) {
   extern __shared__ uint8_t smem_raw[];
@@ -85,7 +86,10 @@ __global__ void __launch_bounds__(kLThreads, 1)
         const uint32_t a = smem_u32(smem + s * kStageBytes);
         mbar_arrive_expect_tx(bar(s), kABytes + tn * kLK * 2);
         tma_load_2d(a, &tmap_h, bar(s), kc * kLK, m0);
-        tma_load_2d(a + kABytes, &tmap_w, bar(s), kc * kLK, v0);
+        if (packed)  // tile-major head: box (vocabulary tile, hidden slice) is one contiguous block
+          tma_load_2d(a + kABytes, &tmap_w, bar(s), 0, (blockIdx.y * nk + kc) * kLN);
+        else
+          tma_load_2d(a + kABytes, &tmap_w, bar(s), kc * kLK, v0);
       }
       issued_s = kc;
     }
@@ -184,6 +188,20 @@ __global__ void __launch_bounds__(kLThreads, 1)
   }
 }
 
+// The head in tile-major order: block (t, c) = rows 256 t .. 256 t + 255, hidden elements
+// 64 c .. 64 c + 63, stored contiguously (zero past V and H).  One CTA per block.
+__global__ void __launch_bounds__(256) lm_head_pack_kernel(const uint16_t* __restrict__ w, int V,
+                                                           int H, int nk,
+                                                           uint16_t* __restrict__ packed) {
+  const int t = blockIdx.x / nk, c = blockIdx.x % nk;
+  uint16_t* dst = packed + (size_t)blockIdx.x * kLN * kLK;
+  for (int e = threadIdx.x; e < kLN * kLK; e += blockDim.x) {
+    const int r = e / kLK, k = e % kLK;
+    const int v = t * kLN + r, h = c * kLK + k;
+    dst[e] = (v < V && h < H) ? w[(size_t)v * H + h] : (uint16_t)0;
+  }
+}
+
 // Per row: merge the vocabulary tiles' (max, sum of exp, argmax).
 __global__ void __launch_bounds__(256) lm_head_combine_kernel(const LmPartial* __restrict__ part,
                                                               int M, int ntiles, float k2,
@@ -229,14 +247,28 @@ size_t lm_head_workspace_bytes(int M, int V) {  // one partial per (tile, row); 
   return (size_t)((V + 127) / 128) * (size_t)M * sizeof(LmPartial);
 }
 
+size_t lm_head_packed_bytes(int V, int H) {
+  return (size_t)((V + kLN - 1) / kLN) * (size_t)((H + kLK - 1) / kLK) * kLN * kLK * 2;
+}
+
+cudaError_t launch_lm_head_pack(const void* weight, int V, int H, void* packed, cudaStream_t s) {
+  const int nk = (H + kLK - 1) / kLK, nvt = (V + kLN - 1) / kLN;
+  lm_head_pack_kernel<<<nvt * nk, 256, 0, s>>>(static_cast<const uint16_t*>(weight), V, H, nk,
+                                               static_cast<uint16_t*>(packed));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t* gather_idx, int M,
                            int H, int V, int G, float T, float* out_max, float* out_sumexp,
                            int32_t* out_argmax, float* out_gather, void* workspace,
-                           int32_t* flag, int num_sms, cudaStream_t s) {
-  const int tn = tile_width(M, V, num_sms);
+                           int32_t* flag, int num_sms, bool packed, cudaStream_t s) {
+  const int tn = packed ? kLN : tile_width(M, V, num_sms);
+  const int nk = (H + kLK - 1) / kLK;
   CUtensorMap mh, mw;
-  if (!encode_bf16_2d(&mh, hidden, H, M, kLK, kLM) || !encode_bf16_2d(&mw, weight, H, V, kLK, tn))
-    return cudaErrorInvalidValue;
+  const bool wmap = packed ? encode_bf16_2d(&mw, weight, kLK,
+                                            (long long)((V + kLN - 1) / kLN) * nk * kLN, kLK, kLN)
+                           : encode_bf16_2d(&mw, weight, H, V, kLK, tn);
+  if (!encode_bf16_2d(&mh, hidden, H, M, kLK, kLM) || !wmap) return cudaErrorInvalidValue;
   const float k2 = (float)(1.4426950408889634 / (double)T);
   const int ntiles = (V + tn - 1) / tn;
   cudaError_t e = cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -253,8 +285,8 @@ cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   LmPartial* part = static_cast<LmPartial*>(workspace);
-  e = cudaLaunchKernelEx(&cfg, lm_head_kernel, mh, mw, M, H, V, G, tn, gather_idx, k2, part,
-                         out_gather, flag);
+  e = cudaLaunchKernelEx(&cfg, lm_head_kernel, mh, mw, M, H, V, G, tn, packed ? 1 : 0, gather_idx,
+                         k2, part, out_gather, flag);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t c2 = {};
   c2.gridDim = dim3((unsigned)((M + 255) / 256));

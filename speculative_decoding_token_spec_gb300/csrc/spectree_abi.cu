@@ -318,10 +318,11 @@ size_t spec_lm_head_stats_workspace(int M, int V) {
   return lm_head_workspace_bytes(M, V);
 }
 
-int spec_lm_head_stats(const void* hidden, const void* weight, const int32_t* gather_idx, int M,
-                       int H, int V, int G, float temperature, float* out_max, float* out_sumexp,
-                       int32_t* out_argmax, float* out_gather, void* workspace,
-                       size_t workspace_bytes, int32_t* status, void* stream) {
+namespace {
+int lm_head_common(const void* hidden, const void* weight, const int32_t* gather_idx, int M, int H,
+                   int V, int G, float temperature, float* out_max, float* out_sumexp,
+                   int32_t* out_argmax, float* out_gather, void* workspace,
+                   size_t workspace_bytes, int32_t* status, void* stream, bool packed) {
   if (!hidden || !weight || M < 1 || H < 8 || (H & 7) || V < 1 || G < 0)
     return SPEC_ERR_INVALID_ARG;
   if (!std::isfinite(temperature) || !(temperature > 0.f)) return SPEC_ERR_INVALID_ARG;
@@ -335,9 +336,42 @@ int spec_lm_head_stats(const void* hidden, const void* weight, const int32_t* ga
   if (sms <= 0) return SPEC_ERR_CUDA;
   const cudaError_t e = launch_lm_head(hidden, weight, gather_idx, M, H, V, G, temperature, out_max,
                                        out_sumexp, out_argmax, out_gather, workspace, status, sms,
-                                       static_cast<cudaStream_t>(stream));
+                                       packed, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorInvalidValue) return SPEC_ERR_INVALID_ARG;  // tensor maps refused
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+}  // namespace
+
+int spec_lm_head_stats(const void* hidden, const void* weight, const int32_t* gather_idx, int M,
+                       int H, int V, int G, float temperature, float* out_max, float* out_sumexp,
+                       int32_t* out_argmax, float* out_gather, void* workspace,
+                       size_t workspace_bytes, int32_t* status, void* stream) {
+  return lm_head_common(hidden, weight, gather_idx, M, H, V, G, temperature, out_max, out_sumexp,
+                        out_argmax, out_gather, workspace, workspace_bytes, status, stream, false);
+}
+
+size_t spec_lm_head_packed_bytes(int V, int H) {
+  if (V < 1 || H < 8 || (H & 7)) return 0;
+  return lm_head_packed_bytes(V, H);
+}
+
+int spec_lm_head_pack(const void* weight, int V, int H, void* packed, size_t packed_bytes,
+                      void* stream) {
+  if (!weight || V < 1 || H < 8 || (H & 7)) return SPEC_ERR_INVALID_ARG;
+  if (!packed || packed_bytes < lm_head_packed_bytes(V, H) || !aligned16(packed))
+    return SPEC_ERR_WORKSPACE;
+  return launch_lm_head_pack(weight, V, H, packed, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
+}
+
+int spec_lm_head_stats_packed(const void* hidden, const void* packed, const int32_t* gather_idx,
+                              int M, int H, int V, int G, float temperature, float* out_max,
+                              float* out_sumexp, int32_t* out_argmax, float* out_gather,
+                              void* workspace, size_t workspace_bytes, int32_t* status,
+                              void* stream) {
+  return lm_head_common(hidden, packed, gather_idx, M, H, V, G, temperature, out_max, out_sumexp,
+                        out_argmax, out_gather, workspace, workspace_bytes, status, stream, true);
 }
 
 const char* spec_status_string(int code) {

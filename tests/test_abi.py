@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
               "spec_kv_compact", "spec_kv_compact_paged", "spec_tree_verify_filtered",
               "spec_tree_verify_filtered_workspace", "spec_tree_build_workspace",
               "spec_tree_expand", "spec_tree_finalize", "spec_lm_head_stats",
-              "spec_lm_head_stats_workspace"):
+              "spec_lm_head_stats_workspace", "spec_lm_head_pack", "spec_lm_head_stats_packed"):
         assert n in names
 
 
@@ -213,3 +213,6 @@ def test_lm_head_arguments(lib):
     assert call(T=0.0) == -1 and call(T=float("nan")) == -1
     assert call(G=3) == -1                  # gathers without ids / outputs
     assert call(nbytes=ws - 16) == -3
+    assert lib.spec_lm_head_packed_bytes(1000, 104) == 4 * 2 * 256 * 64 * 2  # padded tiles
+    assert lib.spec_lm_head_packed_bytes(1000, 60) == 0
+    assert lib.spec_lm_head_pack(fake, 1000, 64, fake, 16, null) == -3

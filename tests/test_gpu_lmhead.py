@@ -96,3 +96,28 @@ def test_statistics_drive_greedy_verification(dev):
         assert len(path) == ref["accept_len"][b]
         assert [int(tok[b, i]) for i in path] == list(ref["accepted_tokens"][b, :len(path)])
         assert am[b, j] == ref["bonus"][b]
+
+
+@pytest.mark.parametrize("M,H,V", [(60, 4096, 32000), (300, 520, 3000), (20, 4096, 1000)])
+def test_packed_head_gives_the_same_bits(dev, M, H, V):
+    """The tile-major head: the packed buffer holds the weight in the stated order (zero padding),
+    and the statistics on it equal those on the row-major head bit for bit."""
+    import torch
+    import speculative_decoding_token_spec_gb300 as st
+    case = W.make_lm_head_case(M, H, V, 5, seed=M * 3 + V)
+    h = P.dev_tensor(case.hidden, dev).view(torch.bfloat16)
+    w = P.dev_tensor(case.weight, dev).view(torch.bfloat16)
+    gi = P.dev_tensor(case.gather_idx, dev)
+    packed = st.spec_lm_head_pack(w)
+    a = st.spec_lm_head_stats(h, w, 0.8, gather_idx=gi)
+    b = st.spec_lm_head_stats(h, packed, 0.8, gather_idx=gi, packed_vocab=V)
+    torch.cuda.synchronize()
+    nk, nv = -(-H // 64), -(-V // 256)
+    pk = packed.cpu().numpy().view(np.uint16).reshape(nv, nk, 256, 64)
+    full = np.zeros((nv * 256, nk * 64), np.uint16)
+    full[:V, :H] = case.weight
+    want = full.reshape(nv, 256, nk, 64).transpose(0, 2, 1, 3)
+    assert np.array_equal(pk, want)
+    for k in ("max", "sumexp", "gather"):
+        assert torch.equal(a[k].view(torch.int32), b[k].view(torch.int32)), k
+    assert torch.equal(a["argmax"], b["argmax"])
