@@ -202,33 +202,52 @@ __global__ void __launch_bounds__(256) lm_head_pack_kernel(const uint16_t* __res
   }
 }
 
-// Per row: merge the vocabulary tiles' (max, sum of exp, argmax).
+// Per row: merge the vocabulary tiles' (max, sum of exp, argmax).  One warp per row; lane l takes
+// tiles l, l + 32, ... so that all of a row's partials are loaded at once (one thread walking the
+// tiles in turn waits on one L2 load per tile), then the lanes combine by shuffles: the larger max,
+// the lower index among equal maxima (tiles ascend in vocabulary order, so the lowest index wins).
+constexpr int kCombineRows = 8;  // rows (warps) per 256-thread block
 __global__ void __launch_bounds__(256) lm_head_combine_kernel(const LmPartial* __restrict__ part,
                                                               int M, int ntiles, float k2,
                                                               float* out_max, float* out_sumexp,
                                                               int32_t* out_argmax) {
   griddep_wait();
   griddep_launch_dependents();
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  const int row = blockIdx.x * kCombineRows + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= M) return;
   float m = -INFINITY;
   int am = 0x7fffffff;
-  for (int t = 0; t < ntiles; ++t) {  // ascending tiles: the first tile with the max has the
-    const LmPartial p = part[(size_t)t * M + row];  // lowest index
+#pragma unroll 4
+  for (int t = lane; t < ntiles; t += 32) {
+    const LmPartial p = part[(size_t)t * M + row];
     if (p.m > m) {
       m = p.m;
       am = p.arg;
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const int oa = __shfl_xor_sync(0xffffffffu, am, o);
+    if (om > m || (om == m && oa < am)) {
+      m = om;
+      am = oa;
+    }
+  }
   float s = 0.f;
   const float mk = __fmul_rn(m, k2);
-  for (int t = 0; t < ntiles; ++t) {
+#pragma unroll 4
+  for (int t = lane; t < ntiles; t += 32) {
     const LmPartial p = part[(size_t)t * M + row];
     if (p.m > -INFINITY) s += p.s * exp2f(fmaf(p.m, k2, -mk));
   }
-  if (out_max) out_max[row] = m;
-  if (out_sumexp) out_sumexp[row] = s;
-  if (out_argmax) out_argmax[row] = am;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) {
+    if (out_max) out_max[row] = m;
+    if (out_sumexp) out_sumexp[row] = s;
+    if (out_argmax) out_argmax[row] = am;
+  }
 }
 
 }  // namespace
@@ -289,7 +308,7 @@ cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t
                          k2, part, out_gather, flag);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t c2 = {};
-  c2.gridDim = dim3((unsigned)((M + 255) / 256));
+  c2.gridDim = dim3((unsigned)((M + kCombineRows - 1) / kCombineRows));
   c2.blockDim = dim3(256);
   c2.stream = s;
   c2.attrs = attr;
