@@ -637,9 +637,26 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
     g_p, g_c = capture(paged, pcs), capture(compact, bufs)
     g_f, g_v = capture(filtered, bufs), capture(plain, bufs)
     g_tb, g_tx = capture(build, tcs), capture(expand_all, tcs)
+    # temperature-0 verification straight from the fused head's argmax (no logit row anywhere)
+    g_st = torch.zeros((B,), dtype=torch.int32, device=dev)
+    g_out = st.spec_tree_verify_greedy(lm_out["argmax"].view(B, N), bufs[0]["tokens"],
+                                       bufs[0]["parent"], V, status=g_st)
+
+    def lm_greedy(_c=None):
+        lmhead()
+        st.spec_tree_verify_greedy(lm_out["argmax"].view(B, N), bufs[0]["tokens"],
+                                   bufs[0]["parent"], V, outputs=g_out, status=g_st)
+
+    lm_greedy()
+    torch.cuda.synchronize()
+    assert int(g_st.sum()) == 0
     reps_lm = 20
     g_lm = capture(lmhead, [None] * reps_lm)
     g_lr = capture(lmhead_rowmajor, [None] * reps_lm)
+    g_lg = capture(lm_greedy, [None] * reps_lm)
+    g_gr = capture(lambda _c: st.spec_tree_verify_greedy(
+        lm_out["argmax"].view(B, N), bufs[0]["tokens"], bufs[0]["parent"], V, outputs=g_out,
+        status=g_st), [None] * reps_lm)
     torch.cuda.current_stream().wait_stream(s)
     for _ in range(2):
         g_p.replay()
@@ -650,6 +667,8 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
         g_tx.replay()
         g_lm.replay()
         g_lr.replay()
+        g_lg.replay()
+        g_gr.replay()
     torch.cuda.synchronize()
     reps = max(1, 600 // ncp)
     p_ms = timed(lambda: [g_p.replay() for _ in range(reps)]) / (reps * ncp)
@@ -663,6 +682,8 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
     tree_bytes = tcase.draft_rows.nbytes  # every draft row read once
     lm_ms = timed(lambda: [g_lm.replay() for _ in range(10)]) / (10 * reps_lm)
     lr_ms = timed(lambda: [g_lr.replay() for _ in range(10)]) / (10 * reps_lm)
+    lg_ms = timed(lambda: [g_lg.replay() for _ in range(10)]) / (10 * reps_lm)
+    gr_ms = timed(lambda: [g_gr.replay() for _ in range(10)]) / (10 * reps_lm)
     lm_bytes = lm_w.numel() * 2 + lm_x.numel() * 2 + lm_m * 12  # head, hidden, statistics
     lm_flops = 2.0 * lm_m * lm_h * V
     fil_gbs = filt_bytes / ((f_ms - v_ms) * 1e-3) / 1e9 if f_ms > v_ms else None
@@ -704,8 +725,11 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
                     "tflops": lm_flops / (lm_ms * 1e-3) / 1e12,
                     "tensor_frac": lm_flops / (lm_ms * 1e-3) / 1e12 / tc_tflops,
                     "rowmajor_us_per_call": lr_ms * 1e3,
+                    "greedy_verify_pipeline_us": lg_ms * 1e3,
+                    "greedy_verify_us": gr_ms * 1e3,
                     "kernel": "lm_head_kernel (tcgen05, 128 x 256 tiles, tile-major head) + "
-                              "lm_head_combine_kernel",
+                              "lm_head_combine_kernel; pipeline: + verify_greedy_kernel (T = 0 "
+                              "verification of the workload's tree from the argmax)",
                     "note": "weights generated on the device (seeded), bf16; the logit matrix is "
                             "never written"},
         "peak_gbs": hbm_gbs,

@@ -308,6 +308,26 @@ int spec_lm_head_stats_packed(const void* hidden, const void* packed, const int3
                               void* workspace, size_t workspace_bytes, int32_t* status,
                               void* stream);
 
+/*
+ * Greedy verification (T = 0) from each node's argmax token: survey explainer, Formal Definition,
+ * 検証フェーズ at temperature 0 -- from the root, move to the first child (ascending index) whose
+ * draft token equals the argmax of the current node's target logits; stop where no child does; the
+ * bonus token is the argmax there.  The results equal spec_tree_verify at temperature 0 on logits
+ * with those argmaxes; with spec_lm_head_stats's out_argmax (row b * N + i = node i of sequence b)
+ * no logit row is ever written.
+ *   node_argmax  int32 [B, N]: the argmax of node i's target logits (lowest index among equal
+ *                maxima); a value outside [0, V) at a node the walk reaches means that row had no
+ *                maximum: the sequence gets SPEC_ST_NONFINITE
+ *   tree_tokens, tree_parent, outputs, status: as in spec_tree_verify (out_accepted_nodes may be
+ *                NULL; a flagged sequence gets accept_len = bonus = -1 and -1 rows)
+ * No workspace; B <= 2^24, N <= 64.  Returns SPEC_OK or a negative spec_err_t before any launch.
+ */
+int spec_tree_verify_greedy(const int32_t* node_argmax, const int32_t* tree_tokens,
+                            const int32_t* tree_parent, int B, int N, int V,
+                            int32_t* out_accept_len, int32_t* out_accepted_tokens,
+                            int32_t* out_bonus_token, int32_t* out_accepted_nodes, int32_t* status,
+                            void* stream);
+
 /* ------------------------------------------------------------------------------------------------
  * Tree attention over a paged KV cache
  * ------------------------------------------------------------------------------------------------

@@ -58,6 +58,7 @@ _SIGNATURES = {
     "spec_lm_head_pack": (_c_int, [_vp, _c_int, _c_int, _vp, _c_size, _vp]),
     "spec_lm_head_stats_packed": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_c_float] + [_vp] * 5
                                   + [_c_size, _vp, _vp]),
+    "spec_tree_verify_greedy": (_c_int, [_vp] * 3 + [_c_int] * 3 + [_vp] * 6),
     "spec_status_string": (ctypes.c_char_p, [_c_int]),
 }
 
@@ -295,6 +296,33 @@ def spec_tree_verify(target_logits, draft_probs, tree_tokens, tree_parent, unifo
         _stream(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_tree_verify", rc)
+    return o
+
+
+def spec_tree_verify_greedy(node_argmax, tree_tokens, tree_parent, V, outputs=None, status=None,
+                            want_nodes=True, stream=None):
+    """Greedy (T = 0) verification from each node's argmax token (node_argmax int32 [B, N], e.g.
+    spec_lm_head_stats's argmax viewed as [B, N]); same outputs as spec_tree_verify."""
+    torch = _torch()
+    B, N = tree_tokens.shape
+    dev = tree_tokens.device
+    _check(node_argmax, "node_argmax", torch.int32, (B, N), dev)
+    _check(tree_tokens, "tree_tokens", torch.int32, (B, N), dev)
+    _check(tree_parent, "tree_parent", torch.int32, (B, N), dev)
+    o = dict(outputs or {})
+    i32 = dict(dtype=torch.int32, device=dev)
+    o.setdefault("accept_len", torch.empty((B,), **i32))
+    o.setdefault("accepted_tokens", torch.empty((B, N), **i32))
+    o.setdefault("bonus", torch.empty((B,), **i32))
+    if want_nodes:
+        o.setdefault("accepted_nodes", torch.empty((B, N), **i32))
+    o["status"] = status if status is not None else torch.zeros((B,), **i32)  # bits are OR-ed in
+    rc = lib().spec_tree_verify_greedy(
+        _ptr(node_argmax), _ptr(tree_tokens), _ptr(tree_parent), B, N, int(V),
+        _ptr(o["accept_len"]), _ptr(o["accepted_tokens"]), _ptr(o["bonus"]),
+        _ptr(o.get("accepted_nodes")), _ptr(o["status"]), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_tree_verify_greedy", rc)
     return o
 
 

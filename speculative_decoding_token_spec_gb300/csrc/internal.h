@@ -56,6 +56,11 @@ cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t
                            int32_t* out_argmax, float* out_gather, void* workspace,
                            int32_t* flag, int num_sms, bool packed, cudaStream_t s);
 size_t lm_head_packed_bytes(int V, int H);
+// Greedy verification from each node's argmax token (verify_greedy.cu).
+cudaError_t launch_verify_greedy(const int32_t* node_argmax, const int32_t* tokens,
+                                 const int32_t* parent, int B, int N, int V, int32_t* accept_len,
+                                 int32_t* acc_tokens, int32_t* bonus, int32_t* acc_nodes,
+                                 int32_t* status, cudaStream_t s);
 cudaError_t launch_lm_head_pack(const void* weight, int V, int H, void* packed, cudaStream_t s);
 
 // dynamic tree construction (tree_build.cu)

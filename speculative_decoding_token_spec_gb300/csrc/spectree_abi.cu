@@ -374,6 +374,22 @@ int spec_lm_head_stats_packed(const void* hidden, const void* packed, const int3
                         out_argmax, out_gather, workspace, workspace_bytes, status, stream, true);
 }
 
+int spec_tree_verify_greedy(const int32_t* node_argmax, const int32_t* tree_tokens,
+                            const int32_t* tree_parent, int B, int N, int V,
+                            int32_t* out_accept_len, int32_t* out_accepted_tokens,
+                            int32_t* out_bonus_token, int32_t* out_accepted_nodes, int32_t* status,
+                            void* stream) {
+  if (!node_argmax || !tree_tokens || !tree_parent || !out_accept_len || !out_accepted_tokens ||
+      !out_bonus_token)
+    return SPEC_ERR_INVALID_ARG;
+  if (B < 1 || B > (1 << 24) || N < 1 || N > kMaxNodes || V < 1) return SPEC_ERR_INVALID_ARG;
+  return launch_verify_greedy(node_argmax, tree_tokens, tree_parent, B, N, V, out_accept_len,
+                              out_accepted_tokens, out_bonus_token, out_accepted_nodes, status,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
+}
+
 const char* spec_status_string(int code) {
   switch (code) {
     case SPEC_OK: return "ok";

@@ -36,7 +36,8 @@ def test_header_declares_the_entry_points():
               "spec_kv_compact", "spec_kv_compact_paged", "spec_tree_verify_filtered",
               "spec_tree_verify_filtered_workspace", "spec_tree_build_workspace",
               "spec_tree_expand", "spec_tree_finalize", "spec_lm_head_stats",
-              "spec_lm_head_stats_workspace", "spec_lm_head_pack", "spec_lm_head_stats_packed"):
+              "spec_lm_head_stats_workspace", "spec_lm_head_pack", "spec_lm_head_stats_packed",
+              "spec_tree_verify_greedy"):
         assert n in names
 
 
@@ -216,3 +217,15 @@ def test_lm_head_arguments(lib):
     assert lib.spec_lm_head_packed_bytes(1000, 104) == 4 * 2 * 256 * 64 * 2  # padded tiles
     assert lib.spec_lm_head_packed_bytes(1000, 60) == 0
     assert lib.spec_lm_head_pack(fake, 1000, 64, fake, 16, null) == -3
+
+
+def test_greedy_verify_arguments(lib):
+    """Argument errors of the greedy verification, before any CUDA call."""
+    fake = ctypes.c_void_p(256)
+    null = None
+
+    def call(B=2, N=10, V=100, am=fake, out=fake):
+        return lib.spec_tree_verify_greedy(am, fake, fake, B, N, V, out, fake, fake, null, null,
+                                           null)
+    assert call(am=null) == -1 and call(out=null) == -1
+    assert call(B=0) == -1 and call(N=0) == -1 and call(N=65) == -1 and call(V=0) == -1
