@@ -448,6 +448,19 @@ def run_ours(args):
 
     attn_gbs = attn_bytes / (attn_ms * 1e-3) / 1e9
     ver_gbs = verify_bytes / (ver_ms * 1e-3) / 1e9
+    # large problems verify along the accepted path only: the rows that form reads
+    path_form = B * N * V * 4 > (64 << 20)
+    path_bytes = None
+    if path_form:
+        out0 = bufs[0]["vout"]
+        lens = out0["accept_len"].cpu().numpy()
+        nodes = out0["accepted_nodes"].cpu().numpy()
+        par0 = vc.tree_parent
+        path_bytes = 0
+        for b in range(B):
+            for j in [0] + [int(x) for x in nodes[b, :max(int(lens[b]), 0)]]:
+                has_kids = bool((par0[b, 1:] == j).any())
+                path_bytes += 4 * V * (2 if (T > 0 and has_kids) else 1)
     step_roof_s = (attn_bytes + verify_bytes) / (hbm_gbs * 1e9)
     traffic = profiled_traffic("tree_attn")
     line = {
@@ -469,6 +482,10 @@ def run_ours(args):
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
         "step": {"attn_us": attn_ms * 1e3, "verify_us": ver_ms * 1e3,
                  "verify_gbs": ver_gbs, "attn_bytes": attn_bytes, "verify_bytes": verify_bytes,
+                 "verify_form": "path only (one cluster per sequence)" if path_form
+                                else "every node at once",
+                 "verify_read_bytes": path_bytes,
+                 "verify_read_gbs": (path_bytes / (ver_ms * 1e-3) / 1e9) if path_bytes else None,
                  "attn_tflops": attn_flops / (attn_ms * 1e-3) / 1e12,
                  "hbm_roofline_frac": step_roof_s / (ms_per_step * 1e-3),
                  "roofline_note": "T_roof = (attn + verify algorithmic bytes) / measured HBM GB/s; "

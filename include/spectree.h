@@ -133,6 +133,12 @@ size_t spec_tree_verify_workspace(int B, int N, int V);
  * ascending index against the current target distribution, which is replaced by its normalised
  * residual norm(max(0, q - p)) after each rejection (kept if that residual is all zero).  The
  * emitted tokens of the step are the accepted tokens followed by the bonus token.
+ *
+ * Rows read.  Small problems (B * N * V * 4 <= 64 MiB) process every node at once; large ones
+ * process every internal node when out_child_q is given, and otherwise only the nodes the walk
+ * reaches (the root, then each accepted child, one step per level).  The results are the same;
+ * SPEC_ST_NONFINITE reports NaN / +Inf in a row that was read, so a non-finite row off the walk
+ * flags the sequence in the first two forms only.
  */
 int spec_tree_verify(const float* target_logits, const float* draft_probs,
                      const int32_t* tree_tokens, const int32_t* tree_parent,

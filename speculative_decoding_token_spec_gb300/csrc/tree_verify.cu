@@ -637,11 +637,14 @@ struct NodeBufs {
 // one node: statistics, sibling tests, residual rounds, bonus if the walk can stop here
 // ------------------------------------------------------------------------------------------------
 // logits_staged: the kernel already issued the copy of this node's logit slice into nb.lbuf.
-// The returned record is complete in CTA `writer` (every CTA gets the same writer).
+// ph_l, ph_p: the phases of the staging barriers' next waits (flipped here after each wait), so
+// that one CTA can process several nodes in turn.
+// The returned record is complete in CTA `writer` (every CTA gets the same writer); first_acc,
+// flags and (at T = 0) the bonus are the same in every CTA.
 template <int CL, bool PGLOBAL>
 __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, const NodeBufs& nb,
                                  bool logits_staged, DF invT_df, float k2, int& xk, int& writer,
-                                 VerifySmem& sm) {
+                                 uint32_t& ph_l, uint32_t& ph_p, VerifySmem& sm) {
   const int N = a.N, V = a.V;
   list_children(j, N, sm);
   const int nk = sm.nk;
@@ -667,7 +670,8 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     sm.g_r[threadIdx.x] = __ldg(a.uniforms + (size_t)b * N + kid);
   }
   const float u_bonus = __ldg(a.uniforms + (size_t)b * N);
-  const int lflags0 = wait_slice(nb.bar_l);
+  const int lflags0 = wait_slice(nb.bar_l, ph_l);
+  ph_l ^= 1u;
   int flags = 0;  // cluster-uniform: only ever updated from published partials
   writer = 0;
   NodeStat st;
@@ -739,7 +743,10 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     // rejected: residual of the current distribution (needed by the next sibling or the draw)
     if (!p_waited) {
       // CTA-local: reaches the cluster through the partials
-      pflags = probs_staged ? wait_slice(nb.bar_p) : 0;
+      if (probs_staged) {
+        pflags = wait_slice(nb.bar_p, ph_p);
+        ph_p ^= 1u;
+      }
       p_waited = true;
     }
     const DF c_next = df_add(c, D);
@@ -765,7 +772,10 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     }
     __syncthreads();
   }
-  if (probs_staged && !p_waited) wait_slice(nb.bar_p);  // no copy left in flight (not needed)
+  if (probs_staged && !p_waited) {  // no copy left in flight (not needed)
+    wait_slice(nb.bar_p, ph_p);
+    ph_p ^= 1u;
+  }
   const bool bad = (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) != 0;
   if ((nk == 0 || all_rejected) && !bad) {  // the walk can stop here: draw its bonus
     const Draw d = cluster_draw<CL>(s, nb.lbuf, pd, rs, u_bonus, rank, sm);
@@ -966,11 +976,12 @@ __global__ void __launch_bounds__(kVThreads)
   }
   cluster_wait_acquire();  // every CTA of the cluster can now receive exchanges
   int xk = 0, writer = 0;
+  uint32_t ph_l = 0, ph_p = 0;
   const bool work = sm.internal[j] || do_leaves;
   NodeStat st;
   if (work)
     st = process_node<CL, PGLOBAL>(a, b, j, rank, nb, early, DF{invT_hi, invT_lo}, k2, xk, writer,
-                                   sm);
+                                   ph_l, ph_p, sm);
 
   // arrival: the last cluster of the sequence to finish walks the tree
   if (do_leaves) {
@@ -1000,6 +1011,74 @@ __global__ void __launch_bounds__(kVThreads)
   cluster_barrier<CL>();
   if (!sm.is_last) return;
   walk_sequence_cluster<CL>(a, b, rank, nb, work, k2, xk, sm);
+  cluster_barrier<CL>();  // keep shared memory alive for remote stores
+}
+
+// Path-only form (large problems, no per-child q requested): one cluster per sequence walks the
+// tree, processing only the nodes the walk reaches -- the root, then each accepted child -- with
+// the same per-node step as above.  A sequence reads (accepted + 1) target rows instead of every
+// internal node's, at the price of one dependent step per accepted level.  No workspace.
+template <int CL, bool PGLOBAL>
+__global__ void __launch_bounds__(kVThreads)
+    verify_path_kernel(const VerifyArgs a, int cap, float invT_hi, float invT_lo, float k2) {
+  extern __shared__ __align__(16) float dyn[];
+  __shared__ VerifySmem sm;
+  __shared__ __align__(8) uint64_t bars[2];
+  const NodeBufs nb{dyn, dyn + cap, smem_u32(&bars[0]), smem_u32(&bars[1])};
+  const int rank = (CL > 1) ? int(cg::this_cluster().block_rank()) : 0;
+  const int b = blockIdx.z;
+  const int N = a.N;
+  if (threadIdx.x == 0) {
+    mbar_init(nb.bar_l, 1);
+    mbar_init(nb.bar_p, 1);
+    mbar_init(smem_u32(&sm.xbar[0]), 1);
+    mbar_init(smem_u32(&sm.xbar[1]), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  cluster_arrive_release();  // exchange barriers initialised (waited for before the first exchange)
+  griddep_wait();  // the inputs may be produced by the preceding kernel in the stream
+  griddep_launch_dependents();
+  const int bad = load_tree(a, b, sm);  // uniform across the cluster: same tree everywhere
+  if (bad) {
+    if (rank == 0) {
+      if (threadIdx.x == 0) {
+        a.accept_len[b] = -1;
+        a.bonus[b] = -1;
+        if (a.status) atomicOr(a.status + b, bad);
+      }
+      for (int i = threadIdx.x; i < N; i += kVThreads) {
+        a.acc_tokens[(size_t)b * N + i] = -1;
+        if (a.acc_nodes) a.acc_nodes[(size_t)b * N + i] = -1;
+      }
+    }
+    cluster_wait_acquire();
+    return;
+  }
+  cluster_wait_acquire();  // every CTA of the cluster can now receive exchanges
+  int xk = 0, writer = 0, c = 0, len = 0, bonus = -1, flags = 0;
+  uint32_t ph_l = 0, ph_p = 0;
+  for (;;) {  // at most N steps: every accepted child has a larger index than its parent
+    const NodeStat st = process_node<CL, PGLOBAL>(a, b, c, rank, nb, false, DF{invT_hi, invT_lo},
+                                                  k2, xk, writer, ph_l, ph_p, sm);
+    flags |= st.flags;  // cluster-uniform, so the loop's control flow is too
+    if (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) break;
+    const int fa = st.first_acc;
+    if (fa <= c || fa >= N) {  // every child rejected (or none): c is the terminal node
+      bonus = st.bonus;  // valid in CTA `writer`
+      break;
+    }
+    if (threadIdx.x == 0) sm.path[len] = fa;
+    ++len;
+    c = fa;
+    // this node's shared state (children, gathers, the slices rewritten in place) is free again;
+    // its generic writes are ordered before the next node's bulk copies into the same buffers
+    fence_async_smem();
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) sm.path_len = len;
+  __syncthreads();
+  if (rank == writer) write_outputs(a, b, bonus, flags, sm);
   cluster_barrier<CL>();  // keep shared memory alive for remote stores
 }
 
@@ -1057,10 +1136,25 @@ static int pick_cluster(long long units, int V, int num_sms, bool small, int nbu
 
 template <int CL>
 static cudaError_t launch_cl(const VerifyArgs& a, dim3 g, size_t smem, cudaStream_t s, int cap,
-                             int leaves, float invT_hi, float invT_lo, float k2) {
+                             int leaves, float invT_hi, float invT_lo, float k2, bool path) {
+  if (path) {
+    if (a.p_global)
+      return launch_ex(verify_path_kernel<CL, true>, g, CL, smem, s, a, cap, invT_hi, invT_lo, k2);
+    return launch_ex(verify_path_kernel<CL, false>, g, CL, smem, s, a, cap, invT_hi, invT_lo, k2);
+  }
   if (a.p_global)
     return launch_ex(verify_kernel<CL, true>, g, CL, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
   return launch_ex(verify_kernel<CL, false>, g, CL, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
+}
+
+// Path-only form: one cluster per sequence, each step a chain of dependent passes over the
+// slices, so clusters grow (up to 8) while about four CTAs per SM cover the batch.
+static int pick_cluster_path(int B, int V, int num_sms) {
+  int cl = 1;
+  while (cl < 8 && slice_capacity(V, cl) > kMaxSliceFloats) cl *= 2;
+  while (cl < 8 && (long long)B * cl * 2 <= (long long)num_sms * 4 && V / (cl * 2) >= 1024)
+    cl *= 2;
+  return cl;
 }
 
 bool verify_supported(int V) { return slice_capacity(V, 8) <= kMaxSliceFloats; }
@@ -1069,23 +1163,29 @@ cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s) {
   const bool small = (long long)a.B * a.N * a.V * 4 <= (64ll << 20);
   // small problems are latency-bound: process leaves speculatively too
   const int leaves = small ? 1 : 0;
+  // large problems walk the accepted path only, unless every child's q is wanted
+  const bool path = !small && a.child_q == nullptr;
   const long long units = (long long)a.B * (leaves ? a.N : (a.N + 1) / 2);
-  const int cl = pick_cluster(units, a.V, num_sms, small, a.T > 0.f ? 2 : 1);
+  const int cl = path ? pick_cluster_path(a.B, a.V, num_sms)
+                      : pick_cluster(units, a.V, num_sms, small, a.T > 0.f ? 2 : 1);
   const int cap = slice_capacity(a.V, cl);
   // large problems whose two slices would still leave one CTA per SM read the draft row from
-  // global memory (L2) instead of staging it
+  // global memory (L2) instead of staging it (the path form stages it when its clusters leave
+  // SMs to spare)
   VerifyArgs ak = a;
-  ak.p_global = (!small && a.T > 0.f && 2 * (size_t)cap * sizeof(float) > kLargeCtaBytes) ? 1 : 0;
+  const bool crowded = !path || (long long)a.B * cl > num_sms;
+  ak.p_global = (!small && a.T > 0.f && crowded &&
+                 2 * (size_t)cap * sizeof(float) > kLargeCtaBytes) ? 1 : 0;
   const size_t smem = (size_t)(a.T > 0.f && !ak.p_global ? 2 : 1) * cap * sizeof(float);
   const double invTd = a.T > 0.f ? 1.0 / (double)a.T : 0.0;
   const float invT_hi = (float)invTd, invT_lo = (float)(invTd - (double)invT_hi);
   const float k2 = (float)(invTd * 1.4426950408889634);  // log2(e) / T
-  const dim3 g(cl, a.N, a.B);
+  const dim3 g(cl, path ? 1 : a.N, a.B);
   switch (cl) {
-    case 1: return launch_cl<1>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2);
-    case 2: return launch_cl<2>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2);
-    case 4: return launch_cl<4>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2);
-    default: return launch_cl<8>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2);
+    case 1: return launch_cl<1>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2, path);
+    case 2: return launch_cl<2>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2, path);
+    case 4: return launch_cl<4>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2, path);
+    default: return launch_cl<8>(ak, g, smem, s, cap, leaves, invT_hi, invT_lo, k2, path);
   }
 }
 

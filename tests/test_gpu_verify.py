@@ -53,14 +53,16 @@ def test_eagle_tree_batched_many_seeds(dev):
         _check(W.make_verify_case(cfg, T, seed=11), dev)
 
 
-def test_llama3_8b_gqa_vocab_128k(dev):
+@pytest.mark.parametrize("child_q", [True, False])  # every internal node / the path only
+def test_llama3_8b_gqa_vocab_128k(dev, child_q):
     cfg = W.config("llama3_8b_gqa")
-    _check(W.make_verify_case(cfg, 0.7, seed=0), dev)
+    _check(W.make_verify_case(cfg, 0.7, seed=0), dev, want_child_q=child_q)
 
 
-def test_llama70b_longctx_vocab_128k(dev):
+@pytest.mark.parametrize("child_q", [True, False])
+def test_llama70b_longctx_vocab_128k(dev, child_q):
     cfg = W.config("llama70b_longctx")
-    _check(W.make_verify_case(cfg, 1.0, seed=0), dev)
+    _check(W.make_verify_case(cfg, 1.0, seed=0), dev, want_child_q=child_q)
 
 
 @pytest.mark.parametrize("N", [10, 40, 60])
@@ -78,6 +80,40 @@ def test_stress_full_batch(dev):
     """Full batch of the stress shape (64 sequences, 60-node trees) at one setting."""
     cfg = W.config("stress")
     _check(W.make_verify_case(cfg, 1.0, seed=3, sigma_d=1.0), dev, want_child_q=False, max_near=4)
+
+
+@pytest.mark.parametrize("T,sd", [(0.0, 1.0), (0.5, 0.25), (1.5, 3.0), (1.0, 0.25)])
+def test_path_form_full_batch(dev, T, sd):
+    """Large problems without per-child q take the path-only form (one cluster per sequence,
+    only the nodes the walk reaches): full stress batch over temperatures and draft noise (long
+    and short accepted paths), chains included."""
+    for N, tree in ((60, "static"), (10, "chain")):
+        cfg = W.config("stress", N=N, tree=tree)
+        _check(W.make_verify_case(cfg, T, seed=int(T * 10 + sd * 100) + N, sigma_d=sd), dev,
+               want_child_q=False, max_near=4)
+
+
+def test_path_form_reads_only_the_walk(dev):
+    """Path-only form: NaN in a row the walk never reaches leaves the sequence alone (its result is
+    the oracle's); NaN in the root row (always read) flags it.  The all-nodes form, taken when
+    per-child q is requested, reads every internal row and flags both."""
+    cfg = W.config("eagle_vicuna7b", B=8, N=60, V=40000)  # 77 MB of logits: a large problem
+    case = W.make_verify_case(cfg, 1.0, seed=31)
+    ref = P.oracle_verify(case, with_table=False)
+    b_off = next(b for b in range(1, 8) if not ref["near_tie"][b])
+    walk = set(int(x) for x in ref["accepted_nodes"][b_off] if x >= 0) | {0}
+    internal = set(int(p) for p in case.tree_parent[b_off, 1:])
+    off = min(internal - walk)
+    case.target_logits[b_off, off, 5] = np.nan
+    case.target_logits[0, 0, 9] = np.nan
+    got = P.run_verify_gpu(case, dev, want_child_q=False)
+    assert got["status"][0] == 8 and got["accept_len"][0] == -1
+    assert got["status"][b_off] == 0
+    assert got["accept_len"][b_off] == ref["accept_len"][b_off]
+    assert got["bonus"][b_off] == ref["bonus"][b_off]
+    np.testing.assert_array_equal(got["accepted_nodes"][b_off], ref["accepted_nodes"][b_off])
+    every = P.run_verify_gpu(case, dev, want_child_q=True)
+    assert every["status"][0] == 8 and every["status"][b_off] == 8
 
 
 # ------------------------------------------------------------------------------------------------
