@@ -7,7 +7,9 @@
 // target distribution, which becomes its normalised residual after every rejection (and stays as it
 // is when that residual sums to zero).
 //
-// One kernel, grid (CL, N, B): a thread-block cluster of CL CTAs per (sequence, node).
+// verify_kernel, grid (CL, N, B): a thread-block cluster of CL CTAs per (sequence, node).
+// verify_path_kernel, grid (CL, 1, B), for large problems: one cluster per sequence runs the same
+// per-node step on the nodes its walk reaches, in turn (the root, then each accepted child).
 //   * Each CTA copies its slice of the node's target-logit row (and, for an internal node at T > 0,
 //     of the draft row) into shared memory with bulk async copies, padded with neutral values so
 //     that every thread owns a run of `ch` consecutive elements (a multiple of 4).  Runs are in
