@@ -41,6 +41,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="eagle_vicuna7b")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the configuration's batch (e.g. a smaller case to profile)")
     ap.add_argument("--temperature", type=float, default=1.0)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -54,9 +56,9 @@ def parse_args(argv=None):
 # ------------------------------------------------------------------------------------------------
 # workload and algorithmic bytes
 # ------------------------------------------------------------------------------------------------
-def make_inputs(cfg_name, T, seed):
+def make_inputs(cfg_name, T, seed, batch=None):
     from speculative_decoding_token_spec_gb300 import workloads as W
-    cfg = W.config(cfg_name)
+    cfg = W.config(cfg_name) if batch is None else W.config(cfg_name, B=batch)
     ac = W.make_attention_case(cfg, seed=seed)
     vc = W.make_verify_case(cfg, T, seed=seed)
     return cfg, ac, vc
@@ -252,7 +254,7 @@ def run_ours(args):
             import torch.distributed as dist
             dist.barrier()
 
-    cfg, ac, vc = make_inputs(args.config, args.temperature, args.seed)
+    cfg, ac, vc = make_inputs(args.config, args.temperature, args.seed, args.batch)
     B, N, Hq, Hkv, D = ac.shape
     V = vc.target_logits.shape[2]
     T = args.temperature

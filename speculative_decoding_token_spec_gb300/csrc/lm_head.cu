@@ -15,15 +15,50 @@
 // in the (then idle) stage memory.  lm_head_combine_kernel merges the tiles of each row.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace spectree {
 
-bool encode_bf16_2d(CUtensorMap* m, const void* ptr, long long inner, long long rows,
-                    int box_inner, int box_rows);
-
 namespace {
+
+extern "C" typedef CUresult (*PFN_encodeTiledLm)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
+                                                 void*, const cuuint64_t*, const cuuint64_t*,
+                                                 const cuuint32_t*, const cuuint32_t*,
+                                                 CUtensorMapInterleave, CUtensorMapSwizzle,
+                                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver (looked up once; null if unavailable).
+PFN_encodeTiledLm lm_encode_fn() {
+  static PFN_encodeTiledLm fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiledLm>(p);
+  });
+  return fn;
+}
+
+// A 2-D bf16 tensor map with 128-byte swizzle: `inner` elements per row (a multiple of 8), `rows`
+// rows, boxes of box_inner x box_rows (box_inner * 2 = 128 bytes); zero fill outside.
+bool encode_bf16_2d(CUtensorMap* m, const void* ptr, long long inner, long long rows,
+                    int box_inner, int box_rows) {
+  PFN_encodeTiledLm fn = lm_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 constexpr int kLM = 128;                        // rows per tile (the MMA's M)
 constexpr int kLN = 256;                        // vocabulary entries per tile at most (MMA N)

@@ -773,21 +773,6 @@ static PFN_encodeTiled encode_fn() {
   return fn;
 }
 
-// A 2-D bf16 tensor map with 128-byte swizzle: `inner` elements per row (a multiple of 8), `rows`
-// rows, boxes of box_inner x box_rows (box_inner * 2 = 128 bytes); zero fill outside.
-bool encode_bf16_2d(CUtensorMap* m, const void* ptr, long long inner, long long rows,
-                    int box_inner, int box_rows) {
-  PFN_encodeTiled fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
-  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 static bool make_kv_map(CUtensorMap* m, const void* ptr, int D, long long rows, int box_rows) {
   PFN_encodeTiled fn = encode_fn();
   if (!fn) return false;
