@@ -77,7 +77,7 @@ cudaError_t launch_tree_finalize(const void* state, int B, int K, int D, const i
 
 bool filter_supported(int V);  // a row fits the filter kernel's clusters
 cudaError_t launch_filter(const float* in, float* out, int rows, int V, float T, int top_k,
-                          float top_p, cudaStream_t s);
+                          float top_p, int num_sms, cudaStream_t s);
 
 struct AttnArgs {
   const void* q;

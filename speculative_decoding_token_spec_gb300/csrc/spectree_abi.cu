@@ -261,7 +261,9 @@ int spec_tree_verify_filtered(const float* target_logits, const float* draft_pro
     return SPEC_ERR_WORKSPACE;
   float* filtered = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_filter(target_logits, filtered, B * N, V, temperature, top_k, top_p, s) !=
+  const int sms = sm_count();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  if (launch_filter(target_logits, filtered, B * N, V, temperature, top_k, top_p, sms, s) !=
       cudaSuccess)
     return SPEC_ERR_CUDA;
   return spec_tree_verify(filtered, draft_probs, tree_tokens, tree_parent, uniforms, temperature,

@@ -106,6 +106,18 @@ def test_llama3_8b_gqa_vocab_128k(dev):
     _check(W.make_verify_case(cfg, 0.7, seed=5, sigma_d=0.3), dev, 40, 0.95, want_child_q=False)
 
 
+@pytest.mark.parametrize("B,N,V", [
+    (3, 60, 12000),   # 180 rows of two 8192-element slices: one CTA per row, 32 per thread
+    (1, 60, 50000),   # 60 rows of seven slices: four CTAs per row, 32 per thread
+    (1, 30, 50000),   # 30 rows: one wave of eight CTAs per row, 16 per thread
+])
+def test_row_count_picks_the_cluster_shape(dev, B, N, V):
+    """Many rows take half the CTAs per row with twice the elements per thread; the kept sets and
+    the verification are the oracle's either way."""
+    cfg = W.config("eagle_vicuna7b", B=B, N=N, V=V, depth=min(6, N - 1))
+    _check(W.make_verify_case(cfg, 1.0, seed=V + N, sigma_d=0.3), dev, 40, 0.9)
+
+
 def test_batched_sequences(dev):
     cfg = W.config("eagle_vicuna7b", B=24, V=4000)
     _check(W.make_verify_case(cfg, 1.0, seed=8, sigma_d=0.4), dev, 30, 0.85,
