@@ -586,8 +586,12 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   float* stage_o = reinterpret_cast<float*>(stage_ml + 256);
   const float m_own = ok_rows ? (l > 0.f ? m_used : -INFINITY) : NAN;
   const float l_own = (ok_rows && l > 0.f) ? l : 0.f;
-  cluster_arrive_release();  // every CTA of the cluster is done with its ring (TMA copies drained)
-  cluster_wait_acquire();    // and its MMAs
+  // Split barrier: this CTA's ring is free for the peers' pushes once every thread arrived (TMA
+  // copies drained, MMAs complete); the in-CTA merge below only touches this CTA's own memory, so
+  // it runs while the slower CTAs arrive, and each thread waits just before its first remote store.
+  cluster_arrive_release();
+  __syncthreads();  // this CTA: the producer drained its copies and the MMAs completed
+  if (warp < 2) cluster_wait_acquire();
   if (warp >= 2) {
     const uint32_t lane_tm = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const int owner = qloc % S, ql = qloc / S;
@@ -645,6 +649,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
           Lsum = fmaf(w[g2][k2], st[g2][k2].y, Lsum);
         }
       const bool has = !tmo && Lsum > 0.f;
+      cluster_wait_acquire();  // every CTA's ring is free: the pushes may start
       if (live && gi == 0 && ks == 0) push_ml(tmo, has, M, Lsum);
       const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
       const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE + my_c, owner);
@@ -676,6 +681,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       const float w1 = s1.y > 0.f ? ex2_approx(s1.x - M) : 0.f;
       const float Lsum = s0.y * w0 + s1.y * w1;
       const bool has = !tmo && Lsum > 0.f;
+      cluster_wait_acquire();  // every CTA's ring is free: the pushes may start
       if (live && ks == 0) push_ml(tmo, has, M, Lsum);
       const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
       const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE, owner);
