@@ -234,6 +234,20 @@ def dist_env():
     return ws, rank, local
 
 
+def combine_ranks(total_ms, units, device):
+    """The job's aggregate over ranks: the longest timed region (max) and the units every rank
+    processed (sum).  Identity without an initialised process group of more than one rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(total_ms), float(units)
+    import torch
+    t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(u)
+    return float(t.item()), float(u.item())
+
+
 # ------------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------------
@@ -374,15 +388,7 @@ def run_ours(args):
                 "the rotated copies (back-to-back launches of that kernel)")
 
     # max over ranks, sum of units
-    units = B * N * K
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        u = torch.tensor([float(units)], device=dev)
-        dist.all_reduce(u)
-        units = float(u.item())
+    total_ms, units = combine_ranks(total_ms, B * N * K, dev)
     value = units / (total_ms / 1e3)
     ms_per_step = total_ms / K
 
@@ -421,14 +427,7 @@ def run_ours(args):
         e1.record()
         torch.cuda.synchronize()
         barrier()
-        e_ms = e0.elapsed_time(e1)
-        e_units = B * N * K2
-        if ws > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-            e_units *= ws
+        e_ms, e_units = combine_ranks(e0.elapsed_time(e1), B * N * K2, dev)
         e2e = {"value": e_units / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": K2,
                "note": "pinned host inputs copied in, C-ABI calls, results copied out, per step"}
