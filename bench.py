@@ -167,8 +167,8 @@ def cpu_oracle_child(spec):
     from oracle import attention as OA
     from oracle import verify as OV
     from speculative_decoding_token_spec_gb300 import workloads as W
-    cfg_name, T, seed, steps, budget = spec.split(":")
-    T, seed, steps, budget = float(T), int(seed), int(steps), float(budget)
+    cfg_name, T, seed, steps, budget, threads = spec.split(":")
+    T, seed, steps, budget, threads = float(T), int(seed), int(steps), float(budget), int(threads)
     cfg, ac, vc = make_inputs(cfg_name, T, seed)
     B, N = ac.q.shape[:2]
     q = W.bf16_to_f64(ac.q)
@@ -197,15 +197,17 @@ def cpu_oracle_child(spec):
         one(sample)
     dt = time.perf_counter() - t0
     print(json.dumps({"value": n_nodes * steps / dt, "steps": steps, "nodes_per_step": n_nodes,
-                      "seconds": dt, "cores": 1,
+                      "seconds": dt, "cores": threads,
                       "sample": f"{steps} oracle step(s) of {cfg_name}: attention for {n_nodes} of "
                                 f"{B * N} nodes (all heads) + full-tree verification at T={T}"}))
 
 
-def run_cpu_oracle(cfg_name, T, seed, steps, budget):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+def run_cpu_oracle(cfg_name, T, seed, steps, budget, threads=1):
+    """The oracle in a child process whose BLAS / OpenMP pools hold `threads` threads."""
+    n = str(int(threads))
+    env = dict(os.environ, OMP_NUM_THREADS=n, OPENBLAS_NUM_THREADS=n, MKL_NUM_THREADS=n,
                CUDA_VISIBLE_DEVICES="")
-    spec = f"{cfg_name}:{T}:{seed}:{steps}:{budget}"
+    spec = f"{cfg_name}:{T}:{seed}:{steps}:{budget}:{n}"
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", spec],
                        capture_output=True, text=True, env=env, timeout=3600)
     if r.returncode != 0:
@@ -446,6 +448,20 @@ def run_ours(args):
         except Exception as exc:  # pragma: no cover
             cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"failed: {exc}"}
+    # the same oracle with every host core in its BLAS / OpenMP pools (a shorter sample)
+    cpu_all = None
+    if not args.no_cpu_baseline and ws == 1:
+        ncores = (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                  else (os.cpu_count() or 1))
+        if ncores > 1:
+            try:
+                r = run_cpu_oracle(args.config, T, args.seed, steps=50, budget=10.0,
+                                   threads=ncores)
+                cpu_all = {"value": r["value"], "unit": UNIT, "cores": r["cores"],
+                           "kind": "oracle", "sample": r["sample"]}
+            except Exception as exc:  # pragma: no cover
+                cpu_all = {"value": None, "unit": UNIT, "cores": ncores, "kind": "oracle",
+                           "sample": f"failed: {exc}"}
 
     attn_gbs = attn_bytes / (attn_ms * 1e-3) / 1e9
     ver_gbs = verify_bytes / (ver_ms * 1e-3) / 1e9
@@ -496,6 +512,7 @@ def run_ours(args):
         "gpu_launches": launches_per_step * K,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "next_rows": nxt,
     }
     print(json.dumps(line))
