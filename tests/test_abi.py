@@ -229,3 +229,31 @@ def test_greedy_verify_arguments(lib):
                                            null)
     assert call(am=null) == -1 and call(out=null) == -1
     assert call(B=0) == -1 and call(N=0) == -1 and call(N=65) == -1 and call(V=0) == -1
+
+
+def test_header_is_plain_c_and_a_c_program_links(lib, tmp_path):
+    """The boundary is a C ABI: the header compiles as strict C99 (no CUDA or C++ types), and a C
+    program built against it links to libspectree.so and calls it (entries that touch no GPU)."""
+    import subprocess
+    from speculative_decoding_token_spec_gb300 import _binding
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    so = _binding.lib_path()
+    src = tmp_path / "use_spectree.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "spectree.h"\n'
+        "int main(void) {\n"
+        "  printf(\"%s\\n\", spec_status_string(SPEC_ST_BAD_TREE));\n"
+        "  return spec_tree_verify_workspace(1, 65, 10) == 0 ? 0 : 1;  /* N > 64: invalid */\n"
+        "}\n")
+    exe = tmp_path / "use_spectree"
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.dirname(HEADER), str(src), "-o", str(exe), so,
+                        "-Wl,-rpath," + os.path.dirname(so)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True,
+                         env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert run.returncode == 0, run.stderr
+    assert "bad tree" in run.stdout
