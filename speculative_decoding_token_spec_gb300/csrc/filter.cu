@@ -44,8 +44,6 @@ constexpr int kRank = 256;        // candidates a selection ranks directly (else
 
 typedef unsigned long long u64;
 
-constexpr u64 kBig = 1ull << 62;  // above every mass total (< 2^59)
-
 __device__ __forceinline__ uint32_t order_key(float x) {  // larger float <-> larger key
   uint32_t u = __float_as_uint(x);
   if (u == 0x80000000u) u = 0u;  // -0 and +0 are equal logits: one key
