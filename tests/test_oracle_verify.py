@@ -14,6 +14,10 @@ What pins what:
 * residual                           -> sums to 1, non-negative, beta = 1 - sum min(p, q)
 * inverse CDF                        -> exact boundaries on rational weights, fallback rule
 * T -> 0                             -> sampling at tiny T equals greedy on untied rows
+* near-tie margins (decision_margin, -> hand-derived rationals, and the defining property: moving
+  the CDF gap of inverse_cdf, a walk's   a decision's uniform by less than its margin keeps the
+  min_margin)                             outcome, by slightly more towards the boundary changes it
+                                        (per test, per draw, and for a whole walk's minimum)
 """
 import itertools
 from fractions import Fraction as F
@@ -386,3 +390,160 @@ def test_monte_carlo_chain_acceptance_fp64():
     mean = tot / n
     # variance of the accept length is at most K^2 / 4
     assert abs(mean - closed) < 4 * (K / 2) / np.sqrt(n)
+
+
+# ----------------------------------------------------------------------------------------------
+# near-tie accounting: the margins that decide which sequences the GPU comparison skips
+# ----------------------------------------------------------------------------------------------
+# The accept test of a child is r * p < q (survey explainer, Formal Definition, 検証フェーズ:
+# r < min(1, q / p)); the bonus is y = min{y : C(y) > u S}.  A decision's margin is how far its
+# uniform may move before the decision changes: |r - q / p| for a test (q itself when p = 0, where
+# no r changes it), and the distance of u from the nearer CDF boundary of y, in units of S, for
+# the draw.  The pins below use hand-derived rationals and the defining property (a move smaller
+# than the margin keeps the outcome, a slightly larger one towards the boundary changes it).
+EPS = F(1, 2**40)
+
+
+def _accept(r, qx, px):
+    return r * px < qx
+
+
+def test_decision_margin_hand_values():
+    assert OV.decision_margin(F(1, 2), F(3, 10), F(1, 2)) == F(1, 10)     # q/p = 3/5
+    assert OV.decision_margin(F(9, 10), F(1, 5), F(1, 10)) == F(11, 10)   # q/p = 2 (> 1)
+    assert OV.decision_margin(F(1, 4), F(1, 8), F(1, 2)) == F(0)          # on the boundary
+    assert OV.decision_margin(F(1, 3), F(3, 7), F(0)) == F(3, 7)          # p = 0: q
+    assert OV.decision_margin(F(1, 3), F(0), F(0)) == F(0)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_decision_margin_is_the_flip_distance(seed):
+    rng = np.random.default_rng(seed)
+    for _ in range(200):
+        r = F(int(rng.integers(0, 2**24)), 2**24)
+        px = F(int(rng.integers(1, 1000)), 1000)
+        qx = F(int(rng.integers(0, 1000)), 1000)
+        m = OV.decision_margin(r, qx, px)
+        d = _accept(r, qx, px)
+        assert m >= 0
+        for s in (1, -1):                      # a smaller move keeps the decision
+            assert _accept(r + s * m * (1 - EPS), qx, px) == d
+        if m > 0:                              # a slightly larger move towards q/p flips it
+            toward = 1 if qx / px > r else -1
+            assert _accept(r + toward * m * (1 + EPS), qx, px) != d
+        # p = 0: no r changes the decision; q moved by its margin (to 0) does
+        assert _accept(r, qx, F(0)) == (qx > 0)
+        assert _accept(r, qx - OV.decision_margin(r, qx, F(0)), F(0)) is False
+
+
+def test_inverse_cdf_gap_hand_values():
+    w = np.array([F(1), F(2), F(3), F(4)], dtype=object)       # S = 10, C = 1, 3, 6, 10
+    assert OV.inverse_cdf(w, F(7, 20)) == (2, F(1, 20))         # uS = 7/2: lower 3, upper 6
+    assert OV.inverse_cdf(w, F(1, 20)) == (0, F(1, 20))         # uS = 1/2: lower 0, upper 1
+    assert OV.inverse_cdf(w, F(1, 2)) == (2, F(1, 10))          # uS = 5: 1 below C(2) = 6
+    assert OV.inverse_cdf(w, F(3, 10)) == (2, F(0))             # uS = C(1): y = 2, on the boundary
+    z = np.array([F(1), F(0), F(3)], dtype=object)              # zero weight: C = 1, 1, 4
+    assert OV.inverse_cdf(z, F(1, 2)) == (2, F(1, 4))           # uS = 2: lower C(1) = 1, S = 4
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_inverse_cdf_gap_is_the_flip_distance(seed):
+    rng = np.random.default_rng(100 + seed)
+    for _ in range(200):
+        V = int(rng.integers(2, 9))
+        w = np.array([F(int(x)) for x in rng.integers(1, 50, size=V)], dtype=object)
+        S = w.sum()
+        u = F(int(rng.integers(0, 2**24)), 2**24)
+        y, gap = OV.inverse_cdf(w, u)
+        assert gap >= 0
+        for s in (1, -1):
+            v = u + s * gap * (1 - EPS)
+            if 0 <= v < 1:
+                assert OV.inverse_cdf(w, v)[0] == y
+        C = np.cumsum(w)
+        lower = C[y - 1] if y > 0 else F(0)
+        # the nearer boundary; its crossing changes y unless it is the total (u -> 1)
+        if u * S - lower <= C[y] - u * S:
+            if gap > 0 and y > 0:
+                assert OV.inverse_cdf(w, u - gap * (1 + EPS))[0] == y - 1
+        elif C[y] < S:
+            assert OV.inverse_cdf(w, u + gap * (1 + EPS))[0] == y + 1
+
+
+def _outcome(tokens, parent, unif, q_of, p_of):
+    res = OV.verify_walk(tokens, parent, unif, q_of, p_of)
+    return tuple(res["path"]), res["bonus"], res
+
+
+@pytest.mark.parametrize("name", sorted(TREES))
+@pytest.mark.parametrize("seed", range(3))
+def test_walk_min_margin_is_smallest_flip_of_any_uniform(name, seed):
+    """min(margins) of a walk: no single uniform moved by less changes the path or the bonus, and
+    some uniform moved by slightly more towards its boundary does.  A test uniform moves over the
+    reals (the test r * p < q is defined there: with q / p > 1 the margin is the distance to a
+    ratio that fp32 rounding could bring below r); the draw's u stays in [0, 1).  The draws avoid
+    p = 0; a draw whose nearer boundary is 0 or the total S is skipped, because no u in [0, 1)
+    crosses it there (the margin is conservative by construction)."""
+    parent = np.array(TREES[name])
+    V = 5
+    rng = np.random.default_rng(7 * seed + len(name))
+    depth = _depth(parent)
+    qtab, ptab = {}, {}
+    for L in range(depth + 1):
+        for s in itertools.product(range(V), repeat=L):
+            qtab[s] = _rand_dist(rng, V)
+            ptab[s] = _rand_dist(rng, V, zeros=False)
+    checked = 0
+    for trial in range(30):
+        tokens = np.array([0] + [int(x) for x in rng.integers(0, V, size=len(parent) - 1)])
+
+        def q_of(j, _t=tokens):
+            return qtab[_path_tokens(parent, _t, j)]
+
+        def p_of(j, _t=tokens):
+            return ptab[_path_tokens(parent, _t, j)]
+
+        unif = [F(int(x), 2**20) for x in rng.integers(0, 2**20, size=len(parent))]
+        path, bonus, res = _outcome(tokens, parent, unif, q_of, p_of)
+        m = min(res["margins"])
+        used = sorted(res["tests"]) + [0]        # the uniforms the walk read
+        for k in used:
+            for s in (1, -1):
+                v = list(unif)
+                v[k] = unif[k] + s * m * (1 - EPS)
+                if k > 0 or 0 <= v[k] < 1:
+                    assert _outcome(tokens, parent, v, q_of, p_of)[:2] == (path, bonus), (k, s)
+        w = res["terminal"]
+        S = w.sum()
+        C = np.cumsum(w)
+        lower, upper = (C[bonus - 1] if bonus else F(0)), C[bonus]
+        near = lower if unif[0] * S - lower <= upper - unif[0] * S else upper
+        if m == 0 or (m == res["margins"][-1] and near in (0, S)):
+            continue          # the draw's nearer boundary is an end of [0, S]: nothing flips
+        flipped = False
+        for k in used:
+            for s in (1, -1):
+                v = list(unif)
+                v[k] = unif[k] + s * m * (1 + EPS)
+                if (k > 0 or 0 <= v[k] < 1) and _outcome(tokens, parent, v, q_of, p_of)[:2] != (path, bonus):
+                    flipped = True
+        assert flipped, (trial, m)
+        checked += 1
+    assert checked >= 10
+
+
+def test_batched_min_margin_and_near_tie_flag():
+    """tree_verify reports the walk's smallest margin per sequence and flags it below 1e-6: a
+    uniform placed 1e-9 from its child's q/p is a near tie, the same draw 0.25 away is not."""
+    V, N = 4, 3
+    parent = np.array([[-1, 0, 0]])
+    logits = np.log(np.array([[[0.4, 0.3, 0.2, 0.1]] * N]))
+    probs = np.array([[[0.1, 0.2, 0.3, 0.4]] * N])
+    tokens = np.array([[0, 3, 1]])
+    q = OV.target_distribution(logits[0, 0], 1.0)
+    ratio = q[3] / probs[0, 0, 3]                               # 0.25
+    for off, near in ((1e-9, True), (0.25, False)):
+        unif = np.array([[0.5, ratio + off, 0.9]])
+        out = OV.tree_verify(logits, probs, tokens, parent, unif, 1.0)
+        assert bool(out["near_tie"][0]) == near
+        assert out["min_margin"][0] <= off + 1e-12
