@@ -158,10 +158,11 @@ int spec_tree_verify(const float* target_logits, const float* draft_probs,
  * Same arguments, outputs and results as spec_tree_verify, minus the workspace.  The scratch lives
  * in one fixed device array inside the library (SPEC_NOALLOC_MAX_NODES * 40 bytes, 160 KB,
  * held on every GPU that loads the library until the process exits).  Calls with
- * B * N > SPEC_NOALLOC_MAX_NODES return SPEC_ERR_NOALLOC_LIMIT.  The first call on a device looks
- * up the array's device address with that device current; make it before any stream capture.
- * All calls share the array (it keeps the last call's contents, none of which needs to start at
- * zero), so calls whose kernels may overlap on the GPU race: serialise them on one stream.
+ * B * N > SPEC_NOALLOC_MAX_NODES return SPEC_ERR_NOALLOC_LIMIT.  Every call made outside stream
+ * capture looks up the array's device address with the caller's device current; a call made while
+ * its stream is being captured reuses the last such address, so make one call on the device before
+ * capturing.  All calls share the array (it keeps the last call's contents, none of which needs to
+ * start at zero), so calls whose kernels may overlap on the GPU race: serialise them on one stream.
  * Allocates nothing (no cudaMalloc / cudaFree / allocating library call).
  */
 #define SPEC_NOALLOC_MAX_NODES 4096
@@ -390,6 +391,22 @@ int spec_kv_compact_paged(void* k_pages, void* v_pages, const int32_t* block_tab
                           const int32_t* accept_len, const int32_t* accepted_nodes,
                           int32_t* new_prefix_lens, int B, int N, int Hkv, int D,
                           int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * Debugging: the timeout path of the verification kernels
+ * ------------------------------------------------------------------------------------------------
+ * The pages have no counterpart; this exists so that tests can make a bounded device-side wait run
+ * out without hanging or faulting a GPU.  Every bounded wait of the verification kernels (the row
+ * copies into shared memory and the cluster exchanges of spec_tree_verify, and so of
+ * spec_tree_verify_noalloc and spec_tree_verify_filtered) first polls at most `polls` times; a wait
+ * that gives up there sets SPEC_ST_TIMEOUT for its sequence (whose outputs become -1) and then
+ * waits for the copies and stores still in flight with the normal limit, so that nothing is left
+ * in flight and the results of later calls are unaffected.  polls = 0 makes every such wait give up
+ * at once; a negative value restores the normal limit (the default).  The setting is process-wide
+ * and is read when a call is made: calls made before it keep theirs, a captured CUDA graph keeps
+ * the value of its capture.  Always returns SPEC_OK.
+ */
+int spec_debug_set_verify_wait_polls(long long polls);
 
 /* Human-readable text for a spec_err_t return value or a SPEC_ST_* bit. */
 const char* spec_status_string(int code);

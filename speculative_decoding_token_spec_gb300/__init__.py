@@ -37,7 +37,9 @@ from ._binding import (  # noqa: F401
     spec_tree_verify_filtered,
     spec_tree_verify_filtered_workspace,
     spec_tree_verify_greedy,
+    spec_tree_verify_noalloc,
     spec_tree_verify_workspace,
     spec_status_string,
+    spec_debug_set_verify_wait_polls,
     lib,
 )

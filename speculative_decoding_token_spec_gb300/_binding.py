@@ -60,6 +60,7 @@ _SIGNATURES = {
                                   + [_c_size, _vp, _vp]),
     "spec_tree_verify_greedy": (_c_int, [_vp] * 3 + [_c_int] * 3 + [_vp] * 6),
     "spec_status_string": (ctypes.c_char_p, [_c_int]),
+    "spec_debug_set_verify_wait_polls": (_c_int, [ctypes.c_longlong]),
 }
 
 
@@ -354,14 +355,28 @@ def spec_tree_verify_filtered(target_logits, draft_probs, tree_tokens, tree_pare
 # verification without a workspace argument
 # ----------------------------------------------------------------------------------------------
 _NOALLOC_ARGS = [_vp] * 5 + [_c_float] + [_c_int] * 3 + [_vp] * 5 + [_vp, _vp]
-NOALLOC_MAX_NODES = 4096
+
+
+def _header_define(name: str) -> int:
+    """An integer #define of the C header (one source of truth for the library's limits)."""
+    import re
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                        "spectree.h")
+    with open(path) as f:
+        m = re.search(r"^#define\s+" + name + r"\s+(\d+)", f.read(), flags=re.M)
+    if m is None:
+        raise RuntimeError(f"{name} not found in {path}")
+    return int(m.group(1))
+
+
+NOALLOC_MAX_NODES = _header_define("SPEC_NOALLOC_MAX_NODES")
 
 
 def spec_tree_verify_noalloc(target_logits, draft_probs, tree_tokens, tree_parent, uniforms,
                              temperature, outputs=None, status=None, stream=None):
     """spec_tree_verify for callers that cannot provide device scratch memory.
 
-    The library keeps the scratch in a fixed device array (B * N <= 4096 nodes per call), so
+    The library keeps the scratch in a fixed device array (B * N <= NOALLOC_MAX_NODES per call), so
     this path allocates nothing on the device besides outputs the caller did not pass.  Calls must
     not overlap on the GPU: they share that array.
     """
@@ -389,6 +404,12 @@ def spec_tree_verify_noalloc(target_logits, draft_probs, tree_tokens, tree_paren
     if rc != SPEC_OK:
         raise SpecError("spec_tree_verify_noalloc", rc)
     return o
+
+
+def spec_debug_set_verify_wait_polls(polls: int) -> None:
+    """Debugging: the first-attempt poll limit of the verification kernels' bounded waits (0 makes
+    every such wait give up at once and flag SPEC_ST_TIMEOUT; negative restores the default)."""
+    lib().spec_debug_set_verify_wait_polls(int(polls))
 
 
 # ----------------------------------------------------------------------------------------------

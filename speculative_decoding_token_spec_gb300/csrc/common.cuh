@@ -59,17 +59,19 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of the barrier; false if it did not complete within kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
+// Wait for phase `parity` of the barrier; false if it did not complete within `polls` polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint32_t polls = kSpinLimit) {
+  for (uint32_t i = 0; i < polls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
 
 // Wait with cluster-scope acquire (data delivered by other CTAs of the cluster, e.g. st.async
-// completing on this barrier); false if it did not complete within kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait_acq_cluster(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+// completing on this barrier); false if it did not complete within `polls` polls.
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint32_t bar, uint32_t parity,
+                                                      uint32_t polls = kSpinLimit) {
+  for (uint32_t i = 0; i < polls; ++i) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"

@@ -758,6 +758,7 @@ __global__ void __launch_bounds__(kFThreads, 2) filter_kernel(const float* __res
 template <int CL, int E>
 cudaError_t launch_fk(const float* in, float* out, int rows, int V, float k2, int top_k,
                       float top_p, cudaStream_t s) {
+  static_assert(CL >= 1 && CL <= 8, "clusters stay within the portable size");
   const size_t smem = (size_t)E * kFThreads * (sizeof(float) + (E == 16 ? 1 : 0));
   if (smem + sizeof(FilterSmem) > 48 * 1024) {  // above the default limit: opt in
     const cudaError_t e = cudaFuncSetAttribute(

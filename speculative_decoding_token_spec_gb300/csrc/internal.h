@@ -35,10 +35,15 @@ struct VerifyArgs {
   float* child_q;
   int32_t* status;
   NodeStat* stats;  // [B, N]
-  unsigned long long* counters;  // [B] arrival counters: (call generation << 16) | arrivals
-  unsigned long long gen;        // this call's generation (48 bits)
+  unsigned long long* counters;  // [B] arrival counters: (generation << 32) | (tag << 16) | arrivals
+  unsigned long long gen;        // this call's generation (32 bits)
   int p_global = 0;  // set by launch_verify: draft rows read from global memory, not staged
+  // polls of the first attempt of each bounded wait (row copies, cluster exchanges); a wait that
+  // gives up flags SPEC_ST_TIMEOUT and then drains with the full limit.  Normally the full limit;
+  // lowered only through spec_debug_set_verify_wait_polls (tests of the timeout path).
+  uint32_t first_polls = 0;
 };
+uint32_t verify_first_polls();  // the current first-attempt limit (spectree_abi.cu)
 
 size_t verify_workspace_bytes(int B, int N, int V);
 bool verify_supported(int V);  // the row slices of a cluster fit in shared memory

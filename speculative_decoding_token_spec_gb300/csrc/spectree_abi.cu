@@ -31,6 +31,9 @@ int sm_count() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// First-attempt polls of the verification kernels' bounded waits (spec_debug_set_verify_wait_polls).
+std::atomic<uint32_t> g_verify_first_polls{kSpinLimit};
+
 // Argument checks shared by the verification entry points (everything but the workspace).
 int verify_check(const float* target_logits, const float* draft_probs, const int32_t* tree_tokens,
                  const int32_t* tree_parent, const float* uniforms, float temperature, int B,
@@ -226,7 +229,8 @@ int spec_tree_verify(const float* target_logits, const float* draft_probs,
   a.stats = reinterpret_cast<NodeStat*>(ws);
   a.counters = reinterpret_cast<unsigned long long*>(ws + (size_t)B * N * sizeof(NodeStat));
   static std::atomic<unsigned long long> call_gen{1};
-  a.gen = call_gen.fetch_add(1) & 0xFFFFFFFFFFFFull;
+  a.gen = call_gen.fetch_add(1) & 0xFFFFFFFFull;
+  a.first_polls = g_verify_first_polls.load(std::memory_order_relaxed);
   cudaError_t e = launch_verify(a, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -390,6 +394,12 @@ int spec_tree_verify_greedy(const int32_t* node_argmax, const int32_t* tree_toke
                               static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SPEC_OK
              : SPEC_ERR_CUDA;
+}
+
+int spec_debug_set_verify_wait_polls(long long polls) {
+  const uint32_t v = polls < 0 || polls > (long long)kSpinLimit ? kSpinLimit : (uint32_t)polls;
+  g_verify_first_polls.store(v, std::memory_order_relaxed);
+  return SPEC_OK;
 }
 
 const char* spec_status_string(int code) {

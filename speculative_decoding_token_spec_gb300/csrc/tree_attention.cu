@@ -11,28 +11,34 @@
 // thread-block cluster and combine their partial results on chip at the end.
 //
 // Key groups.  A tcgen05 MMA always computes 128 rows.  When R <= 64 (multi-head attention over a
-// tree of up to 64 nodes) MMA rows 64..127 repeat query rows 0..63 and are paired with the next
-// 64-key tile: each pipeline step covers two tiles, every TMEM lane quadrant (and so every SM
+// tree of up to 64 nodes) MMA rows 64..127 repeat query rows 0..63: rows 0..63 take keys 0..63 of
+// every 128-key chunk and rows 64..127 keys 64..127, so every TMEM lane quadrant (and so every SM
 // sub-partition) does softmax work, and rows r and r + 64 end with partial results over disjoint
 // key sets that the final combine merges like two more splits.
 //
-// Warp roles (192 threads):
-//   warp 0       TMA producer: K/V tiles of 64 keys into a ring of 192 KB (6 tiles at D = 128),
-//                128-byte swizzled boxes; a split's first tiles are requested right at launch;
-//   warp 1       allocates TMEM; one lane issues the MMAs as soon as their inputs are ready:
-//                  S = Q K_t^T   (M = 128, N = 64 keys, K = D; Q and K from shared memory)
-//                  O += P_t V_t  (M = 128, N = D, K = 64 keys; P from TMEM, V from shared memory)
+// Warp roles (320 threads, one CTA per SM):
+//   warp 0       TMA producer: K/V chunks of 128 keys into a 3-slot ring (192 KB at D = 128: one
+//                chunk's K and V per slot), 128-byte swizzled boxes; a split's first chunks are
+//                requested right after the set-up barrier, before the prefix length is known;
+//   warp 1       allocates 512 TMEM columns; one lane issues the MMAs as soon as their inputs are
+//                ready (a non-blocking state machine over the mbarriers):
+//                  S = Q K_c^T   (M = 128, N = 128 keys, K = D; Q and K from shared memory)
+//                  O += P_c V_c  (M = 128, N = D, K = 128 keys; P from TMEM, V from shared memory)
 //                with completions signalled by tcgen05.commit on mbarriers;
-//   warps 2..5   softmax, one MMA row (= TMEM lane) per thread: mask with the node's visibility
-//                bits (prefix, then the ancestors' tree slots), online softmax in the log2
-//                domain, P as bf16 pairs into TMEM for the PV MMA.  The reference max is only
-//                raised when a tile's max exceeds it by more than 8 (2^8 headroom in fp32); only
-//                then is the O row in TMEM rescaled.
-// Combine.  With key groups, rows r and r + 64 first merge inside the CTA (each thread of the pair
-// takes half of the columns).  Each row's unnormalised O, max m and sum l then go into the
-// shared memory of the cluster CTA that owns the row (row % splits) through distributed-shared-
-// memory stores; the owner weights the S partials by 2^(m - M) / sum(l 2^(m - M)) and writes the
-// bf16 output and the log-sum-exp.
+//   warps 2..9   softmax, one MMA row (= TMEM lane) per thread and two warps per lane quadrant:
+//                key set 0 (warps 2..5) takes the first 32 keys of each 64-key half of a chunk,
+//                key set 1 (warps 6..9) the second 32, each with its own running max, sum and O
+//                accumulator in TMEM (O[0] at column 256, O[1] at 384), so the two warps of a row
+//                never exchange anything in the main loop.  Mask from the node's visibility bits
+//                (prefix, then the ancestors' tree slots), online softmax in the log2 domain, P as
+//                bf16 pairs written over the scores it came from.  The reference max is only raised
+//                when a chunk's max exceeds it by more than 8 (2^8 headroom in fp32); only then is
+//                that key set's O in TMEM rescaled.
+// Combine.  A query's partials inside the CTA (2 key sets, and with key groups the rows r and
+// r + 64) merge with one named barrier; each merged row's unnormalised O, max m and sum l then go
+// into the shared memory of the cluster CTA that owns the row (row % splits) through
+// distributed-shared-memory stores; the owner weights the S partials by 2^(m - M) / sum(l 2^(m - M))
+// and writes the bf16 output and the log-sum-exp.
 #include <cuda.h>
 
 #include <mutex>
@@ -888,6 +894,8 @@ bool attn_plan(int B, int N, int Hq, int Hkv, int D, int Lmax, int num_sms, Attn
 template <int D, bool PAGED>
 static cudaError_t launch_d(const CUtensorMap& mk, const CUtensorMap& mv, const AttnKParams& kp,
                             cudaStream_t s) {
+  // the combine's receive area and owned-row split assume the portable cluster size at most
+  if (kp.splits < 1 || kp.splits > kMaxSplits) return cudaErrorInvalidConfiguration;
   cudaError_t e = prepare_kernel<D, PAGED>();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];

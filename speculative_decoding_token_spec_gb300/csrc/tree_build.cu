@@ -570,6 +570,7 @@ template <int CL, int E>
 cudaError_t launch_expand_cluster(const float* logits, int B, int R, int V, int K, int D, int level,
                                   void* state, int32_t* ftok, int32_t* fslot, int32_t* status,
                                   cudaStream_t s) {
+  static_assert(CL >= 1 && CL <= 8, "clusters stay within the portable size");
   const size_t lists = (size_t)K * kBThreads * (sizeof(float) + sizeof(int));
   if (lists > 48 * 1024 - 24 * 1024) {  // with the static part above the default: opt in
     const cudaError_t e = cudaFuncSetAttribute(

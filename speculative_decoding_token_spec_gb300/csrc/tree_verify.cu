@@ -36,9 +36,12 @@
 // sum is a compensated fp32 sum per thread and a double-float (pair of fp32) sum across threads and
 // CTAs.  No fp64 arithmetic: this part's fp64 pipe is narrow (a dependent operation costs 64
 // cycles, a division about 1 us) and shared by every CTA on the SM.
-// The accept decisions compare double-floats (relative error about 2^-44): n(x) starts as
-// exp((l_x - M)/T) with the argument formed exactly as a double-float, and after a rejection
-// n <- max(0, n - p(x) D), D <- D_k.
+// The accept decisions compare double-floats: n(x) starts as exp((l_x - M)/T) with the argument
+// formed exactly as a double-float and exponentiated by expf (a few ulp, about 1e-7 relative), and
+// after a rejection n <- max(0, n - p(x) D), D <- D_k.  The double-float products and sums carry
+// about 2^-44 themselves; expf's error and that of the fp32 element weights (ex2.approx) summed
+// into S and D bound a decision's accuracy at a few 1e-7 relative -- inside the 1e-6 band in which
+// decisions are counted, not compared.
 #include <cooperative_groups.h>
 #include <float.h>
 
@@ -80,6 +83,7 @@ struct VerifySmem {
   int flags;
   int is_last;
   int found;
+  uint32_t first_polls;  // first-attempt polls of the bounded waits (VerifyArgs::first_polls)
   float g_r[kMaxNodes];         // children's test uniforms
   float g_lx[kMaxNodes];        // gathered target logit / draft probability of each child's token
   float g_px[kMaxNodes];
@@ -186,12 +190,14 @@ __device__ __forceinline__ void stage_slice(const float* row, const Slice& s, fl
 }
 
 // Wait for a staged slice (phase `parity` of its barrier: 0 for the barrier's first use in this
-// launch, 1 for its second); returns SPEC_ST_TIMEOUT if the copy did not land in time.
-__device__ __forceinline__ int wait_slice(uint32_t bar, uint32_t parity = 0) {
+// launch, 1 for its second); returns SPEC_ST_TIMEOUT if the copy did not land within `polls`
+// polls, after giving copies still in flight a second wait with the full limit (so that no copy
+// is left in flight when the CTA moves on).
+__device__ __forceinline__ int wait_slice(uint32_t bar, uint32_t parity, uint32_t polls) {
   int st = 0;
-  if (!mbar_wait(bar, parity)) {
+  if (!mbar_wait(bar, parity, polls)) {
     st = SPEC_ST_TIMEOUT;
-    mbar_wait(bar, parity);  // give copies still in flight a second bounded chance
+    mbar_wait(bar, parity);
   }
   __syncthreads();
   return st;
@@ -313,7 +319,10 @@ __device__ Entry exchange(VerifySmem& sm, int& xk, const Entry& mine, int kind, 
       st_async_v4(dst, v[0], rbar);
       st_async_v4(dst + 16, v[1], rbar);
     }
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_acq_cluster(bar, parity));
+    // a first attempt that gives up flags the exchange, then the peers' stores are waited for
+    // with the full limit: no CTA moves on (or exits) with a store into it still in flight
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_acq_cluster(bar, parity, sm.first_polls));
+    if (!ok) mbar_wait_acq_cluster(bar, parity);
     Entry r = lanes_combine<8>(lane < CL ? sm.cpart[slot][lane] : entry_identity(kind), kind, k);
     if (lane == 0) {
       r.flags |= ok ? 0 : SPEC_ST_TIMEOUT;
@@ -672,7 +681,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     sm.g_r[threadIdx.x] = __ldg(a.uniforms + (size_t)b * N + kid);
   }
   const float u_bonus = __ldg(a.uniforms + (size_t)b * N);
-  const int lflags0 = wait_slice(nb.bar_l, ph_l);
+  const int lflags0 = wait_slice(nb.bar_l, ph_l, sm.first_polls);
   ph_l ^= 1u;
   int flags = 0;  // cluster-uniform: only ever updated from published partials
   writer = 0;
@@ -746,7 +755,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     if (!p_waited) {
       // CTA-local: reaches the cluster through the partials
       if (probs_staged) {
-        pflags = wait_slice(nb.bar_p, ph_p);
+        pflags = wait_slice(nb.bar_p, ph_p, sm.first_polls);
         ph_p ^= 1u;
       }
       p_waited = true;
@@ -775,7 +784,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     __syncthreads();
   }
   if (probs_staged && !p_waited) {  // no copy left in flight (not needed)
-    wait_slice(nb.bar_p, ph_p);
+    wait_slice(nb.bar_p, ph_p, kSpinLimit);
     ph_p ^= 1u;
   }
   const bool bad = (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) != 0;
@@ -870,7 +879,8 @@ __device__ void walk_sequence_cluster(const VerifyArgs& a, int b, int rank, cons
     const float* lrow = a.logits + row_off;
     const Slice s = make_slice(lrow, a.V, rank, CL);
     stage_slice(lrow, s, nb.lbuf, nb.bar_l, -INFINITY);
-    const int lflags = wait_slice(nb.bar_l, bar_l_used ? 1 : 0);  // CTA-local: published below
+    // CTA-local: published below
+    const int lflags = wait_slice(nb.bar_l, bar_l_used ? 1 : 0, sm.first_polls);
     if (a.T == 0.f) {
       float gv;
       int gi;
@@ -896,27 +906,45 @@ __device__ void walk_sequence_cluster(const VerifyArgs& a, int b, int rank, cons
 // ------------------------------------------------------------------------------------------------
 // per-sequence arrival counter
 // ------------------------------------------------------------------------------------------------
-// The counter word holds (call generation << 16) | arrivals.  A word carrying another
-// generation (left by another call, or never initialised) is claimed for this call -- reset to
-// (gen, 0) -- by whichever cluster of the sequence starts first, so no zero-filled workspace is
-// needed; every cluster claims before it can arrive, and the last arrival only comes after all of
-// them started.  Arrivals are plain atomic adds; the last one resets the count, which keeps
-// CUDA-graph replays (same generation) correct.
-__device__ __forceinline__ void claim_counter(unsigned long long* ctr, unsigned long long gen) {
-  const unsigned long long g = gen & 0xFFFFFFFFFFFFull;
+// The counter word holds (call generation << 32) | (kCounterTag << 16) | arrivals.  A word whose
+// upper 48 bits are not this call's (generation, tag), or whose count is not below N, is claimed
+// for this call -- set to (generation, tag, 0) -- by whichever cluster of the sequence starts
+// first, so no zero-filled workspace is needed: whatever a caller's buffer held before (another
+// call's node records, a count left by another call, garbage) is reset.  Only a word of this very
+// generation and tag with a count in [0, N) is kept, i.e. one that a cluster of this call already
+// claimed or arrived at.  Every cluster claims before it can arrive, and the last arrival only
+// comes after all of them started.  Arrivals are plain atomic adds; the last one resets the count,
+// which keeps CUDA-graph replays (same generation) correct.
+constexpr unsigned long long kCounterTag = 0x5EC7ull;
+
+__device__ __forceinline__ unsigned long long counter_id(unsigned long long gen) {
+  return ((gen & 0xFFFFFFFFull) << 16) | kCounterTag;  // bits 16..63 of the word
+}
+
+__device__ __forceinline__ bool counter_valid(unsigned long long w, unsigned long long id, int N) {
+  return (w >> 16) == id && (w & 0xFFFFull) < (unsigned long long)N;
+}
+
+__device__ __forceinline__ void claim_counter(unsigned long long* ctr, unsigned long long gen,
+                                              int N) {
+  const unsigned long long id = counter_id(gen);
   unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
-  for (int it = 0; it < 4 && (old >> 16) != g; ++it) old = atomicCAS(ctr, old, g << 16);
+  for (int it = 0; it < 8 && !counter_valid(old, id, N); ++it) {
+    const unsigned long long prev = atomicCAS(ctr, old, id << 16);
+    if (prev == old) break;  // claimed
+    old = prev;              // changed meanwhile: claimed or arrived at by another cluster?
+  }
 }
 
 // Returns true for the last of the N arrivals.  Release: this thread's earlier global writes (the
 // node record) are visible to whoever sees the count; acquire: the last arriver sees every other
 // cluster's record.
 __device__ __forceinline__ bool arrive(unsigned long long* ctr, unsigned long long gen, int N) {
-  const unsigned long long g = gen & 0xFFFFFFFFFFFFull;
+  const unsigned long long id = counter_id(gen);
   unsigned long long old;
   asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
-  if ((old >> 16) == g && (old & 0xFFFFull) + 1 == (unsigned long long)N) {
-    atomicExch(ctr, g << 16);
+  if ((old >> 16) == id && (old & 0xFFFFull) + 1 == (unsigned long long)N) {
+    atomicExch(ctr, id << 16);
     return true;
   }
   return false;
@@ -943,6 +971,7 @@ __global__ void __launch_bounds__(kVThreads)
     mbar_init(smem_u32(&sm.xbar[0]), 1);
     mbar_init(smem_u32(&sm.xbar[1]), 1);
     mbar_fence_init();
+    sm.first_polls = a.first_polls;
   }
   __syncthreads();
   cluster_arrive_release();  // exchange barriers initialised (waited for before the first exchange)
@@ -957,7 +986,7 @@ __global__ void __launch_bounds__(kVThreads)
   }
   // the claim's round trip overlaps the tree loads (issued by the first threads) instead of
   // delaying thread 0, which issues the copies
-  if (rank == 0 && threadIdx.x == kVThreads - 1) claim_counter(a.counters + b, a.gen);
+  if (rank == 0 && threadIdx.x == kVThreads - 1) claim_counter(a.counters + b, a.gen, N);
   const int bad = load_tree(a, b, sm);  // uniform across the cluster: same tree everywhere
   if (bad) {
     if (j == 0 && rank == 0) {  // one writer per sequence
@@ -972,7 +1001,7 @@ __global__ void __launch_bounds__(kVThreads)
         if (a.child_q) a.child_q[(size_t)b * N + i] = -1.f;
       }
     }
-    if (early) wait_slice(nb.bar_l);  // no copy left in flight
+    if (early) wait_slice(nb.bar_l, 0, kSpinLimit);  // no copy left in flight
     cluster_wait_acquire();
     return;
   }
@@ -1036,6 +1065,7 @@ __global__ void __launch_bounds__(kVThreads)
     mbar_init(smem_u32(&sm.xbar[0]), 1);
     mbar_init(smem_u32(&sm.xbar[1]), 1);
     mbar_fence_init();
+    sm.first_polls = a.first_polls;
   }
   __syncthreads();
   cluster_arrive_release();  // exchange barriers initialised (waited for before the first exchange)
@@ -1095,6 +1125,8 @@ size_t verify_workspace_bytes(int B, int N, int V) {
 template <class... Params, class... Args>
 static cudaError_t launch_ex(void (*kern)(Params...), dim3 grid, int cl, size_t smem,
                              cudaStream_t s, Args... args) {
+  // the exchange arrays (VerifySmem::cpart, ccur) and the 8-lane combines hold kMaxCluster ranks
+  if (cl < 1 || cl > kMaxCluster) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kVThreads);

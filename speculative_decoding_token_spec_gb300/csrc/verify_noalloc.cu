@@ -9,13 +9,16 @@
 // Properties of that array:
 //   * Size: room for B * N <= SPEC_NOALLOC_MAX_NODES tree nodes per call (160 KB).  Every
 //     GPU on which the library is loaded holds it until the process exits.
-//   * Set-up: the first call on a device looks up the array's device address (cudaGetSymbolAddress)
-//     with that device current and caches it; make that first call before any stream capture.
+//   * Set-up: every call made outside stream capture looks up the array's device address
+//     (cudaGetSymbolAddress, a host-side lookup) with the caller's device current, so a module
+//     that was reloaded at another address (after cudaDeviceReset, say) is followed.  A call made
+//     while its stream is being captured uses the address of the last uncaptured call on that
+//     device (looking it up if there was none); make one call before capturing.
 //   * Sharing: all calls share the one array and it keeps the previous call's contents.  Nothing in
-//     it has to start at zero: each call writes every statistics entry it reads, and the
-//     per-sequence arrival counters carry the generation of the call that wrote them, so a count
-//     left by an earlier call is ignored.  Calls whose kernels may overlap on the GPU (different
-//     streams, or concurrent host threads) race on it.
+//     it has to start at zero: each call writes every statistics entry it reads, and a
+//     per-sequence arrival counter is trusted only when it carries the generation and tag of the
+//     call itself, so counts and node records left by earlier calls are reset.  Calls whose
+//     kernels may overlap on the GPU (different streams, or concurrent host threads) race on it.
 //   * No allocation: no cudaMalloc, cudaFree or allocating library routine is called.
 #include <cuda_runtime.h>
 
@@ -41,12 +44,16 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {nullptr};
 
-// Device address of the scratch array on the current device (looked up once per device).
-int scratch_on_current_device(void** out) {
+// Device address of the scratch array on the current device: looked up on every call outside
+// stream capture, the last such address reused while `stream` is being captured.
+int scratch_on_current_device(cudaStream_t stream, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  const bool capturing =
+      cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (!capturing || g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_verify_scratch);
     if (e != cudaSuccess || p == nullptr) return SPEC_ERR_CUDA;
@@ -68,7 +75,7 @@ extern "C" int spec_tree_verify_noalloc(const float* target_logits, const float*
   if (B < 1 || N < 1 || N > kMaxNodes) return SPEC_ERR_INVALID_ARG;
   if ((long long)B * N > SPEC_NOALLOC_MAX_NODES) return SPEC_ERR_NOALLOC_LIMIT;
   void* scratch = nullptr;
-  int rc = scratch_on_current_device(&scratch);
+  int rc = scratch_on_current_device(static_cast<cudaStream_t>(stream), &scratch);
   if (rc != SPEC_OK) return rc;
   return spec_tree_verify(target_logits, draft_probs, tree_tokens, tree_parent, uniforms,
                           temperature, B, N, V, out_accept_len, out_accepted_tokens,

@@ -41,6 +41,18 @@ def test_header_declares_the_entry_points():
         assert n in names
 
 
+def test_binding_limits_match_the_header():
+    from speculative_decoding_token_spec_gb300 import _binding
+    text = open(HEADER).read()
+    m = re.search(r"^#define\s+SPEC_NOALLOC_MAX_NODES\s+(\d+)", text, flags=re.M)
+    assert m and _binding.NOALLOC_MAX_NODES == int(m.group(1))
+
+
+def test_debug_wait_polls_setter(lib):
+    assert lib.spec_debug_set_verify_wait_polls(0) == 0
+    assert lib.spec_debug_set_verify_wait_polls(-1) == 0      # back to the default
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libspectree.so does not export {name}"

@@ -67,11 +67,27 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_lib, T):
     _same(again, P.run_verify_gpu(first, dev, want_child_q=True))
 
 
+def test_noalloc_scratch_layout_changes_between_calls(cuda_lib):
+    """B * N shrinks and grows between calls, so each call's arrival counters sit where an earlier
+    call left node records (leaf records among them); then a large problem (more than 64 MiB of
+    logits) with per-child q, the form in which leaves are not processed but still arrive."""
+    import torch
+    dev = torch.device("cuda:0")
+    fn = _noalloc_fn(cuda_lib)
+    cases = [W.make_verify_case(W.config("eagle_vicuna7b", B=B), 1.0, seed=40 + B)
+             for B in (12, 5, 6, 1, 12)]
+    cases.append(W.make_verify_case(W.config("eagle_vicuna7b", B=16), 1.0, seed=41))
+    assert cases[-1].target_logits.nbytes > (64 << 20)
+    for case in cases:
+        _same(_call_noalloc(fn, case, dev), P.run_verify_gpu(case, dev, want_child_q=True))
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
     import torch
     dev = torch.device("cuda:0")
     fn = _noalloc_fn(cuda_lib)
-    limit = 4096
+    from speculative_decoding_token_spec_gb300 import _binding
+    limit = _binding.NOALLOC_MAX_NODES
     B, N, V = limit // 32 + 1, 32, 8   # B * N = 4128 > limit
     z = torch.zeros((B * N * V + 16,), dtype=torch.float32, device=dev)
     i = torch.zeros((B * N + 16,), dtype=torch.int32, device=dev)
