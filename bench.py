@@ -49,6 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next", action="store_true",
                     help="skip the paged-attention and KV-compaction measurements")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (batched GQA, long context, stress sweep, T=0)")
     ap.add_argument("--cpu-child", default=None, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -62,6 +64,14 @@ def make_inputs(cfg_name, T, seed, batch=None):
     ac = W.make_attention_case(cfg, seed=seed)
     vc = W.make_verify_case(cfg, T, seed=seed)
     return cfg, ac, vc
+
+
+def workload_name(cfg, T):
+    """The workload string both arms print: configuration, shapes, prefix, tree, vocabulary, T."""
+    pre = (f"prefix={cfg.prefix[1]}" if cfg.prefix[0] == "fixed"
+           else f"prefix=U[{cfg.prefix[1]},{cfg.prefix[2]}]")
+    return (f"{cfg.name}: B={cfg.B} Hq={cfg.Hq} Hkv={cfg.Hkv} D={cfg.D} {pre} N={cfg.N} "
+            f"V={cfg.V} T={T}")
 
 
 def algorithmic_bytes(cfg, ac, vc):
@@ -167,8 +177,9 @@ def cpu_oracle_child(spec):
     from oracle import attention as OA
     from oracle import verify as OV
     from speculative_decoding_token_spec_gb300 import workloads as W
-    cfg_name, T, seed, steps, budget, threads = spec.split(":")
+    cfg_name, T, seed, steps, budget, threads, fixed = spec.split(":")
     T, seed, steps, budget, threads = float(T), int(seed), int(steps), float(budget), int(threads)
+    fixed = int(fixed)
     cfg, ac, vc = make_inputs(cfg_name, T, seed)
     B, N = ac.q.shape[:2]
     q = W.bf16_to_f64(ac.q)
@@ -190,6 +201,8 @@ def cpu_oracle_child(spec):
     t_node = (time.perf_counter() - t0) / (B * min(N, 4))
     per_step = budget / max(steps, 1)
     n_nodes = int(max(1, min(B * N, (per_step - t_min) / max(t_node, 1e-9) + 1)))
+    if fixed > 0:  # the same sample as another run of this leg
+        n_nodes = min(fixed, B * N)
     all_nodes = [(b, i) for b in range(B) for i in range(N)]
     sample = all_nodes[:n_nodes]
     t0 = time.perf_counter()
@@ -202,12 +215,13 @@ def cpu_oracle_child(spec):
                                 f"{B * N} nodes (all heads) + full-tree verification at T={T}"}))
 
 
-def run_cpu_oracle(cfg_name, T, seed, steps, budget, threads=1):
-    """The oracle in a child process whose BLAS / OpenMP pools hold `threads` threads."""
+def run_cpu_oracle(cfg_name, T, seed, steps, budget, threads=1, n_nodes=0):
+    """The oracle in a child process whose BLAS / OpenMP pools hold `threads` threads; with
+    n_nodes > 0 the sample is that many attention nodes (else sized by the budget)."""
     n = str(int(threads))
     env = dict(os.environ, OMP_NUM_THREADS=n, OPENBLAS_NUM_THREADS=n, MKL_NUM_THREADS=n,
                CUDA_VISIBLE_DEVICES="")
-    spec = f"{cfg_name}:{T}:{seed}:{steps}:{budget}:{n}"
+    spec = f"{cfg_name}:{T}:{seed}:{steps}:{budget}:{n}:{int(n_nodes)}"
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", spec],
                        capture_output=True, text=True, env=env, timeout=3600)
     if r.returncode != 0:
@@ -259,6 +273,10 @@ def run_ours(args):
     import speculative_decoding_token_spec_gb300 as st
 
     ws, rank, local = dist_env()
+    # the other workloads' CPU legs start first (spawned workers), overlapping the GPU work
+    pool, futs = (None, None)
+    if not args.no_configs and ws == 1:
+        pool, futs = start_cpu_legs(args.seed)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if ws > 1:
@@ -382,12 +400,12 @@ def run_ours(args):
 
     total_ms = timed(run_steps)
     # ---- per-call timed regions: the same rotated copies, one kernel kind per graph
-    reps = max(1, K // copies)
+    reps = max(1, -(-300 // copies))  # about 300 calls per region, whatever --steps is
     attn_ms = timed(lambda: [g_attn.replay() for _ in range(reps)]) / (reps * copies)
     ver_ms = timed(lambda: [g_ver.replay() for _ in range(reps)]) / (reps * copies)
     clk = clocks.stop()
-    per_call = ("separate timed regions of the same length, each replaying graphs of one call over "
-                "the rotated copies (back-to-back launches of that kernel)")
+    per_call = (f"separate timed regions of {reps * copies} calls each, replaying graphs of one call "
+                "over the rotated copies (back-to-back launches of that kernel)")
 
     # max over ranks, sum of units
     total_ms, units = combine_ranks(total_ms, B * N * K, dev)
@@ -470,13 +488,18 @@ def run_ours(args):
         return
     nxt = None if args.no_next else measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs,
                                                       attn_ms, timed, dev, L2, tc_tflops)
+    others = None
+    if futs is not None:
+        others = measure_other_workloads(args, dev, futs, hbm_gbs, tc_tflops, timed, L2)
+        pool.shutdown()
     # ---- CPU oracle baseline (bounded sample)
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
         try:
             r = run_cpu_oracle(args.config, T, args.seed, steps=50, budget=20.0)
             cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
-                   "sample": r["sample"], "cpu": cpu_model()}
+                   "sample": r["sample"], "cpu": cpu_model(),
+                   "nodes_per_step": r["nodes_per_step"]}
         except Exception as exc:  # pragma: no cover
             cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"failed: {exc}"}
@@ -487,8 +510,9 @@ def run_ours(args):
                   else (os.cpu_count() or 1))
         if ncores > 1:
             try:
+                n1 = (cpu or {}).get("nodes_per_step") or 0
                 r = run_cpu_oracle(args.config, T, args.seed, steps=50, budget=10.0,
-                                   threads=ncores)
+                                   threads=ncores, n_nodes=n1)
                 cpu_all = {"value": r["value"], "unit": UNIT, "cores": r["cores"],
                            "kind": "oracle", "sample": r["sample"]}
             except Exception as exc:  # pragma: no cover
@@ -517,8 +541,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes of the EAGLE static-tree workload, no datasets)",
-        "config": {"workload": f"{args.config}: B={B} Hq={Hq} Hkv={Hkv} D={D} prefix="
-                               f"{int(ac.prefix_lens[0])} N={N} V={V} T={T}",
+        "config": {"workload": workload_name(cfg, T),
                    "batch": B, "tree_nodes": N, "vocab": V, "temperature": T,
                    "l2": f"inputs rotated over {copies} device copies "
                          f"({copies * per_copy / 2**20:.0f} MiB > 2x L2 {L2 / 2**20:.0f} MiB)",
@@ -546,6 +569,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
         "next_rows": nxt,
+        "configs": others,
     }
     print(json.dumps(line))
 
@@ -803,6 +827,228 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
     }
 
 
+# ------------------------------------------------------------------------------------------------
+# the other workloads: batched GQA, long context, the stress sweep, temperature 0
+# ------------------------------------------------------------------------------------------------
+# (key, configuration, temperature, batch override or None, timed: attention + verification step)
+OTHER_WORKLOADS = (
+    ("eagle_vicuna7b_T0", "eagle_vicuna7b", 0.0, None, True),
+    ("llama3_8b_gqa", "llama3_8b_gqa", 0.7, None, True),
+    ("llama70b_longctx", "llama70b_longctx", 1.0, None, True),
+    ("stress_T1", "stress", 1.0, None, True),
+    ("stress_T0", "stress", 0.0, 16, False),
+    ("stress_T0.5", "stress", 0.5, 16, False),
+    ("stress_T1.5", "stress", 1.5, 16, False),
+)
+
+
+def cpu_leg_workload(spec):
+    """CPU-baseline leg of one of the other workloads (a spawned worker process, one thread):
+    draws the workload's verification inputs and times the fp64 oracle verifying every sequence of
+    them.  Returns the inputs (for the GPU side), the oracle's outputs (for the near-tie count and
+    the agreement check) and the oracle's time."""
+    name, T, seed, batch = spec
+    from oracle import verify as OV
+    from speculative_decoding_token_spec_gb300 import workloads as W
+    cfg = W.config(name) if batch is None else W.config(name, B=batch)
+    vc = W.make_verify_case(cfg, T, seed=seed)
+    t0 = time.perf_counter()
+    ref = OV.tree_verify(vc.target_logits, vc.draft_probs, vc.tree_tokens, vc.tree_parent,
+                         vc.uniforms, T)
+    dt = time.perf_counter() - t0
+    keep = ("accept_len", "accepted_tokens", "bonus", "near_tie", "status")
+    return {"case": vc, "oracle": {k: ref[k] for k in keep}, "oracle_s": dt}
+
+
+def start_cpu_legs(seed):
+    """Starts the other workloads' CPU legs in a spawned pool (no fork after CUDA is up)."""
+    import concurrent.futures
+    import multiprocessing
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 4
+    env1 = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+    old = {k: os.environ.get(k) for k in env1}
+    os.environ.update(env1)  # inherited by the spawned workers
+    try:
+        pool = concurrent.futures.ProcessPoolExecutor(
+            max_workers=max(1, min(len(OTHER_WORKLOADS), cores - 2)),
+            mp_context=multiprocessing.get_context("spawn"))
+        futs = {key: pool.submit(cpu_leg_workload, (name, T, seed, batch))
+                for key, name, T, batch, _ in OTHER_WORKLOADS}
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return pool, futs
+
+
+def acceptance_stats(accept_len, N_depth):
+    """Mean accepted length, emitted tokens per step and the acceptance rate at each depth d
+    (sequences that accepted a depth-d node / sequences whose walk reached depth d - 1)."""
+    import numpy as np
+    a = np.asarray(accept_len)
+    a = a[a >= 0]
+    per_depth = []
+    for d in range(1, N_depth + 1):
+        reached = int((a >= d - 1).sum())
+        per_depth.append(round(float((a >= d).sum()) / reached, 4) if reached else None)
+    return {"mean_accept_len": float(a.mean()) if len(a) else None,
+            "tokens_per_step": float(a.mean() + 1) if len(a) else None,
+            "accept_rate_per_depth": per_depth, "sequences": int(len(a))}
+
+
+def measure_other_workloads(args, dev, futs, hbm_gbs, tc_tflops, timed, L2):
+    """Per workload: attention, verification and step times from CUDA graphs (inputs larger than
+    L2, or rotated over copies that are), the algorithmic bytes and HBM (or tensor) fractions, the
+    verification statistics of the GPU outputs, and the oracle leg's near-tie count, agreement and
+    time."""
+    import numpy as np
+    import torch
+    import speculative_decoding_token_spec_gb300 as st
+    from speculative_decoding_token_spec_gb300 import workloads as W
+    out = {}
+    s = torch.cuda.Stream(device=dev)
+    for key, name, T, batch, timed_step in OTHER_WORKLOADS:
+        leg = futs[key].result()
+        vc = leg["case"]
+        cfg = W.config(name) if batch is None else W.config(name, B=batch)
+        B, N, V = vc.target_logits.shape
+        lens, par, Lmax = W.attention_layout(cfg, args.seed)
+        assert np.array_equal(par, vc.tree_parent)
+        Hq, Hkv, D = cfg.Hq, cfg.Hkv, cfg.D
+        to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        ver_bytes_per_copy = vc.target_logits.nbytes + (vc.draft_probs.nbytes if T > 0 else 0)
+        kv_bytes = 2 * B * Hkv * Lmax * D * 2 if timed_step else 0
+        per_copy = ver_bytes_per_copy + kv_bytes
+        copies = max(1, min(9, math.ceil(2 * L2 / per_copy)))
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1000 + args.seed)
+        bufs = []
+        for _ in range(copies):
+            c = {"logits": to_dev(vc.target_logits), "probs": to_dev(vc.draft_probs) if T > 0 else None,
+                 "tokens": to_dev(vc.tree_tokens), "parent": to_dev(vc.tree_parent),
+                 "unif": to_dev(vc.uniforms), "st_v": torch.zeros((B,), dtype=torch.int32, device=dev)}
+            c["ws_v"] = torch.empty((max(st.spec_tree_verify_workspace(B, N, V), 16),),
+                                    dtype=torch.uint8, device=dev)
+            i32 = dict(dtype=torch.int32, device=dev)
+            c["vout"] = {"accept_len": torch.empty((B,), **i32),
+                         "accepted_tokens": torch.empty((B, N), **i32),
+                         "bonus": torch.empty((B,), **i32),
+                         "accepted_nodes": torch.empty((B, N), **i32)}
+            if timed_step:
+                rnd = lambda *shape: torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)  # noqa: E731,E501
+                c["q"], c["k"], c["v"] = rnd(B, N, Hq, D), rnd(B, Hkv, Lmax, D), rnd(B, Hkv, Lmax, D)
+                c["lens"] = to_dev(lens)
+                c["out"] = torch.empty((B, N, Hq, D), dtype=torch.bfloat16, device=dev)
+                c["lse"] = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+                c["st_a"] = torch.zeros((B,), dtype=torch.int32, device=dev)
+            bufs.append(c)
+
+        def attn(c):
+            st.spec_tree_attention(c["q"], c["k"], c["v"], c["lens"], c["parent"],
+                                   softmax_scale=1.0 / math.sqrt(D), out=c["out"], out_lse=c["lse"],
+                                   status=c["st_a"])
+
+        def verify(c):
+            st.spec_tree_verify(c["logits"], c["probs"], c["tokens"], c["parent"], c["unif"], T,
+                                outputs=c["vout"], workspace=c["ws_v"], status=c["st_v"])
+
+        def step(c):
+            attn(c)
+            verify(c)
+
+        fns = {"verify": verify}
+        if timed_step:
+            fns.update({"attn": attn, "step": step})
+        for _ in range(3):
+            for c in bufs:
+                for f in fns.values():
+                    f(c)
+        torch.cuda.synchronize()
+        reps_per_graph = max(1, -(-12 // copies))
+        graphs = {}
+        s.wait_stream(torch.cuda.current_stream())
+        for k, f in fns.items():
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    for _ in range(reps_per_graph):
+                        for c in bufs:
+                            f(c)
+            graphs[k] = g
+        torch.cuda.current_stream().wait_stream(s)
+        for g in graphs.values():
+            g.replay()
+            g.replay()
+        torch.cuda.synchronize()
+        calls = reps_per_graph * copies
+        us = {}
+        replays = 20  # a few hundred calls per timed region
+        for k, g in graphs.items():
+            us[k] = timed(lambda: [g.replay() for _ in range(replays)]) * 1e3 / (replays * calls)
+        o = {k: v.cpu().numpy() for k, v in bufs[0]["vout"].items()}
+        o["status"] = bufs[0]["st_v"].cpu().numpy()
+        ref = leg["oracle"]
+        near = ref["near_tie"]
+        agree = sum(1 for b in range(B) if not near[b]
+                    and o["accept_len"][b] == ref["accept_len"][b]
+                    and o["bonus"][b] == ref["bonus"][b]
+                    and np.array_equal(o["accepted_tokens"][b], ref["accepted_tokens"][b]))
+        internal = sum(len(np.unique(par[b, 1:])) for b in range(B)) if N > 1 else 0
+        ver_bytes = internal * 4 * V * (2 if T > 0 else 1) + B * 4 * V * (2 if T > 0 else 1)
+        path_form = B * N * V * 4 > (64 << 20)
+        read_bytes = None
+        if path_form:
+            read_bytes = 0
+            for b in range(B):
+                for j in [0] + [int(x) for x in o["accepted_nodes"][b, :max(int(o["accept_len"][b]), 0)]]:
+                    kids = bool((par[b, 1:] == j).any())
+                    read_bytes += 4 * V * (2 if (T > 0 and kids) else 1)
+        depth = int(max(W.config(name).depth, 1))
+        e = {"workload": workload_name(cfg, T), "temperature": T,
+             "verify_us": us["verify"],
+             "verify_form": "path only (one cluster per sequence)" if path_form
+                            else "every node at once",
+             "verify_algorithmic_bytes": ver_bytes, "verify_read_bytes": read_bytes,
+             "verify_read_gbs": read_bytes / (us["verify"] * 1e-6) / 1e9 if read_bytes else None,
+             "verification": acceptance_stats(o["accept_len"], depth),
+             "status_nonzero": int((o["status"] != 0).sum()),
+             "cpu_baseline": {"kind": "oracle", "cores": 1,
+                              "value": B / leg["oracle_s"], "unit": "sequences/s (verification)",
+                              "sample": f"fp64 oracle verification of all {B} sequences",
+                              "near_ties": int(near.sum()), "compared": int((~near).sum()),
+                              "gpu_agrees": int(agree)},
+             "copies": copies, "calls_per_region": calls * replays}
+        if timed_step:
+            kv = sum(Hkv * (int(L) + N) * D * 2 * 2 for L in lens)
+            attn_bytes = kv + 2 * B * N * Hq * D * 2 + B * Hq * N * 4
+            flops = sum(4 * Hq * N * (int(L) + N) * D for L in lens)
+            step_s = us["step"] * 1e-6
+            e.update({"nodes_per_s": B * N / step_s, "step_us": us["step"], "attn_us": us["attn"],
+                      "attn_algorithmic_bytes": attn_bytes,
+                      "attn_gbs": attn_bytes / (us["attn"] * 1e-6) / 1e9,
+                      "attn_frac": attn_bytes / (us["attn"] * 1e-6) / 1e9 / hbm_gbs,
+                      "attn_tflops": flops / (us["attn"] * 1e-6) / 1e12,
+                      "attn_tensor_frac": flops / (us["attn"] * 1e-6) / 1e12 / tc_tflops,
+                      "step_hbm_frac": (attn_bytes + ver_bytes) / (hbm_gbs * 1e9) / step_s,
+                      "dominant_kernel": "tree_attn_kernel" if us["attn"] >= us["verify"]
+                                         else "verify_kernel"})
+        out[key] = e
+        del bufs, graphs
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    out["note"] = ("per-call times from CUDA graphs of back-to-back calls (inputs larger than 2 x L2 "
+                   "or rotated over copies that are); verify_algorithmic_bytes counts every "
+                   "internal node's rows (the all-nodes count), verify_read_bytes the rows the path "
+                   "form actually reads; Q/K/V drawn on the device (seeded), the verification "
+                   "inputs by the workload generator; cpu_baseline: the fp64 oracle's "
+                   "verification of the same inputs (near ties counted, the GPU's tokens compared "
+                   "outside them)")
+    return out
+
+
+
 def profiled_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
     import hashlib
@@ -841,8 +1087,7 @@ def run_reference(args):
         "ms_per_step": r["seconds"] * 1e3 / max(args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; shapes of the EAGLE static-tree workload, no datasets)",
-        "config": {"workload": f"{args.config}: B={cfg.B} Hq={cfg.Hq} Hkv={cfg.Hkv} D={cfg.D} "
-                               f"N={cfg.N} V={cfg.V} T={args.temperature}",
+        "config": {"workload": workload_name(cfg, args.temperature),
                    "parallelism": "cpu oracle, rank 0 only"},
         "cpu_baseline": {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                          "sample": r["sample"], "cpu": cpu_model()},

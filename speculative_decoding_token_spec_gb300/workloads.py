@@ -25,7 +25,7 @@ import numpy as np
 __all__ = [
     "AttnCase", "VerifyCase", "PagedAttnCase", "CompactCase", "CONFIGS", "make_tree",
     "chain_tree", "make_attention_case", "make_paged_attention_case", "make_compaction_case",
-    "make_verify_case", "bf16_bits", "bf16_to_f64", "config",
+    "make_verify_case", "bf16_bits", "bf16_to_f64", "config", "attention_layout",
 ]
 
 
@@ -148,6 +148,14 @@ def _tree(cfg: Config, seed: int, b: int) -> np.ndarray:
     if cfg.tree == "chain":
         return chain_tree(cfg.N)
     return make_tree(_rng(seed, cfg.cfg_id, b, 1), cfg.N, cfg.depth, cfg.width)
+
+
+def attention_layout(cfg: Config, seed: int = 0):
+    """The prefix lengths [B], trees [B, N] and cache length Lmax that make_attention_case draws for
+    (cfg, seed), without the Q / K / V tensors (for callers that draw those elsewhere)."""
+    lens = _prefix_lens(cfg, seed)
+    par = np.stack([_tree(cfg, seed, b) for b in range(cfg.B)]).astype(np.int32)
+    return lens, par, int(lens.max()) + cfg.N
 
 
 # ----------------------------------------------------------------------------------------------
