@@ -216,13 +216,14 @@ __device__ __forceinline__ double df_to_double(DF a) { return (double)a.hi + (do
 __device__ __forceinline__ DF df_from(const CompSum& c) { return df_fast_two_sum(c.hi, c.lo); }
 
 // Butterfly sum over the warp; the lower lane's operand always goes first, so every lane ends with
-// the same bits.
+// the same bits.  Both lanes of a pair run the same instructions (operands chosen by selects).
 __device__ __forceinline__ DF warp_sum_df(DF v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    DF w{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
-    v = (lane & o) ? df_add(w, v) : df_add(v, w);
+    const DF w{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+    const bool upper = (lane & o) != 0;
+    v = df_add(upper ? w : v, upper ? v : w);
   }
   return v;
 }

@@ -232,64 +232,53 @@ __device__ __forceinline__ void cluster_barrier() {
 // __syncthreads (step 1) after reading exchange x, so slots are never overwritten early.
 enum XKind { kXSum = 0, kXMaxSum = 1, kXArgmax = 2 };
 
-__device__ __forceinline__ Entry entry_identity(int kind) {
-  return kind == kXArgmax ? Entry{-INFINITY, 0x7fffffff, 0.f, 0.f, 0, {0, 0, 0}}
+template <int KIND>
+__device__ __forceinline__ Entry entry_identity() {
+  return KIND == kXArgmax ? Entry{-INFINITY, 0x7fffffff, 0.f, 0.f, 0, {0, 0, 0}}
                           : Entry{-INFINITY, 0, 0.f, 0.f, 0, {0, 0, 0}};
 }
 
-// a then b (a holds the lower lanes / ranks): sums in that order, max-sums rescaled to the larger
-// max (k = log2(e) / T), argmax with the lower index on ties.
-__device__ __forceinline__ Entry entry_combine(const Entry& a, const Entry& b, int kind, float k) {
-  Entry r = a;
-  r.flags = a.flags | b.flags;
-  if (kind == kXArgmax) {
-    argmax_merge(r.m, r.idx, b.m, b.idx);
-  } else if (kind == kXSum) {
-    const DF s = df_add(DF{a.s_hi, a.s_lo}, DF{b.s_hi, b.s_lo});
-    r.s_hi = s.hi;
-    r.s_lo = s.lo;
-  } else {
-    const float m = fmaxf(a.m, b.m);
-    const float fa = (a.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(a.m, m), k));
-    const float fb = (b.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(b.m, m), k));
-    const DF s = df_add(df_scale(DF{a.s_hi, a.s_lo}, fa), df_scale(DF{b.s_hi, b.s_lo}, fb));
-    r.m = m;
-    r.s_hi = s.hi;
-    r.s_lo = s.lo;
-  }
-  return r;
-}
-
-__device__ __forceinline__ Entry shfl_entry(const Entry& e, int o) {
-  Entry f;
-  f.m = __shfl_xor_sync(0xffffffffu, e.m, o);
-  f.idx = __shfl_xor_sync(0xffffffffu, e.idx, o);
-  f.s_hi = __shfl_xor_sync(0xffffffffu, e.s_hi, o);
-  f.s_lo = __shfl_xor_sync(0xffffffffu, e.s_lo, o);
-  f.flags = __shfl_xor_sync(0xffffffffu, e.flags, o);
-  return f;
-}
-
-// Combination of the entries held by lanes 0..W-1 (in lane order), in every one of those lanes.
-// Max-sums take the max first and rescale each lane's sum once.
-template <int W = 8>
-__device__ __forceinline__ Entry lanes_combine(Entry e, int kind, float k) {
+// Combination of the entries held by lanes 0..7 (in lane order; the other lanes hold the identity),
+// in every lane: sums in lane order, max-sums rescaled to the largest max first (k = log2(e) / T),
+// argmax with the lower index on ties.  One code path per kind and no divergence: at every level
+// of the butterfly both lanes of a pair take the lower lane's operand first (selects), so every
+// lane ends with the same bits.
+template <int KIND>
+__device__ __forceinline__ Entry lanes_combine8(Entry e, float k) {
   const int lane = threadIdx.x & 31;
-  if (kind == kXMaxSum) {
-    float M = e.m;
+  e.flags = __reduce_or_sync(0xffffffffu, e.flags);
+  if constexpr (KIND == kXArgmax) {
 #pragma unroll
-    for (int o = W / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float f = (e.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(e.m, M), k));
-    const DF sc = df_scale(DF{e.s_hi, e.s_lo}, f);
-    e.m = M;
-    e.s_hi = sc.hi;
-    e.s_lo = sc.lo;
-    kind = kXSum;
-  }
+    for (int o = 4; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, e.m, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, e.idx, o);
+      const bool upper = (lane & o) != 0;
+      float am = upper ? ov : e.m;
+      int ai = upper ? oi : e.idx;
+      argmax_merge(am, ai, upper ? e.m : ov, upper ? e.idx : oi);
+      e.m = am;
+      e.idx = ai;
+    }
+  } else {
+    if constexpr (KIND == kXMaxSum) {
+      float M = e.m;
 #pragma unroll
-  for (int o = W / 2; o > 0; o >>= 1) {
-    const Entry f = shfl_entry(e, o);
-    e = (lane & o) ? entry_combine(f, e, kind, k) : entry_combine(e, f, kind, k);
+      for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float f = (e.m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(e.m, M), k));
+      const DF sc = df_scale(DF{e.s_hi, e.s_lo}, f);
+      e.m = M;
+      e.s_hi = sc.hi;
+      e.s_lo = sc.lo;
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {
+      const DF w{__shfl_xor_sync(0xffffffffu, e.s_hi, o), __shfl_xor_sync(0xffffffffu, e.s_lo, o)};
+      const DF v{e.s_hi, e.s_lo};
+      const bool upper = (lane & o) != 0;
+      const DF s = df_add(upper ? w : v, upper ? v : w);
+      e.s_hi = s.hi;
+      e.s_lo = s.lo;
+    }
   }
   return e;
 }
@@ -298,8 +287,8 @@ __device__ __forceinline__ Entry lanes_combine(Entry e, int kind, float k) {
 // entry (warp-uniform).  Warp 0 combines the CTA's warps, sends, waits for the CL entries and
 // combines them; the others meet it at a __syncthreads.  After it, sm.cpart[slot][r] holds CTA
 // r's entry (slot returned through xslot).  A wait that gives up sets SPEC_ST_TIMEOUT.
-template <int CL>
-__device__ Entry exchange(VerifySmem& sm, int& xk, const Entry& mine, int kind, float k, int rank,
+template <int CL, int KIND>
+__device__ Entry exchange(VerifySmem& sm, int& xk, const Entry& mine, float k, int rank,
                           int& xslot) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (lane == 0) sm.wpart[wid] = mine;
@@ -310,7 +299,8 @@ __device__ Entry exchange(VerifySmem& sm, int& xk, const Entry& mine, int kind, 
   xslot = slot;
   if (wid == 0) {
     const uint32_t bar = smem_u32(&sm.xbar[slot]);
-    const Entry c = lanes_combine<8>(lane < kVWarps ? sm.wpart[lane] : entry_identity(kind), kind, k);
+    const Entry c =
+        lanes_combine8<KIND>(lane < kVWarps ? sm.wpart[lane] : entry_identity<KIND>(), k);
     if (lane == 0) mbar_arrive_expect_tx(bar, CL * (uint32_t)sizeof(Entry));
     if (lane < CL) {
       const uint32_t dst = dsmem_addr(&sm.cpart[slot][rank], lane);
@@ -323,7 +313,7 @@ __device__ Entry exchange(VerifySmem& sm, int& xk, const Entry& mine, int kind, 
     // with the full limit: no CTA moves on (or exits) with a store into it still in flight
     const bool ok = __all_sync(0xffffffffu, mbar_wait_acq_cluster(bar, parity, sm.first_polls));
     if (!ok) mbar_wait_acq_cluster(bar, parity);
-    Entry r = lanes_combine<8>(lane < CL ? sm.cpart[slot][lane] : entry_identity(kind), kind, k);
+    Entry r = lanes_combine8<KIND>(lane < CL ? sm.cpart[slot][lane] : entry_identity<KIND>(), k);
     if (lane == 0) {
       r.flags |= ok ? 0 : SPEC_ST_TIMEOUT;
       sm.xres = r;
@@ -389,8 +379,8 @@ __device__ void cluster_argmax(const Slice& s, const float* lbuf, int lflags, in
   warp_argmax(bv, bi);
   const int f = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0) | lflags;
   int xs;
-  const Entry r = exchange<CL>(sm, xk, Entry{bv, bi, 0.f, 0.f, f, {0, 0, 0}}, kXArgmax, 0.f,
-                               rank, xs);
+  const Entry r =
+      exchange<CL, kXArgmax>(sm, xk, Entry{bv, bi, 0.f, 0.f, f, {0, 0, 0}}, 0.f, rank, xs);
   gv = r.m;
   gi = r.idx;
   flags |= r.flags;
@@ -433,8 +423,8 @@ __device__ void cluster_stats(const Slice& s, float* lbuf, float k, int lflags, 
   const float g = (m == -INFINITY) ? 0.f : ex2f(__fmul_rn(__fsub_rn(m, mw), k));
   const DF sw = warp_sum_df(df_scale(st, g));
   int xs;
-  const Entry r = exchange<CL>(sm, xk, Entry{mw, 0, sw.hi, sw.lo, lflags, {0, 0, 0}}, kXMaxSum,
-                               k, rank, xs);
+  const Entry r =
+      exchange<CL, kXMaxSum>(sm, xk, Entry{mw, 0, sw.hi, sw.lo, lflags, {0, 0, 0}}, k, rank, xs);
   M = r.m;
   S = DF{r.s_hi, r.s_lo};
   flags |= r.flags;
@@ -479,8 +469,8 @@ __device__ DF cluster_residual(const Slice& s, const float* ebuf, const PD& pd, 
   tot = df_scale(df_from(acc), f);
   wt = warp_sum_df(tot);
   const int wf = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0) | lflags;
-  const Entry r = exchange<CL>(sm, xk, Entry{0.f, 0, wt.hi, wt.lo, wf, {0, 0, 0}}, kXSum, 0.f,
-                               rank, xs);
+  const Entry r =
+      exchange<CL, kXSum>(sm, xk, Entry{0.f, 0, wt.hi, wt.lo, wf, {0, 0, 0}}, 0.f, rank, xs);
   flags |= r.flags;
   return DF{r.s_hi, r.s_lo};
 }
@@ -954,8 +944,11 @@ __device__ __forceinline__ bool arrive(unsigned long long* ctr, unsigned long lo
 // the kernel
 // ------------------------------------------------------------------------------------------------
 // PGLOBAL: draft rows read from global memory instead of staged (large problems with V ~ 128K).
+// Four CTAs per SM (at most 64 registers a thread): at three, the 60 clusters of 8 CTAs of one
+// 60-node tree do not all fit on the GPU at once, and the last clusters start only when the
+// first ones leave.
 template <int CL, bool PGLOBAL>
-__global__ void __launch_bounds__(kVThreads)
+__global__ void __launch_bounds__(kVThreads, 4)
     verify_kernel(const VerifyArgs a, int cap, int do_leaves, float invT_hi, float invT_lo,
                   float k2) {
   extern __shared__ __align__(16) float dyn[];
@@ -1050,7 +1043,7 @@ __global__ void __launch_bounds__(kVThreads)
 // the same per-node step as above.  A sequence reads (accepted + 1) target rows instead of every
 // internal node's, at the price of one dependent step per accepted level.  No workspace.
 template <int CL, bool PGLOBAL>
-__global__ void __launch_bounds__(kVThreads)
+__global__ void __launch_bounds__(kVThreads, 4)
     verify_path_kernel(const VerifyArgs a, int cap, float invT_hi, float invT_lo, float k2) {
   extern __shared__ __align__(16) float dyn[];
   __shared__ VerifySmem sm;
@@ -1159,7 +1152,11 @@ static int pick_cluster(long long units, int V, int num_sms, bool small, int nbu
   int cl = 1;
   while (cl < 8 && slice_capacity(V, cl) > kMaxSliceFloats) cl *= 2;
   if (small) {
-    while (cl < 8 && V / (cl * 2) >= 1024) cl *= 2;
+    // T = 0 (one buffer: an argmax pass and one exchange per node) measured faster with clusters
+    // of 4 (6.3 against 6.7 us for the 60-node tree at V = 32000); T > 0, with its residual rounds,
+    // with clusters of 8 (12.0 against 12.3 us)
+    const int cap = nbuf > 1 ? 8 : 4;
+    while (cl < cap && V / (cl * 2) >= 1024) cl *= 2;
     return cl;
   }
   while (cl < 8 && units * (cl * 2) <= (long long)num_sms * 3 / 2 && V / (cl * 2) >= 2048) cl *= 2;
