@@ -475,11 +475,13 @@ __device__ DF cluster_residual(const Slice& s, const float* ebuf, const PD& pd, 
   return DF{r.s_hi, r.s_lo};
 }
 
-// The current weights became those of this round: record its CTA totals for a draw.
+// The current weights became those of this round: record its CTA totals and this CTA's warp
+// totals `wt` (the same sums a draw would form from the threads' totals) for a draw.
 template <int CL>
-__device__ __forceinline__ void commit_round_totals(VerifySmem& sm, int xs) {
+__device__ __forceinline__ void commit_round_totals(VerifySmem& sm, int xs, const DF& wt) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (wid == 0 && lane < CL) sm.ccur[lane] = DF{sm.cpart[xs][lane].s_hi, sm.cpart[xs][lane].s_lo};
+  if (lane == 0) sm.wcur[wid] = wt;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -519,12 +521,13 @@ struct Draw {
   int writer, tok;
 };
 
-// Levels: CTA of the cluster (sm.ccur, same in every CTA), warp of that CTA (sums of rs.tot),
-// thread of that warp (rs.tot), element of that thread's run.  No exchange: the writer CTA finds
-// the token alone and records the node itself.
+// Levels: CTA of the cluster (sm.ccur, same in every CTA), warp of that CTA (sums of rs.tot; in
+// sm.wcur already when wcur_ready), thread of that warp (rs.tot), element of that thread's run.
+// No exchange: the writer CTA finds the token alone and records the node itself.
 template <int CL, class PD>
 __device__ Draw cluster_draw(const Slice& s, const float* ebuf, const PD& pd,
-                             const RunState& rs, float u, int rank, VerifySmem& sm) {
+                             const RunState& rs, float u, int rank, VerifySmem& sm,
+                             bool wcur_ready = false) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   __syncthreads();  // sm.ccur / sm.wcur are visible
   // level 1: CTA (lanes 0..7; lanes past CL hold zeros)
@@ -536,9 +539,11 @@ __device__ Draw cluster_draw(const Slice& s, const float* ebuf, const PD& pd,
   const int cstar = lane_crossing(cv, cincl, t, before);
   if (cstar < 0) return Draw{0, -1};  // nothing positive anywhere
   if (rank != cstar) return Draw{cstar, -1};
-  const DF wsum = warp_sum_df(rs.tot);
-  if (lane == 0) sm.wcur[wid] = wsum;
-  __syncthreads();
+  if (!wcur_ready) {  // block-uniform
+    const DF wsum = warp_sum_df(rs.tot);
+    if (lane == 0) sm.wcur[wid] = wsum;
+    __syncthreads();
+  }
   // level 2: warp of this CTA (every warp computes it; one acts)
   if (t.hi >= 0.f) t = df_add(t, DF{-before.hi, -before.lo});
   const DF wv = lane < kVWarps ? sm.wcur[lane] : DF{0.f, 0.f};
@@ -642,7 +647,7 @@ struct NodeBufs {
 // that one CTA can process several nodes in turn.
 // The returned record is complete in CTA `writer` (every CTA gets the same writer); first_acc,
 // flags and (at T = 0) the bonus are the same in every CTA.
-template <int CL, bool PGLOBAL>
+template <int CL, bool PGLOBAL, bool SAMPLING>
 __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, const NodeBufs& nb,
                                  bool logits_staged, DF invT_df, float k2, int& xk, int& writer,
                                  uint32_t& ph_l, uint32_t& ph_p, VerifySmem& sm) {
@@ -653,7 +658,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   const float* lrow = a.logits + row_off;
   const float* prow = a.probs ? a.probs + row_off : nullptr;
   const Slice s = make_slice(lrow, V, rank, CL);  // the draft row has the same alignment
-  const bool sampling = a.T > 0.f;
+  constexpr bool sampling = SAMPLING;  // T > 0 (T == 0: greedy)
   if (!logits_staged) stage_slice(lrow, s, nb.lbuf, nb.bar_l, -INFINITY);
   const bool probs_staged = sampling && nk > 0 && !PGLOBAL;
   if (probs_staged) stage_slice(prow, s, nb.pbuf, nb.bar_p, 0.f);
@@ -679,7 +684,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   st.bonus = -1;
   st.s_hi = st.s_lo = 0.f;
 
-  if (!sampling) {
+  if constexpr (!sampling) {
     float gv;
     int gi;
     cluster_argmax<CL>(s, nb.lbuf, lflags0, rank, xk, gv, gi, flags, sm);
@@ -703,7 +708,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     st.flags = flags;
     st.bonus = gi;  // the bonus wherever the walk stops here
     return st;
-  }
+  } else {
 
   // ---- T > 0: statistics of q_j = softmax(l_j / T); e_t(y) replaces the logits in lbuf
   float M;
@@ -723,6 +728,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   bool all_rejected = nk > 0;
   DF c{0.f, 0.f};  // current weights: max(0, e - c p)
   bool frozen = false, p_waited = false;
+  bool wcur_ready = false;  // sm.wcur holds the warp totals of the current weights
   int pflags = 0;
   for (int t = 0; t < nk; ++t) {
     const int kid = sm.kids[t];
@@ -767,7 +773,8 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
       c = c_next;
       rs.tot = tot;
       rs.cw = c_t;
-      commit_round_totals<CL>(sm, xs);
+      commit_round_totals<CL>(sm, xs, wt);
+      wcur_ready = true;
     } else {
       frozen = true;
     }
@@ -779,7 +786,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   }
   const bool bad = (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) != 0;
   if ((nk == 0 || all_rejected) && !bad) {  // the walk can stop here: draw its bonus
-    const Draw d = cluster_draw<CL>(s, nb.lbuf, pd, rs, u_bonus, rank, sm);
+    const Draw d = cluster_draw<CL>(s, nb.lbuf, pd, rs, u_bonus, rank, sm, wcur_ready);
     writer = d.writer;
     st.bonus = d.tok;
   }
@@ -794,6 +801,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   st.flags = flags;
   if (bad) st.bonus = -1;
   return st;
+  }
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -854,7 +862,7 @@ __device__ void write_outputs(const VerifyArgs& a, int b, int bonus, int flags, 
 
 // Leaves not processed (large problems): the whole cluster walks and draws the bonus at a leaf
 // terminal.  bar_l_used: whether this CTA already staged a row on nb.bar_l in this launch.
-template <int CL>
+template <int CL, bool SAMPLING>
 __device__ void walk_sequence_cluster(const VerifyArgs& a, int b, int rank, const NodeBufs& nb,
                                       bool bar_l_used, float k2, int& xk, VerifySmem& sm) {
   walk_path(a, b, false, sm);
@@ -871,7 +879,7 @@ __device__ void walk_sequence_cluster(const VerifyArgs& a, int b, int rank, cons
     stage_slice(lrow, s, nb.lbuf, nb.bar_l, -INFINITY);
     // CTA-local: published below
     const int lflags = wait_slice(nb.bar_l, bar_l_used ? 1 : 0, sm.first_polls);
-    if (a.T == 0.f) {
+    if constexpr (!SAMPLING) {
       float gv;
       int gi;
       cluster_argmax<CL>(s, nb.lbuf, lflags, rank, xk, gv, gi, flags, sm);
@@ -947,9 +955,9 @@ __device__ __forceinline__ bool arrive(unsigned long long* ctr, unsigned long lo
 // Four CTAs per SM (at most 64 registers a thread): at three, the 60 clusters of 8 CTAs of one
 // 60-node tree do not all fit on the GPU at once, and the last clusters start only when the
 // first ones leave.
-template <int CL, bool PGLOBAL>
+template <int CL, bool PGLOBAL, bool SAMPLING, bool LEAVES>
 __global__ void __launch_bounds__(kVThreads, 4)
-    verify_kernel(const VerifyArgs a, int cap, int do_leaves, float invT_hi, float invT_lo,
+    verify_kernel(const VerifyArgs a, int cap, float invT_hi, float invT_lo,
                   float k2) {
   extern __shared__ __align__(16) float dyn[];
   __shared__ VerifySmem sm;
@@ -972,7 +980,8 @@ __global__ void __launch_bounds__(kVThreads, 4)
   griddep_launch_dependents();
   // small problems process every node: its logit row is needed whatever the tree looks like, so
   // the copy goes out before anything else
-  const bool early = do_leaves != 0;
+  constexpr bool do_leaves = LEAVES;  // small problems: every node, leaves included
+  constexpr bool early = LEAVES;
   if (early) {
     const float* lrow = a.logits + ((size_t)b * N + j) * (size_t)a.V;
     stage_slice(lrow, make_slice(lrow, a.V, rank, CL), nb.lbuf, nb.bar_l, -INFINITY);
@@ -1004,11 +1013,12 @@ __global__ void __launch_bounds__(kVThreads, 4)
   const bool work = sm.internal[j] || do_leaves;
   NodeStat st;
   if (work)
-    st = process_node<CL, PGLOBAL>(a, b, j, rank, nb, early, DF{invT_hi, invT_lo}, k2, xk, writer,
+    st = process_node<CL, PGLOBAL, SAMPLING>(a, b, j, rank, nb, early, DF{invT_hi, invT_lo}, k2, xk,
+                                             writer,
                                    ph_l, ph_p, sm);
 
   // arrival: the last cluster of the sequence to finish walks the tree
-  if (do_leaves) {
+  if constexpr (do_leaves) {
     // every possible stop already has its bonus, so the writer CTA finishes alone (this
     // cluster's exchanges are complete: the other CTAs may leave)
     if (rank != writer) return;
@@ -1034,7 +1044,7 @@ __global__ void __launch_bounds__(kVThreads, 4)
   }
   cluster_barrier<CL>();
   if (!sm.is_last) return;
-  walk_sequence_cluster<CL>(a, b, rank, nb, work, k2, xk, sm);
+  walk_sequence_cluster<CL, SAMPLING>(a, b, rank, nb, work, k2, xk, sm);
   cluster_barrier<CL>();  // keep shared memory alive for remote stores
 }
 
@@ -1042,7 +1052,7 @@ __global__ void __launch_bounds__(kVThreads, 4)
 // tree, processing only the nodes the walk reaches -- the root, then each accepted child -- with
 // the same per-node step as above.  A sequence reads (accepted + 1) target rows instead of every
 // internal node's, at the price of one dependent step per accepted level.  No workspace.
-template <int CL, bool PGLOBAL>
+template <int CL, bool PGLOBAL, bool SAMPLING>
 __global__ void __launch_bounds__(kVThreads, 4)
     verify_path_kernel(const VerifyArgs a, int cap, float invT_hi, float invT_lo, float k2) {
   extern __shared__ __align__(16) float dyn[];
@@ -1084,7 +1094,8 @@ __global__ void __launch_bounds__(kVThreads, 4)
   int xk = 0, writer = 0, c = 0, len = 0, bonus = -1, flags = 0;
   uint32_t ph_l = 0, ph_p = 0;
   for (;;) {  // at most N steps: every accepted child has a larger index than its parent
-    const NodeStat st = process_node<CL, PGLOBAL>(a, b, c, rank, nb, false, DF{invT_hi, invT_lo},
+    const NodeStat st = process_node<CL, PGLOBAL, SAMPLING>(a, b, c, rank, nb, false,
+                                                            DF{invT_hi, invT_lo},
                                                   k2, xk, writer, ph_l, ph_p, sm);
     flags |= st.flags;  // cluster-uniform, so the loop's control flow is too
     if (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) break;
@@ -1165,17 +1176,37 @@ static int pick_cluster(long long units, int V, int num_sms, bool small, int nbu
   return cl;
 }
 
+// One instantiation per form (all nodes with or without the leaves, the path only), temperature
+// kind (sampling or greedy) and draft-row staging, so that each kernel holds one code path.
 template <int CL>
 static cudaError_t launch_cl(const VerifyArgs& a, dim3 g, size_t smem, cudaStream_t s, int cap,
                              int leaves, float invT_hi, float invT_lo, float k2, bool path) {
+  const bool sampling = a.T > 0.f;  // p_global is only ever set when sampling
   if (path) {
+    if (!sampling)
+      return launch_ex(verify_path_kernel<CL, false, false>, g, CL, smem, s, a, cap, invT_hi,
+                       invT_lo, k2);
     if (a.p_global)
-      return launch_ex(verify_path_kernel<CL, true>, g, CL, smem, s, a, cap, invT_hi, invT_lo, k2);
-    return launch_ex(verify_path_kernel<CL, false>, g, CL, smem, s, a, cap, invT_hi, invT_lo, k2);
+      return launch_ex(verify_path_kernel<CL, true, true>, g, CL, smem, s, a, cap, invT_hi,
+                       invT_lo, k2);
+    return launch_ex(verify_path_kernel<CL, false, true>, g, CL, smem, s, a, cap, invT_hi,
+                     invT_lo, k2);
   }
+  if (leaves) {
+    if (!sampling)
+      return launch_ex(verify_kernel<CL, false, false, true>, g, CL, smem, s, a, cap, invT_hi,
+                       invT_lo, k2);
+    return launch_ex(verify_kernel<CL, false, true, true>, g, CL, smem, s, a, cap, invT_hi,
+                     invT_lo, k2);
+  }
+  if (!sampling)
+    return launch_ex(verify_kernel<CL, false, false, false>, g, CL, smem, s, a, cap, invT_hi,
+                     invT_lo, k2);
   if (a.p_global)
-    return launch_ex(verify_kernel<CL, true>, g, CL, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
-  return launch_ex(verify_kernel<CL, false>, g, CL, smem, s, a, cap, leaves, invT_hi, invT_lo, k2);
+    return launch_ex(verify_kernel<CL, true, true, false>, g, CL, smem, s, a, cap, invT_hi,
+                     invT_lo, k2);
+  return launch_ex(verify_kernel<CL, false, true, false>, g, CL, smem, s, a, cap, invT_hi,
+                   invT_lo, k2);
 }
 
 // Path-only form: one cluster per sequence, each step a chain of dependent passes over the
