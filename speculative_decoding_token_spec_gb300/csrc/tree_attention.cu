@@ -599,9 +599,22 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   // Split barrier: this CTA's ring is free for the peers' pushes once every thread arrived (TMA
   // copies drained, MMAs complete); the in-CTA merge below only touches this CTA's own memory, so
   // it runs while the slower CTAs arrive, and each thread waits just before its first remote store.
-  cluster_arrive_release();
+  // One split (S == 1): no peer, no push, no owner pass -- each thread normalises its merged piece
+  // of the row and writes it (the owner pass of a single partial gives the same bits).
+  const bool single = S == 1;
+  if (!single) cluster_arrive_release();
   __syncthreads();  // this CTA: the producer drained its copies and the MMAs completed
-  if (warp < 2) cluster_wait_acquire();
+  if (!single && warp < 2) cluster_wait_acquire();
+  // row q = rb * 128 + qloc of this block: node i = q / g, query head kvh * g + q % g
+  auto out_row = [&](int qrow_) -> __nv_bfloat16* {
+    return p.out + (((size_t)b * N + qrow_ / g) * p.Hq + kvh * g + qrow_ % g) * D;
+  };
+  auto put_lse = [&](int qrow_, bool tmo_, bool has_, float m_, float lsum_) {
+    if (p.lse)
+      p.lse[((size_t)b * p.Hq + kvh * g + qrow_ % g) * N + qrow_ / g] =
+          has_ ? (m_ + __log2f(lsum_)) * 0.69314718055994531f : -INFINITY;
+    if (tmo_ && p.status) atomicOr(p.status + b, SPEC_ST_TIMEOUT);
+  };
   if (warp >= 2) {
     const uint32_t lane_tm = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const int owner = qloc % S, ql = qloc / S;
@@ -659,26 +672,47 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
           Lsum = fmaf(w[g2][k2], st[g2][k2].y, Lsum);
         }
       const bool has = !tmo && Lsum > 0.f;
-      cluster_wait_acquire();  // every CTA's ring is free: the pushes may start
-      if (live && gi == 0 && ks == 0) push_ml(tmo, has, M, Lsum);
-      const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
-      const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE + my_c, owner);
       const float* r0 = stage_o + qloc * C::RSTRIDE + my_c;
       const float* r1 = stage_o + (64 + qloc) * C::RSTRIDE + my_c;
       const float wo0 = gi ? w[1][0] : w[0][0], wo1 = gi ? w[1][1] : w[0][1];  // own lane
       const float wx0 = gi ? w[0][0] : w[1][0], wx1 = gi ? w[0][1] : w[1][1];  // the other lane
-      tmem_wait_ld();
-#pragma unroll
-      for (int k = 0; k < Q4; k += 4) {
+      auto merged4 = [&](int k, float (&v)[4]) {  // columns my_c + k .. + 3 of the merged row
         const float4 x0 = *reinterpret_cast<const float4*>(r0 + k);
         const float4 x1 = *reinterpret_cast<const float4*>(r1 + k);
         const float xa[4] = {x0.x, x0.y, x0.z, x0.w}, xb[4] = {x1.x, x1.y, x1.z, x1.w};
-        uint32_t v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          v[j] = __float_as_uint(sel(wo0, o0[k + j]) + sel(wo1, o1[k + j]) + sel(wx0, xa[j]) +
-                                 sel(wx1, xb[j]));
-        dsmem_store_v4(dst + k * 4, make_uint4(v[0], v[1], v[2], v[3]));
+          v[j] = sel(wo0, o0[k + j]) + sel(wo1, o1[k + j]) + sel(wx0, xa[j]) + sel(wx1, xb[j]);
+      };
+      if (single) {
+        tmem_wait_ld();
+        if (live) {
+          const float inv = has ? __frcp_rn(Lsum) : 0.f;
+          __nv_bfloat16* orow = out_row(qrow) + my_c;
+#pragma unroll
+          for (int k = 0; k < Q4; k += 8) {
+            float a[4], c4[4];
+            merged4(k, a);
+            merged4(k + 4, c4);
+            *reinterpret_cast<uint4*>(orow + k) =
+                make_uint4(pack_bf16(a[0] * inv, a[1] * inv), pack_bf16(a[2] * inv, a[3] * inv),
+                           pack_bf16(c4[0] * inv, c4[1] * inv), pack_bf16(c4[2] * inv, c4[3] * inv));
+          }
+          if (gi == 0 && ks == 0) put_lse(qrow, tmo, has, M, Lsum);
+        }
+      } else {
+        cluster_wait_acquire();  // every CTA's ring is free: the pushes may start
+        if (live && gi == 0 && ks == 0) push_ml(tmo, has, M, Lsum);
+        const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
+        const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE + my_c, owner);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < Q4; k += 4) {
+          float v[4];
+          merged4(k, v);
+          dsmem_store_v4(dst + k * 4, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                                                 __float_as_uint(v[2]), __float_as_uint(v[3])));
+        }
       }
     } else {
       // no key groups: the two accumulators of this lane; the thread of key set k pushes half k
@@ -691,34 +725,60 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       const float w1 = s1.y > 0.f ? ex2_approx(s1.x - M) : 0.f;
       const float Lsum = s0.y * w0 + s1.y * w1;
       const bool has = !tmo && Lsum > 0.f;
-      cluster_wait_acquire();  // every CTA's ring is free: the pushes may start
-      if (live && ks == 0) push_ml(tmo, has, M, Lsum);
-      const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
-      const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE, owner);
       constexpr int HC = D / 2 < 32 ? D / 2 : 32;
+      if (single) {
+        const float inv = has ? __frcp_rn(Lsum) : 0.f;
+        __nv_bfloat16* orow = out_row(qrow);
 #pragma unroll 1
-      for (int c0 = ks * (D / 2); c0 < (ks + 1) * (D / 2); c0 += HC) {
-        float a0[HC], a1[HC];
-        tmem_ldq(lane_tm + C::O_COL + (uint32_t)c0, a0);
-        tmem_ldq(lane_tm + C::O_COL + 128u + (uint32_t)c0, a1);
-        tmem_wait_ld();
+        for (int c0 = ks * (D / 2); c0 < (ks + 1) * (D / 2); c0 += HC) {
+          float a0[HC], a1[HC];
+          tmem_ldq(lane_tm + C::O_COL + (uint32_t)c0, a0);
+          tmem_ldq(lane_tm + C::O_COL + 128u + (uint32_t)c0, a1);
+          tmem_wait_ld();
+          if (live) {
 #pragma unroll
-        for (int k = 0; k < HC; k += 4)
-          dsmem_store_v4(dst + (c0 + k) * 4,
-                         make_uint4(__float_as_uint(sel(w0, a0[k]) + sel(w1, a1[k])),
-                                    __float_as_uint(sel(w0, a0[k + 1]) + sel(w1, a1[k + 1])),
-                                    __float_as_uint(sel(w0, a0[k + 2]) + sel(w1, a1[k + 2])),
-                                    __float_as_uint(sel(w0, a0[k + 3]) + sel(w1, a1[k + 3]))));
+            for (int k = 0; k < HC; k += 8) {
+              float v[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] = (sel(w0, a0[k + j]) + sel(w1, a1[k + j])) * inv;
+              *reinterpret_cast<uint4*>(orow + c0 + k) =
+                  make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                             pack_bf16(v[6], v[7]));
+            }
+          }
+        }
+        if (live && ks == 0) put_lse(qrow, tmo, has, M, Lsum);
+      } else {
+        cluster_wait_acquire();  // every CTA's ring is free: the pushes may start
+        if (live && ks == 0) push_ml(tmo, has, M, Lsum);
+        const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
+        const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE, owner);
+#pragma unroll 1
+        for (int c0 = ks * (D / 2); c0 < (ks + 1) * (D / 2); c0 += HC) {
+          float a0[HC], a1[HC];
+          tmem_ldq(lane_tm + C::O_COL + (uint32_t)c0, a0);
+          tmem_ldq(lane_tm + C::O_COL + 128u + (uint32_t)c0, a1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < HC; k += 4)
+            dsmem_store_v4(dst + (c0 + k) * 4,
+                           make_uint4(__float_as_uint(sel(w0, a0[k]) + sel(w1, a1[k])),
+                                      __float_as_uint(sel(w0, a0[k + 1]) + sel(w1, a1[k + 1])),
+                                      __float_as_uint(sel(w0, a0[k + 2]) + sel(w1, a1[k + 2])),
+                                      __float_as_uint(sel(w0, a0[k + 3]) + sel(w1, a1[k + 3]))));
+        }
       }
     }
   }
-  cluster_arrive_release();
-  cluster_wait_acquire();
+  if (!single) {
+    cluster_arrive_release();
+    cluster_wait_acquire();
+  }
   // owner: rows qloc = ql * S + split of this block, 8 output columns per item.  out =
   // sum_e 2^(m_e - M) O_e / sum_e 2^(m_e - M) l_e over the row's S partials e (one per split).
   const int E = S;
   constexpr int C8 = D / 8;
-  for (int it = tid; it < QO * C8; it += C::THREADS) {
+  for (int it = tid; !single && it < QO * C8; it += C::THREADS) {
     const int ql = it / C8, c = (it % C8) * 8, ql_loc = ql * S + split;
     const int q = rb * 128 + ql_loc;
     if (ql_loc >= 128 / kg || q >= p.R) continue;
