@@ -345,9 +345,11 @@ def run_ours(args):
     launches_per_step = 2  # one tree-attention kernel, one verification kernel
 
     # warm-up (eager), also validates the call path
+    torch.cuda.nvtx.range_push("warm-up")
     for i in range(max(args.warmup, 3)):
         step(bufs[i % copies])
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     assert int(bufs[0]["st_a"].sum()) == 0 and int(bufs[0]["st_v"].sum()) == 0, "status"
 
     # CUDA graphs: one step per rotated copy, nothing between the kernels (so each launch can
@@ -375,14 +377,17 @@ def run_ours(args):
                 g.replay()
     torch.cuda.synchronize()
 
-    def timed(fn):
+    def timed(fn, name="timed region"):
+        """CUDA-event time of fn() (ms), inside an NVTX range named `name` for profiler timelines."""
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push(name)
         a0.record()
         fn()
         a1.record()
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         barrier()
         return a0.elapsed_time(a1)
@@ -398,11 +403,13 @@ def run_ours(args):
         if g_rem is not None:
             g_rem.replay()
 
-    total_ms = timed(run_steps)
+    total_ms = timed(run_steps, "steps: attention + verification")
     # ---- per-call timed regions: the same rotated copies, one kernel kind per graph
     reps = max(1, -(-300 // copies))  # about 300 calls per region, whatever --steps is
-    attn_ms = timed(lambda: [g_attn.replay() for _ in range(reps)]) / (reps * copies)
-    ver_ms = timed(lambda: [g_ver.replay() for _ in range(reps)]) / (reps * copies)
+    attn_ms = timed(lambda: [g_attn.replay() for _ in range(reps)],
+                    "per call: spec_tree_attention") / (reps * copies)
+    ver_ms = timed(lambda: [g_ver.replay() for _ in range(reps)],
+                   "per call: spec_tree_verify") / (reps * copies)
     clk = clocks.stop()
     per_call = (f"separate timed regions of {reps * copies} calls each, replaying graphs of one call "
                 "over the rotated copies (back-to-back launches of that kernel)")

@@ -153,9 +153,11 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   uint8_t* ring = base;
   uint8_t* q_s = base + C::OFF_Q;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::OFF_BAR);
+  // B_FULL: a slot's K landed; B_VFULL: its V landed (the QK needs only K, so a chunk's QK does
+  // not wait for its V boxes, which are issued after its K boxes)
   const int B_FULL = 0, B_EMPTY = C::SLOTS, B_SFULL = 2 * C::SLOTS, B_SFREE = 2 * C::SLOTS + 2,
             B_PFULL = 2 * C::SLOTS + 4, B_PV = 2 * C::SLOTS + 6, B_DONE = 2 * C::SLOTS + 7,
-            B_SETUP = 2 * C::SLOTS + 8;
+            B_SETUP = 2 * C::SLOTS + 8, B_VFULL = 2 * C::SLOTS + 9;
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   if (tid == 0) {
     for (int i = 0; i < C::SLOTS; ++i) {
       mbar_init(bar(B_FULL + i), 1);
+      mbar_init(bar(B_VFULL + i), 1);
       mbar_init(bar(B_EMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {  // [S / P buffer]
@@ -235,21 +238,26 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
     }
     return yl;
   };
+  // One chunk: its K boxes complete on B_FULL, its V boxes on B_VFULL, K issued first.
   auto issue_chunk = [&](int sl, int ci, int yl) {
     uint8_t* st = ring + sl * C::TILE;
-    const uint32_t fb = bar(B_FULL + sl);
-    if (lane == 0) mbar_arrive_expect_tx(fb, C::TILE);
-    if (P == 0) {  // contiguous: ten boxes, issued in order by one lane (K first) measured faster
+    const uint32_t fb = bar(B_FULL + sl), fv = bar(B_VFULL + sl);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(fb, C::TILE / 2);
+      mbar_arrive_expect_tx(fv, C::TILE / 2);
+    }
+    if (P == 0) {  // contiguous: issued by one lane (measured faster than spread over lanes)
       if (lane == 0) {
         const int y = row0 + ci * C::KEYS;
 #pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx) {
+        for (int bx = 0; bx < C::NB; ++bx)
           tma_load_2d(smem_u32(st + bx * C::BOX), &tmap_k, fb, bx * 64, y);
 #pragma unroll
+        for (int bx = 0; bx < C::NB; ++bx)
+#pragma unroll
           for (int j = 0; j < 4; ++j)
-            tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX + j * 32 * 128), &tmap_v, fb, bx * 64,
+            tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX + j * 32 * 128), &tmap_v, fv, bx * 64,
                         y + 32 * v_block_key(j));
-        }
       }
       return;
     }
@@ -278,7 +286,8 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       y = __shfl_sync(0xffffffffu, yl, key / P - (ci * C::KEYS) / P);
       y = y >= past ? past : y + key % P;
     }
-    if (lane < nk + nv) tma_load_2d(smem_u32(st + dst), is_v ? &tmap_v : &tmap_k, fb, bx * 64, y);
+    if (lane < nk + nv)  // one instruction for the chunk: the K lanes' boxes come first
+      tma_load_2d(smem_u32(st + dst), is_v ? &tmap_v : &tmap_k, is_v ? fv : fb, bx * 64, y);
   };
   if (warp == 0) {
     // the split's first chunks do not depend on the prefix length: issue them now (a chunk past
@@ -389,7 +398,10 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       // (bounded waits)
       if (abort_s || my_tiles < spec)
         for (int it = max(0, issued - C::SLOTS); it < issued; ++it)
-          if (abort_s || it >= my_tiles) mbar_wait(bar(B_FULL + it % C::SLOTS), (it / C::SLOTS) & 1);
+          if (abort_s || it >= my_tiles) {
+            mbar_wait(bar(B_FULL + it % C::SLOTS), (it / C::SLOTS) & 1);
+            mbar_wait(bar(B_VFULL + it % C::SLOTS), (it / C::SLOTS) & 1);
+          }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: QK of step u once its chunk landed and S[u % 2] is free (and
@@ -426,7 +438,8 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
             progressed = true;
           }
         }
-        if (np < nq && mbar_test(bar(B_PFULL + (np & 1)), (np >> 1) & 1)) {
+        if (np < nq && mbar_test(bar(B_PFULL + (np & 1)), (np >> 1) & 1) &&
+            mbar_test(bar(B_VFULL + np % C::SLOTS), (np / C::SLOTS) & 1)) {
           tc_fence_after();
           const int sl = np % C::SLOTS;
           // V rows 0..63 (keys 0..31, 64..95) belong to key set 0, rows 64..127 to key set 1:
@@ -540,7 +553,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       // there (possibly NaN); their P is 0, but 0 * NaN is not, so zero those rows.
       if (ckey0 + C::KEYS > total_keys) {
         const int sl = u % C::SLOTS;
-        if (__all_sync(0xffffffffu, wait(B_FULL + sl, (u / C::SLOTS) & 1))) {
+        if (__all_sync(0xffffffffu, wait(B_VFULL + sl, (u / C::SLOTS) & 1))) {
           const int nv = total_keys - ckey0;  // 1..127 valid keys
           const int units = C::NB * (C::KEYS - nv) * 8;
           for (int w = tg; w < units; w += 256) {

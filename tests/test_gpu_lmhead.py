@@ -1,7 +1,11 @@
 """GPU parity of the fused LM head (spec_lm_head_stats) against the fp64 oracle, through the C ABI.
 
-Max, log of the sum of exp and the gathered logits within 1e-3 (bf16 products, fp32 accumulation
-over H); the argmax exact except in rows whose two largest logits lie within 1e-3 (counted).
+Max and the gathered logits within tol(H) = H * 7.5e-8, the log of the sum of exp within
+2 tol(H) / T; the argmax exact except in rows whose two largest logits lie within tol(H) (counted).
+The bound: the bf16 x bf16 products are exact in fp32, so the error is the tensor core's fp32
+accumulation over H / 16 steps of K = 16, each taken as losing at most 2^-23 of a logit of magnitude
+<= 10 (logits ~ N(0, 3^2) here): (H / 16) * 2^-23 * 10.  Observed on a GB300: 7.1e-5 at H = 4096,
+0.7e-5 to 1.0e-5 at H = 512 / 520 (float32 BLAS accumulation of the same products: about 4e-6).
 Shapes: one ragged row tile (M = 60) and several (M = 300), H a multiple of 64 or not, V a whole
 number of 256-entry tiles or not, V = 128256; temperatures 1 and 0.7.  The statistics then drive
 greedy verification of a tree: the argmax gives the same walk as the full logits.
@@ -16,7 +20,8 @@ from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
-TOL = 1e-3
+def tol(H):
+    return H * 7.5e-8
 
 
 @pytest.fixture(scope="module")
@@ -40,9 +45,12 @@ def _check(case, dev, T):
     got = _run(case, dev, T)
     ref = OL.lm_head_stats(W.bf16_to_f64(case.hidden), W.bf16_to_f64(case.weight), T,
                            case.gather_idx if case.gather_idx.shape[1] else None)
+    M, H = case.hidden.shape
+    TOL = tol(H)
     assert got["status"][0] == 0
     assert np.abs(got["max"] - ref["max"]).max() <= TOL
-    assert np.abs(np.log(got["sumexp"]) - np.log(ref["sumexp"])).max() <= TOL
+    lse_err = np.abs(np.log(got["sumexp"]) - np.log(ref["sumexp"])).max()
+    assert lse_err <= 2 * TOL / T, lse_err
     near = ref["top_gap"] < TOL
     assert np.array_equal(got["argmax"][~near], ref["argmax"][~near])
     assert near.sum() <= max(1, len(near) // 50), near.sum()
@@ -50,9 +58,9 @@ def _check(case, dev, T):
         ok = ~np.isnan(ref["gather"])
         assert np.array_equal(ok, ~np.isnan(got["gather"]))
         assert np.abs(got["gather"][ok] - ref["gather"][ok]).max() <= TOL
-    M, H = case.hidden.shape
     print(f"M={M} H={H} V={case.weight.shape[0]} T={T}: max err "
-          f"{np.abs(got['max'] - ref['max']).max():.2e}, near-tie rows {int(near.sum())}")
+          f"{np.abs(got['max'] - ref['max']).max():.2e}, log-sum-exp err {lse_err:.2e}, "
+          f"near-tie rows {int(near.sum())}")
 
 
 @pytest.mark.parametrize("M,H,V,G,T", [
@@ -80,7 +88,8 @@ def test_statistics_drive_greedy_verification(dev):
         for i in range(1, N):
             tok[b, i] = am[b, par[b, i]] if rng.random() < 0.6 else int(rng.integers(V))
     ref = OV.tree_verify(lg, None, tok, par, np.zeros((B, N), np.float32), 0.0)
-    near = OL.row_stats(lg.reshape(B * N, V), 1.0)["top_gap"].reshape(B, N) < TOL
+    # near ties: logits ~ N(0, 4^2) here, so the bound of tol(H) scales by 16 / 10; 1e-4 covers it
+    near = OL.row_stats(lg.reshape(B * N, V), 1.0)["top_gap"].reshape(B, N) < 1e-4
     for b in range(B):
         if near[b].any():
             continue
