@@ -90,6 +90,31 @@ __device__ __forceinline__ float ex2_approx(float x) {  // hardware 2^x (P is ro
   return y;
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {  // one three-input max
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (a0, a1) * m + c on the packed fp32 pipe (two lanes of one instruction, each rounded as fmaf)
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float m, float c) {
+  uint64_t a, mm, cc;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(m));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(a) : "l"(a), "l"(mm), "l"(cc));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+}
+
+// (s0, s1) += (a0, a1) on the packed fp32 pipe
+__device__ __forceinline__ void fadd2(float& s0, float& s1, float a0, float a1) {
+  uint64_t s, a;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(s) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(s), "l"(a));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(s));
+}
+
 __device__ __forceinline__ void tmem_ldq(uint32_t taddr, float (&v)[32]) { tmem_ld32(taddr, v); }
 __device__ __forceinline__ void tmem_ldq(uint32_t taddr, float (&v)[16]) { tmem_ld16(taddr, v); }
 
@@ -153,11 +178,13 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   uint8_t* ring = base;
   uint8_t* q_s = base + C::OFF_Q;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::OFF_BAR);
-  // B_FULL: a slot's K landed; B_VFULL: its V landed (the QK needs only K, so a chunk's QK does
-  // not wait for its V boxes, which are issued after its K boxes)
-  const int B_FULL = 0, B_EMPTY = C::SLOTS, B_SFULL = 2 * C::SLOTS, B_SFREE = 2 * C::SLOTS + 2,
+  // A slot's K and V halves fill and drain separately.  B_FULL: its K landed; B_VFULL: its V
+  // landed (a chunk's QK needs only K); B_KEMPTY: the QK that read its K completed; B_VEMPTY: the
+  // PV that read its V completed.  A chunk holds its K for the QK only, so the next K request into
+  // the slot goes out while the softmax of the chunk still runs.
+  const int B_FULL = 0, B_VEMPTY = C::SLOTS, B_SFULL = 2 * C::SLOTS, B_SFREE = 2 * C::SLOTS + 2,
             B_PFULL = 2 * C::SLOTS + 4, B_PV = 2 * C::SLOTS + 6, B_DONE = 2 * C::SLOTS + 7,
-            B_SETUP = 2 * C::SLOTS + 8, B_VFULL = 2 * C::SLOTS + 9;
+            B_SETUP = 2 * C::SLOTS + 8, B_VFULL = 2 * C::SLOTS + 9, B_KEMPTY = 3 * C::SLOTS + 9;
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -182,7 +209,8 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
     for (int i = 0; i < C::SLOTS; ++i) {
       mbar_init(bar(B_FULL + i), 1);
       mbar_init(bar(B_VFULL + i), 1);
-      mbar_init(bar(B_EMPTY + i), 1);
+      mbar_init(bar(B_VEMPTY + i), 1);
+      mbar_init(bar(B_KEMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {  // [S / P buffer]
       mbar_init(bar(B_SFULL + i), 1);
@@ -228,66 +256,63 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   // which reads zeros (the set-up flags it when a slot the call needs is there).  K boxes of
   // min(P, 128) rows, V boxes of min(P, 32) rows in the PV block order (see v_block_key).
   const int P = PAGED ? p.page_size : 0;
+  const int Pd = PAGED ? p.page_size : 1;   // P as a divisor (the paged code only runs with P > 0)
   const int past = p.num_pages * p.Hkv * P;  // paged: first row past the tensor
   auto page_rows = [&](int ci) -> int {     // lane l: first row of the chunk's l-th page
     int yl = past;
-    const int lp0 = (ci * C::KEYS) / P;
-    if (lane < (P >= C::KEYS ? 1 : C::KEYS / P) && lp0 + lane < p.max_pages) {
+    const int lp0 = (ci * C::KEYS) / Pd;
+    if (lane < (P >= C::KEYS ? 1 : C::KEYS / Pd) && lp0 + lane < p.max_pages) {
       const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + lp0 + lane);
       if (pg >= 0 && pg < p.num_pages) yl = (pg * p.Hkv + kvh) * P;
     }
     return yl;
   };
-  // One chunk: its K boxes complete on B_FULL, its V boxes on B_VFULL, K issued first.
-  auto issue_chunk = [&](int sl, int ci, int yl) {
+  // One half of a chunk into ring slot sl: its K boxes (completing on B_FULL) or its V boxes
+  // (on B_VFULL).  Warp 0 calls it with every lane.
+  auto issue_half = [&](int sl, int ci, int yl, bool v) {
     uint8_t* st = ring + sl * C::TILE;
-    const uint32_t fb = bar(B_FULL + sl), fv = bar(B_VFULL + sl);
-    if (lane == 0) {
-      mbar_arrive_expect_tx(fb, C::TILE / 2);
-      mbar_arrive_expect_tx(fv, C::TILE / 2);
-    }
+    const uint32_t fb = bar((v ? B_VFULL : B_FULL) + sl);
+    if (lane == 0) mbar_arrive_expect_tx(fb, C::TILE / 2);
     if (P == 0) {  // contiguous: issued by one lane (measured faster than spread over lanes)
       if (lane == 0) {
         const int y = row0 + ci * C::KEYS;
+        if (!v) {
 #pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx)
-          tma_load_2d(smem_u32(st + bx * C::BOX), &tmap_k, fb, bx * 64, y);
+          for (int bx = 0; bx < C::NB; ++bx)
+            tma_load_2d(smem_u32(st + bx * C::BOX), &tmap_k, fb, bx * 64, y);
+        } else {
 #pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx)
+          for (int bx = 0; bx < C::NB; ++bx)
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX + j * 32 * 128), &tmap_v, fv, bx * 64,
-                        y + 32 * v_block_key(j));
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(smem_u32(st + (C::NB + bx) * C::BOX + j * 32 * 128), &tmap_v, fb,
+                          bx * 64, y + 32 * v_block_key(j));
+        }
       }
       return;
     }
     __syncwarp();
-    const int kb_rows = (P == 0 || P >= C::KEYS) ? C::KEYS : P;
-    const int vb_rows = (P == 0 || P >= 32) ? 32 : P;
-    const int nk = C::NB * (C::KEYS / kb_rows), nv = C::NB * (C::KEYS / vb_rows);
-    int key = ci * C::KEYS, dst = 0, bx = 0;  // this lane's box: list of K boxes, then V boxes
-    const bool is_v = lane >= nk;
-    if (!is_v) {
-      const int i = lane % (C::KEYS / kb_rows);
-      bx = lane / (C::KEYS / kb_rows);
-      key += i * kb_rows;
-      dst = bx * C::BOX + i * kb_rows * 128;
-    } else if (lane < nk + nv) {
-      const int m = lane - nk, i = m % (C::KEYS / vb_rows);
-      bx = m / (C::KEYS / vb_rows);
-      const int j = (i * vb_rows) >> 5, t = (i * vb_rows) & 31;  // V row block j, row t in it
+    const int rows = v ? ((P >= 32) ? 32 : P) : ((P >= C::KEYS) ? C::KEYS : P);  // box rows
+    const int per = C::KEYS / rows;  // boxes per 64-dim block
+    const int nbox = C::NB * per;    // <= 32: one box per lane
+    const int ln = lane < nbox ? lane : 0;
+    const int i = ln % per, bx = ln / per;
+    int key = ci * C::KEYS, dst;
+    if (!v) {
+      key += i * rows;
+      dst = bx * C::BOX + i * rows * 128;
+    } else {
+      const int j = (i * rows) >> 5, t = (i * rows) & 31;  // V row block j, row t in it
       key += 32 * v_block_key(j) + t;
       dst = (C::NB + bx) * C::BOX + (32 * j + t) * 128;
     }
-    int y;
-    if (P == 0) {
-      y = row0 + key;
-    } else {
-      y = __shfl_sync(0xffffffffu, yl, key / P - (ci * C::KEYS) / P);
-      y = y >= past ? past : y + key % P;
-    }
-    if (lane < nk + nv)  // one instruction for the chunk: the K lanes' boxes come first
-      tma_load_2d(smem_u32(st + dst), is_v ? &tmap_v : &tmap_k, is_v ? fv : fb, bx * 64, y);
+    int y = __shfl_sync(0xffffffffu, yl, key / Pd - (ci * C::KEYS) / Pd);
+    y = y >= past ? past : y + key % Pd;
+    if (lane < nbox) tma_load_2d(smem_u32(st + dst), v ? &tmap_v : &tmap_k, fb, bx * 64, y);
+  };
+  auto issue_chunk = [&](int sl, int ci, int yl) {
+    issue_half(sl, ci, yl, false);
+    issue_half(sl, ci, yl, true);
   };
   if (warp == 0) {
     // the split's first chunks do not depend on the prefix length: issue them now (a chunk past
@@ -383,25 +408,56 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   float m_used = -INFINITY, l = 0.f;  // softmax threads: running max (log2 units) and sum
   bool ok_rows = true;                // softmax warps: every step completed (no timeout)
   if (warp == 0) {
-    // ---------------- TMA producer (the whole warp: it reads block-table entries in parallel)
-    int issued = spec;
-    for (int it = spec; it < my_tiles; ++it) {
-      const int s = it % C::SLOTS;
-      const int yl = P > 0 ? page_rows(t_begin + it) : 0;  // in flight during the wait
-      if (it >= C::SLOTS && !__all_sync(0xffffffffu, wait(B_EMPTY + s, ((it / C::SLOTS) - 1) & 1)))
+    // ---------------- TMA producer (the whole warp: it reads block-table entries in parallel).
+    // K of chunk kq goes out once the QK of the chunk before it in the slot completed, V of chunk
+    // vq once that chunk's PV completed; whichever is ready first.
+    int kq = spec, vq = spec;
+    int yk = (P > 0 && kq < my_tiles) ? page_rows(t_begin + kq) : 0;  // page rows of chunk kq
+    int yv = yk;                                                     // ... and of chunk vq
+    uint32_t idle = 0;
+    while (vq < my_tiles) {
+      bool progressed = false;
+      if (kq < my_tiles) {
+        const int s = kq % C::SLOTS;
+        const uint32_t par = ((kq / C::SLOTS) - 1) & 1;
+        if (kq < C::SLOTS || __any_sync(0xffffffffu, mbar_test(bar(B_KEMPTY + s), par))) {
+          if (kq >= C::SLOTS) mbar_wait(bar(B_KEMPTY + s), par);  // complete: every lane acquires
+          issue_half(s, t_begin + kq, yk, false);
+          ++kq;
+          if (P > 0 && kq < my_tiles) yk = page_rows(t_begin + kq);
+          progressed = true;
+        }
+      }
+      if (vq < kq) {
+        const int s = vq % C::SLOTS;
+        const uint32_t par = ((vq / C::SLOTS) - 1) & 1;
+        if (vq < C::SLOTS || __any_sync(0xffffffffu, mbar_test(bar(B_VEMPTY + s), par))) {
+          if (vq >= C::SLOTS) mbar_wait(bar(B_VEMPTY + s), par);
+          issue_half(s, t_begin + vq, yv, true);
+          ++vq;
+          if (P > 0 && vq < my_tiles) yv = page_rows(t_begin + vq);
+          progressed = true;
+        }
+      }
+      if (progressed) {
+        idle = 0;
+      } else if (++idle > kSpinLimit || abort_s) {
+        abort_s = 1;
         break;
-      issue_chunk(s, t_begin + it, yl);
-      issued = it + 1;
+      } else {
+        __nanosleep(20);
+      }
     }
     if (lane == 0) {
       // never leave with a copy in flight: speculative tiles nobody consumed, or an abort
       // (bounded waits)
-      if (abort_s || my_tiles < spec)
-        for (int it = max(0, issued - C::SLOTS); it < issued; ++it)
-          if (abort_s || it >= my_tiles) {
-            mbar_wait(bar(B_FULL + it % C::SLOTS), (it / C::SLOTS) & 1);
+      if (abort_s || my_tiles < spec) {
+        for (int it = max(0, kq - C::SLOTS); it < kq; ++it)
+          if (abort_s || it >= my_tiles) mbar_wait(bar(B_FULL + it % C::SLOTS), (it / C::SLOTS) & 1);
+        for (int it = max(0, vq - C::SLOTS); it < vq; ++it)
+          if (abort_s || it >= my_tiles)
             mbar_wait(bar(B_VFULL + it % C::SLOTS), (it / C::SLOTS) & 1);
-          }
+      }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: QK of step u once its chunk landed and S[u % 2] is free (and
@@ -434,6 +490,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
               tc_mma_bf16(d, ad, bd, IQK, ks > 0 ? 1u : 0u);
             }
             tc_commit(bar(B_SFULL + (nq & 1)));
+            tc_commit(bar(B_KEMPTY + sl));  // the slot's K half may be refilled
             ++nq;
             progressed = true;
           }
@@ -452,7 +509,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
             tc_mma_bf16_ts(tmem + C::O_COL + (uint32_t)((kk >> 2) * 128), p_tm + (uint32_t)(kk * 8),
                            bd, IPV, (np > 0 || (kk & 3) > 0) ? 1u : 0u);
           }
-          tc_commit(bar(B_EMPTY + sl));  // the chunk's slot is free once these MMAs complete
+          tc_commit(bar(B_VEMPTY + sl));  // the slot's V half may be refilled
           tc_commit(bar(B_PV));
           ++np;
           progressed = true;
@@ -502,24 +559,27 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       const uint32_t scol0 = (uint32_t)((u & 1) * C::S_COLS);
       // this thread's 32-key blocks: half hf = gi (key groups) or 0 and 1; S columns
       // 64 hf + 32 ks, P columns 32 ks + 16 hf (inside the S columns this warp has read)
-      float x[2][32];
+      constexpr int NH = (kg == 2) ? 1 : 2;
+      float x[NH][32];
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh)
+        tmem_ld32(lane_base + scol0 + (uint32_t)(64 * ((kg == 2) ? gi : hh) + 32 * ks), x[hh]);
+      tmem_wait_ld();
       float mx = -INFINITY;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        if (hh == 1 && kg == 2) break;
-        const int hf = (kg == 2) ? gi : hh;
-        tmem_ld32(lane_base + scol0 + (uint32_t)(64 * hf + 32 * ks), x[hh]);
-        tmem_wait_ld();
-        const uint32_t vis = visible32(ckey0 + 64 * hf + 32 * ks);
+      for (int hh = 0; hh < NH; ++hh) {
+        const uint32_t vis = visible32(ckey0 + 64 * ((kg == 2) ? gi : hh) + 32 * ks);
+        if (vis != 0xffffffffu) {  // only blocks at the end of the prefix or in the tree
 #pragma unroll
-        for (int c = 0; c < 32; ++c) x[hh][c] = ((vis >> c) & 1u) ? x[hh][c] : -INFINITY;
-        float m0 = fmaxf(x[hh][0], x[hh][1]), m1 = fmaxf(x[hh][2], x[hh][3]);
-#pragma unroll
-        for (int c = 4; c < 32; c += 4) {
-          m0 = fmaxf(m0, fmaxf(x[hh][c], x[hh][c + 1]));
-          m1 = fmaxf(m1, fmaxf(x[hh][c + 2], x[hh][c + 3]));
+          for (int c = 0; c < 32; ++c) x[hh][c] = ((vis >> c) & 1u) ? x[hh][c] : -INFINITY;
         }
-        mx = fmaxf(mx, fmaxf(m0, m1));
+        float m0 = max3f(x[hh][0], x[hh][1], x[hh][2]), m1 = max3f(x[hh][3], x[hh][4], x[hh][5]);
+#pragma unroll
+        for (int c = 6; c < 30; c += 4) {
+          m0 = max3f(m0, x[hh][c], x[hh][c + 1]);
+          m1 = max3f(m1, x[hh][c + 2], x[hh][c + 3]);
+        }
+        mx = max3f(mx, max3f(m0, x[hh][30], x[hh][31]), m1);
       }
       const float mt = mx * sc;  // scale > 0
       const bool raise = mt > m_used + 8.f;
@@ -529,23 +589,23 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
         m_used = mt;
       }
       const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-      float rs = 0.f;
+      float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        if (hh == 1 && kg == 2) break;
+      for (int hh = 0; hh < NH; ++hh) {
         const int hf = (kg == 2) ? gi : hh;
-        float r0 = 0.f, r1 = 0.f;
         float pk[16];  // P as bf16 pairs (bit patterns), key 2c in the low half of column c
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float a0 = ex2_approx(fmaf(x[hh][2 * c], sc, neg_m));
-          const float a1 = ex2_approx(fmaf(x[hh][2 * c + 1], sc, neg_m));
-          if (c & 1) r1 += a0 + a1; else r0 += a0 + a1;
+          float a0 = x[hh][2 * c], a1 = x[hh][2 * c + 1];
+          ffma2(a0, a1, sc, neg_m);
+          a0 = ex2_approx(a0);
+          a1 = ex2_approx(a1);
+          if (c & 1) fadd2(r2, r3, a0, a1); else fadd2(r0, r1, a0, a1);
           pk[c] = __uint_as_float(pack_bf16(a0, a1));
         }
-        rs += r0 + r1;
         tmem_st16(lane_base + scol0 + (uint32_t)(32 * ks + 16 * hf), pk);
       }
+      const float rs = (r0 + r1) + (r2 + r3);
       // key groups: the other group's P columns of this set are zero for this row
       if (kg == 2) tmem_st16(lane_base + scol0 + (uint32_t)(32 * ks + 16 * (1 - gi)), zero16);
       l = l * factor + rs;
