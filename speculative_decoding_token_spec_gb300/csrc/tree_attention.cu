@@ -179,11 +179,12 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   uint8_t* q_s = base + C::OFF_Q;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::OFF_BAR);
   // A slot's K and V halves fill and drain separately.  B_FULL: its K landed; B_VFULL: its V
-  // landed (a chunk's QK needs only K); B_KEMPTY: the QK that read its K completed; B_VEMPTY: the
-  // PV that read its V completed.  A chunk holds its K for the QK only, so the next K request into
-  // the slot goes out while the softmax of the chunk still runs.
+  // landed (a chunk's QK needs only K); B_KEMPTY: the QK that read its K completed (a softmax warp
+  // arrives once it sees the scores); B_VEMPTY: the PV that read its V completed (also how the
+  // softmax warps learn that a chunk's PV is done).  A chunk holds its K for the QK only, so the
+  // next K request into the slot goes out while the softmax of the chunk still runs.
   const int B_FULL = 0, B_VEMPTY = C::SLOTS, B_SFULL = 2 * C::SLOTS, B_SFREE = 2 * C::SLOTS + 2,
-            B_PFULL = 2 * C::SLOTS + 4, B_PV = 2 * C::SLOTS + 6, B_DONE = 2 * C::SLOTS + 7,
+            B_PFULL = 2 * C::SLOTS + 4, B_DONE = 2 * C::SLOTS + 7,
             B_SETUP = 2 * C::SLOTS + 8, B_VFULL = 2 * C::SLOTS + 9, B_KEMPTY = 3 * C::SLOTS + 9;
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
@@ -217,7 +218,6 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       mbar_init(bar(B_SFREE + i), 8);  // one arrival per softmax warp
       mbar_init(bar(B_PFULL + i), 8);
     }
-    mbar_init(bar(B_PV), 1);
     mbar_init(bar(B_DONE), 1);
     mbar_init(bar(B_SETUP), 1);
     mbar_fence_init();
@@ -490,7 +490,6 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
               tc_mma_bf16(d, ad, bd, IQK, ks > 0 ? 1u : 0u);
             }
             tc_commit(bar(B_SFULL + (nq & 1)));
-            tc_commit(bar(B_KEMPTY + sl));  // the slot's K half may be refilled
             ++nq;
             progressed = true;
           }
@@ -510,7 +509,6 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
                            bd, IPV, (np > 0 || (kk & 3) > 0) ? 1u : 0u);
           }
           tc_commit(bar(B_VEMPTY + sl));  // the slot's V half may be refilled
-          tc_commit(bar(B_PV));
           ++np;
           progressed = true;
         }
@@ -555,6 +553,9 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
         break;
       }
       tc_fence_after();
+      // the QK of this chunk completed: its K half of the slot may be refilled (one commit less
+      // for the MMA issuer, whose every instruction delays the next MMA)
+      if (warp == 2 && lane == 0) mbar_arrive(bar(B_KEMPTY + u % C::SLOTS));
       const int ckey0 = (t_begin + u) * C::KEYS;
       const uint32_t scol0 = (uint32_t)((u & 1) * C::S_COLS);
       // this thread's 32-key blocks: half hf = gi (key groups) or 0 and 1; S columns
@@ -627,7 +628,8 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       }
       // O rescale (only after the first step, only if some row of this warp raised its max)
       if (u > 0 && __any_sync(0xffffffffu, raise)) {
-        if (__all_sync(0xffffffffu, wait(B_PV, (u - 1) & 1))) {
+        const int up = u - 1;  // its PV completed: O holds every earlier chunk
+        if (__all_sync(0xffffffffu, wait(B_VEMPTY + up % C::SLOTS, (up / C::SLOTS) & 1))) {
           tc_fence_after();
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -649,7 +651,10 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
         mbar_arrive(bar(B_PFULL + (u & 1)));
       }
     }
-    if (ok_rows && U > 0) ok_rows = __all_sync(0xffffffffu, wait(B_PV, (U - 1) & 1));
+    if (ok_rows && U > 0) {  // the last PV completed
+      const int ul = U - 1;
+      ok_rows = __all_sync(0xffffffffu, wait(B_VEMPTY + ul % C::SLOTS, (ul / C::SLOTS) & 1));
+    }
     if (ok_rows && U > 0) tc_fence_after();
   }
 
