@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   // arrives once it sees the scores); B_VEMPTY: the PV that read its V completed (also how the
   // softmax warps learn that a chunk's PV is done).  A chunk holds its K for the QK only, so the
   // next K request into the slot goes out while the softmax of the chunk still runs.
-  const int B_FULL = 0, B_VEMPTY = C::SLOTS, B_SFULL = 2 * C::SLOTS, B_SFREE = 2 * C::SLOTS + 2,
+  const int B_FULL = 0, B_VEMPTY = C::SLOTS, B_SFULL = 2 * C::SLOTS,
             B_PFULL = 2 * C::SLOTS + 4, B_DONE = 2 * C::SLOTS + 7,
             B_SETUP = 2 * C::SLOTS + 8, B_VFULL = 2 * C::SLOTS + 9, B_KEMPTY = 3 * C::SLOTS + 9;
   auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -215,7 +215,6 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
     }
     for (int i = 0; i < 2; ++i) {  // [S / P buffer]
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SFREE + i), 8);  // one arrival per softmax warp
       mbar_init(bar(B_PFULL + i), 8);
     }
     mbar_init(bar(B_DONE), 1);
@@ -460,10 +459,12 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: QK of step u once its chunk landed and S[u % 2] is free (and
-    // the PV of step u - 2, which read the P that step u overwrites, was issued before it: the
-    // tensor pipe runs a CTA's MMAs in issue order); PV of step u once its P is written.
-    // Whichever is ready goes first.
+    // ---------------- MMA issuer: QK of step u once its K landed and the PV of step u - 2 was
+    // issued (that PV reads the P that step u overwrites, and the tensor pipe runs a CTA's MMAs
+    // in issue order; its issue also means the softmax is done with S[u % 2]); PV of step u once
+    // its P is written (which the softmax signals only after the chunk's V landed).  Whichever is
+    // ready goes first, and each probes one barrier: a probe costs the issuer a shared-memory
+    // round trip, during which the tensor pipe drains.
     if (lane == 0 && my_tiles > 0) {
       constexpr uint32_t IQK = idesc_bf16_f32(128, C::KEYS, false);
       constexpr uint32_t IPV = idesc_bf16_f32(128, D, true);
@@ -474,10 +475,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
         bool progressed = false;
         if (nq < U && nq <= np + 1) {
           const int sl = nq % C::SLOTS;
-          const bool rdy =
-              (nq < 2 || mbar_test(bar(B_SFREE + (nq & 1)), ((nq >> 1) - 1) & 1)) &&
-              mbar_test(bar(B_FULL + sl), (nq / C::SLOTS) & 1);
-          if (rdy) {
+          if (mbar_test(bar(B_FULL + sl), (nq / C::SLOTS) & 1)) {
             tc_fence_after();
             const uint32_t k_addr = smem_u32(ring + sl * C::TILE);
             const uint32_t d = tmem + (uint32_t)((nq & 1) * C::S_COLS);
@@ -494,8 +492,7 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
             progressed = true;
           }
         }
-        if (np < nq && mbar_test(bar(B_PFULL + (np & 1)), (np >> 1) & 1) &&
-            mbar_test(bar(B_VFULL + np % C::SLOTS), (np / C::SLOTS) & 1)) {
+        if (np < nq && mbar_test(bar(B_PFULL + (np & 1)), (np >> 1) & 1)) {
           tc_fence_after();
           const int sl = np % C::SLOTS;
           // V rows 0..63 (keys 0..31, 64..95) belong to key set 0, rows 64..127 to key set 1:
@@ -645,11 +642,14 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       tmem_wait_st();  // P (and a rescaled O) are in TMEM before the PV MMA reads them
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(B_SFREE + (u & 1)));  // QK of step u + 2 may overwrite S[u % 2] (and P
-                                              // once PV of step u, issued before it, has run)
-        mbar_arrive(bar(B_PFULL + (u & 1)));
+      // P is written and the scores read; the chunk's V has landed too, so that the MMA issuer
+      // probes this one barrier before the PV (the QK of step u + 2, which overwrites S[u % 2],
+      // follows that PV)
+      if (!__all_sync(0xffffffffu, wait(B_VFULL + u % C::SLOTS, (u / C::SLOTS) & 1))) {
+        ok_rows = false;
+        break;
       }
+      if (lane == 0) mbar_arrive(bar(B_PFULL + (u & 1)));
     }
     if (ok_rows && U > 0) {  // the last PV completed
       const int ul = U - 1;
