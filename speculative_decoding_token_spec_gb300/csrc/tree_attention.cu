@@ -34,11 +34,13 @@
 //                bf16 pairs written over the scores it came from.  The reference max is only raised
 //                when a chunk's max exceeds it by more than 8 (2^8 headroom in fp32); only then is
 //                that key set's O in TMEM rescaled.
+//   The ring's slots fill and drain by halves: a chunk's K half is refilled once its scores are
+//   read, its V half once its PV completed.
 // Combine.  A query's partials inside the CTA (2 key sets, and with key groups the rows r and
-// r + 64) merge with one named barrier; each merged row's unnormalised O, max m and sum l then go
-// into the shared memory of the cluster CTA that owns the row (row % splits) through
+// r + 64) merge with one named barrier; each merged row's unnormalised O (as bf16), max m and sum
+// l then go into the shared memory of the cluster CTA that owns the row (row % splits) through
 // distributed-shared-memory stores; the owner weights the S partials by 2^(m - M) / sum(l 2^(m - M))
-// and writes the bf16 output and the log-sum-exp.
+// in fp32 and writes the bf16 output and the log-sum-exp.
 #include <cuda.h>
 
 #include <mutex>
@@ -664,8 +666,11 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
   // which goes to the cluster CTA that owns the row.  Partial: (m, l, O) with m = NaN after a
   // timeout and l = 0 when it saw no key (its O is then never read).
   const int QO = owned_rows(kg, S);
-  // [S][QO][RSTRIDE] partial rows, then one trash row that rows without data are pushed into (so
-  // the push has no branch), then the (m, l) pairs [S][QO].  The ring is idle now.
+  // [S][QO][RSTRIDE floats] partial rows, then one trash row that rows without data are pushed into
+  // (so the push has no branch), then the (m, l) pairs [S][QO].  The ring is idle now.  A partial
+  // row travels as bf16 in the first half of its slot: unnormalised O keeps fp32's exponent range,
+  // and half the bytes cross the cluster (measured rel-L2 against the oracle 2.8e-3 against 2.2e-3
+  // with fp32 partials for the 60-node tree on 32 heads of 128; the output is bf16 anyway).
   float* recv_o = reinterpret_cast<float*>(ring);
   float2* recv_ml = reinterpret_cast<float2*>(recv_o + ((size_t)S * QO + 1) * C::RSTRIDE);
   // in-CTA exchange: the (m, l) of every (key set, lane) [2][128], then the raw accumulator
@@ -782,14 +787,16 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
         cluster_wait_acquire();  // every CTA's ring is free: the pushes may start
         if (live && gi == 0 && ks == 0) push_ml(tmo, has, M, Lsum);
         const size_t row = (live && has) ? (size_t)split * QO + ql : (size_t)S * QO;
-        const uint32_t dst = dsmem_addr(recv_o + row * C::RSTRIDE + my_c, owner);
+        const uint32_t dst =
+            dsmem_addr(reinterpret_cast<__nv_bfloat16*>(recv_o + row * C::RSTRIDE) + my_c, owner);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < Q4; k += 4) {
-          float v[4];
+        for (int k = 0; k < Q4; k += 8) {
+          float v[4], u[4];
           merged4(k, v);
-          dsmem_store_v4(dst + k * 4, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
-                                                 __float_as_uint(v[2]), __float_as_uint(v[3])));
+          merged4(k + 4, u);
+          dsmem_store_v4(dst + k * 2, make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
+                                                 pack_bf16(u[0], u[1]), pack_bf16(u[2], u[3])));
         }
       }
     } else {
@@ -838,12 +845,14 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
           tmem_ldq(lane_tm + C::O_COL + 128u + (uint32_t)c0, a1);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < HC; k += 4)
-            dsmem_store_v4(dst + (c0 + k) * 4,
-                           make_uint4(__float_as_uint(sel(w0, a0[k]) + sel(w1, a1[k])),
-                                      __float_as_uint(sel(w0, a0[k + 1]) + sel(w1, a1[k + 1])),
-                                      __float_as_uint(sel(w0, a0[k + 2]) + sel(w1, a1[k + 2])),
-                                      __float_as_uint(sel(w0, a0[k + 3]) + sel(w1, a1[k + 3]))));
+          for (int k = 0; k < HC; k += 8) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = sel(w0, a0[k + j]) + sel(w1, a1[k + j]);
+            dsmem_store_v4(dst + (c0 + k) * 2,
+                           make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
+                                      pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7])));
+          }
         }
       }
     }
@@ -871,10 +880,15 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       const float mn = has ? fmaxf(M, ml.x) : M;
       const float a = (M == mn) ? 1.f : ex2_approx(M - mn);
       const float w = has ? ex2_approx(ml.x - mn) : 0.f;
-      const float* src = recv_o + ((size_t)e * QO + ql) * C::RSTRIDE + c;
-      const float4 v0 = *reinterpret_cast<const float4*>(src);
-      const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
-      const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      const uint4 hv = *reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(recv_o + ((size_t)e * QO + ql) * C::RSTRIDE) + c);
+      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = __uint_as_float(hw[j] << 16);
+        v[2 * j + 1] = __uint_as_float(hw[j] & 0xffff0000u);
+      }
 #pragma unroll
       for (int k = 0; k < 8; ++k) acc[k] = fmaf(acc[k], a, has ? w * v[k] : 0.f);
       Ls = fmaf(Ls, a, w * (has ? ml.y : 0.f));
