@@ -858,20 +858,29 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
     }
   }
   if (!single) {
+    tc_fence_before();  // this thread's TMEM reads are done
     cluster_arrive_release();
     cluster_wait_acquire();
+    // nothing reads TMEM any more: free it now rather than at the end
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
   }
-  // owner: rows qloc = ql * S + split of this block, 8 output columns per item.  out =
-  // sum_e 2^(m_e - M) O_e / sum_e 2^(m_e - M) l_e over the row's S partials e (one per split).
+  // owner: rows qloc = ql * S + split of this block, 16 output columns per item (one round of
+  // items for the 60-node tree on three splits).  out = sum_e 2^(m_e - M) O_e / sum_e 2^(m_e - M)
+  // l_e over the row's S partials e (one per split).
   const int E = S;
-  constexpr int C8 = D / 8;
-  for (int it = tid; !single && it < QO * C8; it += C::THREADS) {
-    const int ql = it / C8, c = (it % C8) * 8, ql_loc = ql * S + split;
+  constexpr int C16 = D / 16;
+  for (int it = tid; !single && it < QO * C16; it += C::THREADS) {
+    const int ql = it / C16, c = (it % C16) * 16, ql_loc = ql * S + split;
     const int q = rb * 128 + ql_loc;
     if (ql_loc >= 128 / kg || q >= p.R) continue;
     // one online pass over the partials (selects, no branches in the body)
     float M = -INFINITY, Ls = 0.f;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
     bool timeout = false;
     for (int e = 0; e < E; ++e) {
       const float2 ml = recv_ml[(size_t)e * QO + ql];
@@ -880,29 +889,32 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       const float mn = has ? fmaxf(M, ml.x) : M;
       const float a = (M == mn) ? 1.f : ex2_approx(M - mn);
       const float w = has ? ex2_approx(ml.x - mn) : 0.f;
-      const uint4 hv = *reinterpret_cast<const uint4*>(
+      const uint4* src = reinterpret_cast<const uint4*>(
           reinterpret_cast<const __nv_bfloat16*>(recv_o + ((size_t)e * QO + ql) * C::RSTRIDE) + c);
-      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-      float v[8];
+      const uint4 h0 = src[0], h1 = src[1];
+      const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[2 * j] = __uint_as_float(hw[j] << 16);
-        v[2 * j + 1] = __uint_as_float(hw[j] & 0xffff0000u);
+      for (int j = 0; j < 8; ++j) {
+        const float v0 = __uint_as_float(hw[j] << 16), v1 = __uint_as_float(hw[j] & 0xffff0000u);
+        acc[2 * j] = fmaf(acc[2 * j], a, has ? w * v0 : 0.f);
+        acc[2 * j + 1] = fmaf(acc[2 * j + 1], a, has ? w * v1 : 0.f);
       }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) acc[k] = fmaf(acc[k], a, has ? w * v[k] : 0.f);
       Ls = fmaf(Ls, a, w * (has ? ml.y : 0.f));
       M = mn;
     }
     const bool row_ok = !timeout && Ls > 0.f;
     const float inv = row_ok ? __frcp_rn(Ls) : 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] *= inv;
     const float Lsum = Ls;
     const int i = q / g, hq = kvh * g + q % g;
-    *reinterpret_cast<uint4*>(p.out + (((size_t)b * N + i) * p.Hq + hq) * D + c) =
-        make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
-                   pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
+    uint4* dst = reinterpret_cast<uint4*>(p.out + (((size_t)b * N + i) * p.Hq + hq) * D + c);
+    auto out8 = [&](int k) {  // columns c + k .. c + k + 7, normalised, as bf16
+      return make_uint4(pack_bf16(acc[k] * inv, acc[k + 1] * inv),
+                        pack_bf16(acc[k + 2] * inv, acc[k + 3] * inv),
+                        pack_bf16(acc[k + 4] * inv, acc[k + 5] * inv),
+                        pack_bf16(acc[k + 6] * inv, acc[k + 7] * inv));
+    };
+    dst[0] = out8(0);
+    dst[1] = out8(8);
     if (c == 0) {
       if (p.lse)
         p.lse[((size_t)b * p.Hq + hq) * N + i] =
@@ -910,11 +922,13 @@ __global__ void __launch_bounds__(320, 1) tree_attn_kernel(
       if (timeout && p.status) atomicOr(p.status + b, SPEC_ST_TIMEOUT);
     }
   }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+  if (single) {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
   }
 }
 
