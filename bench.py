@@ -1038,7 +1038,11 @@ def measure_other_workloads(args, dev, futs, hbm_gbs, tc_tflops, timed, L2):
                       "attn_frac": attn_bytes / (us["attn"] * 1e-6) / 1e9 / hbm_gbs,
                       "attn_tflops": flops / (us["attn"] * 1e-6) / 1e12,
                       "attn_tensor_frac": flops / (us["attn"] * 1e-6) / 1e12 / tc_tflops,
-                      "step_hbm_frac": (attn_bytes + ver_bytes) / (hbm_gbs * 1e9) / step_s,
+                      # the bytes the step reads: the path form reads only the walk's rows
+                      "step_hbm_frac": (attn_bytes + (read_bytes if path_form else ver_bytes))
+                                       / (hbm_gbs * 1e9) / step_s,
+                      "step_hbm_frac_all_rows": (attn_bytes + ver_bytes) / (hbm_gbs * 1e9)
+                                                / step_s,
                       "dominant_kernel": "tree_attn_kernel" if us["attn"] >= us["verify"]
                                          else "verify_kernel"})
         out[key] = e
@@ -1048,7 +1052,9 @@ def measure_other_workloads(args, dev, futs, hbm_gbs, tc_tflops, timed, L2):
     out["note"] = ("per-call times from CUDA graphs of back-to-back calls (inputs larger than 2 x L2 "
                    "or rotated over copies that are); verify_algorithmic_bytes counts every "
                    "internal node's rows (the all-nodes count), verify_read_bytes the rows the path "
-                   "form actually reads; Q/K/V drawn on the device (seeded), the verification "
+                   "form actually reads; step_hbm_frac counts the bytes the step reads (the path "
+                   "form's rows), step_hbm_frac_all_rows every internal row (above 1 where the "
+                   "path form skips rows); Q/K/V drawn on the device (seeded), the verification "
                    "inputs by the workload generator; cpu_baseline: the fp64 oracle's "
                    "verification of the same inputs (near ties counted, the GPU's tokens compared "
                    "outside them)")
