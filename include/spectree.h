@@ -136,9 +136,12 @@ size_t spec_tree_verify_workspace(int B, int N, int V);
  *
  * Rows read.  Small problems (B * N * V * 4 <= 64 MiB) process every node at once; large ones
  * process every internal node when out_child_q is given, and otherwise only the nodes the walk
- * reaches (the root, then each accepted child, one step per level).  The results are the same;
- * SPEC_ST_NONFINITE reports NaN / +Inf in a row that was read, so a non-finite row off the walk
- * flags the sequence in the first two forms only.
+ * reaches (the root, then each accepted child, one step per level).  Without out_child_q the small
+ * form's walk starts as soon as the root's outcome is known and follows each accepted child as its
+ * outcome is published; once it ends, nodes still in their residual rounds stop.  The results are
+ * the same in every form.  SPEC_ST_NONFINITE reports NaN / +Inf in a row the walk depends on;
+ * a non-finite row off the walk flags the sequence only when out_child_q is given (every internal
+ * node is then processed in full).
  */
 int spec_tree_verify(const float* target_logits, const float* draft_probs,
                      const int32_t* tree_tokens, const int32_t* tree_parent,
@@ -156,7 +159,7 @@ int spec_tree_verify(const float* target_logits, const float* draft_probs,
  * only its input and output buffers.
  *
  * Same arguments, outputs and results as spec_tree_verify, minus the workspace.  The scratch lives
- * in one fixed device array inside the library (SPEC_NOALLOC_MAX_NODES * 40 bytes, 160 KB,
+ * in one fixed device array inside the library (SPEC_NOALLOC_MAX_NODES * 56 bytes, 224 KB,
  * held on every GPU that loads the library until the process exits).  Calls with
  * B * N > SPEC_NOALLOC_MAX_NODES return SPEC_ERR_NOALLOC_LIMIT.  Every call made outside stream
  * capture looks up the array's device address with the caller's device current; a call made while

@@ -36,6 +36,10 @@ struct VerifyArgs {
   int32_t* status;
   NodeStat* stats;  // [B, N]
   unsigned long long* counters;  // [B] arrival counters: (generation << 32) | (tag << 16) | arrivals
+  // [B, N] walk hand-over words and [B] walk-done words of the every-node form without per-child
+  // q: (generation << 32) | state (see tree_verify.cu); all reset by each sequence's last arrival
+  unsigned long long* handover;
+  unsigned long long* walk_done;
   unsigned long long gen;        // this call's generation (32 bits)
   int p_global = 0;  // set by launch_verify: draft rows read from global memory, not staged
   // polls of the first attempt of each bounded wait (row copies, cluster exchanges); a wait that

@@ -228,6 +228,8 @@ int spec_tree_verify(const float* target_logits, const float* draft_probs,
   a.status = status;
   a.stats = reinterpret_cast<NodeStat*>(ws);
   a.counters = reinterpret_cast<unsigned long long*>(ws + (size_t)B * N * sizeof(NodeStat));
+  a.handover = a.counters + B;
+  a.walk_done = a.handover + (size_t)B * N;
   static std::atomic<unsigned long long> call_gen{1};
   a.gen = call_gen.fetch_add(1) & 0xFFFFFFFFull;
   a.first_polls = g_verify_first_polls.load(std::memory_order_relaxed);

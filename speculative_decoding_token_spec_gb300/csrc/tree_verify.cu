@@ -443,10 +443,15 @@ __device__ void cluster_stats(const Slice& s, float* lbuf, float k, int lflags, 
 // Residual round: returns D = sum_y max(0, e(y) - c p(y)) (cluster-wide; c_t = c / f).  check_p:
 // flag bad draft values.  The thread's total of the new weights goes to `tot`, the warp's to
 // `wt`; `xs` is the slot whose sm.cpart holds the CTA totals.
-template <int CL, class PD>
+// `late()`: more flags of this thread, taken after its pass over the slice (the results of loads
+// issued before the call, whose round trips the pass hides).
+struct NoLateFlags {
+  __device__ __forceinline__ int operator()() const { return 0; }
+};
+template <int CL, class PD, class Late = NoLateFlags>
 __device__ DF cluster_residual(const Slice& s, const float* ebuf, const PD& pd, float c_t,
                                float f, bool check_p, int lflags, int rank, int& xk, DF& tot,
-                               DF& wt, int& xs, int& flags, VerifySmem& sm) {
+                               DF& wt, int& xs, int& flags, VerifySmem& sm, Late late = Late()) {
   const float4* E4 = reinterpret_cast<const float4*>(ebuf + threadIdx.x * s.ch);
   const int p0 = threadIdx.x * s.ch;
   CompSum acc;
@@ -468,7 +473,7 @@ __device__ DF cluster_residual(const Slice& s, const float* ebuf, const PD& pd, 
   const bool bad = check_p && (pmin < 0.f || !(psum <= FLT_MAX));  // NaN, +Inf or negative p
   tot = df_scale(df_from(acc), f);
   wt = warp_sum_df(tot);
-  const int wf = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0) | lflags;
+  const int wf = __reduce_or_sync(0xffffffffu, bad ? SPEC_ST_NONFINITE : 0) | lflags | late();
   const Entry r =
       exchange<CL, kXSum>(sm, xk, Entry{0.f, 0, wt.hi, wt.lo, wf, {0, 0, 0}}, 0.f, rank, xs);
   flags |= r.flags;
@@ -639,6 +644,75 @@ struct NodeBufs {
   uint32_t bar_l, bar_p;
 };
 
+// Exchange flag (never a status bit): some CTA of the cluster saw that the walk cannot reach the
+// node (it ended, or took another branch), so the node's outcome is no longer needed.
+constexpr int kWalkDone = 1 << 20;
+
+// The upper half of this call's hand-over and walk-done words: a hash of the generation with the
+// top bit set, which no cleared word (0), small integer, non-negative count or record field left
+// by another call carries, and which other words match only by chance.
+__device__ __forceinline__ unsigned long long handover_tag(unsigned long long gen) {
+  uint32_t h = (uint32_t)gen * 0x9E3779B1u;
+  h ^= h >> 15;
+  h |= 0x80000000u;
+  return h == 0xFFFFFFFFu ? 0x80000001ull : (unsigned long long)h;
+}
+
+// Has the walk of sequence b ended in this call?
+__device__ __forceinline__ bool walk_ended(const VerifyArgs& a, int b) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.walk_done + b) : "memory");
+  return (v >> 32) == handover_tag(a.gen) && (v & 1ull);
+}
+
+// The walk can no longer reach node j (its outcome is not needed) once the walk has ended, or once
+// an ancestor P on j's chain handed over an outcome other than "accept the child on the way to j"
+// (a terminal, or another child).  Thread 0 loads the walk-done word and the hand-over words of
+// the nearest kProbeDepth ancestors; `stop` reads them (false in every other thread).
+constexpr int kProbeDepth = 3;
+constexpr uint32_t kHandoverPublished = 1u << 31, kHandoverTerminal = 1u << 29;
+constexpr uint32_t kHandoverValueMask = (1u << 22) - 1u;
+struct StopProbe {
+  unsigned long long done = 0, anc[kProbeDepth];
+  int child[kProbeDepth];  // the child of that ancestor on the way to j
+  int n = 0;
+  __device__ static StopProbe issue(const VerifyArgs& a, int b, int j, bool me,
+                                    const VerifySmem& sm) {
+    StopProbe p;
+    if (!me) return p;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(p.done) : "l"(a.walk_done + b)
+                 : "memory");
+    const unsigned long long* w = a.handover + (size_t)b * a.N;
+#pragma unroll
+    for (int k = 0; k < kProbeDepth; ++k) {
+      const int c = k == 0 ? j : p.child[k - 1] > 0 ? sm.parent[p.child[k - 1]] : 0;
+      p.child[k] = c;
+      p.anc[k] = 0;
+      if (c > 0) {
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(p.anc[k]) : "l"(w + sm.parent[c])
+                     : "memory");
+        p.n = k + 1;
+      }
+    }
+    return p;
+  }
+  __device__ bool stop(const VerifyArgs& a, int j) const {
+    const unsigned long long tag = handover_tag(a.gen);
+    if ((done >> 32) == tag && (done & 1ull)) return true;
+    bool off = false;
+#pragma unroll
+    for (int k = 0; k < kProbeDepth; ++k) {
+      const unsigned long long v = anc[k];
+      const uint32_t lo = (uint32_t)v;
+      if (k < n && (v >> 32) == tag && (lo & kHandoverPublished) &&
+          ((lo & kHandoverTerminal) || (int)(lo & kHandoverValueMask) - 1 != child[k]))
+        off = true;
+    }
+    (void)j;
+    return off;
+  }
+};
+
 // ------------------------------------------------------------------------------------------------
 // one node: statistics, sibling tests, residual rounds, bonus if the walk can stop here
 // ------------------------------------------------------------------------------------------------
@@ -647,7 +721,10 @@ struct NodeBufs {
 // that one CTA can process several nodes in turn.
 // The returned record is complete in CTA `writer` (every CTA gets the same writer); first_acc,
 // flags and (at T = 0) the bonus are the same in every CTA.
-template <int CL, bool PGLOBAL, bool SAMPLING>
+// ONLINE: the walk runs while nodes finish (every-node form without per-child q); a node stops at
+// the residual round in which it learns that the walk cannot reach it (StopProbe; its record then
+// flags kWalkDone).
+template <int CL, bool PGLOBAL, bool SAMPLING, bool ONLINE = false>
 __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, const NodeBufs& nb,
                                  bool logits_staged, DF invT_df, float k2, int& xk, int& writer,
                                  uint32_t& ph_l, uint32_t& ph_p, VerifySmem& sm) {
@@ -760,9 +837,23 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
     const float c_t = rs.f > 0.f ? __fdiv_rn(__fadd_rn(c_next.hi, c_next.lo), rs.f) : 0.f;
     DF tot, wt;
     int xs;
-    const DF G = cluster_residual<CL>(s, nb.lbuf, pd, c_t, rs.f, t == 0, pflags, rank, xk,
-                                      tot, wt, xs, flags, sm);
+    DF G;
+    if constexpr (ONLINE) {
+      // is this node's outcome still needed?  Loads issued now, read after the slice pass
+      const StopProbe probe = StopProbe::issue(a, b, j, threadIdx.x == 0, sm);
+      G = cluster_residual<CL>(s, nb.lbuf, pd, c_t, rs.f, t == 0, pflags, rank, xk, tot, wt, xs,
+                               flags, sm, [&] { return probe.stop(a, j) ? kWalkDone : 0; });
+    } else {
+      G = cluster_residual<CL>(s, nb.lbuf, pd, c_t, rs.f, t == 0, pflags, rank, xk, tot, wt, xs,
+                               flags, sm);
+    }
     pflags = 0;
+    if constexpr (ONLINE) {
+      if (flags & kWalkDone) {  // cluster-uniform (exchanged); no copy is in flight
+        st.flags = flags;
+        return st;
+      }
+    }
     if (G.hi > 0.f) {
       if ((int)threadIdx.x > t && (int)threadIdx.x < nk) {  // n <- max(0, n - p(x) D)
         const DF pD = df_mul(DF{sm.g_px[threadIdx.x], 0.f}, D);
@@ -949,13 +1040,85 @@ __device__ __forceinline__ bool arrive(unsigned long long* ctr, unsigned long lo
 }
 
 // ------------------------------------------------------------------------------------------------
+// walk hand-over (every-node form without per-child q)
+// ------------------------------------------------------------------------------------------------
+// A node's outcome goes into its hand-over word as soon as the node is done, and the walk starts
+// at the root and follows the accepted children as their outcomes appear, instead of waiting for
+// the sequence's last node.  Word: (tag << 32) | kPublished | kWalker | kTerminal |
+// flags << kFlagShift | value, with tag = handover_tag(generation) and value = accepted child + 1,
+// or for a terminal (the walk stops there: no child accepted, or the node hit NaN / a timeout)
+// bonus + 1 (0: no bonus).  A word with another tag is empty.  At most two parties write a word
+// in a call -- the node, and the walk when it reaches the node first (kWalker) -- and whichever
+// comes second continues the walk.
+// Every node still arrives on the sequence's counter (finished, stopped early or timed out); the
+// last arrival clears the words, so a replay of the same call (same generation) starts clean.
+constexpr uint32_t kPublished = kHandoverPublished, kWalker = 1u << 30,
+                   kTerminal = kHandoverTerminal;
+constexpr int kFlagShift = 22;
+constexpr uint32_t kValueMask = kHandoverValueMask;  // bonus + 1 < 2^22: V < 2^22 - 1
+static_assert(kValueMask == (1u << kFlagShift) - 1u, "hand-over word layout");
+
+__device__ __forceinline__ uint32_t handover_payload(const NodeStat& st, int j, int N) {
+  const int fa = st.first_acc;
+  const bool terminal =
+      (st.flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) != 0 || fa <= j || fa >= N;
+  const uint32_t value =
+      terminal ? (uint32_t)min(max(st.bonus + 1, 0), (int)kValueMask) : (uint32_t)(fa + 1);
+  return (terminal ? kTerminal : 0u) | ((uint32_t)(st.flags & 0x7F) << kFlagShift) | value;
+}
+
+// Sets `bits` in the word (an empty word becomes this generation's); returns the word before.
+// `guess`: its probable current value (a cleared word is 0).  Two writers at most: a few tries.
+__device__ unsigned long long handover_set(unsigned long long* w, unsigned long long gen,
+                                           uint32_t bits, unsigned long long guess) {
+  unsigned long long cur = guess;
+  for (int it = 0; it < 16; ++it) {
+    const unsigned long long base = (cur >> 32) == gen ? cur : (gen << 32);
+    const unsigned long long want = base | bits;
+    unsigned long long prev;
+    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+                 : "=l"(prev)
+                 : "l"(w), "l"(cur), "l"(want)
+                 : "memory");
+    if (prev == cur) return cur;
+    cur = prev;
+  }
+  return cur;
+}
+
+__device__ __forceinline__ bool handed_over(unsigned long long v, unsigned long long gen) {
+  return (v >> 32) == gen && (v & (unsigned long long)kPublished);
+}
+
+// Follows the walk from node c (the low half of its word in `lo`): the terminal node where it
+// ended, or -1 if it reached a node that is not done yet (that node takes it over).
+__device__ int walk_from(const VerifyArgs& a, int b, int c, uint32_t& lo) {
+  const unsigned long long gen = handover_tag(a.gen);
+  unsigned long long* w = a.handover + (size_t)b * a.N;
+  for (int steps = 0; steps < a.N; ++steps) {
+    if (lo & kTerminal) return c;
+    const int n = (int)(lo & kValueMask) - 1;  // an accepted child of c: c < n < N
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(w + n) : "memory");
+    if (!handed_over(v, gen)) {
+      v = handover_set(w + n, gen, kWalker, v);
+      if (!handed_over(v, gen)) return -1;
+    }
+    c = n;
+    lo = (uint32_t)v;
+  }
+  return -1;
+}
+
+// ------------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------------
 // PGLOBAL: draft rows read from global memory instead of staged (large problems with V ~ 128K).
 // Four CTAs per SM (at most 64 registers a thread): at three, the 60 clusters of 8 CTAs of one
 // 60-node tree do not all fit on the GPU at once, and the last clusters start only when the
 // first ones leave.
-template <int CL, bool PGLOBAL, bool SAMPLING, bool LEAVES>
+// ONLINE (every node, no per-child q): the walk follows the hand-over words as nodes finish.
+template <int CL, bool PGLOBAL, bool SAMPLING, bool LEAVES, bool ONLINE = false>
 __global__ void __launch_bounds__(kVThreads, 4)
     verify_kernel(const VerifyArgs a, int cap, float invT_hi, float invT_lo,
                   float k2) {
@@ -1013,10 +1176,54 @@ __global__ void __launch_bounds__(kVThreads, 4)
   const bool work = sm.internal[j] || do_leaves;
   NodeStat st;
   if (work)
-    st = process_node<CL, PGLOBAL, SAMPLING>(a, b, j, rank, nb, early, DF{invT_hi, invT_lo}, k2, xk,
+    st = process_node<CL, PGLOBAL, SAMPLING, ONLINE>(a, b, j, rank, nb, early, DF{invT_hi, invT_lo},
+                                                     k2, xk,
                                              writer,
                                    ph_l, ph_p, sm);
 
+  if constexpr (ONLINE) {
+    // hand the outcome over (the root starts the walk), follow the walk while the nodes it
+    // reaches are done, write the outputs where it ends; then arrive
+    if (rank != writer) return;
+    if (threadIdx.x == 0) {
+      int term = -1;
+      uint32_t lo = 0;
+      if (!(st.flags & kWalkDone)) {  // a node that stopped early hands nothing over
+        const unsigned long long gen = handover_tag(a.gen);
+        lo = kPublished | handover_payload(st, j, N);
+        const unsigned long long prev =
+            handover_set(a.handover + (size_t)b * N + j, gen, lo, 0ull);
+        if (j == 0 || ((prev >> 32) == gen && (prev & (unsigned long long)kWalker)))
+          term = walk_from(a, b, j, lo);
+      }
+      sm.terminal = term;
+      if (term >= 0) {
+        int len = 0;
+        for (int c = term; c > 0 && len < N; c = sm.parent[c]) ++len;
+        int c = term;
+        for (int i = len - 1; i >= 0; --i, c = sm.parent[c]) sm.path[i] = c;
+        sm.path_len = len;
+        sm.found = (int)(lo & kValueMask) - 1;  // the bonus
+        sm.flags = (int)((lo >> kFlagShift) & 0x7Fu);
+      }
+    }
+    __syncthreads();
+    if (sm.terminal >= 0) {
+      write_outputs(a, b, sm.found, sm.flags, sm);
+      if (threadIdx.x == 0) {  // the other nodes may stop at their next residual round
+        const unsigned long long v = (handover_tag(a.gen) << 32) | 1ull;
+        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a.walk_done + b), "l"(v)
+                     : "memory");
+      }
+    }
+    if (threadIdx.x == 0) sm.is_last = arrive(a.counters + b, a.gen, N) ? 1 : 0;
+    __syncthreads();
+    if (sm.is_last) {  // every node arrived: no word of this sequence is used any more
+      for (int i = threadIdx.x; i < N; i += kVThreads) a.handover[(size_t)b * N + i] = 0ull;
+      if (threadIdx.x == 0) a.walk_done[b] = 0ull;
+    }
+    return;
+  }
   // arrival: the last cluster of the sequence to finish walks the tree
   if constexpr (do_leaves) {
     // every possible stop already has its bonus, so the writer CTA finishes alone (this
@@ -1123,7 +1330,9 @@ __global__ void __launch_bounds__(kVThreads, 4)
 // ------------------------------------------------------------------------------------------------
 size_t verify_workspace_bytes(int B, int N, int V) {
   (void)V;
-  return (size_t)B * N * sizeof(NodeStat) + (size_t)B * sizeof(unsigned long long);
+  // node records [B, N], arrival counters [B], hand-over words [B, N], walk-done words [B]
+  return (size_t)B * N * (sizeof(NodeStat) + sizeof(unsigned long long)) +
+         (size_t)B * 2 * sizeof(unsigned long long);
 }
 
 template <class... Params, class... Args>
@@ -1193,6 +1402,14 @@ static cudaError_t launch_cl(const VerifyArgs& a, dim3 g, size_t smem, cudaStrea
                      invT_lo, k2);
   }
   if (leaves) {
+    // without per-child q the walk follows the nodes as they finish (bonus + 1 fits the word)
+    if (a.child_q == nullptr && (unsigned)a.V < kValueMask) {
+      if (!sampling)
+        return launch_ex(verify_kernel<CL, false, false, true, true>, g, CL, smem, s, a, cap,
+                         invT_hi, invT_lo, k2);
+      return launch_ex(verify_kernel<CL, false, true, true, true>, g, CL, smem, s, a, cap,
+                       invT_hi, invT_lo, k2);
+    }
     if (!sampling)
       return launch_ex(verify_kernel<CL, false, false, true>, g, CL, smem, s, a, cap, invT_hi,
                        invT_lo, k2);

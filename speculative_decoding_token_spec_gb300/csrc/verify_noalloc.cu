@@ -7,7 +7,7 @@
 // workspace in one fixed, file-scope device array instead.
 //
 // Properties of that array:
-//   * Size: room for B * N <= SPEC_NOALLOC_MAX_NODES tree nodes per call (160 KB).  Every
+//   * Size: room for B * N <= SPEC_NOALLOC_MAX_NODES tree nodes per call (224 KB).  Every
 //     GPU on which the library is loaded holds it until the process exits.
 //   * Set-up: every call made outside stream capture looks up the array's device address
 //     (cudaGetSymbolAddress, a host-side lookup) with the caller's device current, so a module
@@ -15,9 +15,10 @@
 //     while its stream is being captured uses the address of the last uncaptured call on that
 //     device (looking it up if there was none); make one call before capturing.
 //   * Sharing: all calls share the one array and it keeps the previous call's contents.  Nothing in
-//     it has to start at zero: each call writes every statistics entry it reads, and a
-//     per-sequence arrival counter is trusted only when it carries the generation and tag of the
-//     call itself, so counts and node records left by earlier calls are reset.  Calls whose
+//     it has to start at zero: each call writes every statistics entry it reads, a per-sequence
+//     arrival counter is trusted only when it carries the generation and tag of the call itself,
+//     and a hand-over or walk-done word only when it carries the call's generation, so counts,
+//     node records and words left by earlier calls are reset or ignored.  Calls whose
 //     kernels may overlap on the GPU (different streams, or concurrent host threads) race on it.
 //   * No allocation: no cudaMalloc, cudaFree or allocating library routine is called.
 #include <cuda_runtime.h>
@@ -32,8 +33,9 @@ using namespace spectree;
 
 namespace {
 
-// per node: its statistics record; per sequence (B <= B * N): one arrival counter
-constexpr size_t kPerNode = sizeof(NodeStat) + sizeof(unsigned long long);
+// per node: its statistics record and hand-over word; per sequence (B <= B * N): an arrival
+// counter and a walk-done word
+constexpr size_t kPerNode = sizeof(NodeStat) + 3 * sizeof(unsigned long long);
 constexpr size_t kScratchBytes = (size_t)SPEC_NOALLOC_MAX_NODES * kPerNode;
 
 // The fixed scratch.  In host code `g_verify_scratch` names a host-side stand-in, not device
