@@ -35,9 +35,12 @@ struct VerifyArgs {
   float* child_q;
   int32_t* status;
   NodeStat* stats;  // [B, N]
-  unsigned long long* counters;  // [B] arrival counters: (generation << 32) | (tag << 16) | arrivals
+  // [B] arrival counters: (generation << 32) | (tag << 16) | arrivals; in the every-node form
+  // without per-child q, call tickets: (generation << 32) | tickets taken
+  unsigned long long* counters;
   // [B, N] walk hand-over words and [B] walk-done words of the every-node form without per-child
-  // q: (generation << 32) | state (see tree_verify.cu); all reset by each sequence's last arrival
+  // q: (tag << 32) | state, the tag derived from the generation and the call's ticket epoch
+  // (see tree_verify.cu); words of other calls carry other tags, so none is ever cleared
   unsigned long long* handover;
   unsigned long long* walk_done;
   unsigned long long gen;        // this call's generation (32 bits)

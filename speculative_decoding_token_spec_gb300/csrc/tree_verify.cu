@@ -83,6 +83,9 @@ struct VerifySmem {
   int flags;
   int is_last;
   int found;
+  uint32_t ticket;       // rank 0: this node's call ticket (online walk); sent with each exchange
+  uint32_t ticket_c;     // rank 0's ticket, as received through the exchanges
+  unsigned long long hv_guess;  // the node's hand-over word as read at the start (online walk)
   uint32_t first_polls;  // first-attempt polls of the bounded waits (VerifyArgs::first_polls)
   float g_r[kMaxNodes];         // children's test uniforms
   float g_lx[kMaxNodes];        // gathered target logit / draft probability of each child's token
@@ -299,8 +302,8 @@ __device__ Entry exchange(VerifySmem& sm, int& xk, const Entry& mine, float k, i
   xslot = slot;
   if (wid == 0) {
     const uint32_t bar = smem_u32(&sm.xbar[slot]);
-    const Entry c =
-        lanes_combine8<KIND>(lane < kVWarps ? sm.wpart[lane] : entry_identity<KIND>(), k);
+    Entry c = lanes_combine8<KIND>(lane < kVWarps ? sm.wpart[lane] : entry_identity<KIND>(), k);
+    c.pad[0] = (int)sm.ticket;  // rank 0's reaches every CTA (the online walk's call ticket)
     if (lane == 0) mbar_arrive_expect_tx(bar, CL * (uint32_t)sizeof(Entry));
     if (lane < CL) {
       const uint32_t dst = dsmem_addr(&sm.cpart[slot][rank], lane);
@@ -315,6 +318,7 @@ __device__ Entry exchange(VerifySmem& sm, int& xk, const Entry& mine, float k, i
     if (!ok) mbar_wait_acq_cluster(bar, parity);
     Entry r = lanes_combine8<KIND>(lane < CL ? sm.cpart[slot][lane] : entry_identity<KIND>(), k);
     if (lane == 0) {
+      sm.ticket_c = (uint32_t)sm.cpart[slot][0].pad[0];
       r.flags |= ok ? 0 : SPEC_ST_TIMEOUT;
       sm.xres = r;
     }
@@ -648,21 +652,16 @@ struct NodeBufs {
 // node (it ended, or took another branch), so the node's outcome is no longer needed.
 constexpr int kWalkDone = 1 << 20;
 
-// The upper half of this call's hand-over and walk-done words: a hash of the generation with the
-// top bit set, which no cleared word (0), small integer, non-negative count or record field left
-// by another call carries, and which other words match only by chance.
-__device__ __forceinline__ unsigned long long handover_tag(unsigned long long gen) {
+// The upper half of this call's hand-over and walk-done words: a hash of the generation, offset
+// by the call's epoch (replays of one captured call share the generation, not the epoch), with
+// the top bit set -- which no zero word, small integer, non-negative count or record field left by
+// another call carries, and which other words match only by chance.
+__device__ __forceinline__ unsigned long long handover_tag(unsigned long long gen, uint32_t epoch) {
   uint32_t h = (uint32_t)gen * 0x9E3779B1u;
   h ^= h >> 15;
+  h += epoch * 0x2545F491u;  // odd: distinct epochs, distinct tags (below 2^31 apart)
   h |= 0x80000000u;
   return h == 0xFFFFFFFFu ? 0x80000001ull : (unsigned long long)h;
-}
-
-// Has the walk of sequence b ended in this call?
-__device__ __forceinline__ bool walk_ended(const VerifyArgs& a, int b) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.walk_done + b) : "memory");
-  return (v >> 32) == handover_tag(a.gen) && (v & 1ull);
 }
 
 // The walk can no longer reach node j (its outcome is not needed) once the walk has ended, or once
@@ -696,8 +695,7 @@ struct StopProbe {
     }
     return p;
   }
-  __device__ bool stop(const VerifyArgs& a, int j) const {
-    const unsigned long long tag = handover_tag(a.gen);
+  __device__ bool stop(const VerifyArgs& a, int j, unsigned long long tag) const {
     if ((done >> 32) == tag && (done & 1ull)) return true;
     bool off = false;
 #pragma unroll
@@ -708,6 +706,7 @@ struct StopProbe {
           ((lo & kHandoverTerminal) || (int)(lo & kHandoverValueMask) - 1 != child[k]))
         off = true;
     }
+    (void)a;
     (void)j;
     return off;
   }
@@ -792,6 +791,8 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   DF S;
   RunState rs;
   cluster_stats<CL>(s, nb.lbuf, k2, lflags0, rank, xk, M, S, rs, flags, sm);
+  // the online walk's tag: rank 0's call ticket arrived with that exchange
+  const unsigned long long hv_tag = ONLINE ? handover_tag(a.gen, sm.ticket_c / (uint32_t)N) : 0ull;
   // Scalars every thread holds stay double-float: fp64 here is only for the few threads that
   // take a decision or update a numerator.
   DF D = S;
@@ -842,7 +843,8 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
       // is this node's outcome still needed?  Loads issued now, read after the slice pass
       const StopProbe probe = StopProbe::issue(a, b, j, threadIdx.x == 0, sm);
       G = cluster_residual<CL>(s, nb.lbuf, pd, c_t, rs.f, t == 0, pflags, rank, xk, tot, wt, xs,
-                               flags, sm, [&] { return probe.stop(a, j) ? kWalkDone : 0; });
+                               flags, sm,
+                               [&] { return probe.stop(a, j, hv_tag) ? kWalkDone : 0; });
     } else {
       G = cluster_residual<CL>(s, nb.lbuf, pd, c_t, rs.f, t == 0, pflags, rank, xk, tot, wt, xs,
                                flags, sm);
@@ -1025,6 +1027,18 @@ __device__ __forceinline__ void claim_counter(unsigned long long* ctr, unsigned 
   }
 }
 
+// The online walk's counter word: (generation << 32) | tickets taken.  A word of another
+// generation is reset to (generation, 0) by whichever cluster of the sequence starts first.
+__device__ __forceinline__ void claim_tickets(unsigned long long* ctr, unsigned long long gen) {
+  const unsigned long long g = gen & 0xFFFFFFFFull;
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  for (int it = 0; it < 8 && (old >> 32) != g; ++it) {
+    const unsigned long long prev = atomicCAS(ctr, old, g << 32);
+    if (prev == old) break;
+    old = prev;
+  }
+}
+
 // Returns true for the last of the N arrivals.  Release: this thread's earlier global writes (the
 // node record) are visible to whoever sees the count; acquire: the last arriver sees every other
 // cluster's record.
@@ -1050,8 +1064,11 @@ __device__ __forceinline__ bool arrive(unsigned long long* ctr, unsigned long lo
 // bonus + 1 (0: no bonus).  A word with another tag is empty.  At most two parties write a word
 // in a call -- the node, and the walk when it reaches the node first (kWalker) -- and whichever
 // comes second continues the walk.
-// Every node still arrives on the sequence's counter (finished, stopped early or timed out); the
-// last arrival clears the words, so a replay of the same call (same generation) starts clean.
+// Epochs: each node's cluster takes one ticket from the sequence's counter word ((generation <<
+// 32) | tickets, claimed like the arrival counter) at its start, so the N tickets of a call are
+// [kN, kN + N) and k = ticket / N is the call's epoch, the same in every cluster however late it
+// starts; a replay of a captured call (same generation) takes the next N.  Words of earlier
+// calls or replays carry other tags, so nothing has to be cleared and no node arrives at the end.
 constexpr uint32_t kPublished = kHandoverPublished, kWalker = 1u << 30,
                    kTerminal = kHandoverTerminal;
 constexpr int kFlagShift = 22;
@@ -1092,8 +1109,8 @@ __device__ __forceinline__ bool handed_over(unsigned long long v, unsigned long 
 
 // Follows the walk from node c (the low half of its word in `lo`): the terminal node where it
 // ended, or -1 if it reached a node that is not done yet (that node takes it over).
-__device__ int walk_from(const VerifyArgs& a, int b, int c, uint32_t& lo) {
-  const unsigned long long gen = handover_tag(a.gen);
+__device__ int walk_from(const VerifyArgs& a, int b, int c, uint32_t& lo,
+                         unsigned long long gen) {
   unsigned long long* w = a.handover + (size_t)b * a.N;
   for (int steps = 0; steps < a.N; ++steps) {
     if (lo & kTerminal) return c;
@@ -1136,6 +1153,7 @@ __global__ void __launch_bounds__(kVThreads, 4)
     mbar_init(smem_u32(&sm.xbar[1]), 1);
     mbar_fence_init();
     sm.first_polls = a.first_polls;
+    sm.ticket = 0;
   }
   __syncthreads();
   cluster_arrive_release();  // exchange barriers initialised (waited for before the first exchange)
@@ -1151,7 +1169,13 @@ __global__ void __launch_bounds__(kVThreads, 4)
   }
   // the claim's round trip overlaps the tree loads (issued by the first threads) instead of
   // delaying thread 0, which issues the copies
-  if (rank == 0 && threadIdx.x == kVThreads - 1) claim_counter(a.counters + b, a.gen, N);
+  if (rank == 0 && threadIdx.x == kVThreads - 1) {
+    if constexpr (ONLINE) {
+      claim_tickets(a.counters + b, a.gen);
+    } else {
+      claim_counter(a.counters + b, a.gen, N);
+    }
+  }
   const int bad = load_tree(a, b, sm);  // uniform across the cluster: same tree everywhere
   if (bad) {
     if (j == 0 && rank == 0) {  // one writer per sequence
@@ -1171,6 +1195,20 @@ __global__ void __launch_bounds__(kVThreads, 4)
     return;
   }
   cluster_wait_acquire();  // every CTA of the cluster can now receive exchanges
+  if constexpr (ONLINE) {
+    // this node's ticket; its round trip overlaps the wait for the logit slice (rank 0's ticket
+    // reaches the cluster with the first exchange)
+    if (threadIdx.x == kVThreads - 1) {
+      if (rank == 0) sm.ticket = (uint32_t)atomicAdd(a.counters + b, 1ull);
+      // the node's hand-over word as it is now: the likely value its publish replaces
+      unsigned long long w;
+      asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];"
+                   : "=l"(w)
+                   : "l"(a.handover + (size_t)b * N + j)
+                   : "memory");
+      sm.hv_guess = w;
+    }
+  }
   int xk = 0, writer = 0;
   uint32_t ph_l = 0, ph_p = 0;
   const bool work = sm.internal[j] || do_leaves;
@@ -1183,18 +1221,18 @@ __global__ void __launch_bounds__(kVThreads, 4)
 
   if constexpr (ONLINE) {
     // hand the outcome over (the root starts the walk), follow the walk while the nodes it
-    // reaches are done, write the outputs where it ends; then arrive
+    // reaches are done, and write the outputs where it ends
     if (rank != writer) return;
     if (threadIdx.x == 0) {
       int term = -1;
       uint32_t lo = 0;
+      const unsigned long long tag = handover_tag(a.gen, sm.ticket_c / (uint32_t)N);
       if (!(st.flags & kWalkDone)) {  // a node that stopped early hands nothing over
-        const unsigned long long gen = handover_tag(a.gen);
         lo = kPublished | handover_payload(st, j, N);
         const unsigned long long prev =
-            handover_set(a.handover + (size_t)b * N + j, gen, lo, 0ull);
-        if (j == 0 || ((prev >> 32) == gen && (prev & (unsigned long long)kWalker)))
-          term = walk_from(a, b, j, lo);
+            handover_set(a.handover + (size_t)b * N + j, tag, lo, sm.hv_guess);
+        if (j == 0 || ((prev >> 32) == tag && (prev & (unsigned long long)kWalker)))
+          term = walk_from(a, b, j, lo, tag);
       }
       sm.terminal = term;
       if (term >= 0) {
@@ -1205,23 +1243,14 @@ __global__ void __launch_bounds__(kVThreads, 4)
         sm.path_len = len;
         sm.found = (int)(lo & kValueMask) - 1;  // the bonus
         sm.flags = (int)((lo >> kFlagShift) & 0x7Fu);
-      }
-    }
-    __syncthreads();
-    if (sm.terminal >= 0) {
-      write_outputs(a, b, sm.found, sm.flags, sm);
-      if (threadIdx.x == 0) {  // the other nodes may stop at their next residual round
-        const unsigned long long v = (handover_tag(a.gen) << 32) | 1ull;
+        // the other nodes may stop at their next residual round
+        const unsigned long long v = (tag << 32) | 1ull;
         asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a.walk_done + b), "l"(v)
                      : "memory");
       }
     }
-    if (threadIdx.x == 0) sm.is_last = arrive(a.counters + b, a.gen, N) ? 1 : 0;
     __syncthreads();
-    if (sm.is_last) {  // every node arrived: no word of this sequence is used any more
-      for (int i = threadIdx.x; i < N; i += kVThreads) a.handover[(size_t)b * N + i] = 0ull;
-      if (threadIdx.x == 0) a.walk_done[b] = 0ull;
-    }
+    if (sm.terminal >= 0) write_outputs(a, b, sm.found, sm.flags, sm);
     return;
   }
   // arrival: the last cluster of the sequence to finish walks the tree
@@ -1276,6 +1305,7 @@ __global__ void __launch_bounds__(kVThreads, 4)
     mbar_init(smem_u32(&sm.xbar[1]), 1);
     mbar_fence_init();
     sm.first_polls = a.first_polls;
+    sm.ticket = 0;
   }
   __syncthreads();
   cluster_arrive_release();  // exchange barriers initialised (waited for before the first exchange)
