@@ -86,6 +86,8 @@ struct VerifySmem {
   uint32_t ticket;       // rank 0: this node's call ticket (online walk); sent with each exchange
   uint32_t ticket_c;     // rank 0's ticket, as received through the exchanges
   unsigned long long hv_guess;  // the node's hand-over word as read at the start (online walk)
+  unsigned long long hv_snap[kMaxNodes];  // every node's hand-over word, read when walking
+  uint32_t hv_lo;                         // low half of the word the walk continues from
   uint32_t first_polls;  // first-attempt polls of the bounded waits (VerifyArgs::first_polls)
   float g_r[kMaxNodes];         // children's test uniforms
   float g_lx[kMaxNodes];        // gathered target logit / draft probability of each child's token
@@ -1063,7 +1065,10 @@ __device__ __forceinline__ bool arrive(unsigned long long* ctr, unsigned long lo
 // or for a terminal (the walk stops there: no child accepted, or the node hit NaN / a timeout)
 // bonus + 1 (0: no bonus).  A word with another tag is empty.  At most two parties write a word
 // in a call -- the node, and the walk when it reaches the node first (kWalker) -- and whichever
-// comes second continues the walk.
+// comes second continues the walk.  Everything a party needs is in the word itself, so the
+// accesses are relaxed (one word's accesses are ordered by coherence alone).  The walking CTA
+// reads every node's word at once and follows them in shared memory; the root's word has one
+// writer (the walk starts there), so the root publishes it with a plain store.
 // Epochs: each node's cluster takes one ticket from the sequence's counter word ((generation <<
 // 32) | tickets, claimed like the arrival counter) at its start, so the N tickets of a call are
 // [kN, kN + N) and k = ticket / N is the call's epoch, the same in every cluster however late it
@@ -1093,7 +1098,7 @@ __device__ unsigned long long handover_set(unsigned long long* w, unsigned long 
     const unsigned long long base = (cur >> 32) == gen ? cur : (gen << 32);
     const unsigned long long want = base | bits;
     unsigned long long prev;
-    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+    asm volatile("atom.relaxed.gpu.global.cas.b64 %0, [%1], %2, %3;"
                  : "=l"(prev)
                  : "l"(w), "l"(cur), "l"(want)
                  : "memory");
@@ -1105,26 +1110,6 @@ __device__ unsigned long long handover_set(unsigned long long* w, unsigned long 
 
 __device__ __forceinline__ bool handed_over(unsigned long long v, unsigned long long gen) {
   return (v >> 32) == gen && (v & (unsigned long long)kPublished);
-}
-
-// Follows the walk from node c (the low half of its word in `lo`): the terminal node where it
-// ended, or -1 if it reached a node that is not done yet (that node takes it over).
-__device__ int walk_from(const VerifyArgs& a, int b, int c, uint32_t& lo,
-                         unsigned long long gen) {
-  unsigned long long* w = a.handover + (size_t)b * a.N;
-  for (int steps = 0; steps < a.N; ++steps) {
-    if (lo & kTerminal) return c;
-    const int n = (int)(lo & kValueMask) - 1;  // an accepted child of c: c < n < N
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(w + n) : "memory");
-    if (!handed_over(v, gen)) {
-      v = handover_set(w + n, gen, kWalker, v);
-      if (!handed_over(v, gen)) return -1;
-    }
-    c = n;
-    lo = (uint32_t)v;
-  }
-  return -1;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -1223,23 +1208,57 @@ __global__ void __launch_bounds__(kVThreads, 4)
     // hand the outcome over (the root starts the walk), follow the walk while the nodes it
     // reaches are done, and write the outputs where it ends
     if (rank != writer) return;
+    const unsigned long long tag = handover_tag(a.gen, sm.ticket_c / (uint32_t)N);
+    unsigned long long* hw = a.handover + (size_t)b * N;
     if (threadIdx.x == 0) {
-      int term = -1;
+      bool walk = false;
       uint32_t lo = 0;
-      const unsigned long long tag = handover_tag(a.gen, sm.ticket_c / (uint32_t)N);
       if (!(st.flags & kWalkDone)) {  // a node that stopped early hands nothing over
         lo = kPublished | handover_payload(st, j, N);
-        const unsigned long long prev =
-            handover_set(a.handover + (size_t)b * N + j, tag, lo, sm.hv_guess);
-        if (j == 0 || ((prev >> 32) == tag && (prev & (unsigned long long)kWalker)))
-          term = walk_from(a, b, j, lo, tag);
+        if (j == 0) {  // the walk starts here and never comes back: no one else writes this word
+          const unsigned long long v = (tag << 32) | lo;
+          asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(hw), "l"(v) : "memory");
+          walk = true;
+        } else {
+          const unsigned long long prev = handover_set(hw + j, tag, lo, sm.hv_guess);
+          walk = (prev >> 32) == tag && (prev & (unsigned long long)kWalker);
+        }
+      }
+      sm.terminal = walk ? j : -1;  // where the walk continues from
+      sm.hv_lo = lo;
+    }
+    __syncthreads();
+    if (sm.terminal < 0) return;
+    // every node's word in one round trip, then the walk follows them in shared memory
+    for (int i = threadIdx.x; i < N; i += kVThreads) {
+      unsigned long long v;
+      asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(hw + i) : "memory");
+      sm.hv_snap[i] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int c = sm.terminal, term = -1;
+      uint32_t lo = sm.hv_lo;
+      for (int steps = 0; steps < N; ++steps) {
+        if (lo & kTerminal) {
+          term = c;
+          break;
+        }
+        const int n = (int)(lo & kValueMask) - 1;  // an accepted child of c: c < n < N
+        unsigned long long v = sm.hv_snap[n];
+        if (!handed_over(v, tag)) {  // not done when read: leave the walk to it, unless it is now
+          v = handover_set(hw + n, tag, kWalker, v);
+          if (!handed_over(v, tag)) break;
+        }
+        c = n;
+        lo = (uint32_t)v;
       }
       sm.terminal = term;
       if (term >= 0) {
         int len = 0;
-        for (int c = term; c > 0 && len < N; c = sm.parent[c]) ++len;
-        int c = term;
-        for (int i = len - 1; i >= 0; --i, c = sm.parent[c]) sm.path[i] = c;
+        for (int x = term; x > 0 && len < N; x = sm.parent[x]) ++len;
+        int x = term;
+        for (int i = len - 1; i >= 0; --i, x = sm.parent[x]) sm.path[i] = x;
         sm.path_len = len;
         sm.found = (int)(lo & kValueMask) - 1;  // the bonus
         sm.flags = (int)((lo >> kFlagShift) & 0x7Fu);
