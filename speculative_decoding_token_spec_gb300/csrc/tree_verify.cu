@@ -1143,7 +1143,6 @@ __global__ void __launch_bounds__(kVThreads, 4)
   __syncthreads();
   cluster_arrive_release();  // exchange barriers initialised (waited for before the first exchange)
   griddep_wait();  // the inputs may be produced by the preceding kernel in the stream
-  griddep_launch_dependents();
   // small problems process every node: its logit row is needed whatever the tree looks like, so
   // the copy goes out before anything else
   constexpr bool do_leaves = LEAVES;  // small problems: every node, leaves included
@@ -1204,6 +1203,8 @@ __global__ void __launch_bounds__(kVThreads, 4)
                                              writer,
                                    ph_l, ph_p, sm);
 
+  // the next kernel may start launching once every CTA is past its node (see the attention kernel)
+  griddep_launch_dependents();
   if constexpr (ONLINE) {
     // hand the outcome over (the root starts the walk), follow the walk while the nodes it
     // reaches are done, and write the outputs where it ends
@@ -1329,7 +1330,6 @@ __global__ void __launch_bounds__(kVThreads, 4)
   __syncthreads();
   cluster_arrive_release();  // exchange barriers initialised (waited for before the first exchange)
   griddep_wait();  // the inputs may be produced by the preceding kernel in the stream
-  griddep_launch_dependents();
   const int bad = load_tree(a, b, sm);  // uniform across the cluster: same tree everywhere
   if (bad) {
     if (rank == 0) {
@@ -1368,6 +1368,7 @@ __global__ void __launch_bounds__(kVThreads, 4)
     fence_async_smem();
     __syncthreads();
   }
+  griddep_launch_dependents();  // once every sequence's walk is done (see the attention kernel)
   if (threadIdx.x == 0) sm.path_len = len;
   __syncthreads();
   if (rank == writer) write_outputs(a, b, bonus, flags, sm);
