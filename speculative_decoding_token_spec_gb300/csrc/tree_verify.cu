@@ -486,13 +486,11 @@ __device__ DF cluster_residual(const Slice& s, const float* ebuf, const PD& pd, 
   return DF{r.s_hi, r.s_lo};
 }
 
-// The current weights became those of this round: record its CTA totals and this CTA's warp
-// totals `wt` (the same sums a draw would form from the threads' totals) for a draw.
+// The current weights became those of this round: record its CTA totals for a draw.
 template <int CL>
-__device__ __forceinline__ void commit_round_totals(VerifySmem& sm, int xs, const DF& wt) {
+__device__ __forceinline__ void commit_round_totals(VerifySmem& sm, int xs) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (wid == 0 && lane < CL) sm.ccur[lane] = DF{sm.cpart[xs][lane].s_hi, sm.cpart[xs][lane].s_lo};
-  if (lane == 0) sm.wcur[wid] = wt;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -532,15 +530,14 @@ struct Draw {
   int writer, tok;
 };
 
-// Levels: CTA of the cluster (sm.ccur, same in every CTA), warp of that CTA (sums of rs.tot; in
-// sm.wcur already when wcur_ready), thread of that warp (rs.tot), element of that thread's run.
-// No exchange: the writer CTA finds the token alone and records the node itself.
+// Levels: CTA of the cluster (sm.ccur, same in every CTA), warp of that CTA (sums of rs.tot),
+// thread of that warp (rs.tot), element of that thread's run.  No exchange: the writer CTA finds
+// the token alone and records the node itself.
 template <int CL, class PD>
 __device__ Draw cluster_draw(const Slice& s, const float* ebuf, const PD& pd,
-                             const RunState& rs, float u, int rank, VerifySmem& sm,
-                             bool wcur_ready = false) {
+                             const RunState& rs, float u, int rank, VerifySmem& sm) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  __syncthreads();  // sm.ccur / sm.wcur are visible
+  __syncthreads();  // sm.ccur is visible
   // level 1: CTA (lanes 0..7; lanes past CL hold zeros)
   const DF cv = lane < CL ? sm.ccur[lane] : DF{0.f, 0.f};
   const DF cincl = warp_scan8_df(cv);
@@ -550,11 +547,12 @@ __device__ Draw cluster_draw(const Slice& s, const float* ebuf, const PD& pd,
   const int cstar = lane_crossing(cv, cincl, t, before);
   if (cstar < 0) return Draw{0, -1};  // nothing positive anywhere
   if (rank != cstar) return Draw{cstar, -1};
-  if (!wcur_ready) {  // block-uniform
-    const DF wsum = warp_sum_df(rs.tot);
-    if (lane == 0) sm.wcur[wid] = wsum;
-    __syncthreads();
-  }
+  // every warp scans its threads' totals before the warp is chosen (the scans run side by side
+  // instead of one after the search of level 2); a warp's total is its last lane's prefix, so
+  // levels 2 and 3 agree on it
+  const DF lincl = warp_scan_df(rs.tot);
+  if (lane == 31) sm.wcur[wid] = lincl;
+  __syncthreads();
   // level 2: warp of this CTA (every warp computes it; one acts)
   if (t.hi >= 0.f) t = df_add(t, DF{-before.hi, -before.lo});
   const DF wv = lane < kVWarps ? sm.wcur[lane] : DF{0.f, 0.f};
@@ -563,7 +561,7 @@ __device__ Draw cluster_draw(const Slice& s, const float* ebuf, const PD& pd,
   if (wid == wstar) {
     // level 3: thread of the crossing warp
     if (t.hi >= 0.f) t = df_add(t, DF{-before.hi, -before.lo});
-    int Lc = lane_crossing(rs.tot, warp_scan_df(rs.tot), t, before);
+    int Lc = lane_crossing(rs.tot, lincl, t, before);
     if (Lc < 0) Lc = 31;
     // level 4: the elements of that thread's run, 32 at a time, by the whole warp
     const float fL = __shfl_sync(0xffffffffu, rs.f, Lc);
@@ -808,7 +806,6 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   bool all_rejected = nk > 0;
   DF c{0.f, 0.f};  // current weights: max(0, e - c p)
   bool frozen = false, p_waited = false;
-  bool wcur_ready = false;  // sm.wcur holds the warp totals of the current weights
   int pflags = 0;
   for (int t = 0; t < nk; ++t) {
     const int kid = sm.kids[t];
@@ -868,8 +865,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
       c = c_next;
       rs.tot = tot;
       rs.cw = c_t;
-      commit_round_totals<CL>(sm, xs, wt);
-      wcur_ready = true;
+      commit_round_totals<CL>(sm, xs);
     } else {
       frozen = true;
     }
@@ -881,7 +877,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   }
   const bool bad = (flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) != 0;
   if ((nk == 0 || all_rejected) && !bad) {  // the walk can stop here: draw its bonus
-    const Draw d = cluster_draw<CL>(s, nb.lbuf, pd, rs, u_bonus, rank, sm, wcur_ready);
+    const Draw d = cluster_draw<CL>(s, nb.lbuf, pd, rs, u_bonus, rank, sm);
     writer = d.writer;
     st.bonus = d.tok;
   }

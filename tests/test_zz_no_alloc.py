@@ -25,7 +25,7 @@ def _noalloc_fn(lib):
     return fn
 
 
-def _call_noalloc(fn, case, dev):
+def _call_noalloc(fn, case, dev, child_q=True):
     import torch
     B, N, V = case.target_logits.shape
     t = lambda a: P.dev_tensor(a, dev)  # noqa: E731
@@ -39,17 +39,19 @@ def _call_noalloc(fn, case, dev):
     rc = fn(logits.data_ptr(), probs.data_ptr(), toks.data_ptr(), par.data_ptr(), unif.data_ptr(),
             float(case.temperature), B, N, V, out["accept_len"].data_ptr(),
             out["accepted_tokens"].data_ptr(), out["bonus"].data_ptr(),
-            out["accepted_nodes"].data_ptr(), out["child_q"].data_ptr(), out["status"].data_ptr(),
+            out["accepted_nodes"].data_ptr(), out["child_q"].data_ptr() if child_q else None,
+            out["status"].data_ptr(),
             torch.cuda.current_stream().cuda_stream)
     assert rc == 0, rc
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
-def _same(a, ref):
+def _same(a, ref, child_q=True):
     for k in ("accept_len", "accepted_tokens", "bonus", "accepted_nodes", "status"):
         np.testing.assert_array_equal(a[k], ref[k], err_msg=k)
-    assert np.abs(a["child_q"] - ref["child_q"]).max() <= P.CHILD_Q_ABS
+    if child_q:
+        assert np.abs(a["child_q"] - ref["child_q"]).max() <= P.CHILD_Q_ABS
 
 
 @pytest.mark.parametrize("T", [1.0, 0.0])
@@ -80,6 +82,19 @@ def test_noalloc_scratch_layout_changes_between_calls(cuda_lib):
     assert cases[-1].target_logits.nbytes > (64 << 20)
     for case in cases:
         _same(_call_noalloc(fn, case, dev), P.run_verify_gpu(case, dev, want_child_q=True))
+
+
+def test_noalloc_without_child_q_walks_as_nodes_finish(cuda_lib):
+    """Without per-child q small problems take the walk that follows the nodes as they finish
+    (call tickets and hand-over words in the scratch); B * N shrinks and grows between calls, so
+    those words sit where earlier calls left node records, counters and hand-over words."""
+    import torch
+    dev = torch.device("cuda:0")
+    fn = _noalloc_fn(cuda_lib)
+    for B, T in ((12, 1.0), (5, 1.0), (6, 0.0), (1, 1.0), (12, 0.7), (12, 1.0)):
+        case = W.make_verify_case(W.config("eagle_vicuna7b", B=B), T, seed=50 + B)
+        got = _call_noalloc(fn, case, dev, child_q=False)
+        _same(got, P.run_verify_gpu(case, dev, want_child_q=False), child_q=False)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
