@@ -25,12 +25,17 @@
 //     exchange; a zero D_k freezes the distribution, and nothing after it needs a pass.
 //   * Each child is tested with the division-free r * p(x) * D < n(x), n(x) = w(x) tracked in fp64
 //     from an exactly formed exp argument; see "Precision".
-//   * Bonus draw (inverse CDF, y = min{y : C(y) > u * total}): the warp totals of the current
+//   * Bonus draw (inverse CDF, y = min{y : C(y) > u * total}): the CTA totals of the current
 //     weights are known from the last exchange, the thread totals from the last pass, so only the
-//     crossing thread's run is scanned (by its warp) -- no extra pass over the row.
-//   * The last cluster of a sequence to finish (a per-sequence arrival counter in the workspace)
-//     walks the tree from the root along the accepted children and writes the outputs; when leaves
-//     were not processed (large problems) it draws the bonus at a leaf terminal itself.
+//     crossing CTA scans its warps' and threads' totals and the crossing thread's run (by its
+//     warp) -- no extra pass over the row.
+//   * The walk.  Small problems without per-child q: each node hands its outcome over in a
+//     per-node word as soon as it is done, the walk starts at the root and follows the accepted
+//     children as their outcomes appear, and nodes still in their residual rounds stop once the
+//     walk cannot reach them (see "walk hand-over").  Otherwise the last cluster of a sequence to
+//     finish (a per-sequence arrival counter in the workspace) walks the tree from the root along
+//     the accepted children and writes the outputs; when leaves were not processed (large
+//     problems) it draws the bonus at a leaf terminal itself.
 //
 // Precision.  Element weights are fp32 (hardware 2^x on an argument formed as (l - m) * k).  Every
 // sum is a compensated fp32 sum per thread and a double-float (pair of fp32) sum across threads and
