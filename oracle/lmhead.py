@@ -17,6 +17,8 @@ from typing import Dict, Optional
 
 import numpy as np
 
+from . import verify as _verify
+
 
 def logits(hidden, weight) -> np.ndarray:
     """[M, V] = hidden [M, H] @ weight [V, H]^T in float64."""
@@ -46,3 +48,16 @@ def row_stats(lg, T: float, gather_idx: Optional[np.ndarray] = None) -> Dict[str
 
 def lm_head_stats(hidden, weight, T: float, gather_idx=None) -> Dict[str, np.ndarray]:
     return row_stats(logits(hidden, weight), T, gather_idx)
+
+
+def tree_verify_from_head(hidden, weight, draft_probs, tree_tokens, tree_parent, uniforms,
+                          T: float, with_table: bool = False):
+    """Tree verification (oracle/verify.py, survey explainer, Formal Definition, 検証フェーズ) of the
+    logits the LM head gives at every node (EAGLE explainer: the target's forward over the tree):
+    hidden [B, N, H] and weight [V, H], the exact values of the bf16 operands, in float64.  The
+    method never needs the logit matrix as a whole; its results are defined by it."""
+    h = np.asarray(hidden, np.float64)
+    B, N, H = h.shape
+    lg = logits(h.reshape(B * N, H), weight).reshape(B, N, -1)
+    return _verify.tree_verify(lg, draft_probs, tree_tokens, tree_parent, uniforms, T,
+                               with_table=with_table)

@@ -26,6 +26,7 @@ __all__ = [
     "AttnCase", "VerifyCase", "PagedAttnCase", "CompactCase", "CONFIGS", "make_tree",
     "chain_tree", "make_attention_case", "make_paged_attention_case", "make_compaction_case",
     "make_verify_case", "bf16_bits", "bf16_to_f64", "config", "attention_layout",
+    "HeadVerifyCase", "make_head_verify_case", "tree_depth",
 ]
 
 
@@ -366,6 +367,88 @@ def make_tree_build_case(B: int, K: int, D: int, V: int, seed: int = 0,
         rows[b] = rng.standard_normal((rows.shape[1], V), dtype=np.float32) * np.float32(sigma)
         roots[b] = int(rng.integers(V))
     return TreeBuildCase(rows, roots, K, D)
+
+
+@dataclasses.dataclass
+class HeadVerifyCase:
+    """Inputs of verification from the nodes' hidden states and the LM head."""
+    hidden: np.ndarray       # bf16 bits [B, N, H]: node i's final hidden state
+    head: np.ndarray         # bf16 bits [V, H]
+    draft_probs: np.ndarray  # float32 [B, N, V]
+    tree_tokens: np.ndarray  # int32 [B, N]
+    tree_parent: np.ndarray  # int32 [B, N]
+    uniforms: np.ndarray     # float32 [B, N]
+    temperature: float
+    max_depth: int           # the deepest node's depth over the batch (root: 0)
+
+
+def tree_depth(parent_row) -> int:
+    """Depth of the deepest node of a valid tree (parents precede their children)."""
+    d = [0] * len(parent_row)
+    for i in range(1, len(parent_row)):
+        d[i] = d[int(parent_row[i])] + 1
+    return max(d)
+
+
+def make_head_verify_case(cfg: Config, H: int, T: float, seed: int = 0,
+                          sigma_d: Optional[float] = None,
+                          tree_parent: Optional[np.ndarray] = None) -> HeadVerifyCase:
+    """Hidden states and head on a small lattice, so that every logit hidden . w is exact in fp32
+    whatever the order of the sums: hidden = a / 4 with integers a in [-3, 3], head = c / 2^s with
+    integers c in [-7, 7] (|sum| <= 21 H < 2^24 units of 2^-(2+s)); s puts the logits' spread near
+    cfg.sigma_t.
+
+    The draft model follows the EAGLE explainer's design (its own feature prediction, read out by
+    the target's LM head): draft logits = (hidden + noise) @ head^T in float64, the noise scaled so
+    that the draft logits stray from the target's by about sigma_d.  Draft tokens and uniforms as
+    in make_verify_case.
+    """
+    B, N, V = cfg.B, cfg.N, cfg.V
+    sd = cfg.sigma_d if sigma_d is None else float(sigma_d)
+    rng = _rng(seed, cfg.cfg_id, 0, 17)
+    s = int(np.clip(np.round(np.log2(np.sqrt(H * 4.0 * 18.67) / 4.0 / cfg.sigma_t)), 0, 20))
+    a = rng.integers(-3, 4, size=(B, N, H), dtype=np.int8)
+    c = rng.integers(-7, 8, size=(V, H), dtype=np.int8)
+    hidden_f = a.astype(np.float32) * np.float32(0.25)
+    head_f = c.astype(np.float32) * np.float32(2.0 ** -s)
+    hidden, head = bf16_bits(hidden_f), bf16_bits(head_f)
+    wnorm = float(np.sqrt(np.mean(np.sum(np.square(head_f, dtype=np.float64), axis=1))))
+    sigma_h = sd / max(wnorm, 1e-30)
+    dp = np.empty((B, N, V), dtype=np.float32)
+    tok = np.empty((B, N), dtype=np.int32)
+    par = np.empty((B, N), dtype=np.int32)
+    uni = np.empty((B, N), dtype=np.float32)
+    head64 = head_f.astype(np.float64)
+    for b in range(B):
+        rb = _rng(seed, cfg.cfg_id, b, 19)
+        pb = (np.asarray(tree_parent[b], dtype=np.int32) if tree_parent is not None
+              else _tree(cfg, seed, b))
+        par[b] = pb
+        feat = hidden_f[b].astype(np.float64) + rb.standard_normal((N, H)) * sigma_h
+        draft = feat @ head64.T
+        p64 = _draft_distribution(draft, T)
+        dp[b] = p64.astype(np.float32)
+        tok[b, 0] = int(rb.integers(V))
+        rank = np.zeros(N, dtype=np.int64)
+        order_cache = {}
+        for i in range(1, N):
+            j = int(pb[i])
+            if T > 0:
+                cdf = np.cumsum(p64[j])
+                x = float(rb.random()) * cdf[-1]
+                tok[b, i] = int(min(np.searchsorted(cdf, x, side="right"), V - 1))
+            else:
+                if j not in order_cache:
+                    order_cache[j] = np.argsort(-draft[j], kind="stable")
+                tok[b, i] = int(order_cache[j][rank[j] % V])
+                rank[j] += 1
+        uni[b] = rb.integers(0, 1 << 24, size=N).astype(np.float32) / np.float32(1 << 24)
+    depth = 0
+    for b in range(B):
+        pb = par[b]
+        if pb[0] == -1 and all(0 <= pb[i] < i for i in range(1, N)):
+            depth = max(depth, tree_depth(pb))
+    return HeadVerifyCase(hidden, head, dp, tok, par, uni, float(T), depth)
 
 
 @dataclasses.dataclass
