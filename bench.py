@@ -748,7 +748,31 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
     lm_greedy()
     torch.cuda.synchronize()
     assert int(g_st.sum()) == 0
+    # verification from the LM head's statistics at this workload's shape (hidden size Hq D):
+    # lattice operands (exact logits) with an EAGLE-style draft, so that the walk accepts and
+    # rejects as it would on the plain path; the head (> 2 x L2) is read from HBM every pass
+    hcase = W.make_head_verify_case(cfg, lm_h, T, seed=args.seed + 5)
+    h_dev = {"h": to_dev(hcase.hidden).view(torch.bfloat16),
+             "w": to_dev(hcase.head).view(torch.bfloat16), "p": to_dev(hcase.draft_probs),
+             "t": to_dev(hcase.tree_tokens), "par": to_dev(hcase.tree_parent),
+             "u": to_dev(hcase.uniforms)}
+    h_dev["wp"] = st.spec_lm_head_pack(h_dev["w"])
+    h_ws = torch.empty((st.spec_tree_verify_head_workspace(B, N, lm_h, V, hcase.max_depth),),
+                       dtype=torch.uint8, device=dev)
+    h_st = torch.zeros((B,), dtype=torch.int32, device=dev)
+    h_out = st.spec_tree_verify_head(h_dev["h"], h_dev["wp"], h_dev["p"], h_dev["t"],
+                                     h_dev["par"], h_dev["u"], T, hcase.max_depth,
+                                     packed_vocab=V, workspace=h_ws, status=h_st)
+
+    def head_verify(_c=None):
+        st.spec_tree_verify_head(h_dev["h"], h_dev["wp"], h_dev["p"], h_dev["t"], h_dev["par"],
+                                 h_dev["u"], T, hcase.max_depth, packed_vocab=V, outputs=h_out,
+                                 workspace=h_ws, status=h_st)
+
+    torch.cuda.synchronize()
+    assert int(h_st.sum()) == 0
     reps_lm = 20
+    g_hv = capture(head_verify, [None] * 5)
     g_lm = capture(lmhead, [None] * reps_lm)
     g_lr = capture(lmhead_rowmajor, [None] * reps_lm)
     g_lg = capture(lm_greedy, [None] * reps_lm)
@@ -767,6 +791,7 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
         g_lr.replay()
         g_lg.replay()
         g_gr.replay()
+        g_hv.replay()
     torch.cuda.synchronize()
     reps = max(1, 600 // ncp)
     p_ms = timed(lambda: [g_p.replay() for _ in range(reps)]) / (reps * ncp)
@@ -782,6 +807,22 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
     lr_ms = timed(lambda: [g_lr.replay() for _ in range(10)]) / (10 * reps_lm)
     lg_ms = timed(lambda: [g_lg.replay() for _ in range(10)]) / (10 * reps_lm)
     gr_ms = timed(lambda: [g_gr.replay() for _ in range(10)]) / (10 * reps_lm)
+    hv_ms = timed(lambda: [g_hv.replay() for _ in range(10)]) / (10 * 5)
+    # row passes that processed a node: per sequence, the walk's nodes where it did not move on to
+    # the first child (a rejected first child, or the terminal node)
+    h_len = h_out["accept_len"].cpu().numpy()
+    h_nodes = h_out["accepted_nodes"].cpu().numpy()
+    passes = []
+    for b in range(B):
+        par_b = hcase.tree_parent[b]
+        walk = [0] + [int(x) for x in h_nodes[b, :max(int(h_len[b]), 0)]]
+        stops = 1
+        for c, nxt in zip(walk[:-1], walk[1:]):
+            first = next(k for k in range(c + 1, N) if par_b[k] == c)
+            stops += 0 if nxt == first else 1
+        passes.append(stops)
+    head_bytes = V * lm_h * 2
+    internal = int(sum(len(set(int(x) for x in hcase.tree_parent[b, 1:])) for b in range(B)))
     lm_bytes = lm_w.numel() * 2 + lm_x.numel() * 2 + lm_m * 12  # head, hidden, statistics
     lm_flops = 2.0 * lm_m * lm_h * V
     fil_gbs = filt_bytes / ((f_ms - v_ms) * 1e-3) / 1e9 if f_ms > v_ms else None
@@ -830,6 +871,21 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
                               "verification of the workload's tree from the argmax)",
                     "note": "weights generated on the device (seeded), bf16; the logit matrix is "
                             "never written"},
+        "verify_head": {"hidden": lm_h, "vocab": V, "temperature": T,
+                        "max_depth": hcase.max_depth, "us_per_call": hv_ms * 1e3,
+                        "row_passes_used": passes, "row_passes_launched": hcase.max_depth + 1,
+                        "mean_accept_len": float(np.mean(h_len)),
+                        "head_bytes_read": head_bytes * (1 + max(passes)),
+                        "logit_row_bytes": 4 * V * int(sum(passes)),
+                        "logit_row_bytes_plain_verify": 4 * V * internal,
+                        "logit_matrix_bytes_not_written": 4 * V * B * N,
+                        "lm_head_stats_us": lm_ms * 1e3,
+                        "kernel": "head_prep_kernel, lm_head_kernel + lm_head_combine_kernel "
+                                  "(statistics of every node), then per row pass "
+                                  "head_walk_kernel, lm_head_kernel (rows of the pending nodes), "
+                                  "verify_head_step_kernel; head_finish_kernel",
+                        "note": "lattice hidden states and head (exact logits), EAGLE-style "
+                                "draft; one row pass = one more read of the head"},
         "peak_gbs": hbm_gbs,
     }
 

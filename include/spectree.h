@@ -338,6 +338,44 @@ int spec_tree_verify_greedy(const int32_t* node_argmax, const int32_t* tree_toke
                             int32_t* out_bonus_token, int32_t* out_accepted_nodes, int32_t* status,
                             void* stream);
 
+/*
+ * Tree verification from the target's final hidden states and LM head, without the logit matrix:
+ * survey explainer, Formal Definition, 検証フェーズ (child x~ of node c accepted iff
+ * r < min(1, q_c(x~) / p_c(x~)); after a rejection the next sibling is tested against
+ * norm(max(0, q - p_c)); the bonus token is drawn where the walk stops); EAGLE explainer (q_c is the
+ * softmax of the target LM head's logits at node c).  The results are those of spec_tree_verify on
+ * the logits hidden @ head^T (bf16 products, fp32 sums over H), computed as follows.  Every node's
+ * max m, S = sum_y exp((l_y - m) / T) and its first child's logit come from the fused LM head
+ * (spec_lm_head_stats); from the root the walk accepts first children while
+ * r p(x~) S < exp((l_x~ - m) / T) (evaluated in fp64) holds; where it stops (a rejected first
+ * child, or a leaf), one more pass of the LM head writes that node's full logit row and the node
+ * is processed as in spec_tree_verify (its children re-tested in order from that row, residual
+ * rounds, the bonus draw); an accepted child continues the walk.  Per sequence, one full row per
+ * such stop, against every internal node's row for spec_tree_verify.  A first test decided from
+ * the statistics can differ from spec_tree_verify's only when |r - q(x~) / p(x~)| is within the
+ * rounding of S (fp32 sums: about 1e-5 relative).  At T = 0 the walk follows each node's argmax
+ * (spec_tree_verify_greedy on the LM head's argmax).
+ *   hidden      bf16 [B, N, H]: node i's final hidden state (the target's input to the LM head)
+ *   head        bf16 [V, H] (head_packed = 0) or spec_lm_head_pack's tile-major copy (1)
+ *   draft_probs, tree_tokens, tree_parent, uniforms, temperature, outputs, status: as in
+ *               spec_tree_verify (out_accepted_nodes may be NULL; no per-child q); a bad draft
+ *               probability is detected where it is read
+ *   max_depth   >= the depth of every tree (root: 0); the call makes max_depth + 1 row passes at
+ *               T > 0 (those with no node to process end after one flag read); a deeper tree is
+ *               flagged SPEC_ST_BAD_TREE (T > 0)
+ *   workspace   spec_tree_verify_head_workspace(B, N, H, V, max_depth) bytes, 16-byte aligned
+ * H % 8 == 0; hidden, head and draft_probs 16-byte aligned; N <= 64; the V limits of
+ * spec_tree_verify.  Returns SPEC_OK or a negative spec_err_t before any launch.
+ */
+size_t spec_tree_verify_head_workspace(int B, int N, int H, int V, int max_depth);
+int spec_tree_verify_head(const void* hidden, const void* head, int head_packed,
+                          const float* draft_probs, const int32_t* tree_tokens,
+                          const int32_t* tree_parent, const float* uniforms, float temperature,
+                          int B, int N, int H, int V, int max_depth, int32_t* out_accept_len,
+                          int32_t* out_accepted_tokens, int32_t* out_bonus_token,
+                          int32_t* out_accepted_nodes, void* workspace, size_t workspace_bytes,
+                          int32_t* status, void* stream);
+
 /* ------------------------------------------------------------------------------------------------
  * Tree attention over a paged KV cache
  * ------------------------------------------------------------------------------------------------

@@ -13,8 +13,10 @@ Beside them: ``spec_tree_attention_paged`` (the same attention over a paged KV c
 values move next to the root), ``spec_tree_verify_filtered`` (verification against the top-k /
 top-p filtered target distribution), and ``spec_tree_expand`` / ``spec_tree_finalize`` (dynamic
 draft-tree construction, one level per drafter step), ``spec_lm_head_stats`` (the LM head fused
-with the per-row statistics verification reads) and ``spec_tree_verify_greedy`` (temperature-0
-verification from those statistics' argmax, no logit rows).
+with the per-row statistics verification reads), ``spec_tree_verify_greedy`` (temperature-0
+verification from those statistics' argmax, no logit rows) and ``spec_tree_verify_head``
+(verification from the nodes' hidden states and the LM head: full logit rows only where the walk
+needs residual rounds or the bonus draw).
 
 The Python functions of the same names only marshal torch tensors into pointers and the current
 CUDA stream.  There is no CPU fallback: a missing library raises.
@@ -37,6 +39,8 @@ from ._binding import (  # noqa: F401
     spec_tree_verify_filtered,
     spec_tree_verify_filtered_workspace,
     spec_tree_verify_greedy,
+    spec_tree_verify_head,
+    spec_tree_verify_head_workspace,
     spec_tree_verify_noalloc,
     spec_tree_verify_workspace,
     spec_status_string,

@@ -59,6 +59,9 @@ _SIGNATURES = {
     "spec_lm_head_stats_packed": (_c_int, [_vp] * 3 + [_c_int] * 4 + [_c_float] + [_vp] * 5
                                   + [_c_size, _vp, _vp]),
     "spec_tree_verify_greedy": (_c_int, [_vp] * 3 + [_c_int] * 3 + [_vp] * 6),
+    "spec_tree_verify_head_workspace": (_c_size, [_c_int] * 5),
+    "spec_tree_verify_head": (_c_int, [_vp, _vp, _c_int] + [_vp] * 4 + [_c_float] + [_c_int] * 5
+                              + [_vp] * 5 + [_c_size, _vp, _vp]),
     "spec_status_string": (ctypes.c_char_p, [_c_int]),
     "spec_debug_set_verify_wait_polls": (_c_int, [ctypes.c_longlong]),
 }
@@ -324,6 +327,56 @@ def spec_tree_verify_greedy(node_argmax, tree_tokens, tree_parent, V, outputs=No
         _ptr(o.get("accepted_nodes")), _ptr(o["status"]), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_tree_verify_greedy", rc)
+    return o
+
+
+def spec_tree_verify_head_workspace(B, N, H, V, max_depth) -> int:
+    return int(lib().spec_tree_verify_head_workspace(int(B), int(N), int(H), int(V),
+                                                     int(max_depth)))
+
+
+def spec_tree_verify_head(hidden, head, draft_probs, tree_tokens, tree_parent, uniforms,
+                          temperature, max_depth, packed_vocab=None, outputs=None, workspace=None,
+                          status=None, want_nodes=True, stream=None):
+    """Verification from each node's final hidden state (bf16 [B, N, H]) and the LM head (bf16
+    [V, H], or spec_lm_head_pack's copy with packed_vocab = V) without the logit matrix; the trees'
+    depth must not exceed max_depth.  Same outputs as spec_tree_verify (no per-child q)."""
+    torch = _torch()
+    B, N, H = hidden.shape
+    dev = hidden.device
+    _check(hidden, "hidden", torch.bfloat16, (B, N, H), dev)
+    if packed_vocab is None:
+        V = head.shape[0]
+        _check(head, "head", torch.bfloat16, (V, H), dev)
+    else:
+        V = int(packed_vocab)
+        if head.numel() * head.element_size() < spec_lm_head_packed_bytes(V, H):
+            raise ValueError("packed head too small")
+    T = float(temperature)
+    if T > 0:
+        _check(draft_probs, "draft_probs", torch.float32, (B, N, V), dev)
+    _check(tree_tokens, "tree_tokens", torch.int32, (B, N), dev)
+    _check(tree_parent, "tree_parent", torch.int32, (B, N), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, N), dev)
+    o = dict(outputs or {})
+    i32 = dict(dtype=torch.int32, device=dev)
+    o.setdefault("accept_len", torch.empty((B,), **i32))
+    o.setdefault("accepted_tokens", torch.empty((B, N), **i32))
+    o.setdefault("bonus", torch.empty((B,), **i32))
+    if want_nodes:
+        o.setdefault("accepted_nodes", torch.empty((B, N), **i32))
+    o["status"] = status if status is not None else torch.zeros((B,), **i32)  # bits are OR-ed in
+    ws_bytes = spec_tree_verify_head_workspace(B, N, H, V, max_depth)
+    if workspace is None:
+        workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
+    rc = lib().spec_tree_verify_head(
+        _ptr(hidden), _ptr(head), 0 if packed_vocab is None else 1,
+        _ptr(draft_probs) if T > 0 else None, _ptr(tree_tokens), _ptr(tree_parent),
+        _ptr(uniforms), T, B, N, H, V, int(max_depth), _ptr(o["accept_len"]),
+        _ptr(o["accepted_tokens"]), _ptr(o["bonus"]), _ptr(o.get("accepted_nodes")),
+        _ptr(workspace), workspace.numel(), _ptr(o["status"]), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_tree_verify_head", rc)
     return o
 
 

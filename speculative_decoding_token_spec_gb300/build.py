@@ -19,7 +19,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libspectree.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["spectree_abi.cu", "tree_attention.cu", "tree_verify.cu", "verify_noalloc.cu",
-           "kv_compact.cu", "filter.cu", "tree_build.cu", "lm_head.cu", "verify_greedy.cu"]
+           "kv_compact.cu", "filter.cu", "tree_build.cu", "lm_head.cu", "verify_greedy.cu",
+           "verify_head.cu"]
 
 
 def nvcc() -> str:

@@ -20,6 +20,27 @@ struct NodeStat {
 };
 static_assert(sizeof(NodeStat) == 32, "NodeStat layout");
 
+// Walk state of one sequence in verification driven by the LM head's statistics
+// (verify_head.cu): the walk stands at `cur`; `pending` is the node whose full logit row the next
+// node step processes (-1: none).
+constexpr int kHeadMaxNodes = 64;
+struct HeadWalk {
+  int cur;
+  int pending;
+  int len;   // accepted nodes so far, in path[0 .. len)
+  int done;  // the sequence's outputs are written
+  int path[kHeadMaxNodes];
+};
+
+// Slot of node j's logit row in that verification's row buffer: sequence b's stretch of V + 4
+// floats, shifted so that the row has the 16-byte phase of draft row (b, j) (the node step stages
+// both with the same slice bounds).
+__host__ __device__ inline long long head_row_offset(int b, int j, int N, int V) {
+  const unsigned long long e = ((unsigned long long)b * (unsigned)N + (unsigned)j) * (unsigned)V;
+  const unsigned long long base = (unsigned long long)b * (unsigned)(V + 4);
+  return (long long)(base + ((e - base) & 3ull));  // == e (mod 4), within [base, base + 4)
+}
+
 struct VerifyArgs {
   const float* logits;
   const float* probs;
@@ -49,12 +70,18 @@ struct VerifyArgs {
   // gives up flags SPEC_ST_TIMEOUT and then drains with the full limit.  Normally the full limit;
   // lowered only through spec_debug_set_verify_wait_polls (tests of the timeout path).
   uint32_t first_polls = 0;
+  // node steps of the head-driven verification: row (b, j) lives at head_rows + head_row_offset
+  const float* head_rows = nullptr;
+  HeadWalk* head_state = nullptr;
+  const int32_t* head_flag = nullptr;  // non-zero: an LM-head pass gave up (SPEC_ST_TIMEOUT)
 };
 uint32_t verify_first_polls();  // the current first-attempt limit (spectree_abi.cu)
 
 size_t verify_workspace_bytes(int B, int N, int V);
 bool verify_supported(int V);  // the row slices of a cluster fit in shared memory
 cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s);
+// one node step per sequence whose head_state[b].pending >= 0 (T > 0), tree_verify.cu
+cudaError_t launch_verify_head_step(const VerifyArgs& a, int num_sms, cudaStream_t s);
 // rows of V target logits -> the same rows with -inf outside the top-k / top-p set (T > 0)
 // fused LM head (lm_head.cu)
 struct LmPartial {
@@ -68,12 +95,39 @@ cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t
                            int32_t* out_argmax, float* out_gather, void* workspace,
                            int32_t* flag, int num_sms, bool packed, cudaStream_t s);
 size_t lm_head_packed_bytes(int V, int H);
+// Full logit rows of M hidden rows: row r goes to out_rows + row_dst[r] (skipped when negative);
+// every CTA returns at once when *active == 0.  No statistics are kept.
+cudaError_t launch_lm_head_rows(const void* hidden, const void* weight, int M, int H, int V,
+                                const long long* row_dst, float* out_rows, const int32_t* active,
+                                int32_t* flag, bool packed, cudaStream_t s);
 // Greedy verification from each node's argmax token (verify_greedy.cu).
 cudaError_t launch_verify_greedy(const int32_t* node_argmax, const int32_t* tokens,
                                  const int32_t* parent, int B, int N, int V, int32_t* accept_len,
                                  int32_t* acc_tokens, int32_t* bonus, int32_t* acc_nodes,
                                  int32_t* status, cudaStream_t s);
 cudaError_t launch_lm_head_pack(const void* weight, int V, int H, void* packed, cudaStream_t s);
+
+// Verification driven by the LM head's statistics (verify_head.cu).
+struct HeadVerifyArgs {
+  const void* hidden;  // bf16 [B * N, H]
+  const void* head;    // bf16 [V, H], or packed (lm_head_packed_bytes)
+  bool packed;
+  const float* probs;  // [B, N, V] (T > 0)
+  const int32_t* tokens;
+  const int32_t* parent;
+  const float* uniforms;
+  float T;
+  int B, N, H, V, max_depth;
+  int32_t* accept_len;
+  int32_t* acc_tokens;
+  int32_t* bonus;
+  int32_t* acc_nodes;
+  int32_t* status;
+  void* workspace;
+  uint32_t first_polls;
+};
+size_t verify_head_workspace_bytes(int B, int N, int H, int V, int max_depth);
+cudaError_t launch_verify_head(const HeadVerifyArgs& a, int num_sms, cudaStream_t s);
 
 // dynamic tree construction (tree_build.cu)
 constexpr int kMaxTreeK = 16;       // candidates per expanded node, frontier size

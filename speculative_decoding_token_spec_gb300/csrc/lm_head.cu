@@ -13,6 +13,8 @@
 // TMEM) over the whole hidden dimension; warps 4-7 read their row's accumulators from TMEM
 // and write the tile's max, sum of exp and argmax.  Tested tokens are read from a copy of the tile
 // in the (then idle) stage memory.  lm_head_combine_kernel merges the tiles of each row.
+// Row passes (launch_lm_head_rows, for verification driven by these statistics) write the full
+// logits of the few rows whose destination is given, and leave at once when none is requested.
 #include <cuda.h>
 
 #include <mutex>
@@ -77,7 +79,9 @@ __global__ void __launch_bounds__(kLThreads, 1)
                    const __grid_constant__ CUtensorMap tmap_w, int M, int H, int V, int G, int tn,
                    int packed,
                    const int32_t* __restrict__ gather_idx, float k2, LmPartial* __restrict__ part,
-                   float* __restrict__ out_gather, int32_t* flag) {
+                   float* __restrict__ out_gather, int32_t* flag,
+                   const long long* __restrict__ row_dst, float* __restrict__ out_rows,
+                   const int32_t* active) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -103,6 +107,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
   }
   griddep_wait();  // the hidden states may come from the preceding kernel
   griddep_launch_dependents();
+  // a row pass with no row requested (uniform over the grid: nothing allocated or issued yet)
+  if (active && *reinterpret_cast<const volatile int32_t*>(active) == 0) return;
   if (warp == 1) tmem_alloc(smem_u32(&tmem_s), kLN);
   tc_fence_before();
   __syncthreads();
@@ -176,6 +182,11 @@ __global__ void __launch_bounds__(kLThreads, 1)
       }
       const float mk = __fmul_rn(mx, k2);
       float* tile = reinterpret_cast<float*>(smem);  // the stages are idle now
+      float* dst = nullptr;  // this row's full logits (row passes)
+      if (out_rows && row < M) {
+        const long long o = row_dst[row];
+        if (o >= 0) dst = out_rows + o;
+      }
 #pragma unroll 1
       for (int c = 0; c < nch; ++c) {  // sum of exp((l - max) / T); copy for the gathers
         float v[32];
@@ -186,6 +197,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
           const int col = v0 + 32 * c + q;
           if (col < vend) sum += exp2f(fmaf(v[q], k2, -mk));
           if (G > 0) tile[r * kTileStride + 32 * c + q] = v[q];
+          if (dst && col < vend) dst[col] = v[q];
         }
       }
       if (row < M) {
@@ -194,7 +206,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
         p.s = sum;
         p.arg = am;
         p.pad = 0;
-        part[(size_t)blockIdx.y * M + row] = p;
+        if (part) part[(size_t)blockIdx.y * M + row] = p;
         if (G > 0 && out_gather) {
           for (int g = 0; g < G; ++g) {
             const int tok = __ldg(gather_idx + (size_t)row * G + g);
@@ -340,7 +352,8 @@ cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t
   cfg.numAttrs = 1;
   LmPartial* part = static_cast<LmPartial*>(workspace);
   e = cudaLaunchKernelEx(&cfg, lm_head_kernel, mh, mw, M, H, V, G, tn, packed ? 1 : 0, gather_idx,
-                         k2, part, out_gather, flag);
+                         k2, part, out_gather, flag, (const long long*)nullptr, (float*)nullptr,
+                         (const int32_t*)nullptr);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t c2 = {};
   c2.gridDim = dim3((unsigned)((M + kCombineRows - 1) / kCombineRows));
@@ -350,6 +363,35 @@ cudaError_t launch_lm_head(const void* hidden, const void* weight, const int32_t
   c2.numAttrs = 1;
   return cudaLaunchKernelEx(&c2, lm_head_combine_kernel, (const LmPartial*)part, M, ntiles, k2,
                             out_max, out_sumexp, out_argmax);
+}
+
+cudaError_t launch_lm_head_rows(const void* hidden, const void* weight, int M, int H, int V,
+                                const long long* row_dst, float* out_rows, const int32_t* active,
+                                int32_t* flag, bool packed, cudaStream_t s) {
+  const int tn = kLN;
+  const int nk = (H + kLK - 1) / kLK;
+  CUtensorMap mh, mw;
+  const bool wmap = packed ? encode_bf16_2d(&mw, weight, kLK,
+                                            (long long)((V + kLN - 1) / kLN) * nk * kLN, kLK, kLN)
+                           : encode_bf16_2d(&mw, weight, H, V, kLK, tn);
+  if (!encode_bf16_2d(&mh, hidden, H, M, kLK, kLM) || !wmap) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((M + kLM - 1) / kLM), (unsigned)((V + tn - 1) / tn));
+  cfg.blockDim = dim3(kLThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float k2 = 1.4426950408889634f;  // the statistics of a row pass are not kept
+  return cudaLaunchKernelEx(&cfg, lm_head_kernel, mh, mw, M, H, V, 0, tn, packed ? 1 : 0,
+                            (const int32_t*)nullptr, k2, (LmPartial*)nullptr, (float*)nullptr, flag,
+                            row_dst, out_rows, active);
 }
 
 }  // namespace spectree

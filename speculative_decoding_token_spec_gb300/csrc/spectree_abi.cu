@@ -398,6 +398,63 @@ int spec_tree_verify_greedy(const int32_t* node_argmax, const int32_t* tree_toke
              : SPEC_ERR_CUDA;
 }
 
+size_t spec_tree_verify_head_workspace(int B, int N, int H, int V, int max_depth) {
+  if (B < 1 || N < 1 || N > kMaxNodes || H < 8 || (H & 7) || V < 1 || max_depth < 0 ||
+      max_depth >= N)
+    return 0;
+  return verify_head_workspace_bytes(B, N, H, V, max_depth);
+}
+
+int spec_tree_verify_head(const void* hidden, const void* head, int head_packed,
+                          const float* draft_probs, const int32_t* tree_tokens,
+                          const int32_t* tree_parent, const float* uniforms, float temperature,
+                          int B, int N, int H, int V, int max_depth, int32_t* out_accept_len,
+                          int32_t* out_accepted_tokens, int32_t* out_bonus_token,
+                          int32_t* out_accepted_nodes, void* workspace, size_t workspace_bytes,
+                          int32_t* status, void* stream) {
+  if (!hidden || !head || !tree_tokens || !tree_parent || !uniforms || !out_accept_len ||
+      !out_accepted_tokens || !out_bonus_token)
+    return SPEC_ERR_INVALID_ARG;
+  if (!std::isfinite(temperature) || temperature < 0.f) return SPEC_ERR_INVALID_ARG;
+  if (temperature > 0.f && (!draft_probs || !aligned16(draft_probs))) return SPEC_ERR_INVALID_ARG;
+  if (B < 1 || B > 65535 || N < 1 || N > kMaxNodes || V < 1 || H < 8 || (H & 7))
+    return SPEC_ERR_INVALID_ARG;
+  if (max_depth < 0 || max_depth >= N) return SPEC_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(head)) return SPEC_ERR_INVALID_ARG;
+  if (!verify_supported(V) || (long long)(V + 127) / 128 > 65535 ||
+      (long long)B * N * V > (1ll << 40))
+    return SPEC_ERR_UNSUPPORTED;
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < verify_head_workspace_bytes(B, N, H, V, max_depth))
+    return SPEC_ERR_WORKSPACE;
+  const int sms = sm_count();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  HeadVerifyArgs a;
+  a.hidden = hidden;
+  a.head = head;
+  a.packed = head_packed != 0;
+  a.probs = draft_probs;
+  a.tokens = tree_tokens;
+  a.parent = tree_parent;
+  a.uniforms = uniforms;
+  a.T = temperature;
+  a.B = B;
+  a.N = N;
+  a.H = H;
+  a.V = V;
+  a.max_depth = max_depth;
+  a.accept_len = out_accept_len;
+  a.acc_tokens = out_accepted_tokens;
+  a.bonus = out_bonus_token;
+  a.acc_nodes = out_accepted_nodes;
+  a.status = status;
+  a.workspace = workspace;
+  a.first_polls = g_verify_first_polls.load(std::memory_order_relaxed);
+  const cudaError_t e = launch_verify_head(a, sms, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return SPEC_ERR_INVALID_ARG;  // tensor maps refused
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 int spec_debug_set_verify_wait_polls(long long polls) {
   const uint32_t v = polls < 0 || polls > (long long)kSpinLimit ? kSpinLimit : (uint32_t)polls;
   g_verify_first_polls.store(v, std::memory_order_relaxed);

@@ -728,7 +728,8 @@ struct StopProbe {
 // ONLINE: the walk runs while nodes finish (every-node form without per-child q); a node stops at
 // the residual round in which it learns that the walk cannot reach it (StopProbe; its record then
 // flags kWalkDone).
-template <int CL, bool PGLOBAL, bool SAMPLING, bool ONLINE = false>
+// HEAD: the node's logit row is the head-driven verification's row slot (a.head_rows).
+template <int CL, bool PGLOBAL, bool SAMPLING, bool ONLINE = false, bool HEAD = false>
 __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, const NodeBufs& nb,
                                  bool logits_staged, DF invT_df, float k2, int& xk, int& writer,
                                  uint32_t& ph_l, uint32_t& ph_p, VerifySmem& sm) {
@@ -736,7 +737,7 @@ __device__ NodeStat process_node(const VerifyArgs& a, int b, int j, int rank, co
   list_children(j, N, sm);
   const int nk = sm.nk;
   const size_t row_off = ((size_t)b * N + j) * (size_t)V;
-  const float* lrow = a.logits + row_off;
+  const float* lrow = HEAD ? a.head_rows + head_row_offset(b, j, N, V) : a.logits + row_off;
   const float* prow = a.probs ? a.probs + row_off : nullptr;
   const Slice s = make_slice(lrow, V, rank, CL);  // the draft row has the same alignment
   constexpr bool sampling = SAMPLING;  // T > 0 (T == 0: greedy)
@@ -1376,6 +1377,90 @@ __global__ void __launch_bounds__(kVThreads, 4)
   cluster_barrier<CL>();  // keep shared memory alive for remote stores
 }
 
+// Node step of the verification driven by the LM head's statistics (verify_head.cu): one cluster
+// per sequence processes the node head_state[b].pending, whose full logit row a row pass of the LM
+// head has just written, with the per-node step above (sibling tests in order, residual rounds,
+// the bonus draw).  An accepted child becomes the walk's position (the next statistics walk
+// continues from it); otherwise the sequence's outputs are written.  Sequences without a pending
+// node return at once.
+template <int CL>
+__global__ void __launch_bounds__(kVThreads, 4)
+    verify_head_step_kernel(const VerifyArgs a, int cap, float invT_hi, float invT_lo, float k2) {
+  extern __shared__ __align__(16) float dyn[];
+  __shared__ VerifySmem sm;
+  __shared__ __align__(8) uint64_t bars[2];
+  const NodeBufs nb{dyn, dyn + cap, smem_u32(&bars[0]), smem_u32(&bars[1])};
+  const int rank = (CL > 1) ? int(cg::this_cluster().block_rank()) : 0;
+  const int b = blockIdx.z;
+  const int N = a.N;
+  if (threadIdx.x == 0) {
+    mbar_init(nb.bar_l, 1);
+    mbar_init(nb.bar_p, 1);
+    mbar_init(smem_u32(&sm.xbar[0]), 1);
+    mbar_init(smem_u32(&sm.xbar[1]), 1);
+    mbar_fence_init();
+    sm.first_polls = a.first_polls;
+    sm.ticket = 0;
+  }
+  __syncthreads();
+  cluster_arrive_release();  // exchange barriers initialised (waited for before the first exchange)
+  griddep_wait();  // the walk state and the row come from the preceding kernels
+  HeadWalk* hw = a.head_state + b;
+  // the same value in every CTA of the cluster (written by an earlier kernel)
+  const int c = *reinterpret_cast<const volatile int*>(&hw->pending);
+  const int head_flags = (a.head_flag && *reinterpret_cast<const volatile int*>(a.head_flag))
+                             ? SPEC_ST_TIMEOUT
+                             : 0;
+  const int bad = (c >= 0 && c < N) ? load_tree(a, b, sm) : SPEC_ST_BAD_TREE;
+  if (bad || head_flags) {
+    // no pending node (or a row pass gave up: the sequence ends flagged, without outputs)
+    if (head_flags && c >= 0 && rank == 0 && threadIdx.x == 0) {
+      a.accept_len[b] = -1;
+      a.bonus[b] = -1;
+      if (a.status) atomicOr(a.status + b, head_flags);
+      hw->pending = -1;
+      hw->done = 1;
+    }
+    if (head_flags && c >= 0 && rank == 0)
+      for (int i = threadIdx.x; i < N; i += kVThreads) {
+        a.acc_tokens[(size_t)b * N + i] = -1;
+        if (a.acc_nodes) a.acc_nodes[(size_t)b * N + i] = -1;
+      }
+    griddep_launch_dependents();
+    cluster_wait_acquire();
+    return;
+  }
+  cluster_wait_acquire();  // every CTA of the cluster can now receive exchanges
+  int xk = 0, writer = 0;
+  uint32_t ph_l = 0, ph_p = 0;
+  const NodeStat st = process_node<CL, false, true, false, true>(
+      a, b, c, rank, nb, false, DF{invT_hi, invT_lo}, k2, xk, writer, ph_l, ph_p, sm);
+  griddep_launch_dependents();
+  const int flags = st.flags;  // cluster-uniform, as first_acc
+  const int fa = st.first_acc;
+  const bool next = !(flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) && fa > c && fa < N;
+  if (next) {
+    if (rank == 0 && threadIdx.x == 0) {
+      const int len = hw->len;
+      if (len < kMaxNodes) hw->path[len] = fa;
+      hw->len = len + 1;
+      hw->cur = fa;
+      hw->pending = -1;
+    }
+  } else if (rank == writer) {  // c is the terminal node: the bonus is valid in this CTA
+    const int len = min(hw->len, kMaxNodes);
+    for (int i = threadIdx.x; i < len; i += kVThreads) sm.path[i] = hw->path[i];
+    if (threadIdx.x == 0) sm.path_len = len;
+    __syncthreads();
+    write_outputs(a, b, st.bonus, flags, sm);
+    if (threadIdx.x == 0) {
+      hw->pending = -1;
+      hw->done = 1;
+    }
+  }
+  cluster_barrier<CL>();  // keep shared memory alive for remote stores
+}
+
 // ------------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------------
@@ -1488,6 +1573,25 @@ static int pick_cluster_path(int B, int V, int num_sms) {
 }
 
 bool verify_supported(int V) { return slice_capacity(V, 8) <= kMaxSliceFloats; }
+
+cudaError_t launch_verify_head_step(const VerifyArgs& a, int num_sms, cudaStream_t s) {
+  if (!(a.T > 0.f) || !a.head_rows || !a.head_state) return cudaErrorInvalidValue;
+  const int cl = pick_cluster_path(a.B, a.V, num_sms);
+  const int cap = slice_capacity(a.V, cl);
+  // both rows staged: two slices of at most kMaxSliceFloats fit in shared memory
+  const size_t smem = 2 * (size_t)cap * sizeof(float);
+  const double invTd = 1.0 / (double)a.T;
+  const float invT_hi = (float)invTd, invT_lo = (float)(invTd - (double)invT_hi);
+  const float k2 = (float)(invTd * 1.4426950408889634);  // log2(e) / T
+  const dim3 g(cl, 1, a.B);
+  switch (cl) {
+    case 1: return launch_ex(verify_head_step_kernel<1>, g, 1, smem, s, a, cap, invT_hi, invT_lo, k2);
+    case 2: return launch_ex(verify_head_step_kernel<2>, g, 2, smem, s, a, cap, invT_hi, invT_lo, k2);
+    case 4: return launch_ex(verify_head_step_kernel<4>, g, 4, smem, s, a, cap, invT_hi, invT_lo, k2);
+    default:
+      return launch_ex(verify_head_step_kernel<8>, g, 8, smem, s, a, cap, invT_hi, invT_lo, k2);
+  }
+}
 
 cudaError_t launch_verify(const VerifyArgs& a, int num_sms, cudaStream_t s) {
   const bool small = (long long)a.B * a.N * a.V * 4 <= (64ll << 20);
