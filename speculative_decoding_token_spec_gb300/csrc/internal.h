@@ -41,6 +41,21 @@ __host__ __device__ inline long long head_row_offset(int b, int j, int N, int V)
   return (long long)(base + ((e - base) & 3ull));  // == e (mod 4), within [base, base + 4)
 }
 
+// What the statistics walk of the head-driven verification reads and writes (verify_head.cu; the
+// node step continues the walk in its tail, tree_verify.cu).
+struct HeadWalkIn {
+  const uint16_t* hidden = nullptr;  // bf16 [B * N, H]
+  const int32_t* fchild = nullptr;   // [B, N] first child (-1: leaf)
+  const float* stat_m = nullptr;     // [B, N] row max, sum of exp, first child's logit
+  const float* stat_s = nullptr;
+  const float* gath = nullptr;
+  long long* row_dst = nullptr;  // [B] row slot of the pending node (-1: none)
+  int32_t* active = nullptr;     // the next row pass's flag (null: no next pass)
+  uint16_t* hrow = nullptr;      // bf16 [B, H] hidden states of the pending nodes
+  double invT = 0.0;
+  int H = 0;
+};
+
 struct VerifyArgs {
   const float* logits;
   const float* probs;
@@ -74,6 +89,7 @@ struct VerifyArgs {
   const float* head_rows = nullptr;
   HeadWalk* head_state = nullptr;
   const int32_t* head_flag = nullptr;  // non-zero: an LM-head pass gave up (SPEC_ST_TIMEOUT)
+  HeadWalkIn head_walk;                // the walk continued after an accepted child
 };
 uint32_t verify_first_polls();  // the current first-attempt limit (spectree_abi.cu)
 

@@ -51,6 +51,7 @@
 #include <float.h>
 
 #include "common.cuh"
+#include "head_walk.cuh"
 #include "internal.h"
 
 namespace cg = cooperative_groups;
@@ -1420,6 +1421,7 @@ __global__ void __launch_bounds__(kVThreads, 4)
       if (a.status) atomicOr(a.status + b, head_flags);
       hw->pending = -1;
       hw->done = 1;
+      a.head_walk.row_dst[b] = -1;
     }
     if (head_flags && c >= 0 && rank == 0)
       for (int i = threadIdx.x; i < N; i += kVThreads) {
@@ -1440,12 +1442,39 @@ __global__ void __launch_bounds__(kVThreads, 4)
   const int fa = st.first_acc;
   const bool next = !(flags & (SPEC_ST_NONFINITE | SPEC_ST_TIMEOUT)) && fa > c && fa < N;
   if (next) {
-    if (rank == 0 && threadIdx.x == 0) {
-      const int len = hw->len;
-      if (len < kMaxNodes) hw->path[len] = fa;
-      hw->len = len + 1;
-      hw->cur = fa;
-      hw->pending = -1;
+    // the walk moves to fa and goes on from there on the statistics, marking the next pass's row
+    // (the last pass has none: the depth bound leaves no sequence open after it)
+    if (rank == 0) {
+      if (threadIdx.x == 0) {
+        const int len = hw->len;
+        if (len < kMaxNodes) hw->path[len] = fa;
+        hw->len = len + 1;
+        hw->cur = fa;
+        hw->pending = -1;
+        int wflags = 0, pend = -1;
+        if (a.head_walk.active) {
+          pend = head_stats_walk(a.head_walk, a.probs, a.tokens, a.uniforms, b, N, a.V, fa, hw,
+                                 wflags);
+          if (wflags) {
+            a.accept_len[b] = -1;
+            a.bonus[b] = -1;
+            if (a.status) atomicOr(a.status + b, wflags);
+            hw->done = 1;
+          }
+        }
+        if (pend < 0) a.head_walk.row_dst[b] = -1;
+        sm.found = wflags ? -2 : pend;
+      }
+      __syncthreads();
+      const int pend = sm.found;
+      if (pend == -2) {
+        for (int i = threadIdx.x; i < N; i += kVThreads) {
+          a.acc_tokens[(size_t)b * N + i] = -1;
+          if (a.acc_nodes) a.acc_nodes[(size_t)b * N + i] = -1;
+        }
+      } else if (pend >= 0) {
+        head_copy_hidden(a.head_walk, b, N, pend, threadIdx.x, kVThreads);
+      }
     }
   } else if (rank == writer) {  // c is the terminal node: the bonus is valid in this CTA
     const int len = min(hw->len, kMaxNodes);
@@ -1456,6 +1485,7 @@ __global__ void __launch_bounds__(kVThreads, 4)
     if (threadIdx.x == 0) {
       hw->pending = -1;
       hw->done = 1;
+      a.head_walk.row_dst[b] = -1;
     }
   }
   cluster_barrier<CL>();  // keep shared memory alive for remote stores

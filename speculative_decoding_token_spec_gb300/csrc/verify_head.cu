@@ -13,20 +13,22 @@
 //   1. head_prep_kernel: validate each tree, find every node's first child and its token, check
 //      the depth against the caller's bound;
 //   2. the LM head over every node's hidden state (lm_head.cu): m, S and the first child's logit;
-//   3. per row pass (at most max_depth + 1):
-//      a. head_walk_kernel: from the walk's position, accept first children while the test from
-//         the statistics accepts them; the node where it stops is pending (its first child was
-//         rejected, or it is a leaf); its hidden state is copied out;
-//      b. the LM head over the pending nodes' hidden states writes their full logit rows;
-//      c. verify_head_step_kernel (tree_verify.cu): the per-node step of spec_tree_verify on that
+//   3. head_walk_kernel: from the root, accept first children while the test from the statistics
+//      accepts them (head_walk.cuh); the node where it stops is pending (its first child was
+//      rejected, or it is a leaf); its hidden state is copied out;
+//   4. per row pass (max_depth + 1 of them):
+//      a. the LM head over the pending nodes' hidden states writes their full logit rows;
+//      b. verify_head_step_kernel (tree_verify.cu): the per-node step of spec_tree_verify on that
 //         row -- sibling tests from the first child, residual rounds, the bonus draw; an accepted
-//         child becomes the walk's position, otherwise the outputs are written;
-//   4. head_finish_kernel: flags what no pass finished (cannot happen after the depth check).
+//         child becomes the walk's position and the walk continues from it as in 3 (marking the
+//         next pass's row), otherwise the outputs are written;
+//   5. head_finish_kernel: flags what no pass finished (cannot happen after the depth check).
 // Each pass moves a sequence down at least one level or finishes it, so max_depth + 1 passes
 // suffice; passes with no pending node leave after one flag read.
 #include <cfloat>
 
 #include "common.cuh"
+#include "head_walk.cuh"
 #include "internal.h"
 #include "spectree.h"
 
@@ -132,25 +134,18 @@ __global__ void __launch_bounds__(kMaxNodes)
 }
 
 struct WalkArgs {
-  const uint16_t* hidden;  // bf16 [B * N, H]
-  const float* probs;      // [B, N, V]
+  HeadWalkIn in;
+  const float* probs;  // [B, N, V]
   const int32_t* tokens;
   const float* uniforms;
-  const int32_t* fchild;
-  const float* stat_m;
-  const float* stat_s;
-  const float* gath;
   const int32_t* lmflag;
   HeadWalk* state;
-  long long* row_dst;
-  int32_t* active;  // this pass's flag
-  uint16_t* hrow;   // bf16 [B, H]
-  double invT;
-  int B, N, H, V;
+  int B, N, V;
   Outs o;
 };
 
-// One warp per sequence: lane 0 walks, the warp copies the pending node's hidden state.
+// The walk's first stretch, after the statistics pass: one warp per sequence; lane 0 walks, the
+// warp copies the pending node's hidden state.  Later stretches run in the node step's tail.
 __global__ void __launch_bounds__(32 * kWalkWarps) head_walk_kernel(const WalkArgs w) {
   const int b = blockIdx.x * kWalkWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   griddep_wait();  // the statistics and the walk state come from the preceding kernels
@@ -161,58 +156,24 @@ __global__ void __launch_bounds__(32 * kWalkWarps) head_walk_kernel(const WalkAr
   int pend = -1;  // >= 0: pending node; -2: flagged here
   int flags = 0;
   if (lane == 0) {
+    w.in.row_dst[b] = -1;
     if (!hw->done) {
-      int c = hw->cur, len = hw->len;
       if (*reinterpret_cast<const volatile int32_t*>(w.lmflag)) flags |= SPEC_ST_TIMEOUT;
-      while (!flags) {  // at most one step per level: first children have larger indices
-        const size_t r = (size_t)b * N + c;
-        const int fc = w.fchild[r];
-        if (fc <= c || fc >= N) break;  // a leaf: the bonus draw needs the row
-        const float m = w.stat_m[r], S = w.stat_s[r], lx = w.gath[r];
-        if (!(m <= FLT_MAX) || !(S > 0.f && S <= FLT_MAX) || !(lx <= FLT_MAX)) {
-          flags |= SPEC_ST_NONFINITE;  // +Inf or NaN in the row (or no finite logit at all)
-          break;
-        }
-        const int x = w.tokens[(size_t)b * N + fc];
-        const float p = w.probs[r * (size_t)w.V + x];
-        const float u = w.uniforms[(size_t)b * N + fc];
-        if (!(p >= 0.f && p <= FLT_MAX)) {
-          flags |= SPEC_ST_NONFINITE;
-          break;
-        }
-        // r p(x~) S < exp((l_x~ - m) / T), the test r < q(x~) / p(x~) without the division
-        const double n = exp(((double)lx - (double)m) * w.invT);
-        if (!((double)u * (double)p * (double)S < n)) break;  // rejected: residual rounds follow
-        hw->path[len] = fc;  // len < N: one entry per level
-        ++len;
-        c = fc;
-      }
+      if (!flags)
+        pend = head_stats_walk(w.in, w.probs, w.tokens, w.uniforms, b, N, w.V, hw->cur, hw, flags);
       if (flags) {
         hw->done = 1;
         hw->pending = -1;
-        w.row_dst[b] = -1;
         pend = -2;
-      } else {
-        hw->cur = c;
-        hw->len = len;
-        hw->pending = c;
-        w.row_dst[b] = head_row_offset(b, c, N, w.V);
-        *w.active = 1;
-        pend = c;
       }
-    } else {
-      w.row_dst[b] = -1;
     }
   }
   pend = __shfl_sync(0xffffffffu, pend, 0);
   flags = __shfl_sync(0xffffffffu, flags, 0);
-  if (pend == -2) {
+  if (pend == -2)
     flag_sequence(w.o, b, N, flags, lane, 32);
-  } else if (pend >= 0) {  // 16-byte pieces: H % 8 == 0 and the buffers are 16-byte aligned
-    const uint4* src = reinterpret_cast<const uint4*>(w.hidden + ((size_t)b * N + pend) * w.H);
-    uint4* dst = reinterpret_cast<uint4*>(w.hrow + (size_t)b * w.H);
-    for (int k = lane; k < w.H / 8; k += 32) dst[k] = src[k];
-  }
+  else if (pend >= 0)
+    head_copy_hidden(w.in, b, N, pend, lane, 32);
 }
 
 // What no pass finished, and LM-head passes that gave up (every sequence flagged).
@@ -314,25 +275,30 @@ cudaError_t launch_verify_head(const HeadVerifyArgs& a, int num_sms, cudaStream_
                      at(L.part), lmflag, num_sms, a.packed, s);
   if (e != cudaSuccess) return e;
 
+  HeadWalkIn in;
+  in.hidden = static_cast<const uint16_t*>(a.hidden);
+  in.fchild = fchild;
+  in.stat_m = stat_m;
+  in.stat_s = stat_s;
+  in.gath = gath;
+  in.row_dst = static_cast<long long*>(at(L.row_dst));
+  in.active = active;  // pass 0
+  in.hrow = static_cast<uint16_t*>(at(L.hrow));
+  in.invT = 1.0 / (double)a.T;
+  in.H = a.H;
   WalkArgs w;
-  w.hidden = static_cast<const uint16_t*>(a.hidden);
+  w.in = in;
   w.probs = a.probs;
   w.tokens = a.tokens;
   w.uniforms = a.uniforms;
-  w.fchild = fchild;
-  w.stat_m = stat_m;
-  w.stat_s = stat_s;
-  w.gath = gath;
   w.lmflag = lmflag;
   w.state = state;
-  w.row_dst = static_cast<long long*>(at(L.row_dst));
-  w.hrow = static_cast<uint16_t*>(at(L.hrow));
-  w.invT = 1.0 / (double)a.T;
   w.B = a.B;
   w.N = a.N;
-  w.H = a.H;
   w.V = a.V;
   w.o = o;
+  e = launch_pdl(head_walk_kernel, wgrid, wblock, s, w);
+  if (e != cudaSuccess) return e;
 
   VerifyArgs va;
   va.logits = nullptr;
@@ -359,14 +325,14 @@ cudaError_t launch_verify_head(const HeadVerifyArgs& a, int num_sms, cudaStream_
   va.head_rows = static_cast<const float*>(at(L.rows));
   va.head_state = state;
   va.head_flag = lmflag;
+  va.head_walk = in;
 
   for (int it = 0; it <= a.max_depth; ++it) {
-    w.active = active + it;
-    e = launch_pdl(head_walk_kernel, wgrid, wblock, s, w);
-    if (e != cudaSuccess) return e;
-    e = launch_lm_head_rows(at(L.hrow), a.head, a.B, a.H, a.V, w.row_dst,
+    e = launch_lm_head_rows(at(L.hrow), a.head, a.B, a.H, a.V, in.row_dst,
                             static_cast<float*>(at(L.rows)), active + it, lmflag, a.packed, s);
     if (e != cudaSuccess) return e;
+    // the step continues the walk after an accepted child and marks the next pass's rows
+    va.head_walk.active = it < a.max_depth ? active + it + 1 : nullptr;
     e = launch_verify_head_step(va, num_sms, s);
     if (e != cudaSuccess) return e;
   }
