@@ -881,9 +881,10 @@ def measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs, attn_ms, timed, dev,
                         "logit_matrix_bytes_not_written": 4 * V * B * N,
                         "lm_head_stats_us": lm_ms * 1e3,
                         "kernel": "head_prep_kernel, lm_head_kernel + lm_head_combine_kernel "
-                                  "(statistics of every node), then per row pass "
-                                  "head_walk_kernel, lm_head_kernel (rows of the pending nodes), "
-                                  "verify_head_step_kernel; head_finish_kernel",
+                                  "(statistics of every node), head_walk_kernel, then per row "
+                                  "pass lm_head_kernel (rows of the pending nodes) and "
+                                  "verify_head_step_kernel (which continues the walk); "
+                                  "head_finish_kernel",
                         "note": "lattice hidden states and head (exact logits), EAGLE-style "
                                 "draft; one row pass = one more read of the head"},
         "peak_gbs": hbm_gbs,

@@ -1445,25 +1445,29 @@ __global__ void __launch_bounds__(kVThreads, 4)
     // the walk moves to fa and goes on from there on the statistics, marking the next pass's row
     // (the last pass has none: the depth bound leaves no sequence open after it)
     if (rank == 0) {
-      if (threadIdx.x == 0) {
-        const int len = hw->len;
-        if (len < kMaxNodes) hw->path[len] = fa;
-        hw->len = len + 1;
-        hw->cur = fa;
-        hw->pending = -1;
+      if (threadIdx.x < 32) {  // warp 0
+        if (threadIdx.x == 0) {
+          const int len = hw->len;
+          if (len < kMaxNodes) hw->path[len] = fa;
+          hw->len = len + 1;
+          hw->cur = fa;
+          hw->pending = -1;
+        }
+        __syncwarp();
         int wflags = 0, pend = -1;
-        if (a.head_walk.active) {
+        if (a.head_walk.active)
           pend = head_stats_walk(a.head_walk, a.probs, a.tokens, a.uniforms, b, N, a.V, fa, hw,
                                  wflags);
+        if (threadIdx.x == 0) {
           if (wflags) {
             a.accept_len[b] = -1;
             a.bonus[b] = -1;
             if (a.status) atomicOr(a.status + b, wflags);
             hw->done = 1;
           }
+          if (pend < 0) a.head_walk.row_dst[b] = -1;
+          sm.found = wflags ? -2 : pend;
         }
-        if (pend < 0) a.head_walk.row_dst[b] = -1;
-        sm.found = wflags ? -2 : pend;
       }
       __syncthreads();
       const int pend = sm.found;

@@ -155,21 +155,20 @@ __global__ void __launch_bounds__(32 * kWalkWarps) head_walk_kernel(const WalkAr
   HeadWalk* hw = w.state + b;
   int pend = -1;  // >= 0: pending node; -2: flagged here
   int flags = 0;
-  if (lane == 0) {
-    w.in.row_dst[b] = -1;
-    if (!hw->done) {
-      if (*reinterpret_cast<const volatile int32_t*>(w.lmflag)) flags |= SPEC_ST_TIMEOUT;
-      if (!flags)
-        pend = head_stats_walk(w.in, w.probs, w.tokens, w.uniforms, b, N, w.V, hw->cur, hw, flags);
-      if (flags) {
+  if (lane == 0) w.in.row_dst[b] = -1;
+  __syncwarp();
+  if (!hw->done) {  // the same value in every lane (written by an earlier kernel)
+    if (*reinterpret_cast<const volatile int32_t*>(w.lmflag)) flags |= SPEC_ST_TIMEOUT;
+    if (!flags)
+      pend = head_stats_walk(w.in, w.probs, w.tokens, w.uniforms, b, N, w.V, hw->cur, hw, flags);
+    if (flags) {
+      if (lane == 0) {
         hw->done = 1;
         hw->pending = -1;
-        pend = -2;
       }
+      pend = -2;
     }
   }
-  pend = __shfl_sync(0xffffffffu, pend, 0);
-  flags = __shfl_sync(0xffffffffu, flags, 0);
   if (pend == -2)
     flag_sequence(w.o, b, N, flags, lane, 32);
   else if (pend >= 0)

@@ -37,7 +37,8 @@ def test_header_declares_the_entry_points():
               "spec_tree_verify_filtered_workspace", "spec_tree_build_workspace",
               "spec_tree_expand", "spec_tree_finalize", "spec_lm_head_stats",
               "spec_lm_head_stats_workspace", "spec_lm_head_pack", "spec_lm_head_stats_packed",
-              "spec_tree_verify_greedy"):
+              "spec_tree_verify_greedy", "spec_tree_verify_head",
+              "spec_tree_verify_head_workspace"):
         assert n in names
 
 
@@ -241,6 +242,30 @@ def test_greedy_verify_arguments(lib):
                                            null)
     assert call(am=null) == -1 and call(out=null) == -1
     assert call(B=0) == -1 and call(N=0) == -1 and call(N=65) == -1 and call(V=0) == -1
+
+
+def test_head_verify_arguments(lib):
+    """Workspace query and argument errors of verification from the LM head, before any CUDA
+    call."""
+    assert lib.spec_tree_verify_head_workspace(1, 60, 4096, 32000, 6) > 0
+    assert lib.spec_tree_verify_head_workspace(1, 60, 4096, 32000, 60) == 0  # depth >= N
+    assert lib.spec_tree_verify_head_workspace(1, 60, 4100, 32000, 6) == 0   # H % 8
+    assert lib.spec_tree_verify_head_workspace(1, 65, 4096, 32000, 6) == 0   # N > 64
+    fake = ctypes.c_void_p(256)
+    odd = ctypes.c_void_p(260)
+    null = None
+    ws = lib.spec_tree_verify_head_workspace(2, 10, 64, 1000, 3)
+
+    def call(B=2, N=10, H=64, V=1000, depth=3, T=1.0, h=fake, p=fake, nbytes=ws, wsp=fake,
+             out=fake):
+        return lib.spec_tree_verify_head(h, fake, 0, p, fake, fake, fake, T, B, N, H, V, depth,
+                                         out, fake, fake, null, wsp, nbytes, null, null)
+    assert call(h=null) == -1 and call(out=null) == -1
+    assert call(h=odd) == -1 and call(p=odd) == -1      # 16-byte alignment
+    assert call(p=null) == -1 and call(T=-1.0) == -1 and call(T=float("inf")) == -1
+    assert call(H=60) == -1 and call(N=65) == -1 and call(B=0) == -1
+    assert call(depth=10) == -1 and call(depth=-1) == -1
+    assert call(nbytes=ws - 16) == -3 and call(wsp=null) == -3
 
 
 def test_header_is_plain_c_and_a_c_program_links(lib, tmp_path):
