@@ -74,11 +74,23 @@ __device__ inline int head_stats_walk(const HeadWalkIn& w, const float* probs,
 
 // The pending node's hidden state into the row pass's input (threads t of nt; 16-byte pieces:
 // H % 8 == 0 and both buffers 16-byte aligned).
+// Eight loads in flight per thread before their stores (a plain copy loop waits for each load:
+// the compiler cannot move a load above the previous store to a possibly aliasing buffer).
 __device__ inline void head_copy_hidden(const HeadWalkIn& w, int b, int N, int node, int t,
                                         int nt) {
+  constexpr int kBatch = 8;
   const uint4* src = reinterpret_cast<const uint4*>(w.hidden + ((size_t)b * N + node) * w.H);
   uint4* dst = reinterpret_cast<uint4*>(w.hrow + (size_t)b * w.H);
-  for (int k = t; k < w.H / 8; k += nt) dst[k] = src[k];
+  const int n = w.H / 8;
+  for (int k0 = t; k0 < n; k0 += nt * kBatch) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (k0 + i * nt < n) v[i] = src[k0 + i * nt];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (k0 + i * nt < n) dst[k0 + i * nt] = v[i];
+  }
 }
 
 }  // namespace spectree

@@ -170,6 +170,11 @@ def test_shapes_and_trees(dev):
     cases.append(W.make_head_verify_case(cfg, 256, 0.7, seed=5, sigma_d=1.0, tree_parent=two))
     cfg = W.config("eagle_vicuna7b", B=2, N=64, depth=7, width=10, V=4003)
     cases.append(W.make_head_verify_case(cfg, 192, 1.0, seed=5))
+    # batches: 16 walk blocks; row passes over two 128-row tiles
+    cfg = W.config("eagle_vicuna7b", B=64, N=20, depth=4, width=8, V=3000)
+    cases.append(W.make_head_verify_case(cfg, 256, 1.0, seed=6))
+    cfg = W.config("eagle_vicuna7b", B=130, N=4, depth=2, width=2, V=600)
+    cases.append(W.make_head_verify_case(cfg, 64, 0.7, seed=8, sigma_d=0.5))
     for case in cases:
         check(case, dev)
 
