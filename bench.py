@@ -273,10 +273,6 @@ def run_ours(args):
     import speculative_decoding_token_spec_gb300 as st
 
     ws, rank, local = dist_env()
-    # the other workloads' CPU legs start first (spawned workers), overlapping the GPU work
-    pool, futs = (None, None)
-    if not args.no_configs and ws == 1:
-        pool, futs = start_cpu_legs(args.seed)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if ws > 1:
@@ -493,6 +489,12 @@ def run_ours(args):
 
     if rank != 0:
         return
+    # the other workloads' CPU legs (spawned workers) overlap the GPU work from here on; started
+    # earlier, their input generation and fp64 oracle compete with the e2e region's copies for the
+    # host's memory bandwidth (e2e 150 K against 320 K nodes/s measured)
+    pool, futs = (None, None)
+    if not args.no_configs and ws == 1:
+        pool, futs = start_cpu_legs(args.seed)
     nxt = None if args.no_next else measure_next_rows(args, cfg, bufs, attn_bytes, hbm_gbs,
                                                       attn_ms, timed, dev, L2, tc_tflops)
     others = None
